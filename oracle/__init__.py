@@ -1,0 +1,281 @@
+"""CPU oracle for retrieval-based sparse decode attention.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` may import this package. The
+CUDA library and its Python binding never import it, and it imports nothing
+from them.
+
+The arithmetic lives in ``kvr_oracle.c`` (plain single-threaded C, built with
+``-O2 -ffp-contract=off``); this module only builds it, loads it with ctypes
+and loops over the independent (batch, kv-head) units. Inputs are numpy
+arrays or CPU torch tensors; bf16 tensors are widened to fp32 exactly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = [os.path.join(_HERE, "kvr_oracle.c"), os.path.join(_HERE, "kvr_tiers_oracle.c")]
+_LIB = os.path.join(_HERE, "libkvr_oracle.so")
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/libkvr_oracle.so`` (gcc, no fast-math)."""
+    srcs = [s for s in _SRC if os.path.exists(s)]
+    newest = max(os.path.getmtime(s) for s in srcs)
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= newest:
+        return _LIB
+    tmp = _LIB + ".tmp%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-fPIC",
+           "-shared", "-o", tmp] + srcs + ["-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        L.orc_fwht_f32.argtypes = [_P, _I32]
+        L.orc_srht_unit_f64.argtypes = [_P, _I32, _P, _P]
+        L.orc_encode.argtypes = [_P, _I64, _I32, _P, _P]
+        L.orc_group_mean.argtypes = [_P, _I32, _I32, _P]
+        L.orc_coarse_scores.argtypes = [_P, _I64, _I32, _P, _P, _P]
+        L.orc_top_by_int.argtypes = [_P, _I64, _I64, _P]
+        L.orc_top_by_int.restype = _I64
+        L.orc_top_by_float.argtypes = [_P, _P, _I64, _I64, _P]
+        L.orc_top_by_float.restype = _I64
+        L.orc_exact_score.argtypes = [_P, _P, _I32]
+        L.orc_exact_score.restype = ctypes.c_float
+        L.orc_select_unit.argtypes = [_P, _I32, _P, _P, _I64, _I32, _P, _I64, _I64, _I64,
+                                      _P, _P, _P, _P, _P, _P, _P]
+        L.orc_attend_unit.argtypes = [_P, _I32, _P, _P, _I64, _I32, _P, _I64, _I64,
+                                      ctypes.c_float, _P]
+        _tier_signatures(L)
+        _lib = L
+    return _lib
+
+
+def _tier_signatures(L):
+    if not hasattr(L, "orc_int2_quantize_group"):
+        return
+    L.orc_f32_to_f16_rd.argtypes = [ctypes.c_float]
+    L.orc_f32_to_f16_rd.restype = ctypes.c_uint16
+    L.orc_f32_to_f16_ru.argtypes = [ctypes.c_float]
+    L.orc_f32_to_f16_ru.restype = ctypes.c_uint16
+    L.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
+    L.orc_f16_to_f32.restype = ctypes.c_float
+    L.orc_int2_quantize_group.argtypes = [_P, _P, _P, _P]
+    L.orc_int2_dequantize_group.argtypes = [_P, ctypes.c_uint16, ctypes.c_uint16, _P]
+    L.orc_ledger_write_window.argtypes = [_P, _P, _P]
+    L.orc_ledger_read_window.argtypes = [_P, _P, _P]
+    L.orc_tiered_attend_unit.argtypes = [_P, _I32, _P, _P, _P, _P, _I64, _P, _I64, _I64,
+                                         ctypes.c_float, _P, _P]
+    L.orc_tiered_attend_unit.restype = _I32
+    L.orc_tier_route_unit.argtypes = [_P, _P, _P, _I64, _I64, _I64, _I64, _P]
+    L.orc_tier_route_unit.restype = _I32
+
+
+# --------------------------------------------------------------------------
+# array helpers
+# --------------------------------------------------------------------------
+
+def f32(x) -> np.ndarray:
+    """fp32 C-contiguous numpy copy; bf16 / fp16 torch tensors widen exactly."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return np.ascontiguousarray(x.detach().to("cpu", torch.float32).numpy())
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(np.asarray(a, dtype=dtype))
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+# --------------------------------------------------------------------------
+# the steps, exposed one by one
+# --------------------------------------------------------------------------
+
+def fwht(x) -> np.ndarray:
+    """Natural-order FWHT of each row of x (fp32, canonical stage order)."""
+    a = f32(x).copy()
+    d = a.shape[-1]
+    flat = a.reshape(-1, d)
+    for r in range(flat.shape[0]):
+        row = np.ascontiguousarray(flat[r])
+        lib().orc_fwht_f32(_p(row), d)
+        flat[r] = row
+    return flat.reshape(a.shape)
+
+
+def srht_unit(x, sgn) -> np.ndarray:
+    """fp64 rotated unit vector (1/sqrt(d)) H D x / ||x|| of one vector."""
+    a = f32(x)
+    s = _c(sgn, np.int8)
+    y = np.zeros(a.shape[-1], dtype=np.float64)
+    lib().orc_srht_unit_f64(_p(a), a.shape[-1], _p(s), _p(y))
+    return y
+
+
+def encode(x, sgn) -> np.ndarray:
+    """Sign codes [..., d/8] uint8 of the rows of x [..., d]."""
+    a = f32(x)
+    d = a.shape[-1]
+    n = a.size // d
+    s = _c(sgn, np.int8)
+    out = np.zeros(a.shape[:-1] + (d // 8,), dtype=np.uint8)
+    rc = lib().orc_encode(_p(a), n, d, _p(s), _p(out))
+    if rc != 0:
+        raise ValueError("unsupported head_dim %d" % d)
+    return out
+
+
+def group_mean(q) -> np.ndarray:
+    """Mean query q_bar [d] of the group's heads q [G, d]."""
+    a = f32(q)
+    G, d = a.shape
+    out = np.zeros(d, dtype=np.float32)
+    lib().orc_group_mean(_p(a), G, d, _p(out))
+    return out
+
+
+def coarse_scores(codes, qcode, lut) -> np.ndarray:
+    c = _c(codes, np.uint8)
+    nb = c.shape[-1]
+    n = c.size // nb
+    qc = _c(qcode, np.uint8)
+    lt = _c(lut, np.int32)
+    out = np.zeros(n, dtype=np.int32)
+    lib().orc_coarse_scores(_p(c), n, nb, _p(qc), _p(lt), _p(out))
+    return out
+
+
+def top_by_int(score, c) -> np.ndarray:
+    s = _c(score, np.int32)
+    out = np.zeros(max(1, min(c, s.size)), dtype=np.int64)
+    n = lib().orc_top_by_int(_p(s), s.size, c, _p(out))
+    return out[:n]
+
+
+def top_by_float(score, index, c) -> np.ndarray:
+    s = _c(score, np.float32)
+    ix = _c(index, np.int64)
+    out = np.zeros(max(1, min(c, s.size)), dtype=np.int64)
+    n = lib().orc_top_by_float(_p(s), _p(ix), s.size, c, _p(out))
+    if n < 0:
+        raise ValueError("NaN exact score")
+    return out[:n]
+
+
+def exact_score(qbar, k) -> np.float32:
+    a = f32(qbar)
+    b = f32(k)
+    return np.float32(lib().orc_exact_score(_p(a), _p(b), a.shape[-1]))
+
+
+# --------------------------------------------------------------------------
+# whole calls over [B, H, ...] tensors
+# --------------------------------------------------------------------------
+
+def encode_cache(K, sgn) -> np.ndarray:
+    """Codes [B, Hkv, n, d/8] of a whole cache K [B, Hkv, n, d]."""
+    return encode(K, sgn)
+
+
+def select_unit(q_group, K_unit, codes_unit, N, sgn, C, k, W, lut, diagnostics=False):
+    """Steps 1-4 of one unit; returns (idx[k] padded -1, count[, diag dict])."""
+    q = f32(q_group)
+    G, d = q.shape
+    Kf = f32(K_unit)
+    cd = _c(codes_unit, np.uint8)
+    s = _c(sgn, np.int8)
+    lt = _c(lut, np.int32)
+    idx = np.full(max(k, 1), -1, dtype=np.int32)
+    cnt = np.zeros(1, dtype=np.int32)
+    pool = max(0, N - W)
+    nc = max(0, min(C, pool))
+    cand = np.full(max(nc, 1), -1, dtype=np.int32)
+    candS = np.zeros(max(nc, 1), dtype=np.float32)
+    coarse = np.zeros(max(pool, 1), dtype=np.int32)
+    qcode = np.zeros(d // 8, dtype=np.uint8)
+    if diagnostics:
+        extra = (_p(cand), _p(candS), _p(coarse), _p(qcode))
+    else:
+        extra = (None, None, None, None)
+    rc = lib().orc_select_unit(_p(q), G, _p(Kf), _p(cd), N, d, _p(s), C, k, W, _p(lt),
+                               _p(idx), _p(cnt), *extra)
+    if rc != 0:
+        raise ValueError("oracle selection failed (NaN score or bad shape)")
+    if not diagnostics:
+        return idx[:k], int(cnt[0])
+    return idx[:k], int(cnt[0]), dict(cand=cand[:nc], cand_S=candS[:nc],
+                                      coarse=coarse[:pool], qcode=qcode)
+
+
+def select(q, K, codes, seq_len, sgn, C, k, W, lut, units=None):
+    """kvr_select over all units. q [B,Hq,d]; K [B,Hkv,cap,d]; codes [B,Hkv,cap,nb].
+
+    Returns idx [B, Hkv, k] int32 (ascending, -1 padded) and count [B, Hkv].
+    ``units`` optionally restricts the work to a list of (b, h) pairs (the
+    other rows are left at -1 / 0).
+    """
+    B, Hq, d = q.shape
+    Hkv = K.shape[1]
+    G = Hq // Hkv
+    out = np.full((B, Hkv, k), -1, dtype=np.int32)
+    cnt = np.zeros((B, Hkv), dtype=np.int32)
+    todo = units if units is not None else [(b, h) for b in range(B) for h in range(Hkv)]
+    for b, h in todo:
+        N = int(seq_len[b])
+        i, c = select_unit(q[b, h * G:(h + 1) * G], K[b, h, :N], codes[b, h, :N], N, sgn,
+                           C, k, W, lut)
+        out[b, h] = i
+        cnt[b, h] = c
+    return out, cnt
+
+
+def attend_unit(q_group, K_unit, V_unit, N, idx, count, W, scale) -> np.ndarray:
+    q = f32(q_group)
+    G, d = q.shape
+    Kf = f32(K_unit)
+    Vf = f32(V_unit)
+    ix = _c(idx, np.int32)
+    out = np.zeros((G, d), dtype=np.float64)
+    rc = lib().orc_attend_unit(_p(q), G, _p(Kf), _p(Vf), N, d, _p(ix), count, W,
+                               float(scale), _p(out))
+    if rc != 0:
+        raise ValueError("selected index outside the pool")
+    return out
+
+
+def attend(q, K, V, idx, count, seq_len, W, scale, units=None):
+    """kvr_sparse_attend over all units; returns out [B, Hq, d] fp64."""
+    B, Hq, d = q.shape
+    Hkv = K.shape[1]
+    G = Hq // Hkv
+    out = np.zeros((B, Hq, d), dtype=np.float64)
+    todo = units if units is not None else [(b, h) for b in range(B) for h in range(Hkv)]
+    for b, h in todo:
+        N = int(seq_len[b])
+        c = int(count[b, h])
+        out[b, h * G:(h + 1) * G] = attend_unit(q[b, h * G:(h + 1) * G], K[b, h, :N],
+                                                V[b, h, :N], N, idx[b, h, :c], c, W, scale)
+    return out
