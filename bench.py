@@ -1,0 +1,426 @@
+#!/usr/bin/env python
+"""Decode-step throughput of retrieval-based sparse decode attention.
+
+Workload: one Llama-3-8B-shaped decode-attention layer at 128K context
+(B=1, 32 query / 8 KV heads, head_dim 128, bf16 K/V, candidate budget 8192,
+top-k 2048, local window 128). A step is one pass of the whole hot path for
+one layer: encode the appended key, kvr_select (coarse score, candidates,
+exact rescoring, top-k) and kvr_sparse_attend. Steps rotate over 32 layer
+caches (17.7 GB) so every step reads its cache cold from HBM (inputs larger
+than L2). Each layer's step is one captured CUDA graph.
+
+Output: one JSON line (rank 0). --impl reference times the CPU oracle on the
+host cores instead, on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse decode-attention steps/s at 128K ctx; achieved HBM GB/s vs peak"
+LAYERS = 32
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def algorithmic_bytes(w):
+    """Bytes the hot path must read per step per unit (batch x kv head)."""
+    N = w.N
+    pool = N - w.W
+    Cp = min(w.C, pool)
+    kp = min(w.k, Cp)
+    row = w.d * 2  # bf16 row
+    codes = pool * (w.d // 8)
+    cand_rows = Cp * row
+    sel_kv = (kp + w.W) * 2 * row
+    q = w.G * w.d * 2
+    units = w.B * w.Hkv
+    return dict(select=units * (codes + cand_rows + q), attend=units * (sel_kv + q),
+                encode=units * (row + w.d // 8), units=units)
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.strip().split(", ") for r in self.f.read().splitlines() if r.strip()]
+        self.f.close()
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = max(mx, float(r[2]))
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() in ("active", "1"):
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, local, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# CPU oracle arm (cpu_baseline leg and --impl reference)
+# --------------------------------------------------------------------------
+
+def oracle_unit_inputs(w, device):
+    """Unit (b=0, h=0) of layer 0 of the workload, as host fp32 arrays."""
+    import numpy as np
+    import torch
+    import workloads as wl
+    import oracle
+    K, V, qb = wl.make_cache(w.with_(B=1), device=device, cap=w.N)
+    K0 = oracle.f32(K[0, 0].cpu())
+    V0 = oracle.f32(V[0, 0].cpu())
+    sgn = wl.srht_signs(w.d).numpy()
+    codes = oracle.encode(K0, sgn)
+    qs = [oracle.f32(wl.step_query(w, qb, t)[0, :w.G].cpu()) for t in range(64)]
+    del K, V
+    if device != "cpu":
+        torch.cuda.empty_cache()
+    return K0, V0, codes, sgn, qs
+
+
+def time_oracle(w, budget_s, device, min_steps=1, max_steps=None):
+    """Oracle decode steps on the host: each step runs one unit and counts
+    1/units of a whole step. Returns (steps/s, seconds, unit-steps done)."""
+    import numpy as np
+    import oracle
+    K0, V0, codes, sgn, qs = oracle_unit_inputs(w, device)
+    units = w.B * w.Hkv
+    scale = np.float32(1 / math.sqrt(w.d))
+    done, t0 = 0, time.perf_counter()
+    while True:
+        q = qs[done % len(qs)]
+        idx, cnt = oracle.select_unit(q, K0, codes, w.N, sgn, w.C, w.k, w.W, w.lut)
+        oracle.attend_unit(q, K0, V0, w.N, idx[:cnt], cnt, w.W, scale)
+        done += 1
+        el = time.perf_counter() - t0
+        if (el >= budget_s and done >= min_steps) or (max_steps and done >= max_steps):
+            break
+    return (done / units) / el, el, done
+
+
+def run_reference(args, w):
+    rank, local, world = dist_setup(args)
+    if rank != 0:
+        return
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    per_step_budget = float(os.environ.get("KVR_REF_STEP_SECONDS", "0.5"))
+    # warm-up: one unit-step per warm-up step (untimed)
+    time_oracle(w, 0.0, dev, max_steps=max(1, min(args.warmup, 3)))
+    budget = per_step_budget * args.steps
+    value, el, done = time_oracle(w, budget, dev, min_steps=args.steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 / value, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle",
+                         "sample": "%d unit-steps (batch 0, kv head 0 of %d units) of the 128K "
+                                   "workload, %.1f s; steps/s = unit-steps / %d / s"
+                                   % (done, w.B * w.Hkv, el, w.B * w.Hkv)},
+        "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w):
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.d,
+            "context": w.N, "C": w.C, "k": w.k, "W": w.W, "lut": list(w.lut),
+            "layers_rotated": LAYERS,
+            "l2": "inputs larger than L2: steps rotate over %d layer caches" % LAYERS,
+            "parallelism": "replicas (independent units per GPU)"}
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+class Layer:
+    def __init__(self, w, l, kvr, wl, torch, sgn):
+        dev = "cuda"
+        K, V, qb = wl.make_cache(w, device=dev, cap=w.N, seed=w.seed + 1000 * l)
+        self.K, self.V = K, V
+        self.q = wl.step_query(w, qb, 0, seed=w.seed + 1000 * l).contiguous()
+        self.codes = torch.empty((w.B, w.Hkv, w.N, w.d // 8), dtype=torch.uint8, device=dev)
+        kvr.kvr_encode_keys(K, torch.zeros(w.B, dtype=torch.int32, device=dev), w.N, sgn,
+                            self.codes)
+        self.out = torch.empty((w.B, w.Hq, w.d), dtype=torch.float32, device=dev)
+
+
+def run_gpu(args, w):
+    import numpy as np
+    import torch
+    import sparse_decode_attention_gb300 as kvr
+    import workloads as wl
+
+    rank, local, world = dist_setup(args)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    kvr.load()
+    sgn = wl.srht_signs(w.d, device=dev)
+    layers = [Layer(w, l, kvr, wl, torch, sgn) for l in range(LAYERS)]
+    shape = kvr.Shape.of(layers[0].K, layers[0].q)
+    params = kvr.SelectParams(w.C, w.k, w.W, w.lut)
+    ws_s = kvr.workspace(kvr.kvr_select_workspace_size(shape, params), dev)
+    ws_a = kvr.workspace(kvr.kvr_attend_workspace_size(shape, w.k, w.W), dev)
+    idx = torch.empty((w.B, w.Hkv, w.k), dtype=torch.int32, device=dev)
+    cnt = torch.empty((w.B, w.Hkv), dtype=torch.int32, device=dev)
+    seq = torch.full((w.B,), w.N, dtype=torch.int32, device=dev)
+    pos_new = torch.full((w.B,), w.N - 1, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    scale = 1.0 / math.sqrt(w.d)
+
+    def step(L, ev=None):
+        if ev:
+            ev[0].record()
+        kvr.kvr_encode_keys(L.K, pos_new, 1, sgn, L.codes, err)
+        if ev:
+            ev[1].record()
+        kvr.kvr_select(L.q, L.K, L.codes, seq, sgn, params, idx, cnt, ws_s, err)
+        if ev:
+            ev[2].record()
+        kvr.kvr_sparse_attend(L.q, L.K, L.V, idx, cnt, seq, w.W, scale, L.out, ws_a, err)
+        if ev:
+            ev[3].record()
+
+    launches_per_step = 1 + 4 + 2
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    # eager warm-up on the capture stream, then one graph per layer
+    with torch.cuda.stream(stream):
+        for L in layers[:2]:
+            step(L)
+    stream.synchronize()
+    if kvr.kvr_read_error(err):
+        raise RuntimeError("device error bits during warm-up")
+    try:
+        mk = lambda: torch.cuda.Event(enable_timing=True, external=True)
+        mk()
+        external = True
+    except TypeError:
+        external = False
+    graphs, evs = [], []
+    for L in layers:
+        g = torch.cuda.CUDAGraph()
+        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)] \
+            if external else None
+        with torch.cuda.graph(g, stream=stream):
+            step(L, ev)
+        graphs.append(g)
+        evs.append(ev)
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % LAYERS].replay()
+    stream.synchronize()
+
+    clocks = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.25 if clocks else 0)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t_start.record()
+        for i in range(args.steps):
+            graphs[i % LAYERS].replay()
+        t_end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    ms = t_start.elapsed_time(t_end)
+    ms = max_over_ranks(ms, world)
+    if kvr.kvr_read_error(err):
+        raise RuntimeError("device error bits during the timed region")
+
+    # per-call durations from the last replay of every layer graph
+    per = {"encode": [], "select": [], "attend": []}
+    if external:
+        last = set(range(max(0, args.steps - LAYERS), args.steps))
+        for i in sorted(last):
+            ev = evs[i % LAYERS]
+            per["encode"].append(ev[0].elapsed_time(ev[1]))
+            per["select"].append(ev[1].elapsed_time(ev[2]))
+            per["attend"].append(ev[2].elapsed_time(ev[3]))
+    avg = {k: (sum(v) / len(v) if v else None) for k, v in per.items()}
+
+    # end to end through the public API with pinned host buffers
+    e2e = run_e2e(args, w, layers, kvr, torch, sgn, params, ws_s, ws_a, idx, cnt, seq, pos_new,
+                  err, scale, world)
+
+    steps_total = args.steps * world
+    value = steps_total / (ms / 1000.0)
+    if rank != 0:
+        return
+    ab = algorithmic_bytes(w)
+    peak, peak_kind = peaks()
+    roof = None
+    if avg["select"]:
+        ach = ab["select"] / (avg["select"] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": "kvr_select (score, threshold, rescore, top-k "
+                                            "launches)",
+                "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                "peak_kind": peak_kind, "traffic": None,
+                "algorithmic_bytes": ab["select"], "avg_ms": avg["select"]}
+    path = None
+    if avg["select"] and avg["attend"]:
+        tsum = (avg["select"] + avg["attend"]) * 1e-3
+        ach = (ab["select"] + ab["attend"]) / tsum / 1e9
+        path = {"calls": "kvr_select + kvr_sparse_attend", "achieved": ach, "peak": peak,
+                "unit": "GB/s", "frac": ach / peak, "frac_of_8TBs": ach / 8000.0,
+                "us": tsum * 1e6, "algorithmic_bytes": ab["select"] + ab["attend"],
+                "attend_us": avg["attend"] * 1e3, "encode_us": avg["encode"] * 1e3}
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        v, el, done = time_oracle(w, args.cpu_seconds, "cuda")
+        cpu = {"value": v, "unit": "steps/s", "cores": 1, "kind": "oracle",
+               "sample": "%d unit-steps (batch 0, kv head 0) of the 128K workload in %.1f s, "
+                         "single-threaded; steps/s = unit-steps / %d / s" % (done, el, ab["units"])}
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_of(w), "roofline": roof, "path_roofline": path,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, w, layers, kvr, torch, sgn, params, ws_s, ws_a, idx, cnt, seq, pos_new, err,
+            scale, world):
+    """Per step: copy the query and the appended K/V row from pinned host memory,
+    run the three public calls, copy the output back, synchronise."""
+    dev = layers[0].K.device
+    n = min(args.steps, args.e2e_steps)
+    hq = [L.q.cpu().pin_memory() for L in layers]
+    hk = [L.K[:, :, w.N - 1].cpu().pin_memory() for L in layers]
+    hv = [L.V[:, :, w.N - 1].cpu().pin_memory() for L in layers]
+    hout = torch.empty((w.B, w.Hq, w.d), dtype=torch.float32).pin_memory()
+    h2d = hq[0].numel() * hq[0].element_size() + 2 * hk[0].numel() * hk[0].element_size()
+    d2h = hout.numel() * hout.element_size()
+
+    def one(i):
+        L = layers[i % LAYERS]
+        L.q.copy_(hq[i % LAYERS], non_blocking=True)
+        L.K[:, :, w.N - 1].copy_(hk[i % LAYERS], non_blocking=True)
+        L.V[:, :, w.N - 1].copy_(hv[i % LAYERS], non_blocking=True)
+        kvr.kvr_encode_keys(L.K, pos_new, 1, sgn, L.codes, err)
+        kvr.kvr_select(L.q, L.K, L.codes, seq, sgn, params, idx, cnt, ws_s, err)
+        kvr.kvr_sparse_attend(L.q, L.K, L.V, idx, cnt, seq, w.W, scale, L.out, ws_a, err)
+        hout.copy_(L.out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for i in range(min(args.warmup, 8)):
+        one(i)
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(n):
+        one(i)
+    el = time.perf_counter() - t0
+    el = max_over_ranks(el, world)
+    return {"value": n * world / el, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n, "mode": "eager C-ABI calls, sync per step"}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--impl", choices=["kvr", "reference"], default="kvr")
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    import workloads as wl
+    w = wl.LLAMA_128K
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    main()

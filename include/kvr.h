@@ -1,0 +1,210 @@
+/*
+ * kvr.h -- C ABI of libkvr: retrieval-based sparse decode attention over a
+ * long KV cache on one NVIDIA GB300 (sm_103a).
+ *
+ * Per decode step and KV head the library
+ *   1. rotates keys and the query with a shared SRHT after l2 normalisation
+ *      (ParisKV, "Centroidi Analitici Robusti al Drift"),
+ *   2. codes each key by its nearest analytic sign-pattern centroid
+ *      +-1/sqrt(8) per 8-dim sub-block, i.e. by its sign bits (same section),
+ *   3. scores the codes against the query code with tiered collision votes
+ *      and keeps a candidate set (ParisKV, "Pipeline di Recupero Nativa su GPU
+ *      in Due Stadi"),
+ *   4. rescores the candidates exactly with q.k and keeps the top-k,
+ *   5. attends over the top-k tokens plus a local window of the newest tokens
+ *      (ParisKV, "Problematica"; the local region of "Meccanismo di
+ *      Aggiornamento a Finestra Scorrevole").
+ *
+ * Conventions shared by every call
+ *   - Every pointer argument named as "device" is a device pointer into memory
+ *     the caller allocated and owns; the library never allocates, frees or
+ *     retains a pointer after the call returns.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and runs asynchronously: no call synchronises the host, so a
+ *     sequence of calls can be captured into a CUDA graph.
+ *   - Arguments are validated on the host before anything is enqueued; an
+ *     invalid call returns an error status and enqueues nothing.
+ *   - Conditions only the device can see (a sequence length beyond the
+ *     capacity, a selected index outside the pool, a non-finite score) set
+ *     bits of the optional device word `err_word` (int32, may be NULL) with
+ *     atomicOr and are otherwise handled as documented per call; the caller
+ *     clears the word and reads it when convenient (kvr_read_error).
+ *
+ * Layouts (row-major, element strides 1; "unit" = one (batch b, kv head h)):
+ *   K, V      [B, Hkv, cap, d]  dtype KVR_BF16 or KVR_F32; token stride d.
+ *   codes     [B, Hkv, cap, d/8] uint8: byte j of a key's code holds bit t set
+ *             iff coordinate 8j+t of its rotated vector is negative.
+ *   q         [B, Hq, d]        same dtype as K; query head g belongs to kv
+ *             head g / (Hq/Hkv) (contiguous GQA groups).
+ *   seq_len   [B] int32 device: tokens 0..seq_len[b]-1 of batch b are valid.
+ *   srht_sign [d] int8 device: the +-1 diagonal of the rotation.
+ * All base pointers must be 16-byte aligned.
+ */
+#ifndef KVR_H_
+#define KVR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvr_status {
+    KVR_OK = 0,
+    KVR_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad size or range */
+    KVR_ERR_UNSUPPORTED = 2, /* head_dim not in {64, 128}, group size, dtype */
+    KVR_ERR_WORKSPACE = 3,   /* workspace smaller than the *_workspace_size value */
+    KVR_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, attribute) */
+    KVR_ERR_DEVICE = 5       /* kvr_read_error found device-side error bits */
+} kvr_status;
+
+typedef enum kvr_dtype { KVR_F32 = 0, KVR_BF16 = 1 } kvr_dtype;
+
+/* Device error bits written to err_word. */
+#define KVR_DEVERR_SEQ_LEN 0x1    /* seq_len[b] > cap or < 0: unit treated as empty */
+#define KVR_DEVERR_POSITION 0x2   /* encode row outside [0, cap): row skipped */
+#define KVR_DEVERR_INDEX 0x4      /* attend index outside the pool: token skipped */
+#define KVR_DEVERR_NONFINITE 0x8  /* NaN exact score: its order is unspecified */
+
+/* Shape of one layer's cache and query. */
+typedef struct kvr_shape {
+    int B;         /* batch */
+    int Hq;        /* query heads; a multiple of Hkv, Hq/Hkv <= 16 */
+    int Hkv;       /* kv heads */
+    int d;         /* head dim: 64 or 128 */
+    int64_t cap;   /* token capacity per unit of K, V and codes */
+    kvr_dtype dtype;
+} kvr_shape;
+
+/* Selection parameters. */
+typedef struct kvr_select_params {
+    int C;       /* candidate budget of the coarse stage, 0 <= C <= 32768 */
+    int k;       /* final top-k, 0 <= k <= C */
+    int W;       /* local window: tokens [N-W, N) are always attended and never
+                    selected; the pool is [0, max(0, N-W)) */
+    int lut[9];  /* vote weight by Hamming distance 0..8 between a key's and
+                    the query's sub-block codes; each in [0, 15] */
+} kvr_select_params;
+
+/* Byte offsets of the inspectable parts of the select workspace after a
+   kvr_select call (see kvr_select_workspace_views). */
+typedef struct kvr_select_views {
+    size_t coarse;     /* uint8 [B*Hkv, cap]: coarse score of every pool key */
+    size_t cand_idx;   /* int32 [B*Hkv, C]: candidate indices, ascending */
+    size_t cand_score; /* float [B*Hkv, C]: exact q_bar.k of cand_idx entries */
+    size_t cand_count; /* int32 [B*Hkv]: C' = min(C, pool) */
+    size_t qbar;       /* float [B*Hkv, d]: group-mean query */
+} kvr_select_views;
+
+/* Human-readable name of a status. Never NULL. */
+const char *kvr_status_string(kvr_status s);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int kvr_version(void);
+
+/*
+ * kvr_encode_keys -- append-time rotation and sign code (steps 1-2).
+ * Source: ParisKV, "Centroidi Analitici Robusti al Drift" (rotation and
+ * analytic centroids) and "Pipeline di Recupero Nativa su GPU in Due Stadi"
+ * (sub-blocks, nearest centroid per sub-block).
+ *
+ * For every unit (b, h) and t in [0, n_new): row r = pos0[b] + t of K is
+ * transformed as z = FWHT(D * k) in fp32 (natural Hadamard order, butterfly
+ * spans ascending; D = diag(srht_sign)) and codes[b, h, r, :] receives the
+ * sign bits of z. The l2 normalisation and the 1/sqrt(d) factor are positive
+ * scales and leave the code unchanged, so they are not computed.
+ *   K         device, [B, Hkv, cap, d] of shape->dtype (read).
+ *   pos0      device int32 [B]: first row to encode per batch entry.
+ *   n_new     rows per unit, >= 0 (0 enqueues nothing).
+ *   srht_sign device int8 [d], entries +1 or -1.
+ *   codes     device uint8 [B, Hkv, cap, d/8] (written rows only).
+ *   err_word  device int32 or NULL: KVR_DEVERR_POSITION for rows outside
+ *             [0, cap) (those rows are skipped).
+ */
+kvr_status kvr_encode_keys(const kvr_shape *shape, const void *K, const int32_t *pos0,
+                           int n_new, const int8_t *srht_sign, uint8_t *codes,
+                           int32_t *err_word, void *stream);
+
+/* Bytes of device workspace kvr_select needs for this shape and params. */
+size_t kvr_select_workspace_size(const kvr_shape *shape, const kvr_select_params *p);
+
+/* Fills *views with byte offsets into the select workspace. */
+kvr_status kvr_select_workspace_views(const kvr_shape *shape, const kvr_select_params *p,
+                                      kvr_select_views *views);
+
+/*
+ * kvr_select -- coarse scoring, candidate set, exact rescoring, top-k
+ * (steps 1-4 for the query).
+ * Source: ParisKV, "Pipeline di Recupero Nativa su GPU in Due Stadi" (coarse
+ * collision votes prune to a candidate set); exact q.k rescoring of the
+ * candidates replaces the page's code-only reranker.
+ *
+ * Per unit (b, h), with N = seq_len[b], pool = max(0, N - W),
+ * C' = min(C, pool), k' = min(k, C'):
+ *   q_bar  = mean of the G = Hq/Hkv query heads of the group, summed left to
+ *            right in fp32 and divided by G;
+ *   qcode  = sign code of q_bar (as kvr_encode_keys);
+ *   s_i    = sum over sub-blocks j of lut[popcount(code_i[j] ^ qcode[j])];
+ *   cand   = the first C' pool tokens by (s desc, index asc);
+ *   S_i    = q_bar . k_i in fp32: 16 contiguous chunks of d/16 dims, each an
+ *            fma chain from +0 over its dims ascending, then butterfly sums
+ *            over chunk spans 8, 4, 2, 1; the result of chunk 0;
+ *   top    = the first k' candidates by (S desc, index asc), -0 == +0.
+ * out_idx[b, h, 0..k'-1] receives `top` ascending, the rest of the row -1;
+ * out_count[b, h] = k'.
+ *   q         device [B, Hq, d] of shape->dtype.
+ *   K, codes  device, as in the layouts above; codes of rows [0, pool) must
+ *             be current (kvr_encode_keys).
+ *   seq_len   device int32 [B]; a value outside [0, cap] sets
+ *             KVR_DEVERR_SEQ_LEN and the unit selects nothing.
+ *   out_idx   device int32 [B, Hkv, p->k];  out_count device int32 [B, Hkv].
+ *   workspace device, >= kvr_select_workspace_size bytes, 256-byte aligned;
+ *             contents on entry are ignored; see kvr_select_workspace_views.
+ */
+kvr_status kvr_select(const kvr_shape *shape, const kvr_select_params *p, const void *q,
+                      const void *K, const uint8_t *codes, const int32_t *seq_len,
+                      const int8_t *srht_sign, int32_t *out_idx, int32_t *out_count,
+                      void *workspace, size_t workspace_bytes, int32_t *err_word,
+                      void *stream);
+
+/* Bytes of device workspace kvr_sparse_attend needs (kmax = row length of idx). */
+size_t kvr_attend_workspace_size(const kvr_shape *shape, int kmax, int W);
+
+/*
+ * kvr_sparse_attend -- fused gather + online-softmax GQA attention over the
+ * selected tokens plus the local window (step 5).
+ * Source: ParisKV, "Problematica" (attention restricted to a top-k subset of
+ * past tokens) and "Meccanismo di Aggiornamento a Finestra Scorrevole"
+ * (recent tokens kept in a local region).
+ *
+ * Per unit (b, h) with N = seq_len[b] and T = {idx[b,h,0..count[b,h]-1]} U
+ * [max(0, N-W), N), for every query head g of the group:
+ *   out[b, g, :] = sum_{t in T} softmax_t(scale * q_g . k_t) v_t,
+ * accumulated in fp32 with an online softmax; an empty T gives zeros.
+ *   q            device [B, Hq, d]; K, V device [B, Hkv, cap, d] (shape->dtype).
+ *   idx          device int32 [B, Hkv, kmax] (e.g. kvr_select's out_idx);
+ *                entries must lie in [0, N-W): others set KVR_DEVERR_INDEX and
+ *                are skipped.
+ *   count        device int32 [B, Hkv], each clamped to [0, kmax].
+ *   out          device float [B, Hq, d] (written).
+ *   workspace    device, >= kvr_attend_workspace_size bytes, 256-byte aligned.
+ */
+kvr_status kvr_sparse_attend(const kvr_shape *shape, const void *q, const void *K,
+                             const void *V, const int32_t *idx, int kmax,
+                             const int32_t *count, const int32_t *seq_len, int W,
+                             float scale, float *out, void *workspace, size_t workspace_bytes,
+                             int32_t *err_word, void *stream);
+
+/*
+ * kvr_read_error -- synchronise `stream`, read the device error word into
+ * *bits_out (may be NULL) and clear it. Returns KVR_ERR_DEVICE when a bit was
+ * set, KVR_ERR_CUDA when the synchronisation or copy failed, else KVR_OK.
+ */
+kvr_status kvr_read_error(int32_t *err_word, int32_t *bits_out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVR_H_ */

@@ -1,0 +1,230 @@
+"""Python binding of libkvr: retrieval-based sparse decode attention on GB300.
+
+The functions below carry the C ABI's names (include/kvr.h) and only marshal
+arguments: torch CUDA tensors become device pointers, shapes become the
+``kvr_shape`` / ``kvr_select_params`` structs, and the caller's current CUDA
+stream is passed through. Every step of the computation runs in the CUDA
+kernels of ``libkvr.so``; there is no CPU or PyTorch fallback, and a missing
+library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "KvrError", "Shape", "SelectParams", "load", "kvr_status_string", "kvr_version",
+    "kvr_encode_keys", "kvr_select_workspace_size", "kvr_select_workspace_views",
+    "kvr_select", "kvr_attend_workspace_size", "kvr_sparse_attend", "kvr_read_error",
+    "DEFAULT_LUT", "DEVERR",
+]
+
+KVR_F32, KVR_BF16 = 0, 1
+DEFAULT_LUT = (3, 2, 1, 0, 0, 0, 0, 0, 0)
+DEVERR = {"seq_len": 0x1, "position": 0x2, "index": 0x4, "nonfinite": 0x8}
+
+
+class KvrError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (where, kvr_status_string(status), status))
+
+
+class _Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
+                ("d", ctypes.c_int), ("cap", ctypes.c_int64), ("dtype", ctypes.c_int)]
+
+
+class _Params(ctypes.Structure):
+    _fields_ = [("C", ctypes.c_int), ("k", ctypes.c_int), ("W", ctypes.c_int),
+                ("lut", ctypes.c_int * 9)]
+
+
+class _Views(ctypes.Structure):
+    _fields_ = [("coarse", ctypes.c_size_t), ("cand_idx", ctypes.c_size_t),
+                ("cand_score", ctypes.c_size_t), ("cand_count", ctypes.c_size_t),
+                ("qbar", ctypes.c_size_t)]
+
+
+class Shape:
+    """Cache / query shape: K, V [B, Hkv, cap, d]; q [B, Hq, d]."""
+
+    def __init__(self, B, Hq, Hkv, d, cap, dtype):
+        self.B, self.Hq, self.Hkv, self.d, self.cap = int(B), int(Hq), int(Hkv), int(d), int(cap)
+        if dtype in (torch.bfloat16, "bf16"):
+            self.dtype = torch.bfloat16
+        elif dtype in (torch.float32, "f32"):
+            self.dtype = torch.float32
+        else:
+            raise ValueError("dtype must be bf16 or f32")
+
+    @classmethod
+    def of(cls, K: torch.Tensor, q: torch.Tensor) -> "Shape":
+        B, Hkv, cap, d = K.shape
+        return cls(B, q.shape[1], Hkv, d, cap, K.dtype)
+
+    def c(self) -> _Shape:
+        return _Shape(self.B, self.Hq, self.Hkv, self.d, self.cap,
+                      KVR_BF16 if self.dtype == torch.bfloat16 else KVR_F32)
+
+
+class SelectParams:
+    def __init__(self, C, k, W, lut=DEFAULT_LUT):
+        self.C, self.k, self.W = int(C), int(k), int(W)
+        self.lut = tuple(int(v) for v in lut)
+        if len(self.lut) != 9:
+            raise ValueError("lut needs 9 entries (Hamming distance 0..8)")
+
+    def c(self) -> _Params:
+        return _Params(self.C, self.k, self.W, (ctypes.c_int * 9)(*self.lut))
+
+
+_lib = None
+_P = ctypes.c_void_p
+
+
+def load(build_if_missing: bool = True):
+    """Load libkvr.so (built in-tree by ``_build.build``). Raises if unavailable."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB) or not _build.up_to_date():
+        if not build_if_missing:
+            raise RuntimeError("libkvr.so is not built; run sparse_decode_attention_gb300._build")
+        _build.build()
+    L = ctypes.CDLL(_build.LIB)
+    S, Pp, V = ctypes.POINTER(_Shape), ctypes.POINTER(_Params), ctypes.POINTER(_Views)
+    L.kvr_status_string.argtypes = [ctypes.c_int]
+    L.kvr_status_string.restype = ctypes.c_char_p
+    L.kvr_version.restype = ctypes.c_int
+    L.kvr_encode_keys.argtypes = [S, _P, _P, ctypes.c_int, _P, _P, _P, _P]
+    L.kvr_select_workspace_size.argtypes = [S, Pp]
+    L.kvr_select_workspace_size.restype = ctypes.c_size_t
+    L.kvr_select_workspace_views.argtypes = [S, Pp, V]
+    L.kvr_select.argtypes = [S, Pp, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
+    L.kvr_attend_workspace_size.argtypes = [S, ctypes.c_int, ctypes.c_int]
+    L.kvr_attend_workspace_size.restype = ctypes.c_size_t
+    L.kvr_sparse_attend.argtypes = [S, _P, _P, _P, _P, ctypes.c_int, _P, _P, ctypes.c_int,
+                                    ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P]
+    L.kvr_read_error.argtypes = [_P, _P, _P]
+    for fn in ("kvr_encode_keys", "kvr_select_workspace_views", "kvr_select",
+               "kvr_sparse_attend", "kvr_read_error"):
+        getattr(L, fn).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def kvr_status_string(status: int) -> str:
+    return load().kvr_status_string(int(status)).decode()
+
+
+def kvr_version() -> int:
+    return load().kvr_version()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status, where):
+    if status != 0:
+        raise KvrError(status, where)
+
+
+def _cuda(t, name, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return t
+
+
+def kvr_encode_keys(K, pos0, n_new, srht_sign, codes, err=None, stream=None, shape=None):
+    """Encode rows [pos0[b], pos0[b] + n_new) of every unit of K into codes."""
+    _cuda(K, "K")
+    shape = shape or Shape(K.shape[0], K.shape[1], K.shape[1], K.shape[3], K.shape[2], K.dtype)
+    _cuda(pos0, "pos0", torch.int32)
+    _cuda(srht_sign, "srht_sign", torch.int8)
+    _cuda(codes, "codes", torch.uint8)
+    st = load().kvr_encode_keys(ctypes.byref(shape.c()), _ptr(K), _ptr(pos0), int(n_new),
+                                _ptr(srht_sign), _ptr(codes), _ptr(err), _stream(stream))
+    _check(st, "kvr_encode_keys")
+
+
+def kvr_select_workspace_size(shape: Shape, params: SelectParams) -> int:
+    return int(load().kvr_select_workspace_size(ctypes.byref(shape.c()),
+                                                ctypes.byref(params.c())))
+
+
+def kvr_select_workspace_views(shape: Shape, params: SelectParams) -> dict:
+    v = _Views()
+    st = load().kvr_select_workspace_views(ctypes.byref(shape.c()), ctypes.byref(params.c()),
+                                           ctypes.byref(v))
+    _check(st, "kvr_select_workspace_views")
+    return {f: int(getattr(v, f)) for f, _ in _Views._fields_}
+
+
+def kvr_select(q, K, codes, seq_len, srht_sign, params: SelectParams, out_idx, out_count,
+               workspace, err=None, stream=None):
+    """Coarse score, candidate set, exact rescoring and top-k for every unit."""
+    shape = Shape.of(_cuda(K, "K"), _cuda(q, "q", K.dtype))
+    _cuda(codes, "codes", torch.uint8)
+    _cuda(seq_len, "seq_len", torch.int32)
+    _cuda(srht_sign, "srht_sign", torch.int8)
+    _cuda(out_idx, "out_idx", torch.int32)
+    _cuda(out_count, "out_count", torch.int32)
+    _cuda(workspace, "workspace")
+    st = load().kvr_select(ctypes.byref(shape.c()), ctypes.byref(params.c()), _ptr(q), _ptr(K),
+                           _ptr(codes), _ptr(seq_len), _ptr(srht_sign), _ptr(out_idx),
+                           _ptr(out_count), _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), _ptr(err),
+                           _stream(stream))
+    _check(st, "kvr_select")
+
+
+def kvr_attend_workspace_size(shape: Shape, kmax: int, W: int) -> int:
+    return int(load().kvr_attend_workspace_size(ctypes.byref(shape.c()), int(kmax), int(W)))
+
+
+def kvr_sparse_attend(q, K, V, idx, count, seq_len, W, scale, out, workspace, err=None,
+                      stream=None):
+    """Gather + online-softmax attention over idx[b, h, :count] plus the window."""
+    shape = Shape.of(_cuda(K, "K"), _cuda(q, "q", K.dtype))
+    _cuda(V, "V", K.dtype)
+    _cuda(idx, "idx", torch.int32)
+    _cuda(count, "count", torch.int32)
+    _cuda(seq_len, "seq_len", torch.int32)
+    _cuda(out, "out", torch.float32)
+    _cuda(workspace, "workspace")
+    kmax = idx.shape[-1]
+    st = load().kvr_sparse_attend(ctypes.byref(shape.c()), _ptr(q), _ptr(K), _ptr(V), _ptr(idx),
+                                  int(kmax), _ptr(count), _ptr(seq_len), int(W), float(scale),
+                                  _ptr(out), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _ptr(err),
+                                  _stream(stream))
+    _check(st, "kvr_sparse_attend")
+
+
+def kvr_read_error(err, stream=None) -> int:
+    """Synchronise, return and clear the device error bits."""
+    bits = ctypes.c_int32(0)
+    st = load().kvr_read_error(_ptr(err), ctypes.byref(bits), _stream(stream))
+    if st not in (0, 5):
+        _check(st, "kvr_read_error")
+    return int(bits.value)
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A 256-byte aligned device buffer of at least nbytes (torch allocation)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)

@@ -1,0 +1,237 @@
+// kvr_api.cu -- the extern "C" entry points of libkvr: argument validation,
+// workspace plans and dispatch to the kernel files. Nothing here allocates
+// device memory or synchronises, except kvr_read_error, whose job it is.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "kvr_launch.h"
+
+namespace kvr {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxC = 32768;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kvr_status check_shape(const kvr_shape *s)
+{
+    if (!s) return KVR_ERR_INVALID_ARG;
+    if (s->B < 1 || s->Hkv < 1 || s->Hq < 1 || s->cap < 1) return KVR_ERR_INVALID_ARG;
+    if (s->Hq % s->Hkv != 0) return KVR_ERR_INVALID_ARG;
+    if (s->d != 64 && s->d != 128) return KVR_ERR_UNSUPPORTED;
+    if (s->dtype != KVR_BF16 && s->dtype != KVR_F32) return KVR_ERR_UNSUPPORTED;
+    if (s->Hq / s->Hkv > 16) return KVR_ERR_UNSUPPORTED;
+    if ((int64_t)s->B * s->Hkv > 65535) return KVR_ERR_UNSUPPORTED;  // grid.y
+    if (s->cap > ((int64_t)1 << 31) - 1) return KVR_ERR_UNSUPPORTED;  // int32 indices
+    return KVR_OK;
+}
+
+kvr_status check_params(const kvr_select_params *p)
+{
+    if (!p) return KVR_ERR_INVALID_ARG;
+    if (p->C < 0 || p->C > kMaxC || p->k < 0 || p->k > p->C || p->W < 0)
+        return KVR_ERR_INVALID_ARG;
+    for (int i = 0; i < 9; i++)
+        if (p->lut[i] < 0 || p->lut[i] > 15) return KVR_ERR_INVALID_ARG;
+    return KVR_OK;
+}
+
+}  // namespace
+
+kvr_status raise_smem_limit(const void *kernel, int bytes)
+{
+    static std::mutex mu;
+    static const void *done[kMaxDevices][8];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVR_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < 8; i++)
+        if (done[dev][i] == kernel) return KVR_OK;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+        cudaSuccess)
+        return KVR_ERR_CUDA;
+    for (int i = 0; i < 8; i++)
+        if (!done[dev][i]) {
+            done[dev][i] = kernel;
+            break;
+        }
+    return KVR_OK;
+}
+
+SelectPlan plan_select(const kvr_shape &s, const kvr_select_params &p)
+{
+    SelectPlan pl;
+    const int64_t U = (int64_t)s.B * s.Hkv;
+    pl.cap_pad = (int64_t)align_up((size_t)s.cap, 16);
+    // about 2048 CTAs for the pool scan, at least 2048 keys each, <= 1024 chunks
+    int chunk = 2048;
+    while (chunk < (1 << 22) &&
+           (((s.cap + chunk - 1) / chunk) * U > 2048 || (s.cap + chunk - 1) / chunk > 1024))
+        chunk <<= 1;
+    pl.chunk = chunk;
+    pl.nchunk = (int)((s.cap + chunk - 1) / chunk);
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    pl.off_coarse = take((size_t)U * pl.cap_pad);
+    pl.off_cand_idx = take((size_t)U * p.C * 4);
+    pl.off_cand_score = take((size_t)U * p.C * 4);
+    pl.off_cand_count = take((size_t)U * 4);
+    pl.off_qbar = take((size_t)U * s.d * 4);
+    pl.off_chunk_hist = take((size_t)U * pl.nchunk * 256 * 4);
+    pl.off_chunk_off = take((size_t)U * pl.nchunk * 4);
+    pl.off_chunk_take = take((size_t)U * pl.nchunk * 4);
+    pl.off_unit_T = take((size_t)U * 4);
+    pl.bytes = o;
+    return pl;
+}
+
+AttendPlan plan_attend(const kvr_shape &s, int kmax, int W)
+{
+    AttendPlan pl;
+    const int64_t U = (int64_t)s.B * s.Hkv;
+    const int G = s.Hq / s.Hkv;
+    pl.tpc = 128;
+    const int64_t most = (int64_t)kmax + W;  // a unit never attends more tokens
+    pl.nsplit = (int)std::max<int64_t>(1, (most + pl.tpc - 1) / pl.tpc);
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    pl.off_m = take((size_t)U * pl.nsplit * G * 4);
+    pl.off_l = take((size_t)U * pl.nsplit * G * 4);
+    pl.off_o = take((size_t)U * pl.nsplit * G * s.d * 4);
+    pl.bytes = o;
+    return pl;
+}
+
+}  // namespace kvr
+
+using namespace kvr;
+
+extern "C" {
+
+const char *kvr_status_string(kvr_status s)
+{
+    switch (s) {
+    case KVR_OK: return "ok";
+    case KVR_ERR_INVALID_ARG: return "invalid argument";
+    case KVR_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case KVR_ERR_WORKSPACE: return "workspace too small";
+    case KVR_ERR_CUDA: return "CUDA runtime error";
+    case KVR_ERR_DEVICE: return "device-side error bits set";
+    }
+    return "unknown status";
+}
+
+int kvr_version(void) { return 100; }
+
+kvr_status kvr_encode_keys(const kvr_shape *shape, const void *K, const int32_t *pos0, int n_new,
+                           const int8_t *srht_sign, uint8_t *codes, int32_t *err_word,
+                           void *stream)
+{
+    kvr_status st = check_shape(shape);
+    if (st != KVR_OK) return st;
+    if (n_new < 0) return KVR_ERR_INVALID_ARG;
+    if (!K || !pos0 || !srht_sign || !codes) return KVR_ERR_INVALID_ARG;
+    if (!aligned16(K) || !aligned16(codes)) return KVR_ERR_INVALID_ARG;
+    if (n_new == 0) return KVR_OK;
+    if ((int64_t)shape->B * shape->Hkv * n_new > ((int64_t)1 << 40)) return KVR_ERR_INVALID_ARG;
+    LaunchCtx c{*shape, static_cast<cudaStream_t>(stream)};
+    return encode_dispatch(c, K, pos0, n_new, srht_sign, codes, err_word);
+}
+
+size_t kvr_select_workspace_size(const kvr_shape *shape, const kvr_select_params *p)
+{
+    if (check_shape(shape) != KVR_OK || check_params(p) != KVR_OK) return 0;
+    return plan_select(*shape, *p).bytes;
+}
+
+kvr_status kvr_select_workspace_views(const kvr_shape *shape, const kvr_select_params *p,
+                                      kvr_select_views *views)
+{
+    kvr_status st = check_shape(shape);
+    if (st != KVR_OK) return st;
+    if ((st = check_params(p)) != KVR_OK) return st;
+    if (!views) return KVR_ERR_INVALID_ARG;
+    const SelectPlan pl = plan_select(*shape, *p);
+    views->coarse = pl.off_coarse;
+    views->cand_idx = pl.off_cand_idx;
+    views->cand_score = pl.off_cand_score;
+    views->cand_count = pl.off_cand_count;
+    views->qbar = pl.off_qbar;
+    return KVR_OK;
+}
+
+kvr_status kvr_select(const kvr_shape *shape, const kvr_select_params *p, const void *q,
+                      const void *K, const uint8_t *codes, const int32_t *seq_len,
+                      const int8_t *srht_sign, int32_t *out_idx, int32_t *out_count,
+                      void *workspace, size_t workspace_bytes, int32_t *err_word, void *stream)
+{
+    kvr_status st = check_shape(shape);
+    if (st != KVR_OK) return st;
+    if ((st = check_params(p)) != KVR_OK) return st;
+    if (!q || !K || !codes || !seq_len || !srht_sign || !out_count || !workspace)
+        return KVR_ERR_INVALID_ARG;
+    if (p->k > 0 && !out_idx) return KVR_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(K) || !aligned16(codes) || !aligned16(out_idx) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return KVR_ERR_INVALID_ARG;
+    const SelectPlan pl = plan_select(*shape, *p);
+    if (workspace_bytes < pl.bytes) return KVR_ERR_WORKSPACE;
+    LaunchCtx c{*shape, static_cast<cudaStream_t>(stream)};
+    return select_dispatch(c, *p, pl, q, K, codes, seq_len, srht_sign, out_idx, out_count,
+                           static_cast<uint8_t *>(workspace), err_word);
+}
+
+size_t kvr_attend_workspace_size(const kvr_shape *shape, int kmax, int W)
+{
+    if (check_shape(shape) != KVR_OK || kmax < 0 || W < 0) return 0;
+    return plan_attend(*shape, kmax, W).bytes;
+}
+
+kvr_status kvr_sparse_attend(const kvr_shape *shape, const void *q, const void *K,
+                             const void *V, const int32_t *idx, int kmax,
+                             const int32_t *count, const int32_t *seq_len, int W,
+                             float scale, float *out, void *workspace, size_t workspace_bytes,
+                             int32_t *err_word, void *stream)
+{
+    kvr_status st = check_shape(shape);
+    if (st != KVR_OK) return st;
+    if (kmax < 0 || W < 0) return KVR_ERR_INVALID_ARG;
+    if (!q || !K || !V || !count || !seq_len || !out || !workspace) return KVR_ERR_INVALID_ARG;
+    if (kmax > 0 && !idx) return KVR_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return KVR_ERR_INVALID_ARG;
+    if (!(scale == scale)) return KVR_ERR_INVALID_ARG;
+    const AttendPlan pl = plan_attend(*shape, kmax, W);
+    if (workspace_bytes < pl.bytes) return KVR_ERR_WORKSPACE;
+    LaunchCtx c{*shape, static_cast<cudaStream_t>(stream)};
+    return attend_dispatch(c, pl, q, K, V, idx, kmax, count, seq_len, W, scale, out,
+                           static_cast<uint8_t *>(workspace), err_word);
+}
+
+kvr_status kvr_read_error(int32_t *err_word, int32_t *bits_out, void *stream)
+{
+    if (!err_word) return KVR_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t host = 0;
+    if (cudaMemcpyAsync(&host, err_word, sizeof(host), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return KVR_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KVR_ERR_CUDA;
+    if (cudaMemsetAsync(err_word, 0, sizeof(int32_t), s) != cudaSuccess) return KVR_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KVR_ERR_CUDA;
+    if (bits_out) *bits_out = host;
+    return host ? KVR_ERR_DEVICE : KVR_OK;
+}
+
+}  // extern "C"

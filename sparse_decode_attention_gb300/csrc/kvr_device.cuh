@@ -1,0 +1,158 @@
+// kvr_device.cuh -- device helpers shared by the libkvr kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvr.h"
+
+namespace kvr {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---------------------------------------------------------------- elements
+
+// Element traits: a 16-byte vector holds kVec elements.
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static constexpr int kVec = 4;
+};
+template <> struct Elem<__nv_bfloat16> {
+    static constexpr int kVec = 8;
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Widen n (4 or 8) consecutive elements at a 16-byte aligned address.
+template <int N> __device__ __forceinline__ void widen(const float *p, float (&x)[N])
+{
+#pragma unroll
+    for (int i = 0; i < N; i += 4) {
+        float4 v = *reinterpret_cast<const float4 *>(p + i);
+        x[i] = v.x; x[i + 1] = v.y; x[i + 2] = v.z; x[i + 3] = v.w;
+    }
+}
+template <int N> __device__ __forceinline__ void widen(const __nv_bfloat16 *p, float (&x)[N])
+{
+    static_assert(N % 4 == 0, "bf16 widen works on 8-byte groups");
+#pragma unroll
+    for (int i = 0; i < N; i += 8) {
+        if (N - i >= 8) {
+            uint4 v = *reinterpret_cast<const uint4 *>(p + i);
+            x[i] = bf16_lo(v.x); x[i + 1] = bf16_hi(v.x);
+            x[i + 2] = bf16_lo(v.y); x[i + 3] = bf16_hi(v.y);
+            x[i + 4] = bf16_lo(v.z); x[i + 5] = bf16_hi(v.z);
+            x[i + 6] = bf16_lo(v.w); x[i + 7] = bf16_hi(v.w);
+        } else {
+            uint2 v = *reinterpret_cast<const uint2 *>(p + i);
+            x[i] = bf16_lo(v.x); x[i + 1] = bf16_hi(v.x);
+            x[i + 2] = bf16_lo(v.y); x[i + 3] = bf16_hi(v.y);
+        }
+    }
+}
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// ---------------------------------------------------------------- rotation
+
+// Natural-order fast Walsh-Hadamard transform of one vector spread over a
+// group of L lanes (aligned, power of two) that hold E consecutive elements
+// each: element index = gl * E + r. Butterfly spans run ascending: first the
+// spans inside a lane (h < E), then across lanes (h = E, 2E, ...). The lower
+// element of a pair receives a + b and the upper a - b, each one fp32
+// round-to-nearest addition, so every output matches the canonical
+// sequential transform bit for bit. All 32 lanes of the warp must call it.
+template <int E, int L>
+__device__ __forceinline__ void fwht_lanes(float (&x)[E], int gl)
+{
+#pragma unroll
+    for (int h = 1; h < E; h <<= 1) {
+#pragma unroll
+        for (int r = 0; r < E; r++) {
+            if (r & h) continue;
+            float a = x[r], b = x[r + h];
+            x[r] = a + b;
+            x[r + h] = a - b;
+        }
+    }
+#pragma unroll
+    for (int m = 1; m < L; m <<= 1) {
+        const bool upper = (gl & m) != 0;
+#pragma unroll
+        for (int r = 0; r < E; r++) {
+            float p = __shfl_xor_sync(kFull, x[r], m);
+            x[r] = upper ? (p - x[r]) : (x[r] + p);
+        }
+    }
+}
+
+// Sign bits of the E elements a lane holds, placed at their bit position in
+// the 32-bit code word (element i -> word i/32, bit i%32), OR-ed across the
+// 32/E lanes sharing the word. Every lane returns its word; lanes with
+// gl % (32/E) == 0 own it. All 32 lanes must call it.
+template <int E>
+__device__ __forceinline__ uint32_t sign_word(const float (&x)[E], int gl)
+{
+    uint32_t bits = 0;
+#pragma unroll
+    for (int r = 0; r < E; r++)
+        bits |= (x[r] < 0.0f ? 1u : 0u) << r;
+    uint32_t v = bits << ((gl * E) & 31);
+#pragma unroll
+    for (int off = 1; off < 32 / E; off <<= 1)
+        v |= __shfl_xor_sync(kFull, v, off);
+    return v;
+}
+
+// ---------------------------------------------------------------- scans
+
+// Exclusive prefix sum over the block of one value per thread; *total gets
+// the block sum. blockDim.x must be a multiple of 32, <= 1024. scratch holds
+// 33 ints. Contains __syncthreads: call from uniform control flow.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *scratch, int *total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int y = __shfl_up_sync(kFull, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) scratch[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = (lane < nwarps) ? scratch[lane] : 0;
+        int s = w;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int y = __shfl_up_sync(kFull, s, off);
+            if (lane >= off) s += y;
+        }
+        scratch[lane] = s - w;  // exclusive warp offsets
+        if (lane == 31) scratch[32] = s;
+    }
+    __syncthreads();
+    int res = scratch[warp] + x - v;
+    *total = scratch[32];
+    __syncthreads();
+    return res;
+}
+
+__device__ __forceinline__ void set_err(int32_t *err, int bit)
+{
+    if (err) atomicOr(err, bit);
+}
+
+// fp32 -> uint32 key whose unsigned order is the float order; -0 maps as +0.
+__device__ __forceinline__ uint32_t order_key(float s)
+{
+    uint32_t u = __float_as_uint(s);
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+}  // namespace kvr

@@ -1,0 +1,61 @@
+// kvr_launch.h -- host-side glue between the C ABI (kvr_api.cu) and the
+// kernel files. Arguments reaching these functions are already validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kvr.h"
+
+namespace kvr {
+
+struct LaunchCtx {
+    kvr_shape shape;
+    cudaStream_t stream;
+};
+
+inline kvr_status check_launch()
+{
+    return cudaGetLastError() == cudaSuccess ? KVR_OK : KVR_ERR_CUDA;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Opt a kernel into `bytes` of dynamic shared memory on the current device
+// (once per kernel and device; later calls are a table lookup).
+kvr_status raise_smem_limit(const void *kernel, int bytes);
+
+// Select workspace plan: offsets (bytes) and the chunking of the pool scan.
+struct SelectPlan {
+    int64_t cap_pad;  // row length of the coarse-score array (multiple of 16)
+    int chunk;        // keys per chunk of the coarse scan
+    int nchunk;       // chunks per unit = ceil(cap / chunk)
+    size_t off_coarse, off_cand_idx, off_cand_score, off_cand_count, off_qbar;
+    size_t off_chunk_hist, off_chunk_off, off_chunk_take, off_unit_T;
+    size_t bytes;
+};
+SelectPlan plan_select(const kvr_shape &s, const kvr_select_params &p);
+
+struct AttendPlan {
+    int tpc;     // tokens per CTA
+    int nsplit;  // CTAs per unit
+    size_t off_m, off_l, off_o;
+    size_t bytes;
+};
+AttendPlan plan_attend(const kvr_shape &s, int kmax, int W);
+
+kvr_status encode_dispatch(const LaunchCtx &c, const void *K, const int32_t *pos0, int n_new,
+                           const int8_t *sgn, uint8_t *codes, int32_t *err);
+
+kvr_status select_dispatch(const LaunchCtx &c, const kvr_select_params &p, const SelectPlan &plan,
+                           const void *q, const void *K, const uint8_t *codes,
+                           const int32_t *seq_len, const int8_t *sgn, int32_t *out_idx,
+                           int32_t *out_count, uint8_t *ws, int32_t *err);
+
+kvr_status attend_dispatch(const LaunchCtx &c, const AttendPlan &plan, const void *q,
+                           const void *K, const void *V, const int32_t *idx, int kmax,
+                           const int32_t *count, const int32_t *seq_len, int W, float scale,
+                           float *out, uint8_t *ws, int32_t *err);
+
+}  // namespace kvr

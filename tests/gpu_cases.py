@@ -1,0 +1,72 @@
+"""Helpers for the GPU parity tests: run the CUDA path through the C ABI and
+the oracle on the same seeded inputs, unit by unit."""
+import numpy as np
+import torch
+
+import oracle
+import sparse_decode_attention_gb300 as kvr
+
+
+def encode_gpu(K, sgn, rows, pos0=0):
+    B, Hkv, cap, d = K.shape
+    codes = torch.zeros((B, Hkv, cap, d // 8), dtype=torch.uint8, device=K.device)
+    p0 = torch.full((B,), pos0, dtype=torch.int32, device=K.device)
+    kvr.kvr_encode_keys(K, p0, rows, sgn, codes)
+    return codes
+
+
+def select_gpu(q, K, codes, seq_len, sgn, params):
+    """kvr_select; returns outputs and the inspectable workspace parts (CPU)."""
+    B, Hkv, cap, d = K.shape
+    shape = kvr.Shape.of(K, q)
+    ws = kvr.workspace(kvr.kvr_select_workspace_size(shape, params))
+    ws.fill_(0xAB)  # stale contents must not matter
+    out_idx = torch.full((B, Hkv, params.k), 7, dtype=torch.int32, device=K.device)
+    out_cnt = torch.full((B, Hkv), 7, dtype=torch.int32, device=K.device)
+    err = torch.zeros(1, dtype=torch.int32, device=K.device)
+    kvr.kvr_select(q, K, codes, seq_len, sgn, params, out_idx, out_cnt, ws, err)
+    bits = kvr.kvr_read_error(err)
+    v = kvr.kvr_select_workspace_views(shape, params)
+    U, C = B * Hkv, params.C
+    cap_pad = (cap + 15) // 16 * 16
+    wsc = ws.cpu()
+    res = dict(
+        idx=out_idx.cpu().numpy(), count=out_cnt.cpu().numpy(), err=bits,
+        coarse=wsc[v["coarse"]:v["coarse"] + U * cap_pad].numpy().reshape(U, cap_pad),
+        cand=wsc[v["cand_idx"]:v["cand_idx"] + U * C * 4].view(torch.int32).numpy().reshape(U, C),
+        cand_S=wsc[v["cand_score"]:v["cand_score"] + U * C * 4].view(torch.float32).numpy()
+        .reshape(U, C),
+        cand_count=wsc[v["cand_count"]:v["cand_count"] + U * 4].view(torch.int32).numpy(),
+    )
+    return res
+
+
+def attend_gpu(q, K, V, idx, count, seq_len, W, scale):
+    B, Hkv, cap, d = K.shape
+    shape = kvr.Shape.of(K, q)
+    ws = kvr.workspace(kvr.kvr_attend_workspace_size(shape, idx.shape[-1], W))
+    ws.fill_(0xCD)
+    out = torch.full(q.shape, float("nan"), dtype=torch.float32, device=K.device)
+    err = torch.zeros(1, dtype=torch.int32, device=K.device)
+    kvr.kvr_sparse_attend(q, K, V, idx, count, seq_len, W, scale, out, ws, err)
+    bits = kvr.kvr_read_error(err)
+    return out.cpu().numpy(), bits
+
+
+def compare_select_unit(res, u, q_group, K_unit, codes_unit, N, sgn, params, check_diag=True):
+    """Bit-exact comparison of one unit's selection with the oracle."""
+    idx, cnt, dg = oracle.select_unit(q_group, K_unit, codes_unit, N, sgn, params.C, params.k,
+                                      params.W, params.lut, diagnostics=True)
+    b, h = divmod(u, res["idx"].shape[1])
+    pool = max(0, N - params.W)
+    Cp = min(params.C, pool)
+    if check_diag:
+        assert np.array_equal(res["coarse"][u, :pool].astype(np.int32), dg["coarse"]), \
+            "coarse scores differ (unit %d)" % u
+        assert res["cand_count"][u] == Cp
+        assert np.array_equal(res["cand"][u, :Cp], dg["cand"]), "candidate sets differ (unit %d)" % u
+        assert np.array_equal(res["cand_S"][u, :Cp].view(np.int32), dg["cand_S"].view(np.int32)), \
+            "exact scores differ (unit %d)" % u
+    assert res["count"][b, h] == cnt, "count differs (unit %d)" % u
+    assert np.array_equal(res["idx"][b, h], idx), "top-k sets differ (unit %d)" % u
+    return idx, cnt

@@ -1,0 +1,97 @@
+"""The C-ABI library builds, loads and exports every symbol include/kvr.h
+declares; host-side validation rejects bad calls before any launch (these
+calls return before touching the GPU, so they run without one)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(kvr_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_header_declares_the_four_calls():
+    names = declared_functions()
+    for n in ("kvr_encode_keys", "kvr_select", "kvr_sparse_attend"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(kvr_lib):
+    lib = kvr_lib.load()
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(kvr_lib):
+    assert kvr_lib.kvr_status_string(0) == "ok"
+    assert kvr_lib.kvr_status_string(3) == "workspace too small"
+    assert kvr_lib.kvr_status_string(99) == "unknown status"
+    assert kvr_lib.kvr_version() >= 100
+
+
+def _shape(kvr, **kw):
+    base = dict(B=1, Hq=32, Hkv=8, d=128, cap=1024, dtype="bf16")
+    base.update(kw)
+    return kvr.Shape(**base)
+
+
+def test_workspace_sizes(kvr_lib):
+    kvr = kvr_lib
+    s = _shape(kvr, cap=131072)
+    p = kvr.SelectParams(8192, 2048, 128)
+    n = kvr.kvr_select_workspace_size(s, p)
+    # coarse scores (1 B per key) + candidates (8 B each) dominate
+    assert n >= 8 * 131072 + 8 * 8192 * 8
+    assert n < 8 * 131072 * 2 + 8 * 8192 * 8 + (1 << 22)
+    v = kvr.kvr_select_workspace_views(s, p)
+    assert v["coarse"] == 0 and all(x % 256 == 0 for x in v.values())
+    assert kvr.kvr_select_workspace_size(_shape(kvr, d=96), p) == 0
+    assert kvr.kvr_select_workspace_size(s, kvr.SelectParams(10, 20, 0)) == 0  # k > C
+    assert kvr.kvr_attend_workspace_size(s, 2048, 128) > 0
+
+
+def test_validation_before_launch(kvr_lib):
+    """Invalid calls return a status and enqueue nothing (no GPU involved)."""
+    kvr = kvr_lib
+    L = kvr.load()
+    fake = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    s = _shape(kvr)
+    p = kvr.SelectParams(64, 16, 8)
+    enc = lambda shp, K, n, codes: L.kvr_encode_keys(ctypes.byref(shp.c()), K, fake, n, fake,
+                                                    codes, None, None)
+    assert enc(s, None, 1, fake) == 1
+    assert enc(s, odd, 1, fake) == 1
+    assert enc(_shape(kvr, d=96), fake, 1, fake) == 2
+    assert enc(_shape(kvr, Hq=20, Hkv=8), fake, 1, fake) == 1
+    assert enc(_shape(kvr, Hq=8 * 17, Hkv=8), fake, 1, fake) == 2
+    assert enc(s, fake, -1, fake) == 1
+    assert enc(s, fake, 0, fake) == 0  # nothing to do
+
+    def sel(shp, prm, ws_bytes, ws=fake):
+        return L.kvr_select(ctypes.byref(shp.c()), ctypes.byref(prm.c()), fake, fake, fake, fake,
+                            fake, fake, fake, ws, ws_bytes, None, None)
+    need = kvr.kvr_select_workspace_size(s, p)
+    assert sel(s, p, need - 1) == 3
+    assert sel(s, kvr.SelectParams(64, 65, 8), need) == 1
+    assert sel(s, kvr.SelectParams(40000, 16, 8), need) == 1
+    assert sel(s, kvr.SelectParams(64, 16, 8, lut=(16, 0, 0, 0, 0, 0, 0, 0, 0)), need) == 1
+    assert sel(s, p, need, ws=ctypes.c_void_p((1 << 20) + 16)) == 1  # ws not 256-aligned
+
+    def att(shp, kmax, W, ws_bytes, scale=0.1):
+        return L.kvr_sparse_attend(ctypes.byref(shp.c()), fake, fake, fake, fake, kmax, fake,
+                                   fake, W, scale, fake, fake, ws_bytes, None, None)
+    need = kvr.kvr_attend_workspace_size(s, 16, 8)
+    assert att(s, 16, 8, need - 1) == 3
+    assert att(s, -1, 8, need) == 1
+    assert att(s, 16, 8, need, scale=float("nan")) == 1
