@@ -168,6 +168,41 @@ kvr_status kvr_select(const kvr_shape *shape, const kvr_select_params *p, const 
                       void *workspace, size_t workspace_bytes, int32_t *err_word,
                       void *stream);
 
+/* Size of the fixed device scratch array behind kvr_select_static_scratch. */
+#define KVR_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * kvr_select_static_scratch -- kvr_select without a caller-provided
+ * workspace. No counterpart in the paper: this is a deployment variant.
+ *
+ * For callers that may not allocate device memory at all: plugin interfaces
+ * that hand a kernel only its inputs and outputs, runtimes that reserve every
+ * byte of device memory up front and expose no allocator, and hot loops where
+ * a cudaMalloc (which can synchronise the device) is not acceptable. The
+ * scratch kvr_select needs lives instead in a fixed file-scope device array of
+ * KVR_STATIC_SCRATCH_BYTES (16 MiB) that every GPU loading this library holds
+ * until the process exits; this call allocates and frees nothing.
+ *
+ * Arguments, results and errors are those of kvr_select minus the workspace.
+ * A shape / params pair whose kvr_select_workspace_size exceeds
+ * KVR_STATIC_SCRATCH_BYTES returns KVR_ERR_WORKSPACE and enqueues nothing
+ * (for scale: 8 units of 1M tokens at C = 16384 need about 11 MiB, 8 units of
+ * 128K tokens at C = 8192 about 2.1 MiB).
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     with that device current (cudaGetSymbolAddress); make that first call
+ *     before any stream capture on the device.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; kvr_select reads nothing from scratch that the same call did not
+ *     write first, so no clearing is needed. Calls whose GPU work overlaps
+ *     (different streams, or different host threads) race on the array: order
+ *     them on one stream or serialise them.
+ */
+kvr_status kvr_select_static_scratch(const kvr_shape *shape, const kvr_select_params *p,
+                                     const void *q, const void *K, const uint8_t *codes,
+                                     const int32_t *seq_len, const int8_t *srht_sign,
+                                     int32_t *out_idx, int32_t *out_count, int32_t *err_word,
+                                     void *stream);
+
 /* Bytes of device workspace kvr_sparse_attend needs (kmax = row length of idx). */
 size_t kvr_attend_workspace_size(const kvr_shape *shape, int kmax, int W);
 

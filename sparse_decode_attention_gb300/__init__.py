@@ -19,7 +19,8 @@ from . import _build
 __all__ = [
     "KvrError", "Shape", "SelectParams", "load", "kvr_status_string", "kvr_version",
     "kvr_encode_keys", "kvr_select_workspace_size", "kvr_select_workspace_views",
-    "kvr_select", "kvr_attend_workspace_size", "kvr_sparse_attend", "kvr_read_error",
+    "kvr_select", "kvr_select_static_scratch", "kvr_attend_workspace_size",
+    "kvr_sparse_attend", "kvr_read_error",
     "DEFAULT_LUT", "DEVERR",
 ]
 
@@ -106,12 +107,14 @@ def load(build_if_missing: bool = True):
     L.kvr_select_workspace_size.restype = ctypes.c_size_t
     L.kvr_select_workspace_views.argtypes = [S, Pp, V]
     L.kvr_select.argtypes = [S, Pp, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
+    L.kvr_select_static_scratch.argtypes = [S, Pp, _P, _P, _P, _P, _P, _P, _P, _P, _P]
     L.kvr_attend_workspace_size.argtypes = [S, ctypes.c_int, ctypes.c_int]
     L.kvr_attend_workspace_size.restype = ctypes.c_size_t
     L.kvr_sparse_attend.argtypes = [S, _P, _P, _P, _P, ctypes.c_int, _P, _P, ctypes.c_int,
                                     ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P]
     L.kvr_read_error.argtypes = [_P, _P, _P]
     for fn in ("kvr_encode_keys", "kvr_select_workspace_views", "kvr_select",
+               "kvr_select_static_scratch",
                "kvr_sparse_attend", "kvr_read_error"):
         getattr(L, fn).restype = ctypes.c_int
     _lib = L
@@ -191,6 +194,23 @@ def kvr_select(q, K, codes, seq_len, srht_sign, params: SelectParams, out_idx, o
                            workspace.numel() * workspace.element_size(), _ptr(err),
                            _stream(stream))
     _check(st, "kvr_select")
+
+
+def kvr_select_static_scratch(q, K, codes, seq_len, srht_sign, params: SelectParams, out_idx,
+                              out_count, err=None, stream=None):
+    """kvr_select for callers that cannot allocate: scratch is a fixed device
+    array inside the library (16 MiB per GPU), shared by every call on a device."""
+    shape = Shape.of(_cuda(K, "K"), _cuda(q, "q", K.dtype))
+    _cuda(codes, "codes", torch.uint8)
+    _cuda(seq_len, "seq_len", torch.int32)
+    _cuda(srht_sign, "srht_sign", torch.int8)
+    _cuda(out_idx, "out_idx", torch.int32)
+    _cuda(out_count, "out_count", torch.int32)
+    st = load().kvr_select_static_scratch(ctypes.byref(shape.c()), ctypes.byref(params.c()),
+                                          _ptr(q), _ptr(K), _ptr(codes), _ptr(seq_len),
+                                          _ptr(srht_sign), _ptr(out_idx), _ptr(out_count),
+                                          _ptr(err), _stream(stream))
+    _check(st, "kvr_select_static_scratch")
 
 
 def kvr_attend_workspace_size(shape: Shape, kmax: int, W: int) -> int:
