@@ -32,8 +32,15 @@
  *
  * Layouts (row-major, element strides 1; "unit" = one (batch b, kv head h)):
  *   K, V      [B, Hkv, cap, d]  dtype KVR_BF16 or KVR_F32; token stride d.
- *   codes     [B, Hkv, cap, d/8] uint8: byte j of a key's code holds bit t set
- *             iff coordinate 8j+t of its rotated vector is negative.
+ *   codes     bit-planes, kvr_codes_bytes(shape) bytes. A token's code has d
+ *             bits; bit p is set iff coordinate p of its rotated vector is
+ *             negative (sub-block j = bits 8j..8j+7). Per unit, tokens are
+ *             grouped in tiles of 1024 = 32 blocks of 32; a tile is
+ *             d*128 bytes laid out as [chunk c < d/4][block j < 32] 16-byte
+ *             units of four uint32 words; word w of unit (c, j) holds code bit
+ *             p = 4c + w of the 32 tokens of block j, bit i for token
+ *             tile*1024 + 32j + i. Unit (b, h) starts at byte
+ *             (b*Hkv + h) * ceil(cap/1024) * d*128.
  *   q         [B, Hq, d]        same dtype as K; query head g belongs to kv
  *             head g / (Hq/Hkv) (contiguous GQA groups).
  *   seq_len   [B] int32 device: tokens 0..seq_len[b]-1 of batch b are valid.
@@ -66,6 +73,11 @@ typedef enum kvr_dtype { KVR_F32 = 0, KVR_BF16 = 1 } kvr_dtype;
 #define KVR_DEVERR_POSITION 0x2   /* encode row outside [0, cap): row skipped */
 #define KVR_DEVERR_INDEX 0x4      /* attend index outside the pool: token skipped */
 #define KVR_DEVERR_NONFINITE 0x8  /* NaN exact score: its order is unspecified */
+#define KVR_DEVERR_TIMEOUT 0x10   /* a bounded wait for a bulk copy ran out: outputs invalid */
+
+/* kvr_select_params.flags */
+#define KVR_SELECT_STORE_COARSE 0x1 /* also write every pool key's coarse score to the
+                                       workspace (diagnostics; costs time) */
 
 /* Shape of one layer's cache and query. */
 typedef struct kvr_shape {
@@ -85,12 +97,14 @@ typedef struct kvr_select_params {
                     selected; the pool is [0, max(0, N-W)) */
     int lut[9];  /* vote weight by Hamming distance 0..8 between a key's and
                     the query's sub-block codes; each in [0, 15] */
+    int flags;   /* KVR_SELECT_* bits, 0 for none */
 } kvr_select_params;
 
 /* Byte offsets of the inspectable parts of the select workspace after a
    kvr_select call (see kvr_select_workspace_views). */
 typedef struct kvr_select_views {
-    size_t coarse;     /* uint8 [B*Hkv, cap]: coarse score of every pool key */
+    size_t coarse;     /* uint8 [B*Hkv, roundup(cap, 16)]: coarse score of every pool
+                          key; SIZE_MAX unless flags has KVR_SELECT_STORE_COARSE */
     size_t cand_idx;   /* int32 [B*Hkv, C]: candidate indices, ascending */
     size_t cand_score; /* float [B*Hkv, C]: exact q_bar.k of cand_idx entries */
     size_t cand_count; /* int32 [B*Hkv]: C' = min(C, pool) */
@@ -103,6 +117,10 @@ const char *kvr_status_string(kvr_status s);
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int kvr_version(void);
 
+/* Bytes of the code buffer of a cache of this shape (layout above), 0 when
+   the shape is invalid. */
+size_t kvr_codes_bytes(const kvr_shape *shape);
+
 /*
  * kvr_encode_keys -- append-time rotation and sign code (steps 1-2).
  * Source: ParisKV, "Centroidi Analitici Robusti al Drift" (rotation and
@@ -111,14 +129,15 @@ int kvr_version(void);
  *
  * For every unit (b, h) and t in [0, n_new): row r = pos0[b] + t of K is
  * transformed as z = FWHT(D * k) in fp32 (natural Hadamard order, butterfly
- * spans ascending; D = diag(srht_sign)) and codes[b, h, r, :] receives the
- * sign bits of z. The l2 normalisation and the 1/sqrt(d) factor are positive
- * scales and leave the code unchanged, so they are not computed.
+ * spans ascending; D = diag(srht_sign)) and the code bits of token r in
+ * `codes` receive the sign bits of z; the bits of every other token are kept.
+ * The l2 normalisation and the 1/sqrt(d) factor are positive scales and leave
+ * the code unchanged, so they are not computed.
  *   K         device, [B, Hkv, cap, d] of shape->dtype (read).
  *   pos0      device int32 [B]: first row to encode per batch entry.
  *   n_new     rows per unit, >= 0 (0 enqueues nothing).
  *   srht_sign device int8 [d], entries +1 or -1.
- *   codes     device uint8 [B, Hkv, cap, d/8] (written rows only).
+ *   codes     device, kvr_codes_bytes(shape) bytes (bits of the rows only).
  *   err_word  device int32 or NULL: KVR_DEVERR_POSITION for rows outside
  *             [0, cap) (those rows are skipped).
  */

@@ -21,7 +21,7 @@ __all__ = [
     "kvr_encode_keys", "kvr_select_workspace_size", "kvr_select_workspace_views",
     "kvr_select", "kvr_select_static_scratch", "kvr_attend_workspace_size",
     "kvr_sparse_attend", "kvr_read_error",
-    "DEFAULT_LUT", "DEVERR",
+    "DEFAULT_LUT", "DEVERR", "SELECT_STORE_COARSE", "kvr_codes_bytes", "codes_buffer",
 ]
 
 KVR_F32, KVR_BF16 = 0, 1
@@ -42,7 +42,10 @@ class _Shape(ctypes.Structure):
 
 class _Params(ctypes.Structure):
     _fields_ = [("C", ctypes.c_int), ("k", ctypes.c_int), ("W", ctypes.c_int),
-                ("lut", ctypes.c_int * 9)]
+                ("lut", ctypes.c_int * 9), ("flags", ctypes.c_int)]
+
+
+SELECT_STORE_COARSE = 0x1
 
 
 class _Views(ctypes.Structure):
@@ -74,14 +77,15 @@ class Shape:
 
 
 class SelectParams:
-    def __init__(self, C, k, W, lut=DEFAULT_LUT):
+    def __init__(self, C, k, W, lut=DEFAULT_LUT, flags=0):
         self.C, self.k, self.W = int(C), int(k), int(W)
         self.lut = tuple(int(v) for v in lut)
+        self.flags = int(flags)
         if len(self.lut) != 9:
             raise ValueError("lut needs 9 entries (Hamming distance 0..8)")
 
     def c(self) -> _Params:
-        return _Params(self.C, self.k, self.W, (ctypes.c_int * 9)(*self.lut))
+        return _Params(self.C, self.k, self.W, (ctypes.c_int * 9)(*self.lut), self.flags)
 
 
 _lib = None
@@ -102,6 +106,8 @@ def load(build_if_missing: bool = True):
     L.kvr_status_string.argtypes = [ctypes.c_int]
     L.kvr_status_string.restype = ctypes.c_char_p
     L.kvr_version.restype = ctypes.c_int
+    L.kvr_codes_bytes.argtypes = [S]
+    L.kvr_codes_bytes.restype = ctypes.c_size_t
     L.kvr_encode_keys.argtypes = [S, _P, _P, ctypes.c_int, _P, _P, _P, _P]
     L.kvr_select_workspace_size.argtypes = [S, Pp]
     L.kvr_select_workspace_size.restype = ctypes.c_size_t
@@ -123,6 +129,16 @@ def load(build_if_missing: bool = True):
 
 def kvr_status_string(status: int) -> str:
     return load().kvr_status_string(int(status)).decode()
+
+
+def kvr_codes_bytes(shape: Shape) -> int:
+    """Bytes of the bit-plane code buffer for a cache of this shape."""
+    return int(load().kvr_codes_bytes(ctypes.byref(shape.c())))
+
+
+def codes_buffer(shape: Shape, device="cuda") -> torch.Tensor:
+    """A zeroed device buffer for the codes of a cache of this shape."""
+    return torch.zeros(max(kvr_codes_bytes(shape), 16), dtype=torch.uint8, device=device)
 
 
 def kvr_version() -> int:
@@ -153,13 +169,20 @@ def _cuda(t, name, dtype=None):
     return t
 
 
+def _codes(codes, shape):
+    _cuda(codes, "codes", torch.uint8)
+    if codes.numel() < kvr_codes_bytes(shape):
+        raise ValueError("codes holds %d bytes, the cache needs %d (kvr_codes_bytes)"
+                         % (codes.numel(), kvr_codes_bytes(shape)))
+
+
 def kvr_encode_keys(K, pos0, n_new, srht_sign, codes, err=None, stream=None, shape=None):
     """Encode rows [pos0[b], pos0[b] + n_new) of every unit of K into codes."""
     _cuda(K, "K")
     shape = shape or Shape(K.shape[0], K.shape[1], K.shape[1], K.shape[3], K.shape[2], K.dtype)
     _cuda(pos0, "pos0", torch.int32)
     _cuda(srht_sign, "srht_sign", torch.int8)
-    _cuda(codes, "codes", torch.uint8)
+    _codes(codes, shape)
     st = load().kvr_encode_keys(ctypes.byref(shape.c()), _ptr(K), _ptr(pos0), int(n_new),
                                 _ptr(srht_sign), _ptr(codes), _ptr(err), _stream(stream))
     _check(st, "kvr_encode_keys")
@@ -182,7 +205,7 @@ def kvr_select(q, K, codes, seq_len, srht_sign, params: SelectParams, out_idx, o
                workspace, err=None, stream=None):
     """Coarse score, candidate set, exact rescoring and top-k for every unit."""
     shape = Shape.of(_cuda(K, "K"), _cuda(q, "q", K.dtype))
-    _cuda(codes, "codes", torch.uint8)
+    _codes(codes, shape)
     _cuda(seq_len, "seq_len", torch.int32)
     _cuda(srht_sign, "srht_sign", torch.int8)
     _cuda(out_idx, "out_idx", torch.int32)
@@ -201,7 +224,7 @@ def kvr_select_static_scratch(q, K, codes, seq_len, srht_sign, params: SelectPar
     """kvr_select for callers that cannot allocate: scratch is a fixed device
     array inside the library (16 MiB per GPU), shared by every call on a device."""
     shape = Shape.of(_cuda(K, "K"), _cuda(q, "q", K.dtype))
-    _cuda(codes, "codes", torch.uint8)
+    _codes(codes, shape)
     _cuda(seq_len, "seq_len", torch.int32)
     _cuda(srht_sign, "srht_sign", torch.int8)
     _cuda(out_idx, "out_idx", torch.int32)

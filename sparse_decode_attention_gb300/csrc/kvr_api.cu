@@ -36,6 +36,7 @@ kvr_status check_params(const kvr_select_params *p)
         return KVR_ERR_INVALID_ARG;
     for (int i = 0; i < 9; i++)
         if (p->lut[i] < 0 || p->lut[i] > 15) return KVR_ERR_INVALID_ARG;
+    if (p->flags & ~KVR_SELECT_STORE_COARSE) return KVR_ERR_INVALID_ARG;
     return KVR_OK;
 }
 
@@ -44,16 +45,38 @@ kvr_status check_params(const kvr_select_params *p)
 kvr_status raise_smem_limit(const void *kernel, int bytes)
 {
     static std::mutex mu;
-    static const void *done[kMaxDevices][8];
+    static const void *done[kMaxDevices][64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVR_ERR_CUDA;
     std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < 8; i++)
+    for (int i = 0; i < 64; i++)
         if (done[dev][i] == kernel) return KVR_OK;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
         cudaSuccess)
         return KVR_ERR_CUDA;
-    for (int i = 0; i < 8; i++)
+    for (int i = 0; i < 64; i++)
+        if (!done[dev][i]) {
+            done[dev][i] = kernel;
+            break;
+        }
+    return KVR_OK;
+}
+
+kvr_status prepare_cluster_kernel(const void *kernel, int smem_bytes)
+{
+    static std::mutex mu;
+    static const void *done[kMaxDevices][64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVR_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < 64; i++)
+        if (done[dev][i] == kernel) return KVR_OK;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess)
+        return KVR_ERR_CUDA;
+    for (int i = 0; i < 64; i++)
         if (!done[dev][i]) {
             done[dev][i] = kernel;
             break;
@@ -66,28 +89,21 @@ SelectPlan plan_select(const kvr_shape &s, const kvr_select_params &p)
     SelectPlan pl;
     const int64_t U = (int64_t)s.B * s.Hkv;
     pl.cap_pad = (int64_t)align_up((size_t)s.cap, 16);
-    // about 2048 CTAs for the pool scan, at least 2048 keys each, <= 1024 chunks
-    int chunk = 2048;
-    while (chunk < (1 << 22) &&
-           (((s.cap + chunk - 1) / chunk) * U > 2048 || (s.cap + chunk - 1) / chunk > 1024))
-        chunk <<= 1;
-    pl.chunk = chunk;
-    pl.nchunk = (int)((s.cap + chunk - 1) / chunk);
+    pl.nblk = (s.cap + 31) / 32;
+    pl.tiles = (s.cap + 1023) / 1024;
+    pl.has_coarse = (p.flags & KVR_SELECT_STORE_COARSE) != 0;
     size_t o = 0;
     auto take = [&](size_t bytes) {
         const size_t at = o;
         o = align_up(o + bytes, 256);
         return at;
     };
-    pl.off_coarse = take((size_t)U * pl.cap_pad);
+    pl.off_planes = take((size_t)U * 8 * pl.nblk * 4);
     pl.off_cand_idx = take((size_t)U * p.C * 4);
     pl.off_cand_score = take((size_t)U * p.C * 4);
     pl.off_cand_count = take((size_t)U * 4);
     pl.off_qbar = take((size_t)U * s.d * 4);
-    pl.off_chunk_hist = take((size_t)U * pl.nchunk * 256 * 4);
-    pl.off_chunk_off = take((size_t)U * pl.nchunk * 4);
-    pl.off_chunk_take = take((size_t)U * pl.nchunk * 4);
-    pl.off_unit_T = take((size_t)U * 4);
+    pl.off_coarse = pl.has_coarse ? take((size_t)U * pl.cap_pad) : 0;
     pl.bytes = o;
     return pl;
 }
@@ -132,7 +148,13 @@ const char *kvr_status_string(kvr_status s)
     return "unknown status";
 }
 
-int kvr_version(void) { return 100; }
+int kvr_version(void) { return 200; }
+
+size_t kvr_codes_bytes(const kvr_shape *shape)
+{
+    if (check_shape(shape) != KVR_OK) return 0;
+    return (size_t)shape->B * shape->Hkv * codes_bytes_per_unit(shape->cap, shape->d);
+}
 
 kvr_status kvr_encode_keys(const kvr_shape *shape, const void *K, const int32_t *pos0, int n_new,
                            const int8_t *srht_sign, uint8_t *codes, int32_t *err_word,
@@ -163,7 +185,7 @@ kvr_status kvr_select_workspace_views(const kvr_shape *shape, const kvr_select_p
     if ((st = check_params(p)) != KVR_OK) return st;
     if (!views) return KVR_ERR_INVALID_ARG;
     const SelectPlan pl = plan_select(*shape, *p);
-    views->coarse = pl.off_coarse;
+    views->coarse = pl.has_coarse ? pl.off_coarse : (size_t)-1;
     views->cand_idx = pl.off_cand_idx;
     views->cand_score = pl.off_cand_score;
     views->cand_count = pl.off_cand_count;

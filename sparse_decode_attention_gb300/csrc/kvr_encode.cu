@@ -5,11 +5,18 @@
 // the sub-block split of "Pipeline di Recupero Nativa su GPU in Due Stadi"
 // the code of a key is the sign bits of its rotated vector.
 //
-// One key is spread over L = d / E lanes (E = 16 bytes / element size), so
-// each lane issues one 16-byte load of its row and a warp covers 32 / L keys
-// whose rows are contiguous when the positions are (coalesced). The FWHT runs
-// in registers with warp shuffles; the code words are gathered with shuffles
-// and written as 32-bit stores.
+// Codes are stored as bit-planes so that the scorer works on 32 keys per
+// 32-bit word: 32 consecutive tokens form a block whose d code bits are d
+// words (word p holds bit p of the 32 codes, bit i for token i); 32 blocks
+// form a 1024-token tile stored as [chunk c = 4 planes][block j] 16-byte
+// units, so that a warp reading one chunk of 32 blocks reads 512 contiguous
+// bytes.
+//
+// One warp handles one 32-token block: it rotates the block's new rows
+// (a row spread over d*sizeof(T)/16 lanes, one 16-byte load each, FWHT in
+// registers with shuffles), then transposes the codes into planes with
+// ballots and merges them into the block, keeping the bits of tokens outside
+// the encoded range.
 #include "kvr_device.cuh"
 #include "kvr_launch.h"
 
@@ -17,63 +24,93 @@ namespace kvr {
 
 template <int D, typename T>
 __global__ void __launch_bounds__(256)
-encode_kernel(const T *__restrict__ K, int Hkv, int64_t cap, const int32_t *__restrict__ pos0,
-              int n_new, int64_t total, const int8_t *__restrict__ sgn,
-              uint32_t *__restrict__ codes, int32_t *err)
+encode_kernel(const T *__restrict__ K, int Hkv, int64_t cap, int64_t tiles,
+              const int32_t *__restrict__ pos0, int n_new, int64_t units, int blocks_per_unit,
+              const int8_t *__restrict__ sgn, uint8_t *__restrict__ codes, int32_t *err)
 {
     constexpr int E = Elem<T>::kVec;  // elements per lane
-    constexpr int L = D / E;          // lanes per key
-    constexpr int KPW = 32 / L;       // keys per warp
-    constexpr int NW = D / 32;        // code words per key
+    constexpr int L = D / E;          // lanes per row
+    constexpr int KPW = 32 / L;       // rows per warp pass
+    constexpr int NW = D / 32;        // code words per token
+    constexpr int NCH = D / 4;        // 16-byte chunks per block
     static_assert(L >= 32 / E && L <= 32, "lane split");
+    __shared__ uint32_t s_code[8][32][NW];
 
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
     const int gl = lane % L;
-    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t key = warp * KPW + lane / L;
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t unit = gw / blocks_per_unit;
+    if (unit >= units) return;  // whole warp
+    const int kb = (int)(gw - unit * blocks_per_unit);
+    const int b = (int)(unit / Hkv);
+    const int64_t p0 = pos0[b];
+    if ((p0 < 0 || p0 + n_new > cap) && kb == 0 && lane == 0) set_err(err, KVR_DEVERR_POSITION);
+    const int64_t lo = p0 > 0 ? p0 : 0;
+    const int64_t hi = (p0 + n_new < cap) ? p0 + n_new : cap;
+    if (lo >= hi) return;
+    const int64_t blk = lo / 32 + kb;
+    if (blk * 32 >= hi) return;  // whole warp
+    const int64_t t_lane = blk * 32 + lane;
+    const uint32_t inmask = __ballot_sync(kFull, t_lane >= lo && t_lane < hi);
 
-    bool valid = key < total;
-    int64_t base = 0;
-    if (valid) {
-        const int64_t unit = key / n_new;
-        const int t = (int)(key - unit * n_new);
-        const int b = (int)(unit / Hkv);
-        const int64_t row = (int64_t)pos0[b] + t;
-        if (row < 0 || row >= cap) {
-            if (gl == 0) set_err(err, KVR_DEVERR_POSITION);
-            valid = false;
+    const T *Ku = K + (size_t)unit * cap * D;
+    for (int s0 = 0; s0 < 32; s0 += KPW) {
+        if (((inmask >> s0) & ((1u << KPW) - 1u)) == 0u && KPW < 32) continue;  // warp-uniform
+        const int slot = s0 + lane / L;
+        const bool v = (inmask >> slot) & 1u;
+        float x[E];
+        if (v) {
+            widen<E>(Ku + (size_t)(blk * 32 + slot) * D + gl * E, x);
         } else {
-            base = unit * cap + row;
+#pragma unroll
+            for (int r = 0; r < E; r++) x[r] = 0.0f;
+        }
+        // D x: exact sign flips, no multiply (nothing for the compiler to contract)
+#pragma unroll
+        for (int r = 0; r < E; r++)
+            if (sgn[gl * E + r] < 0) x[r] = -x[r];
+        fwht_lanes<E, L>(x, gl);
+        const uint32_t w = sign_word<E>(x, gl);
+        if (v && (gl % (32 / E)) == 0) s_code[wib][slot][(gl * E) / 32] = w;
+    }
+    __syncwarp();
+
+    // transpose: plane p = ballot over tokens of code bit p; lane c keeps chunk c
+    uint32_t mine[4] = {0u, 0u, 0u, 0u};
+    const bool have = (inmask >> lane) & 1u;
+    for (int c = 0; c < NCH; c++) {
+#pragma unroll
+        for (int w4 = 0; w4 < 4; w4++) {
+            const int p = 4 * c + w4;
+            const uint32_t bit = have ? (s_code[wib][lane][p >> 5] >> (p & 31)) & 1u : 0u;
+            const uint32_t word = __ballot_sync(kFull, bit);
+            if (lane == c) mine[w4] = word;
         }
     }
-    float x[E];
-    if (valid) {
-        widen<E>(K + base * D + gl * E, x);
-    } else {
-#pragma unroll
-        for (int r = 0; r < E; r++) x[r] = 0.0f;
+    if (lane < NCH) {
+        uint4 *dst = reinterpret_cast<uint4 *>(codes + ((size_t)unit * tiles + (size_t)(blk >> 5)) *
+                                                          (D * 128)) +
+                     ((size_t)lane * 32 + (size_t)(blk & 31));
+        uint4 old = make_uint4(0u, 0u, 0u, 0u);
+        if (inmask != 0xffffffffu) old = *dst;
+        const uint32_t keep = ~inmask;
+        *dst = make_uint4((old.x & keep) | (mine[0] & inmask), (old.y & keep) | (mine[1] & inmask),
+                          (old.z & keep) | (mine[2] & inmask), (old.w & keep) | (mine[3] & inmask));
     }
-    // D x: exact sign flips, no multiply (nothing for the compiler to contract).
-#pragma unroll
-    for (int r = 0; r < E; r++)
-        if (sgn[gl * E + r] < 0) x[r] = -x[r];
-    fwht_lanes<E, L>(x, gl);
-    const uint32_t w = sign_word<E>(x, gl);
-    if (valid && (gl % (32 / E)) == 0)
-        codes[base * NW + (gl * E) / 32] = w;
 }
 
 template <int D, typename T>
 static kvr_status launch_encode(const LaunchCtx &c, const void *K, const int32_t *pos0, int n_new,
                                 const int8_t *sgn, uint8_t *codes, int32_t *err)
 {
-    constexpr int L = D / Elem<T>::kVec;
-    constexpr int KPB = 8 * (32 / L);  // 8 warps per block
-    const int64_t total = (int64_t)c.shape.B * c.shape.Hkv * n_new;
-    const int64_t blocks = (total + KPB - 1) / KPB;
+    const int64_t units = (int64_t)c.shape.B * c.shape.Hkv;
+    const int bpu = (int)((n_new + 31) / 32 + 1);  // blocks a range of n_new tokens can touch
+    const int64_t warps = units * bpu;
+    const int64_t blocks = (warps + 7) / 8;
+    const int64_t tiles = (c.shape.cap + 1023) / 1024;
     encode_kernel<D, T><<<(unsigned)blocks, 256, 0, c.stream>>>(
-        static_cast<const T *>(K), c.shape.Hkv, c.shape.cap, pos0, n_new, total, sgn,
-        reinterpret_cast<uint32_t *>(codes), err);
+        static_cast<const T *>(K), c.shape.Hkv, c.shape.cap, tiles, pos0, n_new, units, bpu, sgn,
+        codes, err);
     return check_launch();
 }
 

@@ -26,13 +26,19 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // (once per kernel and device; later calls are a table lookup).
 kvr_status raise_smem_limit(const void *kernel, int bytes);
 
-// Select workspace plan: offsets (bytes) and the chunking of the pool scan.
+// raise_smem_limit plus permission for cluster sizes above 8.
+kvr_status prepare_cluster_kernel(const void *kernel, int smem_bytes);
+
+// Bytes of the bit-plane code buffer of one unit: ceil(cap/1024) tiles of d*128 bytes.
+inline size_t codes_bytes_per_unit(int64_t cap, int d) { return (size_t)((cap + 1023) / 1024) * d * 128; }
+
+// Select workspace plan (byte offsets).
 struct SelectPlan {
     int64_t cap_pad;  // row length of the coarse-score array (multiple of 16)
-    int chunk;        // keys per chunk of the coarse scan
-    int nchunk;       // chunks per unit = ceil(cap / chunk)
-    size_t off_coarse, off_cand_idx, off_cand_score, off_cand_count, off_qbar;
-    size_t off_chunk_hist, off_chunk_off, off_chunk_take, off_unit_T;
+    int64_t nblk;     // 32-token blocks per unit row of the score planes
+    int64_t tiles;    // 1024-token code tiles per unit
+    bool has_coarse;
+    size_t off_planes, off_cand_idx, off_cand_score, off_cand_count, off_qbar, off_coarse;
     size_t bytes;
 };
 SelectPlan plan_select(const kvr_shape &s, const kvr_select_params &p);

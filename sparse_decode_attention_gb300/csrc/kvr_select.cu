@@ -1,455 +1,741 @@
 // kvr_select.cu -- coarse collision scoring, candidate set, exact rescoring
-// and final top-k for one decode step (kvr_select).
+// and final top-k of one decode step, as ONE kernel launch (kvr_select).
 //
 // ParisKV, "Pipeline di Recupero Nativa su GPU in Due Stadi": the query votes,
 // per sub-block, for the centroids near its own with tiered weights; a key's
-// coarse score is the sum of the votes of the buckets it sits in; the best
-// few percent become candidates. The candidates are then rescored exactly
-// with q.k and the top-k kept.
+// coarse score is the sum of the votes of the buckets it sits in; the best few
+// percent become candidates. The candidates are rescored exactly with q.k and
+// the top-k kept.
 //
-// Kernel chain per call (grid = chunks x units unless noted):
-//   score_kernel     stream every pool code with 16-byte loads, XOR with the
-//                    query code, per-byte popcount -> vote LUT -> integer
-//                    score (uint8), per-chunk 256-bin histogram.
-//   threshold_kernel (one CTA per unit) total histogram -> the score
-//                    threshold T of the C'-th candidate, how many of the
-//                    tied T-scores each chunk contributes (lowest indices
-//                    first) and each chunk's output offset.
-//   rescore_kernel   order-preserving compaction of the chunk's candidates
-//                    (so the candidate list is ascending by index), then a
-//                    gather of their K rows (16 lanes per row, 16-byte loads)
-//                    and the canonical fp32 dot with q_bar.
-//   topk_kernel      (one CTA per unit) 4-pass 8-bit radix select of the
-//                    k'-th largest exact score in shared memory, then a
-//                    stable compaction that emits the winners ascending.
+// One thread-block cluster of CS CTAs serves one (batch, kv head) unit; the
+// CTAs exchange histograms through distributed shared memory, so the whole
+// step needs no second launch and no global synchronisation:
+//   P1 each CTA streams its share of the unit's code tiles into shared memory
+//      with 1-D bulk copies (one mbarrier-tracked slot per warp) and scores 32
+//      keys at a time on bit-planes: XOR with the query planes, a carry-save
+//      popcount of each 8-bit sub-block, the vote table as a mux tree, a
+//      ripple adder into the score planes; a histogram of the top score bits
+//      is kept in registers.
+//   P2 two cluster exchanges of 16-bin histograms fix the threshold score T,
+//      the tie quota and every CTA's output offset (ties by lowest index).
+//   P3 candidates are compacted in index order into the workspace.
+//   P4 after a cluster barrier every CTA takes an equal slice of the candidate
+//      list, bulk-copies the K rows into double-buffered shared memory and
+//      computes the canonical fp32 dot q_bar . k (half-warp per row).
+//   P5 four 8-bit radix passes over the exact scores, one cluster exchange of
+//      256-bin histograms each, find the k'-th largest (score, index) pair.
+//   P6 winners are written ascending by index.
+// Every cluster barrier is reached by every CTA on every path (control flow
+// around them depends only on per-unit values), and every bulk-copy wait is
+// bounded.
+#include <cooperative_groups.h>
+
 #include "kvr_device.cuh"
 #include "kvr_launch.h"
 
+namespace cg = cooperative_groups;
+
 namespace kvr {
+
+constexpr int kSelThreads = 256;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kMaxSlice = 2048;  // candidates per CTA in P4-P6
 
 struct SelArgs {
     int Hq, Hkv, G;
     int64_t cap;
     int C, k, W;
-    uint32_t lut_lo, lut_hi;  // vote weights for Hamming distance 0..3 and 4..7 (bytes)
-    int lut8_minus_lut0;      // correction for distance 8 (selector index 8 reads lut[0])
+    uint32_t leaf[4];  // bit m of leaf[j] = bit j of lut[m], m = 0..8
     const void *q;
     const void *K;
-    const uint32_t *codes;
+    const uint8_t *codes;
     const int32_t *seq_len;
     const int8_t *sgn;
     int32_t *out_idx;
     int32_t *out_count;
-    uint8_t *coarse;
+    uint32_t *planes;  // [U][8][nblk] score bit-planes
     int32_t *cand_idx;
     float *cand_score;
     int32_t *cand_count;
     float *qbar;
-    int32_t *chunk_hist;
-    int32_t *chunk_off;
-    int32_t *chunk_take;
-    int32_t *unit_T;
-    int64_t cap_pad;
-    int chunk, nchunk;
+    uint8_t *coarse;  // [U][cap_pad] or null
+    int64_t nblk, cap_pad, tiles;
     int32_t *err;
 };
 
-// Valid length of batch entry b, or 0 (with an error bit) when out of range.
-__device__ __forceinline__ int64_t unit_len(const SelArgs &a, int b, bool report)
+__host__ __device__ constexpr int bit_width(int v)
 {
-    const int64_t n = a.seq_len[b];
-    if (n < 0 || n > a.cap) {
-        if (report) set_err(a.err, KVR_DEVERR_SEQ_LEN);
-        return 0;
+    int b = 0;
+    while (v > 0) {
+        b++;
+        v >>= 1;
     }
-    return n;
+    return b;
+}
+// score bits for nb sub-blocks of votes below 2^vb
+__host__ __device__ constexpr int acc_bits(int nb, int vb) { return bit_width(nb * ((1 << vb) - 1)); }
+
+__device__ __forceinline__ uint32_t maj3(uint32_t a, uint32_t b, uint32_t c)
+{
+    return (a & b) | (c & (a | b));
+}
+__device__ __forceinline__ uint32_t mux(uint32_t s, uint32_t one, uint32_t zero)
+{
+    return (s & one) | (~s & zero);
 }
 
-// q_bar of unit u and its sign code, computed by one warp: lane l holds dims
-// [l*E, l*E+E). q_bar_j = (q_0j + q_1j + ... + q_{G-1}j) / G, left to right.
-template <int D, typename T>
-__device__ __forceinline__ void query_code(const SelArgs &a, int u, uint32_t *s_qcode,
-                                           float *g_qbar)
+// Bit-sliced popcount of 8 planes (32 keys at once): c = x0 + ... + x7, 4 bits.
+__device__ __forceinline__ void count8(const uint32_t (&x)[8], uint32_t &c0, uint32_t &c1,
+                                       uint32_t &c2, uint32_t &c3)
 {
-    constexpr int E = D / 32;
-    const int lane = threadIdx.x & 31;
+    const uint32_t sa = x[0] ^ x[1] ^ x[2], ka = maj3(x[0], x[1], x[2]);
+    const uint32_t sb = x[3] ^ x[4] ^ x[5], kb = maj3(x[3], x[4], x[5]);
+    const uint32_t sc = sa ^ sb ^ x[6], kc = maj3(sa, sb, x[6]);
+    c0 = sc ^ x[7];
+    const uint32_t kd = sc & x[7];
+    const uint32_t se = ka ^ kb ^ kc, ke = maj3(ka, kb, kc);
+    c1 = se ^ kd;
+    const uint32_t kf = se & kd;
+    c2 = ke ^ kf;
+    c3 = ke & kf;
+}
+
+// Bit-sliced table lookup v = lut[c] (c = 0..8) for one output bit; L[m] are
+// all-ones / all-zero words holding that bit of lut[m].
+__device__ __forceinline__ uint32_t lut_bit(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                            const uint32_t (&L)[9])
+{
+    const uint32_t m01 = mux(c0, L[1], L[0]), m23 = mux(c0, L[3], L[2]);
+    const uint32_t m45 = mux(c0, L[5], L[4]), m67 = mux(c0, L[7], L[6]);
+    const uint32_t m03 = mux(c1, m23, m01), m47 = mux(c1, m67, m45);
+    return mux(c3, L[8], mux(c2, m47, m03));
+}
+
+// acc += v, bit-sliced, acc has A bits, v has V <= A bits (no overflow by design).
+template <int A, int V>
+__device__ __forceinline__ void add_planes(uint32_t (&acc)[A], const uint32_t (&v)[V])
+{
+    uint32_t carry = 0;
+#pragma unroll
+    for (int j = 0; j < A; j++) {
+        const uint32_t x = (j < V) ? v[j] : 0u;
+        const uint32_t t = acc[j] ^ x;
+        const uint32_t nc = (acc[j] & x) | (carry & t);
+        acc[j] = t ^ carry;
+        carry = nc;
+    }
+}
+
+// Masks of the keys whose A-bit score is > T and == T.
+template <int A>
+__device__ __forceinline__ void compare_planes(const uint32_t (&p)[A], int T, uint32_t &gt,
+                                               uint32_t &eq)
+{
+    gt = 0u;
+    eq = 0xffffffffu;
+#pragma unroll
+    for (int j = A - 1; j >= 0; j--) {
+        if ((T >> j) & 1) {
+            eq &= p[j];
+        } else {
+            gt |= eq & p[j];
+            eq &= ~p[j];
+        }
+    }
+}
+
+// Keys of a 32-token block that lie in the pool [0, pool).
+__device__ __forceinline__ uint32_t pool_mask(int64_t blk, int64_t pool)
+{
+    const int64_t lo = blk * 32;
+    if (lo + 32 <= pool) return 0xffffffffu;
+    if (lo >= pool) return 0u;
+    return (1u << (uint32_t)(pool - lo)) - 1u;
+}
+
+template <int D, typename T> struct SelSmem {
+    static constexpr int kChunks = D / 4;             // 16-byte chunks (4 planes) per block
+    static constexpr int kHalfBytes = kChunks * 256;  // 16 blocks = 512 tokens
+    static constexpr int kRingBytes = kSelWarps * kHalfBytes;
+    static constexpr int kRowBytes = D * (int)sizeof(T);
+    static constexpr int kRowsPerBuf = kRingBytes / 2 / kRowBytes;
+    static constexpr int oS = kRingBytes;
+    static constexpr int oI = oS + kMaxSlice * 4;
+    static constexpr int oQm = oI + kMaxSlice * 4;
+    static constexpr int oQbar = oQm + kChunks * 16;
+    static constexpr int oQsgn = oQbar + D * 4;
+    static constexpr int oH1 = oQsgn + D * 4;
+    static constexpr int oH2 = oH1 + 16 * 4;
+    static constexpr int oRad = oH2 + 16 * 4;    // [2][256]
+    static constexpr int oAll = oRad + 512 * 4;  // [16][16] level 1, [16][16] level 2
+    static constexpr int oScan = oAll + 512 * 4;
+    static constexpr int oMisc = oScan + 40 * 4;
+    static constexpr int oBar = oMisc + 64 * 4;  // kSelWarps + 2 mbarriers
+    static constexpr int bytes = oBar + (kSelWarps + 2) * 8;
+    static_assert(16 * 256 * 4 <= kRingBytes, "radix exchange scratch must fit the ring");
+};
+
+enum {
+    M_U1 = 0, M_REM1, M_T, M_TAKE, M_OFF, M_KTAKE, M_KOFF, M_DIGIT, M_BEFORE,
+    M_ABOVE = 16,  // [16] per-CTA count of keys above the radix prefix
+};
+
+template <int D, typename T, int VB>
+__global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
+{
+    using SM = SelSmem<D, T>;
+    constexpr int NB = D / 8;
+    constexpr int NCH = SM::kChunks;
+    constexpr int ACC = acc_bits(NB, VB);
+    constexpr int LOWB = ACC < 4 ? ACC : 4;
+    constexpr int H1 = ACC - LOWB;
+    constexpr int NL1 = 1 << H1, NL2 = 1 << LOWB;
+    constexpr int RB = SM::kRowBytes;
+    constexpr int P = D / 16;  // dims per lane in the exact dot
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *ring = smem;
+    float *sS = reinterpret_cast<float *>(smem + SM::oS);
+    int32_t *sI = reinterpret_cast<int32_t *>(smem + SM::oI);
+    uint4 *sQm = reinterpret_cast<uint4 *>(smem + SM::oQm);
+    float *sQbar = reinterpret_cast<float *>(smem + SM::oQbar);
+    int *sQsgn = reinterpret_cast<int *>(smem + SM::oQsgn);
+    int *sH1 = reinterpret_cast<int *>(smem + SM::oH1);
+    int *sH2 = reinterpret_cast<int *>(smem + SM::oH2);
+    int *sRad = reinterpret_cast<int *>(smem + SM::oRad);
+    int *sAll = reinterpret_cast<int *>(smem + SM::oAll);
+    int *sScan = reinterpret_cast<int *>(smem + SM::oScan);
+    int *sMisc = reinterpret_cast<int *>(smem + SM::oMisc);
+    uint64_t *sBar = reinterpret_cast<uint64_t *>(smem + SM::oBar);
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int CS = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int u = blockIdx.y;
     const int b = u / a.Hkv, h = u % a.Hkv;
-    const T *qg = static_cast<const T *>(a.q) + ((int64_t)b * a.Hq + (int64_t)h * a.G) * D;
-    float x[E];
-#pragma unroll
-    for (int r = 0; r < E; r++) {
-        const int j = lane * E + r;
-        float acc = to_f32(qg[j]);
-        for (int g = 1; g < a.G; g++) acc = acc + to_f32(qg[(int64_t)g * D + j]);
-        x[r] = acc / (float)a.G;
-        if (g_qbar) g_qbar[(int64_t)u * D + j] = x[r];
-        if (a.sgn[j] < 0) x[r] = -x[r];
+
+    int64_t N = a.seq_len[b];
+    if (N < 0 || N > a.cap) {
+        if (rank == 0 && tid == 0 && h == 0) set_err(a.err, KVR_DEVERR_SEQ_LEN);
+        N = 0;
     }
-    fwht_lanes<E, 32>(x, lane);
-    const uint32_t w = sign_word<E>(x, lane);
-    if ((lane % (32 / E)) == 0) s_qcode[(lane * E) / 32] = w;
-}
-
-// Votes of the 4 sub-blocks in one 32-bit code word XOR-ed with the query:
-// per byte popcount (SWAR), then a 4-byte table lookup with prmt selecting
-// lut[popcount & 7]; bytes at distance 8 are fixed up by the caller.
-__device__ __forceinline__ uint32_t vote_bytes(uint32_t x, uint32_t lo, uint32_t hi,
-                                               uint32_t &c8)
-{
-    x = x - ((x >> 1) & 0x55555555u);
-    x = (x & 0x33333333u) + ((x >> 2) & 0x33333333u);
-    x = (x + (x >> 4)) & 0x0f0f0f0fu;  // popcount per byte, 0..8
-    c8 += (x >> 3) & 0x01010101u;      // bytes at distance 8
-    const uint32_t y = x | (x >> 4);
-    const uint32_t sel = (y & 0x77u) | ((y >> 8) & 0x7700u);
-    return __byte_perm(lo, hi, sel);
-}
-
-template <int NW>
-__device__ __forceinline__ int score_words(const uint32_t (&w)[NW], const uint32_t (&qw)[NW],
-                                           const SelArgs &a)
-{
-    uint32_t acc = 0, c8 = 0;
-#pragma unroll
-    for (int i = 0; i < NW; i++) acc += vote_bytes(w[i] ^ qw[i], a.lut_lo, a.lut_hi, c8);
-    int s = (int)((acc * 0x01010101u) >> 24);
-    if (a.lut8_minus_lut0 != 0) s += a.lut8_minus_lut0 * (int)((c8 * 0x01010101u) >> 24);
-    return s;
-}
-
-template <int D, typename T>
-__global__ void __launch_bounds__(256) score_kernel(SelArgs a)
-{
-    constexpr int NW = D / 32;  // 32-bit code words per key
-    constexpr int UNR = 4;
-    __shared__ uint32_t s_qcode[NW];
-    __shared__ int s_hist[256];
-    const int u = blockIdx.y, c = blockIdx.x;
-    const int b = u / a.Hkv;
-    const int64_t N = unit_len(a, b, c == 0 && threadIdx.x == 0 && (u % a.Hkv) == 0);
-    const int64_t pool = N > a.W ? N - a.W : 0;
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) s_hist[i] = 0;
-    if (threadIdx.x < 32) query_code<D, T>(a, u, s_qcode, c == 0 ? a.qbar : nullptr);
-    __syncthreads();
-    uint32_t qw[NW];
-#pragma unroll
-    for (int i = 0; i < NW; i++) qw[i] = s_qcode[i];
-
-    const int64_t start = (int64_t)c * a.chunk;
-    const int64_t end = min(start + (int64_t)a.chunk, pool);
-    const uint32_t *__restrict__ cw = a.codes + (int64_t)u * a.cap * NW;
-    uint8_t *__restrict__ out = a.coarse + (int64_t)u * a.cap_pad;
-    for (int64_t i0 = start + threadIdx.x; i0 < end; i0 += (int64_t)UNR * blockDim.x) {
-        uint32_t w[UNR][NW];
-#pragma unroll
-        for (int r = 0; r < UNR; r++) {
-            const int64_t i = i0 + (int64_t)r * blockDim.x;
-            if (i < end) {
-                if constexpr (NW == 4) {
-                    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(cw + i * 4));
-                    w[r][0] = v.x; w[r][1] = v.y; w[r][2] = v.z; w[r][3] = v.w;
-                } else {
-                    const uint2 v = __ldg(reinterpret_cast<const uint2 *>(cw + i * 2));
-                    w[r][0] = v.x; w[r][1] = v.y;
-                }
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < UNR; r++) {
-            const int64_t i = i0 + (int64_t)r * blockDim.x;
-            if (i < end) {
-                const int s = score_words<NW>(w[r], qw, a);
-                out[i] = (uint8_t)s;
-                atomicAdd(&s_hist[s], 1);
-            }
-        }
-    }
-    __syncthreads();
-    int32_t *gh = a.chunk_hist + ((int64_t)u * a.nchunk + c) * 256;
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) gh[i] = s_hist[i];
-}
-
-__global__ void __launch_bounds__(1024) threshold_kernel(SelArgs a)
-{
-    __shared__ int s_part[4][256];
-    __shared__ int s_ge[257];
-    __shared__ int s_scan[33];
-    __shared__ int s_vmax;
-    const int u = blockIdx.x, tid = threadIdx.x;
-    const int b = u / a.Hkv;
-    const int64_t N = unit_len(a, b, false);
     const int64_t pool = N > a.W ? N - a.W : 0;
     const int Cp = (int)min((int64_t)a.C, pool);
-
-    const int bin = tid & 255, part = tid >> 8;
-    int sum = 0;
-    const int32_t *hist = a.chunk_hist + (int64_t)u * a.nchunk * 256;
-    for (int c = part; c < a.nchunk; c += 4) sum += hist[(int64_t)c * 256 + bin];
-    s_part[part][bin] = sum;
-    if (tid == 0) s_vmax = -1;
-    __syncthreads();
-    // s_ge[t] = number of pool keys with score >= t (scan over bins 255 .. 0)
-    const int tot = (tid < 256) ? s_part[0][255 - tid] + s_part[1][255 - tid] +
-                                      s_part[2][255 - tid] + s_part[3][255 - tid]
-                                : 0;
-    if (tid < 256 && tot > 0) atomicMax(&s_vmax, 255 - tid);
-    int total;
-    const int ex = block_exclusive_scan(tot, s_scan, &total);
-    if (tid < 256) s_ge[255 - tid] = ex + tot;
-    if (tid == 0) s_ge[256] = 0;
-    __syncthreads();
-    // T = largest t with ge[t] >= Cp (ge is non-increasing in t)
-    const int n_ok = __syncthreads_count(tid < 256 && s_ge[tid] >= Cp);
-    const int T = (Cp == 0) ? 256 : n_ok - 1;
-    const int n_gt = (T < 256) ? s_ge[T + 1] : 0;
-    const int quota = Cp - n_gt;
-    const int vmax = s_vmax;
-
-    // per chunk: keys above T, ties at T, ties taken (lowest indices first), offset
-    int gt = 0, eq = 0;
-    const int c = tid;
-    if (c < a.nchunk && T < 256) {
-        const int32_t *hc = hist + (int64_t)c * 256;
-        for (int v = T + 1; v <= vmax; v++) gt += hc[v];
-        eq = hc[T];
-    }
-    int eq_tot;
-    const int eq_before = block_exclusive_scan(eq, s_scan, &eq_tot);
-    const int take = max(0, min(quota - eq_before, eq));
-    int sel_tot;
-    const int off = block_exclusive_scan(gt + take, s_scan, &sel_tot);
-    if (c < a.nchunk) {
-        a.chunk_off[(int64_t)u * a.nchunk + c] = off;
-        a.chunk_take[(int64_t)u * a.nchunk + c] = take;
-    }
-    if (tid == 0) {
-        a.unit_T[u] = T;
-        a.cand_count[u] = Cp;
-    }
-}
-
-// Keep the lowest n set bits of m.
-__device__ __forceinline__ uint32_t lowest_bits(uint32_t m, int n)
-{
-    uint32_t r = 0;
-    for (int i = 0; i < n && m; i++) {
-        const uint32_t low = m & (0u - m);
-        r |= low;
-        m ^= low;
-    }
-    return r;
-}
-
-// Canonical exact score of the candidates in list[0..n): half-warp per row,
-// lane gl holds dims [gl*D/16, (gl+1)*D/16), fma chain, butterfly 8,4,2,1.
-template <int D, typename T>
-__device__ __forceinline__ void rescore_list(const SelArgs &a, int u, const int32_t *list, int n,
-                                             int64_t out_base, const float (&qv)[D / 16])
-{
-    constexpr int P = D / 16;
-    constexpr int R = 4;  // rows in flight per half-warp
-    const int hw = threadIdx.x >> 4, gl = threadIdx.x & 15;
-    const int nhw = blockDim.x >> 4;
-    const T *Ku = static_cast<const T *>(a.K) + (int64_t)u * a.cap * D;
-    for (int base = 0; base < n; base += R * nhw) {
-        float kv[R][P];
-        int row[R];
-#pragma unroll
-        for (int r = 0; r < R; r++) {
-            const int j = base + r * nhw + hw;
-            row[r] = (j < n) ? list[j] : -1;
-            if (row[r] >= 0) {
-                widen<P>(Ku + (int64_t)row[r] * D + gl * P, kv[r]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < P; e++) kv[r][e] = 0.0f;
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < R; r++) {
-            float acc = 0.0f;
-#pragma unroll
-            for (int e = 0; e < P; e++) acc = __fmaf_rn(qv[e], kv[r][e], acc);
-#pragma unroll
-            for (int span = 8; span >= 1; span >>= 1) acc = acc + __shfl_xor_sync(kFull, acc, span);
-            const int j = base + r * nhw + hw;
-            if (gl == 0 && j < n) {
-                if (acc != acc) set_err(a.err, KVR_DEVERR_NONFINITE);
-                a.cand_score[(int64_t)u * a.C + out_base + j] = acc;
-            }
-        }
-    }
-}
-
-template <int D, typename T>
-__global__ void __launch_bounds__(256) rescore_kernel(SelArgs a)
-{
-    constexpr int ITEMS = 8;
-    constexpr int TILE = 256 * ITEMS;
-    __shared__ int s_scan[33];
-    __shared__ int32_t s_list[TILE];
-    __shared__ float s_qbar[D];
-    const int u = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
-    const int thr = a.unit_T[u];
-    if (thr > 255) return;
-    const int b = u / a.Hkv;
-    const int64_t N = unit_len(a, b, false);
-    const int64_t pool = N > a.W ? N - a.W : 0;
-    const int64_t start = (int64_t)c * a.chunk;
-    const int64_t end = min(start + (int64_t)a.chunk, pool);
-    if (start >= end) return;
-    const int take = a.chunk_take[(int64_t)u * a.nchunk + c];
-    const int off = a.chunk_off[(int64_t)u * a.nchunk + c];
-    for (int j = tid; j < D; j += blockDim.x) s_qbar[j] = a.qbar[(int64_t)u * D + j];
-    __syncthreads();
-    float qv[D / 16];
-#pragma unroll
-    for (int e = 0; e < D / 16; e++) qv[e] = s_qbar[(tid & 15) * (D / 16) + e];
-
-    const uint8_t *sc = a.coarse + (int64_t)u * a.cap_pad;
-    int32_t *cidx = a.cand_idx + (int64_t)u * a.C;
-    int tie_carry = 0, sel_carry = 0;
-    for (int64_t t0 = start; t0 < end; t0 += TILE) {
-        const int64_t i0 = t0 + (int64_t)tid * ITEMS;
-        uint32_t gtm = 0, eqm = 0;
-        if (i0 + ITEMS <= end) {
-            const uint2 v = *reinterpret_cast<const uint2 *>(sc + i0);
-#pragma unroll
-            for (int r = 0; r < ITEMS; r++) {
-                const int s = (int)(((r < 4 ? v.x : v.y) >> (8 * (r & 3))) & 0xffu);
-                gtm |= (s > thr ? 1u : 0u) << r;
-                eqm |= (s == thr ? 1u : 0u) << r;
-            }
-        } else {
-            for (int r = 0; r < ITEMS; r++) {
-                if (i0 + r >= end) break;
-                const int s = sc[i0 + r];
-                gtm |= (s > thr ? 1u : 0u) << r;
-                eqm |= (s == thr ? 1u : 0u) << r;
-            }
-        }
-        int eq_tot;
-        const int eq_before = block_exclusive_scan(__popc(eqm), s_scan, &eq_tot);
-        const int allow = max(0, min(take - tie_carry - eq_before, __popc(eqm)));
-        const uint32_t selm = gtm | lowest_bits(eqm, allow);
-        int sel_tot;
-        const int sel_before = block_exclusive_scan(__popc(selm), s_scan, &sel_tot);
-        int r = 0;
-        for (uint32_t m = selm; m; m &= m - 1, r++) {
-            const int32_t idx = (int32_t)(i0 + __ffs(m) - 1);
-            s_list[sel_before + r] = idx;
-            cidx[off + sel_carry + sel_before + r] = idx;
-        }
-        __syncthreads();
-        rescore_list<D, T>(a, u, s_list, sel_tot, off + sel_carry, qv);
-        __syncthreads();
-        tie_carry += eq_tot;
-        sel_carry += sel_tot;
-    }
-}
-
-__global__ void __launch_bounds__(1024) topk_kernel(SelArgs a)
-{
-    extern __shared__ uint32_t s_key[];
-    __shared__ int s_hist[256];
-    __shared__ int s_scan[33];
-    __shared__ uint32_t s_prefix;
-    __shared__ int s_remaining;
-    const int u = blockIdx.x, tid = threadIdx.x;
-    const int Cp = a.cand_count[u];
     const int kp = min(a.k, Cp);
-    int32_t *orow = a.out_idx + (int64_t)u * a.k;
-    for (int j = kp + tid; j < a.k; j += blockDim.x) orow[j] = -1;
-    if (tid == 0) a.out_count[u] = kp;
-    if (kp == 0) return;
-    const float *S = a.cand_score + (int64_t)u * a.C;
-    const int32_t *I = a.cand_idx + (int64_t)u * a.C;
-    for (int j = tid; j < Cp; j += blockDim.x) s_key[j] = order_key(S[j]);
+    const int64_t nhalf = (pool + 511) / 512;
+    const int64_t h0 = (int64_t)rank * nhalf / CS, h1 = (int64_t)(rank + 1) * nhalf / CS;
+    const int64_t nb_pool = (pool + 31) / 32;
+    const int64_t blk0 = min(h0 * 16, nb_pool), blk1 = min(h1 * 16, nb_pool);
+    const uint8_t *codes_u = a.codes + (size_t)u * a.tiles * (D * 128);
 
-    // radix select of the kp-th largest key, 8 bits at a time from the top
-    uint32_t prefix = 0, mask = 0;
-    int remaining = kp;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += blockDim.x) s_hist[i] = 0;
-        __syncthreads();
-        for (int j = tid; j < Cp; j += blockDim.x) {
-            const uint32_t key = s_key[j];
-            if ((key & mask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1);
+    if (tid == 0) {
+        for (int i = 0; i < kSelWarps + 2; i++) mbar_init(&sBar[i], 1);
+        mbar_fence_init();
+    }
+    for (int i = tid; i < 16; i += kSelThreads) {
+        sH1[i] = 0;
+        sH2[i] = 0;
+    }
+    __syncthreads();
+
+    // Issue the first code half-tile of every warp before anything else.
+    uint32_t parity = 0;
+    int64_t hh = (Cp > 0 || a.coarse != nullptr) ? h0 + warp : h1;
+    uint8_t *slot = ring + warp * SM::kHalfBytes;
+    auto issue_half = [&](int64_t half) {
+        if (lane == 0) mbar_arrive_expect_tx(&sBar[warp], SM::kHalfBytes);
+        __syncwarp();
+        if (lane < NCH) {
+            const uint8_t *src = codes_u + (size_t)(half >> 1) * (D * 128) +
+                                 ((size_t)lane * 32 + (size_t)(half & 1) * 16) * 16;
+            bulk_g2s(slot + lane * 256, src, 256, &sBar[warp]);
         }
+    };
+    if (hh < h1) issue_half(hh);
+
+    // q_bar and its code (every CTA of the cluster computes them)
+    if (warp == 0) {
+        constexpr int E = D / 32;
+        const T *qg = static_cast<const T *>(a.q) + ((int64_t)b * a.Hq + (int64_t)h * a.G) * D;
+        float x[E];
+#pragma unroll
+        for (int r = 0; r < E; r++) {
+            const int j = lane * E + r;
+            float acc = to_f32(qg[j]);
+            for (int g = 1; g < a.G; g++) acc = acc + to_f32(qg[(int64_t)g * D + j]);
+            x[r] = acc / (float)a.G;
+            sQbar[j] = x[r];
+            if (rank == 0) a.qbar[(int64_t)u * D + j] = x[r];
+            if (a.sgn[j] < 0) x[r] = -x[r];
+        }
+        fwht_lanes<E, 32>(x, lane);
+#pragma unroll
+        for (int r = 0; r < E; r++) sQsgn[lane * E + r] = x[r] < 0.0f ? -1 : 0;
+    }
+    __syncthreads();
+    for (int c = tid; c < NCH; c += kSelThreads)
+        sQm[c] = make_uint4((uint32_t)sQsgn[4 * c], (uint32_t)sQsgn[4 * c + 1],
+                            (uint32_t)sQsgn[4 * c + 2], (uint32_t)sQsgn[4 * c + 3]);
+    uint32_t L[VB][9];  // vote-table leaves
+#pragma unroll
+    for (int j = 0; j < VB; j++)
+#pragma unroll
+        for (int m = 0; m < 9; m++) L[j][m] = ((a.leaf[j] >> m) & 1u) ? 0xffffffffu : 0u;
+    __syncthreads();
+
+    // ---------------------------------------------------------------- P1
+    int cnt1[NL1];
+#pragma unroll
+    for (int i = 0; i < NL1; i++) cnt1[i] = 0;
+    const int jb = lane & 15, sh = lane >> 4;  // block within the half-tile, sub-block half
+    uint32_t *planes_u = a.planes + (size_t)u * 8 * a.nblk;
+    for (; hh < h1; hh += kSelWarps) {
+        mbar_wait(&sBar[warp], parity, a.err);
+        parity ^= 1u;
+        uint32_t acc[ACC];
+#pragma unroll
+        for (int j = 0; j < ACC; j++) acc[j] = 0u;
+#pragma unroll 2
+        for (int sb = sh * (NB / 2); sb < (sh + 1) * (NB / 2); sb++) {
+            const uint4 v0 = *reinterpret_cast<const uint4 *>(slot + (2 * sb) * 256 + jb * 16);
+            const uint4 v1 = *reinterpret_cast<const uint4 *>(slot + (2 * sb + 1) * 256 + jb * 16);
+            const uint4 q0 = sQm[2 * sb], q1 = sQm[2 * sb + 1];
+            const uint32_t x[8] = {v0.x ^ q0.x, v0.y ^ q0.y, v0.z ^ q0.z, v0.w ^ q0.w,
+                                   v1.x ^ q1.x, v1.y ^ q1.y, v1.z ^ q1.z, v1.w ^ q1.w};
+            uint32_t c0, c1, c2, c3;
+            count8(x, c0, c1, c2, c3);
+            uint32_t vote[VB];
+#pragma unroll
+            for (int j = 0; j < VB; j++) vote[j] = lut_bit(c0, c1, c2, c3, L[j]);
+            add_planes<ACC, VB>(acc, vote);
+        }
+        uint32_t other[ACC];  // the other half of the sub-blocks sits in lane ^ 16
+#pragma unroll
+        for (int j = 0; j < ACC; j++) other[j] = __shfl_xor_sync(kFull, acc[j], 16);
+        add_planes<ACC, ACC>(acc, other);
+        // every lane has read the slot: refill it
+        __syncwarp();
+        fence_proxy_async();
+        const int64_t blk = hh * 16 + jb;
+        if (hh + kSelWarps < h1) issue_half(hh + kSelWarps);
+        if (sh == 0 && blk < nb_pool) {
+            const uint32_t vm = pool_mask(blk, pool);
+#pragma unroll
+            for (int j = 0; j < ACC; j++) planes_u[(size_t)j * a.nblk + blk] = acc[j];
+#pragma unroll
+            for (int v = 0; v < NL1; v++) {
+                uint32_t m = vm;
+#pragma unroll
+                for (int j = 0; j < H1; j++) m &= ((v >> j) & 1) ? acc[LOWB + j] : ~acc[LOWB + j];
+                cnt1[v] += __popc(m);
+            }
+        }
+    }
+#pragma unroll
+    for (int v = 0; v < NL1; v++) {
+        int s = cnt1[v];
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+        if (lane == 0 && s) atomicAdd(&sH1[v], s);
+    }
+    __syncthreads();
+    cluster.sync();  // #1: level-1 histograms published
+
+    // ---------------------------------------------------------------- P2
+    for (int t = tid; t < CS * NL1; t += kSelThreads) {
+        const int r = t / NL1, v = t % NL1;
+        sAll[r * 16 + v] = *cluster.map_shared_rank(&sH1[v], r);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int u1 = -1, rem = Cp, cum = 0;
+        if (Cp > 0) {
+            for (int v = NL1 - 1; v >= 0; v--) {
+                int tot = 0;
+                for (int r = 0; r < CS; r++) tot += sAll[r * 16 + v];
+                if (cum + tot >= Cp) {
+                    u1 = v;
+                    rem = Cp - cum;
+                    break;
+                }
+                cum += tot;
+            }
+        }
+        sMisc[M_U1] = u1;
+        sMisc[M_REM1] = rem;
+    }
+    __syncthreads();
+    const int u1 = sMisc[M_U1];
+    if (u1 >= 0) {
+        int cnt2[NL2];
+#pragma unroll
+        for (int i = 0; i < NL2; i++) cnt2[i] = 0;
+        for (int64_t blk = blk0 + tid; blk < blk1; blk += kSelThreads) {
+            uint32_t p[ACC];
+#pragma unroll
+            for (int j = 0; j < ACC; j++) p[j] = planes_u[(size_t)j * a.nblk + blk];
+            uint32_t inb = pool_mask(blk, pool);
+#pragma unroll
+            for (int j = 0; j < H1; j++) inb &= ((u1 >> j) & 1) ? p[LOWB + j] : ~p[LOWB + j];
+#pragma unroll
+            for (int v = 0; v < NL2; v++) {
+                uint32_t m = inb;
+#pragma unroll
+                for (int j = 0; j < LOWB; j++) m &= ((v >> j) & 1) ? p[j] : ~p[j];
+                cnt2[v] += __popc(m);
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < NL2; v++) {
+            int s = cnt2[v];
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+            if (lane == 0 && s) atomicAdd(&sH2[v], s);
+        }
+    }
+    __syncthreads();
+    cluster.sync();  // #2: level-2 histograms published
+
+    for (int t = tid; t < CS * NL2; t += kSelThreads) {
+        const int r = t / NL2, v = t % NL2;
+        sAll[256 + r * 16 + v] = *cluster.map_shared_rank(&sH2[v], r);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int Tthr = 1 << 30, take = 0, off = 0;
+        if (u1 >= 0) {
+            const int rem = sMisc[M_REM1];
+            int cum = 0, v2 = 0;
+            for (int v = NL2 - 1; v >= 0; v--) {
+                int tot = 0;
+                for (int r = 0; r < CS; r++) tot += sAll[256 + r * 16 + v];
+                if (cum + tot >= rem) {
+                    v2 = v;
+                    break;
+                }
+                cum += tot;
+            }
+            const int quota = rem - cum;  // ties at T taken, lowest indices first
+            Tthr = (u1 << LOWB) | v2;
+            int eq_before = 0, sel_before = 0;
+            for (int r = 0; r < CS; r++) {
+                int gt = 0;
+                for (int v = u1 + 1; v < NL1; v++) gt += sAll[r * 16 + v];
+                for (int v = v2 + 1; v < NL2; v++) gt += sAll[256 + r * 16 + v];
+                const int eq = sAll[256 + r * 16 + v2];
+                const int tk = max(0, min(quota - eq_before, eq));
+                if (r == rank) {
+                    take = tk;
+                    off = sel_before;
+                }
+                eq_before += eq;
+                sel_before += gt + tk;
+            }
+        }
+        sMisc[M_T] = Tthr;
+        sMisc[M_TAKE] = take;
+        sMisc[M_OFF] = off;
+        if (rank == 0) a.cand_count[u] = Cp;
+    }
+    __syncthreads();
+
+    // ---------------------------------------------------------------- P3
+    const int Tthr = sMisc[M_T];
+    int32_t *cidx = a.cand_idx + (size_t)u * a.C;
+    {
+        const int64_t nbc = blk1 - blk0;
+        const int64_t bpt = (nbc + kSelThreads - 1) / kSelThreads;
+        const int64_t my0 = blk0 + min((int64_t)tid * bpt, nbc);
+        const int64_t my1 = blk0 + min((int64_t)(tid + 1) * bpt, nbc);
+        int n_eq = 0;
+        if (u1 >= 0)
+            for (int64_t blk = my0; blk < my1; blk++) {
+                uint32_t p[ACC], gt, eq;
+#pragma unroll
+                for (int j = 0; j < ACC; j++) p[j] = planes_u[(size_t)j * a.nblk + blk];
+                compare_planes<ACC>(p, Tthr, gt, eq);
+                n_eq += __popc(eq & pool_mask(blk, pool));
+            }
+        int tot;
+        const int eq_before = block_exclusive_scan(n_eq, sScan, &tot);
+        const int allow0 = max(0, min(sMisc[M_TAKE] - eq_before, n_eq));
+        int n_sel = 0, allow = allow0;
+        if (u1 >= 0)
+            for (int64_t blk = my0; blk < my1; blk++) {
+                uint32_t p[ACC], gt, eq;
+#pragma unroll
+                for (int j = 0; j < ACC; j++) p[j] = planes_u[(size_t)j * a.nblk + blk];
+                compare_planes<ACC>(p, Tthr, gt, eq);
+                const uint32_t vm = pool_mask(blk, pool);
+                const int ne = __popc(eq & vm);
+                n_sel += __popc(gt & vm) + min(allow, ne);
+                allow -= min(allow, ne);
+            }
+        int pos = block_exclusive_scan(n_sel, sScan, &tot) + sMisc[M_OFF];
+        allow = allow0;
+        for (int64_t blk = my0; blk < my1; blk++) {
+            uint32_t p[ACC], gt = 0, eq = 0;
+#pragma unroll
+            for (int j = 0; j < ACC; j++) p[j] = planes_u[(size_t)j * a.nblk + blk];
+            const uint32_t vm = pool_mask(blk, pool);
+            if (u1 >= 0) {
+                compare_planes<ACC>(p, Tthr, gt, eq);
+                gt &= vm;
+                eq &= vm;
+                uint32_t te = 0;
+                for (uint32_t m = eq; m && allow > 0; m &= m - 1, allow--) te |= m & (0u - m);
+                for (uint32_t m = gt | te; m; m &= m - 1)
+                    cidx[pos++] = (int32_t)(blk * 32 + __ffs(m) - 1);
+            }
+            if (a.coarse) {
+                uint8_t *co = a.coarse + (size_t)u * a.cap_pad + blk * 32;
+                for (int i = 0; i < 32; i++) {
+                    if (!((vm >> i) & 1u)) continue;
+                    int s = 0;
+#pragma unroll
+                    for (int j = 0; j < ACC; j++) s |= (int)((p[j] >> i) & 1u) << j;
+                    co[i] = (uint8_t)s;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    cluster.sync();  // #3: the unit's candidate list is complete
+
+    // ---------------------------------------------------------------- P4
+    const int lo = (int)((int64_t)rank * Cp / CS), hi = (int)((int64_t)(rank + 1) * Cp / CS);
+    const int n = hi - lo;  // <= kMaxSlice (the host picks CS so)
+    for (int j = tid; j < n; j += kSelThreads) sI[j] = cidx[lo + j];
+    {
+        float qv[P];
+#pragma unroll
+        for (int e = 0; e < P; e++) qv[e] = sQbar[(tid & 15) * P + e];
+        const uint8_t *Ku = static_cast<const uint8_t *>(a.K) + (size_t)u * a.cap * RB;
+        const int nbatch = (n + SM::kRowsPerBuf - 1) / SM::kRowsPerBuf;
+        auto issue_rows = [&](int bi) {
+            uint8_t *buf = ring + (bi & 1) * (SM::kRingBytes / 2);
+            const int r0 = bi * SM::kRowsPerBuf, rn = min(SM::kRowsPerBuf, n - r0);
+            if (tid == 0) mbar_arrive_expect_tx(&sBar[kSelWarps + (bi & 1)], (uint32_t)(rn * RB));
+            __syncthreads();
+            for (int j = tid; j < rn; j += kSelThreads)
+                bulk_g2s(buf + j * RB, Ku + (size_t)sI[r0 + j] * RB, RB,
+                         &sBar[kSelWarps + (bi & 1)]);
+        };
+        fence_proxy_async();
         __syncthreads();
-        if (tid < 32) {
-            int cnt[8], sum = 0;
+        if (nbatch > 0) issue_rows(0);
+        if (nbatch > 1) issue_rows(1);
+        const int hw = tid >> 4, gl = tid & 15;
+        for (int bi = 0; bi < nbatch; bi++) {
+            mbar_wait(&sBar[kSelWarps + (bi & 1)], (uint32_t)((bi >> 1) & 1), a.err);
+            const uint8_t *buf = ring + (bi & 1) * (SM::kRingBytes / 2);
+            const int r0 = bi * SM::kRowsPerBuf, rn = min(SM::kRowsPerBuf, n - r0);
+            for (int base = 0; base < rn; base += kSelThreads / 16) {
+                const int j = base + hw;
+                float kv[P];
+                if (j < rn) {
+                    widen<P>(reinterpret_cast<const T *>(buf + j * RB) + gl * P, kv);
+                } else {
 #pragma unroll
-            for (int r = 0; r < 8; r++) {
-                cnt[r] = s_hist[255 - (tid * 8 + r)];
-                sum += cnt[r];
-            }
-            int incl = sum;
+                    for (int e = 0; e < P; e++) kv[e] = 0.0f;
+                }
+                float acc = 0.0f;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(kFull, incl, o);
-                if (tid >= o) incl += y;
+                for (int e = 0; e < P; e++) acc = __fmaf_rn(qv[e], kv[e], acc);
+#pragma unroll
+                for (int span = 8; span >= 1; span >>= 1)
+                    acc = acc + __shfl_xor_sync(kFull, acc, span);
+                if (gl == 0 && j < rn) {
+                    if (acc != acc) set_err(a.err, KVR_DEVERR_NONFINITE);
+                    sS[r0 + j] = acc;
+                    a.cand_score[(size_t)u * a.C + lo + r0 + j] = acc;
+                }
             }
-            int run = incl - sum;
-            if (run < remaining && remaining <= incl) {
-                for (int r = 0; r < 8; r++) {
-                    if (run + cnt[r] >= remaining) {
-                        s_prefix = prefix | ((uint32_t)(255 - (tid * 8 + r)) << shift);
-                        s_remaining = remaining - run;
-                        break;
-                    }
-                    run += cnt[r];
+            fence_proxy_async();
+            __syncthreads();
+            if (bi + 2 < nbatch) issue_rows(bi + 2);
+        }
+    }
+    __syncthreads();
+
+    // ---------------------------------------------------------------- P5
+    // radix select of the kp-th largest order key over the cluster's slices
+    uint32_t prefix = 0, mask = 0;
+    int rem = kp;
+    if (tid < 16) sMisc[M_ABOVE + tid] = 0;
+    int *scratch = reinterpret_cast<int *>(ring);  // [CS][256] copy of every CTA's histogram
+    for (int pass = 0; pass < 4; pass++) {
+        const int shift = 24 - 8 * pass;
+        int *hist = sRad + (pass & 1) * 256;
+        for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0;
+        __syncthreads();
+        if (kp > 0) {
+            const int iters = (n + kSelThreads - 1) / kSelThreads;
+            for (int it = 0; it < iters; it++) {
+                const int j = it * kSelThreads + tid;
+                uint32_t key = 0;
+                bool part = false;
+                if (j < n) {
+                    key = order_key(sS[j]);
+                    part = (key & mask) == prefix;
+                }
+                const unsigned act = __ballot_sync(kFull, part);
+                if (part) {
+                    const uint32_t bin = (key >> shift) & 255u;
+                    const unsigned peers = __match_any_sync(act, bin);
+                    if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
                 }
             }
         }
         __syncthreads();
-        prefix = s_prefix;
-        remaining = s_remaining;
-        mask |= 255u << shift;
+        cluster.sync();  // #4..#7: this pass's histograms published
+        if (kp > 0) {
+            for (int t = tid; t < CS * 256; t += kSelThreads)
+                scratch[t] = *cluster.map_shared_rank(&hist[t & 255], t >> 8);
+            __syncthreads();
+            if (warp == 0) {
+                int cnt[8], sum = 0;
+#pragma unroll
+                for (int r = 0; r < 8; r++) {
+                    const int bin = 255 - (lane * 8 + r);
+                    int c = 0;
+                    for (int x = 0; x < CS; x++) c += scratch[x * 256 + bin];
+                    cnt[r] = c;
+                    sum += c;
+                }
+                int incl = sum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(kFull, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                int run = incl - sum;
+                if (run < rem && rem <= incl) {
+                    for (int r = 0; r < 8; r++) {
+                        if (run + cnt[r] >= rem) {
+                            sMisc[M_DIGIT] = 255 - (lane * 8 + r);
+                            sMisc[M_BEFORE] = run;
+                            break;
+                        }
+                        run += cnt[r];
+                    }
+                }
+            }
+            __syncthreads();
+            const int digit = sMisc[M_DIGIT];
+            if (tid < CS) {
+                int above = 0;
+                for (int bin = digit + 1; bin < 256; bin++) above += scratch[tid * 256 + bin];
+                sMisc[M_ABOVE + tid] += above;
+                if (pass == 3) sAll[tid] = scratch[tid * 256 + digit];  // ties per CTA
+            }
+            rem -= sMisc[M_BEFORE];
+            prefix |= (uint32_t)digit << shift;
+            mask |= 255u << shift;
+            __syncthreads();
+        }
     }
-    const uint32_t keyT = prefix;  // the kp-th largest key
-    const int quota = remaining;   // how many keys equal to keyT are taken
 
-    // stable compaction in candidate order (= ascending token index)
-    const int seg = (Cp + blockDim.x - 1) / blockDim.x;
-    const int j0 = min(tid * seg, Cp), j1 = min(j0 + seg, Cp);
-    int n_eq = 0;
-    for (int j = j0; j < j1; j++) n_eq += (s_key[j] == keyT);
-    int eq_tot;
-    const int eq_before = block_exclusive_scan(n_eq, s_scan, &eq_tot);
-    int n_sel = 0, seen = 0;
-    for (int j = j0; j < j1; j++) {
-        const uint32_t key = s_key[j];
-        if (key > keyT) n_sel++;
-        else if (key == keyT) n_sel += (eq_before + seen++ < quota);
+    // ---------------------------------------------------------------- P6
+    if (kp > 0) {
+        if (tid == 0) {
+            int eq_before = 0, sel_before = 0, take = 0, off = 0;
+            for (int r = 0; r < CS; r++) {
+                const int tk = max(0, min(rem - eq_before, sAll[r]));
+                if (r == rank) {
+                    take = tk;
+                    off = sel_before;
+                }
+                eq_before += sAll[r];
+                sel_before += sMisc[M_ABOVE + r] + tk;
+            }
+            sMisc[M_KTAKE] = take;
+            sMisc[M_KOFF] = off;
+        }
+        __syncthreads();
+        const uint32_t keyT = prefix;
+        const int spt = (n + kSelThreads - 1) / kSelThreads;
+        const int j0 = min(tid * spt, n), j1 = min(j0 + spt, n);
+        int n_eq = 0;
+        for (int j = j0; j < j1; j++) n_eq += order_key(sS[j]) == keyT;
+        int tot;
+        const int eq_before = block_exclusive_scan(n_eq, sScan, &tot);
+        const int allow0 = max(0, min(sMisc[M_KTAKE] - eq_before, n_eq));
+        int n_sel = 0, allow = allow0;
+        for (int j = j0; j < j1; j++) {
+            const uint32_t key = order_key(sS[j]);
+            if (key > keyT) {
+                n_sel++;
+            } else if (key == keyT && allow > 0) {
+                n_sel++;
+                allow--;
+            }
+        }
+        int pos = block_exclusive_scan(n_sel, sScan, &tot) + sMisc[M_KOFF];
+        int32_t *orow = a.out_idx + (size_t)u * a.k;
+        allow = allow0;
+        for (int j = j0; j < j1; j++) {
+            const uint32_t key = order_key(sS[j]);
+            bool take = key > keyT;
+            if (key == keyT && allow > 0) {
+                take = true;
+                allow--;
+            }
+            if (take) orow[pos++] = sI[j];
+        }
     }
-    int sel_tot;
-    int pos = block_exclusive_scan(n_sel, s_scan, &sel_tot);
-    seen = 0;
-    for (int j = j0; j < j1; j++) {
-        const uint32_t key = s_key[j];
-        bool take = key > keyT;
-        if (key == keyT) take = (eq_before + seen++ < quota);
-        if (take) orow[pos++] = I[j];
+    if (rank == 0) {
+        int32_t *orow = a.out_idx + (size_t)u * a.k;
+        for (int j = kp + tid; j < a.k; j += kSelThreads) orow[j] = -1;
+        if (tid == 0) a.out_count[u] = kp;
     }
+    __syncthreads();
+    cluster.sync();  // #8: no CTA leaves while another may read its shared memory
+}
+
+// ------------------------------------------------------------------ host side
+
+int select_cluster_size(int U, int C)
+{
+    int cs = 16;
+    while (cs > 1 && (int64_t)U * cs > 2 * 152) cs >>= 1;
+    while (cs < 16 && (int64_t)cs * kMaxSlice < C) cs <<= 1;
+    return cs;
+}
+
+template <int D, typename T, int VB>
+static kvr_status launch_select_t(const LaunchCtx &c, const SelArgs &a, int cs)
+{
+    auto kern = select_kernel<D, T, VB>;
+    const int smem = SelSmem<D, T>::bytes;
+    kvr_status st = prepare_cluster_kernel(reinterpret_cast<const void *>(kern), smem);
+    if (st != KVR_OK) return st;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs, c.shape.B * c.shape.Hkv, 1);
+    cfg.blockDim = dim3(kSelThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return KVR_ERR_CUDA;
+    return check_launch();
 }
 
 template <int D, typename T>
-static kvr_status launch_select(const LaunchCtx &c, SelArgs &a)
+static kvr_status launch_select_vb(const LaunchCtx &c, const SelArgs &a, int cs, int vb)
 {
-    const int U = c.shape.B * c.shape.Hkv;
-    const dim3 g(a.nchunk, U);
-    score_kernel<D, T><<<g, 256, 0, c.stream>>>(a);
-    threshold_kernel<<<U, 1024, 0, c.stream>>>(a);
-    rescore_kernel<D, T><<<g, 256, 0, c.stream>>>(a);
-    const size_t smem = (size_t)a.C * sizeof(uint32_t);
-    if (smem > 48 * 1024) {
-        kvr_status st = raise_smem_limit(reinterpret_cast<const void *>(topk_kernel),
-                                         32768 * (int)sizeof(uint32_t));
-        if (st != KVR_OK) return st;
+    switch (vb) {
+    case 1: return launch_select_t<D, T, 1>(c, a, cs);
+    case 2: return launch_select_t<D, T, 2>(c, a, cs);
+    case 3: return launch_select_t<D, T, 3>(c, a, cs);
+    default: return launch_select_t<D, T, 4>(c, a, cs);
     }
-    topk_kernel<<<U, 1024, smem, c.stream>>>(a);
-    return check_launch();
 }
 
 kvr_status select_dispatch(const LaunchCtx &c, const kvr_select_params &p, const SelectPlan &plan,
@@ -465,35 +751,38 @@ kvr_status select_dispatch(const LaunchCtx &c, const kvr_select_params &p, const
     a.C = p.C;
     a.k = p.k;
     a.W = p.W;
-    a.lut_lo = (uint32_t)p.lut[0] | ((uint32_t)p.lut[1] << 8) | ((uint32_t)p.lut[2] << 16) |
-               ((uint32_t)p.lut[3] << 24);
-    a.lut_hi = (uint32_t)p.lut[4] | ((uint32_t)p.lut[5] << 8) | ((uint32_t)p.lut[6] << 16) |
-               ((uint32_t)p.lut[7] << 24);
-    a.lut8_minus_lut0 = p.lut[8] - p.lut[0];
+    int maxw = 0;
+    for (int m = 0; m < 9; m++) maxw = p.lut[m] > maxw ? p.lut[m] : maxw;
+    const int vb = maxw > 0 ? bit_width(maxw) : 1;
+    for (int j = 0; j < 4; j++) {
+        uint32_t bits = 0;
+        for (int m = 0; m < 9; m++) bits |= (uint32_t)((p.lut[m] >> j) & 1) << m;
+        a.leaf[j] = bits;
+    }
     a.q = q;
     a.K = K;
-    a.codes = reinterpret_cast<const uint32_t *>(codes);
+    a.codes = codes;
     a.seq_len = seq_len;
     a.sgn = sgn;
     a.out_idx = out_idx;
     a.out_count = out_count;
-    a.coarse = ws + plan.off_coarse;
+    a.planes = reinterpret_cast<uint32_t *>(ws + plan.off_planes);
     a.cand_idx = reinterpret_cast<int32_t *>(ws + plan.off_cand_idx);
     a.cand_score = reinterpret_cast<float *>(ws + plan.off_cand_score);
     a.cand_count = reinterpret_cast<int32_t *>(ws + plan.off_cand_count);
     a.qbar = reinterpret_cast<float *>(ws + plan.off_qbar);
-    a.chunk_hist = reinterpret_cast<int32_t *>(ws + plan.off_chunk_hist);
-    a.chunk_off = reinterpret_cast<int32_t *>(ws + plan.off_chunk_off);
-    a.chunk_take = reinterpret_cast<int32_t *>(ws + plan.off_chunk_take);
-    a.unit_T = reinterpret_cast<int32_t *>(ws + plan.off_unit_T);
+    a.coarse = plan.has_coarse ? ws + plan.off_coarse : nullptr;
+    a.nblk = plan.nblk;
     a.cap_pad = plan.cap_pad;
-    a.chunk = plan.chunk;
-    a.nchunk = plan.nchunk;
+    a.tiles = plan.tiles;
     a.err = err;
+    const int cs = select_cluster_size(c.shape.B * c.shape.Hkv, p.C);
     const bool bf = c.shape.dtype == KVR_BF16;
     if (c.shape.d == 128)
-        return bf ? launch_select<128, __nv_bfloat16>(c, a) : launch_select<128, float>(c, a);
-    return bf ? launch_select<64, __nv_bfloat16>(c, a) : launch_select<64, float>(c, a);
+        return bf ? launch_select_vb<128, __nv_bfloat16>(c, a, cs, vb)
+                  : launch_select_vb<128, float>(c, a, cs, vb);
+    return bf ? launch_select_vb<64, __nv_bfloat16>(c, a, cs, vb)
+              : launch_select_vb<64, float>(c, a, cs, vb);
 }
 
 }  // namespace kvr

@@ -7,17 +7,46 @@ import oracle
 import sparse_decode_attention_gb300 as kvr
 
 
-def encode_gpu(K, sgn, rows, pos0=0):
+def shape_of_cache(K, Hq=None):
     B, Hkv, cap, d = K.shape
-    codes = torch.zeros((B, Hkv, cap, d // 8), dtype=torch.uint8, device=K.device)
+    return kvr.Shape(B, Hq or Hkv, Hkv, d, cap, K.dtype)
+
+
+def planes_to_bytes(codes, B, Hkv, cap, d):
+    """Per-token code bytes [B, Hkv, cap, d/8] from the library's bit-plane
+    tiles (test-side reading of the documented layout)."""
+    raw = codes.detach().cpu().numpy() if isinstance(codes, torch.Tensor) else codes
+    tiles = (cap + 1023) // 1024
+    words = raw[:B * Hkv * tiles * d * 128].view(np.uint32).reshape(B * Hkv, tiles, d // 4, 32, 4)
+    out = np.zeros((B * Hkv, tiles * 1024, d // 8), dtype=np.uint8)
+    shifts = np.arange(32, dtype=np.uint32)
+    for u in range(B * Hkv):
+        # [tile, block, plane] -> bits [tile, block, token-in-block, plane]
+        planes = words[u].transpose(0, 2, 1, 3).reshape(tiles, 32, d)
+        bits = ((planes[:, :, None, :] >> shifts[None, None, :, None]) & 1).astype(np.uint8)
+        bits = bits.reshape(tiles * 1024, d)
+        out[u] = np.packbits(bits.reshape(-1, d // 8, 8), axis=-1, bitorder="little")[..., 0]
+    return out.reshape(B, Hkv, tiles * 1024, d // 8)[:, :, :cap]
+
+
+def encode_gpu(K, sgn, rows, pos0=0):
+    B = K.shape[0]
+    codes = kvr.codes_buffer(shape_of_cache(K), K.device)
     p0 = torch.full((B,), pos0, dtype=torch.int32, device=K.device)
     kvr.kvr_encode_keys(K, p0, rows, sgn, codes)
     return codes
 
 
-def select_gpu(q, K, codes, seq_len, sgn, params):
-    """kvr_select; returns outputs and the inspectable workspace parts (CPU)."""
+def codes_bytes_gpu(codes, K):
     B, Hkv, cap, d = K.shape
+    return planes_to_bytes(codes, B, Hkv, cap, d)
+
+
+def select_gpu(q, K, codes, seq_len, sgn, params):
+    """kvr_select (with coarse scores stored); outputs and workspace parts on the CPU."""
+    B, Hkv, cap, d = K.shape
+    params = kvr.SelectParams(params.C, params.k, params.W, params.lut,
+                              params.flags | kvr.SELECT_STORE_COARSE)
     shape = kvr.Shape.of(K, q)
     ws = kvr.workspace(kvr.kvr_select_workspace_size(shape, params))
     ws.fill_(0xAB)  # stale contents must not matter
@@ -30,7 +59,7 @@ def select_gpu(q, K, codes, seq_len, sgn, params):
     U, C = B * Hkv, params.C
     cap_pad = (cap + 15) // 16 * 16
     wsc = ws.cpu()
-    res = dict(
+    return dict(
         idx=out_idx.cpu().numpy(), count=out_cnt.cpu().numpy(), err=bits,
         coarse=wsc[v["coarse"]:v["coarse"] + U * cap_pad].numpy().reshape(U, cap_pad),
         cand=wsc[v["cand_idx"]:v["cand_idx"] + U * C * 4].view(torch.int32).numpy().reshape(U, C),
@@ -38,11 +67,9 @@ def select_gpu(q, K, codes, seq_len, sgn, params):
         .reshape(U, C),
         cand_count=wsc[v["cand_count"]:v["cand_count"] + U * 4].view(torch.int32).numpy(),
     )
-    return res
 
 
 def attend_gpu(q, K, V, idx, count, seq_len, W, scale):
-    B, Hkv, cap, d = K.shape
     shape = kvr.Shape.of(K, q)
     ws = kvr.workspace(kvr.kvr_attend_workspace_size(shape, idx.shape[-1], W))
     ws.fill_(0xCD)

@@ -54,7 +54,15 @@ def test_workspace_sizes(kvr_lib):
     assert n >= 8 * 131072 + 8 * 8192 * 8
     assert n < 8 * 131072 * 2 + 8 * 8192 * 8 + (1 << 22)
     v = kvr.kvr_select_workspace_views(s, p)
-    assert v["coarse"] == 0 and all(x % 256 == 0 for x in v.values())
+    assert v["coarse"] == 2 ** 64 - 1  # not stored without the flag
+    assert all(x % 256 == 0 for k, x in v.items() if k != "coarse")
+    pc = kvr.SelectParams(8192, 2048, 128, flags=kvr.SELECT_STORE_COARSE)
+    vc = kvr.kvr_select_workspace_views(s, pc)
+    assert vc["coarse"] % 256 == 0
+    assert kvr.kvr_select_workspace_size(s, pc) >= n + 8 * 131072
+    assert kvr.kvr_select_workspace_size(s, kvr.SelectParams(8, 4, 0, flags=2)) == 0
+    assert kvr.kvr_codes_bytes(s) == 8 * 128 * 128 * 128  # 128 tiles of 1024 tokens per unit
+    assert kvr.kvr_codes_bytes(_shape(kvr, cap=1025, d=64)) == 8 * 2 * 64 * 128
     assert kvr.kvr_select_workspace_size(_shape(kvr, d=96), p) == 0
     assert kvr.kvr_select_workspace_size(s, kvr.SelectParams(10, 20, 0)) == 0  # k > C
     assert kvr.kvr_attend_workspace_size(s, 2048, 128) > 0

@@ -13,7 +13,8 @@ import torch
 import oracle
 import workloads as wl
 import sparse_decode_attention_gb300 as kvr
-from gpu_cases import attend_gpu, compare_select_unit, encode_gpu, select_gpu
+from gpu_cases import (attend_gpu, codes_bytes_gpu, compare_select_unit, encode_gpu, select_gpu,
+                       shape_of_cache)
 
 pytestmark = pytest.mark.gpu
 ATOL = 2e-3
@@ -49,22 +50,37 @@ def test_encode_bit_exact(d, dtype):
     K[1, 2, 5, 2:] = 0.0
     K = K.to(dtype)
     sgn = wl.srht_signs(d)
-    codes = encode_gpu(K.cuda(), sgn.cuda(), cap).cpu().numpy()
+    Kd = K.cuda()
+    codes = codes_bytes_gpu(encode_gpu(Kd, sgn.cuda(), cap), Kd)
     ref = oracle.encode(K, sgn.numpy())
     assert np.array_equal(codes, ref)
+
+
+def test_encode_in_pieces_matches_one_pass():
+    """Appending one row at a time, or ranges that start and end inside 32-token
+    blocks, leaves the same codes as encoding everything at once."""
+    d = 128
+    K = torch.randn((1, 2, 2100, d)).to(torch.bfloat16).cuda()
+    sgn = wl.srht_signs(d).cuda()
+    whole = codes_bytes_gpu(encode_gpu(K, sgn, 2100), K)
+    codes = kvr.codes_buffer(shape_of_cache(K))
+    for p0, n in [(0, 5), (5, 1), (6, 57), (63, 1000), (1063, 1), (1064, 1036)]:
+        kvr.kvr_encode_keys(K, torch.tensor([p0], dtype=torch.int32, device="cuda"), n, sgn,
+                            codes)
+    assert np.array_equal(codes_bytes_gpu(codes, K), whole)
 
 
 def test_encode_rows_window_and_bad_position():
     d = 128
     K = torch.randn((2, 2, 300, d)).to(torch.bfloat16).cuda()
     sgn = wl.srht_signs(d).cuda()
-    codes = torch.zeros((2, 2, 300, d // 8), dtype=torch.uint8, device="cuda")
+    codes = kvr.codes_buffer(shape_of_cache(K))
     pos0 = torch.tensor([10, 295], dtype=torch.int32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     kvr.kvr_encode_keys(K, pos0, 7, sgn, codes, err)
     assert kvr.kvr_read_error(err) == kvr.DEVERR["position"]  # rows 300, 301 of batch 1
     ref = oracle.encode(K.cpu(), sgn.cpu().numpy())
-    c = codes.cpu().numpy()
+    c = codes_bytes_gpu(codes, K)
     assert np.array_equal(c[0, :, 10:17], ref[0, :, 10:17])
     assert np.array_equal(c[1, :, 295:300], ref[1, :, 295:300])
     assert not c[0, :, :10].any() and not c[0, :, 17:].any() and not c[1, :, :295].any()
@@ -81,7 +97,7 @@ def run_and_compare(K, q, seq, params, sgn, units=None, check_diag=True):
     seq_d = torch.tensor(seq, dtype=torch.int32, device="cuda")
     res = select_gpu(qd, Kd, codes, seq_d, sgn_d, params)
     ref_codes = oracle.encode(K, sgn.numpy())
-    assert np.array_equal(codes.cpu().numpy(), ref_codes)
+    assert np.array_equal(codes_bytes_gpu(codes, Kd), ref_codes)
     out = {}
     for u in (units if units is not None else range(B * Hkv)):
         b, h = divmod(u, Hkv)
