@@ -23,7 +23,8 @@ kvr_status check_shape(const kvr_shape *s)
     if (s->Hq % s->Hkv != 0) return KVR_ERR_INVALID_ARG;
     if (s->d != 64 && s->d != 128) return KVR_ERR_UNSUPPORTED;
     if (s->dtype != KVR_BF16 && s->dtype != KVR_F32) return KVR_ERR_UNSUPPORTED;
-    if (s->Hq / s->Hkv > 16) return KVR_ERR_UNSUPPORTED;
+    const int G = s->Hq / s->Hkv;
+    if (G > 16 || (G & (G - 1)) != 0) return KVR_ERR_UNSUPPORTED;  // 1, 2, 4, 8, 16
     if ((int64_t)s->B * s->Hkv > 65535) return KVR_ERR_UNSUPPORTED;  // grid.y
     if (s->cap > ((int64_t)1 << 31) - 1) return KVR_ERR_UNSUPPORTED;  // int32 indices
     return KVR_OK;
@@ -110,22 +111,12 @@ SelectPlan plan_select(const kvr_shape &s, const kvr_select_params &p)
 
 AttendPlan plan_attend(const kvr_shape &s, int kmax, int W)
 {
+    // the cluster kernel merges its partials in distributed shared memory
+    (void)s;
+    (void)kmax;
+    (void)W;
     AttendPlan pl;
-    const int64_t U = (int64_t)s.B * s.Hkv;
-    const int G = s.Hq / s.Hkv;
-    pl.tpc = 128;
-    const int64_t most = (int64_t)kmax + W;  // a unit never attends more tokens
-    pl.nsplit = (int)std::max<int64_t>(1, (most + pl.tpc - 1) / pl.tpc);
-    size_t o = 0;
-    auto take = [&](size_t bytes) {
-        const size_t at = o;
-        o = align_up(o + bytes, 256);
-        return at;
-    };
-    pl.off_m = take((size_t)U * pl.nsplit * G * 4);
-    pl.off_l = take((size_t)U * pl.nsplit * G * 4);
-    pl.off_o = take((size_t)U * pl.nsplit * G * s.d * 4);
-    pl.bytes = o;
+    pl.bytes = 0;
     return pl;
 }
 
@@ -229,7 +220,7 @@ kvr_status kvr_sparse_attend(const kvr_shape *shape, const void *q, const void *
     kvr_status st = check_shape(shape);
     if (st != KVR_OK) return st;
     if (kmax < 0 || W < 0) return KVR_ERR_INVALID_ARG;
-    if (!q || !K || !V || !count || !seq_len || !out || !workspace) return KVR_ERR_INVALID_ARG;
+    if (!q || !K || !V || !count || !seq_len || !out) return KVR_ERR_INVALID_ARG;
     if (kmax > 0 && !idx) return KVR_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)

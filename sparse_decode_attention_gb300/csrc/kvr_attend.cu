@@ -1,35 +1,39 @@
 // kvr_attend.cu -- fused gather + online-softmax GQA attention over the
-// selected tokens plus the local window (kvr_sparse_attend).
+// selected tokens plus the local window (kvr_sparse_attend), one launch.
 //
 // ParisKV, "Problematica": decode attends only to a top-k subset of past
 // tokens; "Meccanismo di Aggiornamento a Finestra Scorrevole": the most
 // recent tokens stay in a local region that is always attended.
 //
-// Split-K ("flash-decoding") layout: the token list of a unit (selected
-// indices, then the window) is cut into segments of kTPC tokens; one CTA per
-// (segment, unit) stages the K and V rows of its segment into shared memory
-// with 16-byte cp.async copies (rows padded by 16 bytes so that 8 lanes
-// reading 8 different rows hit 8 different bank groups), then walks the
-// segment in tiles of 32 tokens: one warp computes the 32 logits of one
-// query head, updates that head's running max / sum, and all threads
-// accumulate p * v in registers (thread = one dim of a group of heads). The
-// partial (m, l, o) of every CTA goes to the workspace and combine_kernel
-// merges the partials of a unit.
+// One thread-block cluster per (batch, kv head) unit. The unit's token list
+// (selected indices, then the window) is cut into equal slices, one per CTA.
+// A CTA bulk-copies the K and V rows of its slice, in batches of 32 KB, into
+// double-buffered shared memory (mbarrier completion, bounded waits). Each
+// warp takes a strided share of a batch: a token's K row is spread over the
+// 32 lanes (d/32 dims each), the G per-head partial dots are reduced with a
+// butterfly that hands head h to lanes [h*32/G, (h+1)*32/G), the softmax
+// state is updated once per batch (log2 domain), and p*v is accumulated in
+// registers for all heads. Warps merge in shared memory, CTAs merge their
+// (max, sum, output) partials through distributed shared memory, each CTA
+// finishing an equal share of the output.
+#include <cooperative_groups.h>
+
 #include "kvr_device.cuh"
 #include "kvr_launch.h"
 
+namespace cg = cooperative_groups;
+
 namespace kvr {
 
-constexpr int kTPC = 128;   // tokens per CTA
-constexpr int kTile = 32;   // tokens per softmax tile
-constexpr int kAttThreads = 128;
+constexpr int kAttThreads = 256;
+constexpr int kAttWarps = kAttThreads / 32;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct AttArgs {
-    int Hq, Hkv, G;
+    int Hq, Hkv;
     int64_t cap;
-    int W, kmax, nsplit;
-    float scale_log2;  // scale * log2(e): logits are kept in the log2 domain
+    int W, kmax;
+    float scale_log2;  // scale * log2(e)
     const void *q;
     const void *K;
     const void *V;
@@ -37,242 +41,323 @@ struct AttArgs {
     const int32_t *count;
     const int32_t *seq_len;
     float *out;
-    float *part_m, *part_l, *part_o;  // [U][nsplit][G], [U][nsplit][G], [U][nsplit][G][D]
     int32_t *err;
 };
 
-__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes)
-{
-    const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
-
-// Number of tokens a unit attends to and the start of its window.
-__device__ __forceinline__ void unit_tokens(const AttArgs &a, int u, int64_t &w0, int &cnt,
-                                            int64_t &nT, bool report)
-{
-    const int b = u / a.Hkv;
-    int64_t N = a.seq_len[b];
-    if (N < 0 || N > a.cap) {
-        if (report) set_err(a.err, KVR_DEVERR_SEQ_LEN);
-        N = 0;
-    }
-    w0 = N > a.W ? N - a.W : 0;
-    cnt = max(0, min(a.count[u], a.kmax));
-    nT = cnt + (N - w0);
-}
-
-template <int D, typename T> struct AttSmem {
+template <int D, typename T, int G> struct AttCfg {
     static constexpr int kRowBytes = D * (int)sizeof(T);
-    static constexpr int kRowStride = kRowBytes + 16;
-    static constexpr int kChunks = kRowBytes / 16;
-    static constexpr size_t kKV = (size_t)kTPC * kRowStride;  // one of K, V
-    static constexpr size_t bytes(int G)
-    {
-        return 2 * kKV + (size_t)G * D * 4 + 2 * (size_t)G * kTile * 4 + 3 * (size_t)G * 4 +
-               kTPC * 4;
-    }
+    static constexpr int kTok = 16384 / kRowBytes;  // tokens per batch (K + V = 32 KB)
+    static constexpr int kBatchBytes = 2 * kTok * kRowBytes;
+    static constexpr int kE = D / 32;  // dims per lane
+    static constexpr int kWarpPart = kAttWarps * G * (D + 2) * 4;
+    static constexpr int kBufBytes =
+        (2 * kBatchBytes > kWarpPart) ? 2 * kBatchBytes : kWarpPart;
+    static constexpr int oTok = kBufBytes;             // [2][kTok] int32
+    static constexpr int oPm = oTok + 2 * kTok * 4;    // [G]
+    static constexpr int oPl = oPm + 16 * 4;           // [G]
+    static constexpr int oPo = oPl + 16 * 4;           // [G][D]
+    static constexpr int oBar = oPo + G * D * 4;       // 2 mbarriers
+    static constexpr int bytes = oBar + 16;
+    static_assert(kTok % kAttWarps == 0 && kTok <= kAttThreads, "batch split");
 };
 
-template <int D, typename T>
-__global__ void __launch_bounds__(kAttThreads) attend_partial_kernel(AttArgs a)
+template <int E, typename T>
+__device__ __forceinline__ void load_lane(const uint8_t *row, int lane, float (&x)[E])
 {
-    using SM = AttSmem<D, T>;
-    constexpr int E = Elem<T>::kVec;  // elements per 16-byte chunk
-    constexpr int HG = kAttThreads / D;  // head groups in the V accumulation (1 or 2)
-    constexpr int MAXH = 16 / HG;        // accumulators per thread (G <= 16)
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint8_t *sK = smem;
-    uint8_t *sV = smem + SM::kKV;
-    float *sQ = reinterpret_cast<float *>(smem + 2 * SM::kKV);  // [G][D], pre-scaled
-    float *sLogit = sQ + a.G * D;                                  // [G][kTile]
-    float *sP = sLogit + a.G * kTile;                              // [G][kTile]
-    float *sM = sP + a.G * kTile;                                  // [G]
-    float *sL = sM + a.G;                                          // [G]
-    float *sAlpha = sL + a.G;                                      // [G]
-    int32_t *sTok = reinterpret_cast<int32_t *>(sAlpha + a.G);     // [kTPC]
-
-    const int u = blockIdx.y, s = blockIdx.x, tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5;
-    const int b = u / a.Hkv, h = u % a.Hkv;
-    const int G = a.G;
-    int64_t w0, nT;
-    int cnt;
-    unit_tokens(a, u, w0, cnt, nT, s == 0 && tid == 0 && h == 0);
-    const int64_t seg0 = (int64_t)s * kTPC;
-    const int ntok = (int)max((int64_t)0, min(nT - seg0, (int64_t)kTPC));
-    const size_t pbase = ((size_t)u * a.nsplit + s) * G;
-    if (ntok == 0) {
-        for (int i = tid; i < G; i += blockDim.x) {
-            a.part_m[pbase + i] = -INFINITY;
-            a.part_l[pbase + i] = 0.0f;
-        }
-        for (int i = tid; i < G * D; i += blockDim.x) a.part_o[pbase * D + i] = 0.0f;
-        return;
+    const T *p = reinterpret_cast<const T *>(row) + lane * E;
+    if constexpr (sizeof(T) == 2 && E == 2) {
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(p);
+        x[0] = bf16_lo(w);
+        x[1] = bf16_hi(w);
+    } else if constexpr (sizeof(T) == 4 && E == 2) {
+        const float2 v = *reinterpret_cast<const float2 *>(p);
+        x[0] = v.x;
+        x[1] = v.y;
+    } else {
+        widen<E>(p, x);
     }
+}
 
-    // token ids of the segment (-1 = skipped)
-    for (int j = tid; j < kTPC; j += blockDim.x) {
+// Sum G per-lane values over the warp; lane l returns the total of head
+// l / (32 / G). Splitting halves of the value set between partner lanes costs
+// G - 1 + 5 - log2(G) shuffles instead of 5G.
+template <int G>
+__device__ __forceinline__ float reduce_heads(float (&v)[G], int lane)
+{
+    constexpr int LG = (G >= 16) ? 4 : (G >= 8) ? 3 : (G >= 4) ? 2 : (G >= 2) ? 1 : 0;
+#pragma unroll
+    for (int s = 0; s < LG; s++) {
+        const int o = 16 >> s;
+        const int half = G >> (s + 1);
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < half; i++) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(kFull, send, o);
+        }
+    }
+    float x = v[0];
+#pragma unroll
+    for (int o = 16 >> LG; o >= 1; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+    return x;
+}
+
+template <int D, typename T, int G>
+__global__ void __launch_bounds__(kAttThreads, (G >= 16) ? 1 : 2) attend_kernel(AttArgs a)
+{
+    using CF = AttCfg<D, T, G>;
+    constexpr int E = CF::kE;
+    constexpr int RB = CF::kRowBytes;
+    constexpr int TOK = CF::kTok;
+    constexpr int TPW = TOK / kAttWarps;  // tokens per warp per batch
+    constexpr int LPH = 32 / G;           // lanes per head after the reduction
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    int32_t *sTok = reinterpret_cast<int32_t *>(smem + CF::oTok);
+    float *sPm = reinterpret_cast<float *>(smem + CF::oPm);
+    float *sPl = reinterpret_cast<float *>(smem + CF::oPl);
+    float *sPo = reinterpret_cast<float *>(smem + CF::oPo);
+    uint64_t *sBar = reinterpret_cast<uint64_t *>(smem + CF::oBar);
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int CS = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int u = blockIdx.y;
+    const int b = u / a.Hkv, hk = u % a.Hkv;
+
+    int64_t N = a.seq_len[b];
+    if (N < 0 || N > a.cap) {
+        if (rank == 0 && tid == 0 && hk == 0) set_err(a.err, KVR_DEVERR_SEQ_LEN);
+        N = 0;
+    }
+    const int64_t w0 = N > a.W ? N - a.W : 0;
+    const int cnt = max(0, min(a.count[u], a.kmax));
+    const int64_t nT = cnt + (N - w0);
+    const int64_t lo = (int64_t)rank * nT / CS, hi = (int64_t)(rank + 1) * nT / CS;
+    const int n = (int)(hi - lo);
+    const int nbatch = (n + TOK - 1) / TOK;
+
+    if (tid == 0) {
+        mbar_init(&sBar[0], 1);
+        mbar_init(&sBar[1], 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    const uint8_t *Ku = static_cast<const uint8_t *>(a.K) + (size_t)u * a.cap * RB;
+    const uint8_t *Vu = static_cast<const uint8_t *>(a.V) + (size_t)u * a.cap * RB;
+    // token ids of batch bi, then the bulk copies of their K and V rows
+    auto issue = [&](int bi) {
+        int32_t *tok = sTok + (bi & 1) * TOK;
+        uint8_t *buf = smem + (bi & 1) * CF::kBatchBytes;
         int32_t t = -1;
-        if (j < ntok) {
-            const int64_t p = seg0 + j;
-            if (p < cnt) {
-                t = a.idx[(int64_t)u * a.kmax + p];
-                if (t < 0 || t >= w0) {
-                    set_err(a.err, KVR_DEVERR_INDEX);
-                    t = -1;
+        if (tid < TOK) {
+            const int64_t p = lo + (int64_t)bi * TOK + tid;
+            if (p < hi) {
+                if (p < cnt) {
+                    t = a.idx[(size_t)u * a.kmax + p];
+                    if (t < 0 || t >= w0) {
+                        set_err(a.err, KVR_DEVERR_INDEX);
+                        t = -1;
+                    }
+                } else {
+                    t = (int32_t)(w0 + (p - cnt));
                 }
-            } else {
-                t = (int32_t)(w0 + (p - cnt));
+            }
+            tok[tid] = t;
+        }
+        const int nvalid = __syncthreads_count(t >= 0);
+        if (tid == 0) mbar_arrive_expect_tx(&sBar[bi & 1], (uint32_t)(nvalid * 2 * RB));
+        __syncthreads();
+        if (t >= 0) {
+            bulk_g2s(buf + tid * RB, Ku + (size_t)t * RB, RB, &sBar[bi & 1]);
+            bulk_g2s(buf + (TOK + tid) * RB, Vu + (size_t)t * RB, RB, &sBar[bi & 1]);
+        }
+    };
+    if (nbatch > 0) issue(0);
+    if (nbatch > 1) issue(1);
+
+    // the group's query heads, pre-scaled into the log2 domain
+    float qr[G][E];
+    {
+        const T *qg = static_cast<const T *>(a.q) + ((size_t)b * a.Hq + (size_t)hk * G) * D;
+#pragma unroll
+        for (int g = 0; g < G; g++)
+#pragma unroll
+            for (int e = 0; e < E; e++) qr[g][e] = to_f32(qg[g * D + lane * E + e]) * a.scale_log2;
+    }
+    float acc[G][E];
+#pragma unroll
+    for (int g = 0; g < G; g++)
+#pragma unroll
+        for (int e = 0; e < E; e++) acc[g][e] = 0.0f;
+    float m = -INFINITY, l = 0.0f;  // softmax state of head lane / LPH
+
+    for (int bi = 0; bi < nbatch; bi++) {
+        mbar_wait(&sBar[bi & 1], (uint32_t)((bi >> 1) & 1), a.err);
+        const int32_t *tok = sTok + (bi & 1) * TOK;
+        const uint8_t *buf = smem + (bi & 1) * CF::kBatchBytes;
+        const int rows = min(TOK, n - bi * TOK);
+        float s[TPW];
+#pragma unroll
+        for (int jj = 0; jj < TPW; jj++) {
+            const int j = warp + jj * kAttWarps;
+            s[jj] = -INFINITY;
+            if (j < rows && tok[j] >= 0) {  // warp-uniform
+                float kv[E];
+                load_lane<E, T>(buf + j * RB, lane, kv);
+                float part[G];
+#pragma unroll
+                for (int g = 0; g < G; g++) {
+                    float d = 0.0f;
+#pragma unroll
+                    for (int e = 0; e < E; e++) d = fmaf(qr[g][e], kv[e], d);
+                    part[g] = d;
+                }
+                s[jj] = reduce_heads<G>(part, lane);
             }
         }
-        sTok[j] = t;
+        float mb = -INFINITY;
+#pragma unroll
+        for (int jj = 0; jj < TPW; jj++) mb = fmaxf(mb, s[jj]);
+        const float m_new = fmaxf(m, mb);
+        const float alpha = (m == -INFINITY) ? 0.0f : exp2f(m - m_new);
+        float p[TPW], ps = 0.0f;
+#pragma unroll
+        for (int jj = 0; jj < TPW; jj++) {
+            p[jj] = (s[jj] == -INFINITY) ? 0.0f : exp2f(s[jj] - m_new);
+            ps += p[jj];
+        }
+        l = l * alpha + ps;
+        m = m_new;
+#pragma unroll
+        for (int g = 0; g < G; g++) {
+            const float ag = __shfl_sync(kFull, alpha, g * LPH);
+#pragma unroll
+            for (int e = 0; e < E; e++) acc[g][e] *= ag;
+        }
+#pragma unroll
+        for (int jj = 0; jj < TPW; jj++) {
+            const int j = warp + jj * kAttWarps;
+            if (j < rows && tok[j] >= 0) {
+                float vv[E];
+                load_lane<E, T>(buf + (TOK + j) * RB, lane, vv);
+#pragma unroll
+                for (int g = 0; g < G; g++) {
+                    const float pg = __shfl_sync(kFull, p[jj], g * LPH);
+#pragma unroll
+                    for (int e = 0; e < E; e++) acc[g][e] = fmaf(pg, vv[e], acc[g][e]);
+                }
+            }
+        }
+        fence_proxy_async();
+        __syncthreads();
+        if (bi + 2 < nbatch) issue(bi + 2);
+    }
+
+    // merge the warps (their partials reuse the batch buffers)
+    float *sWm = reinterpret_cast<float *>(smem);  // [warps][G]
+    float *sWl = sWm + kAttWarps * G;              // [warps][G]
+    float *sWo = sWl + kAttWarps * G;              // [warps][G][D]
+    __syncthreads();
+    if ((lane % LPH) == 0) {
+        sWm[warp * G + lane / LPH] = m;
+        sWl[warp * G + lane / LPH] = l;
+    }
+#pragma unroll
+    for (int g = 0; g < G; g++)
+#pragma unroll
+        for (int e = 0; e < E; e++) sWo[(warp * G + g) * D + lane * E + e] = acc[g][e];
+    __syncthreads();
+    for (int t = tid; t < G * D; t += kAttThreads) {
+        const int g = t / D, dim = t % D;
+        float M = -INFINITY;
+        for (int w = 0; w < kAttWarps; w++) M = fmaxf(M, sWm[w * G + g]);
+        float L = 0.0f, O = 0.0f;
+        if (M != -INFINITY) {
+            for (int w = 0; w < kAttWarps; w++) {
+                const float mw = sWm[w * G + g];
+                if (mw == -INFINITY) continue;
+                const float f = exp2f(mw - M);
+                L = fmaf(sWl[w * G + g], f, L);
+                O = fmaf(sWo[(w * G + g) * D + dim], f, O);
+            }
+        }
+        sPo[t] = O;
+        if (dim == 0) {
+            sPm[g] = M;
+            sPl[g] = L;
+        }
     }
     __syncthreads();
+    cluster.sync();  // CTA partials published
 
-    // stage K and V rows (zero-filled for skipped slots)
-    const uint8_t *Kb = static_cast<const uint8_t *>(a.K) + (size_t)u * a.cap * SM::kRowBytes;
-    const uint8_t *Vb = static_cast<const uint8_t *>(a.V) + (size_t)u * a.cap * SM::kRowBytes;
-    const int nrows = (ntok + kTile - 1) / kTile * kTile;
-    for (int e = tid; e < nrows * SM::kChunks; e += blockDim.x) {
-        const int j = e / SM::kChunks, ch = e % SM::kChunks;
-        const int32_t t = sTok[j];
-        const size_t go = (t >= 0 ? (size_t)t * SM::kRowBytes : 0) + (size_t)ch * 16;
-        const int nb = t >= 0 ? 16 : 0;
-        cp_async16(sK + (size_t)j * SM::kRowStride + ch * 16, Kb + go, nb);
-        cp_async16(sV + (size_t)j * SM::kRowStride + ch * 16, Vb + go, nb);
+    // every CTA finishes an equal share of the unit's G*D outputs
+    const int e0 = rank * (G * D) / CS, e1 = (rank + 1) * (G * D) / CS;
+    for (int t = e0 + tid; t < e1; t += kAttThreads) {
+        const int g = t / D, dim = t % D;
+        float M = -INFINITY;
+        for (int r = 0; r < CS; r++) M = fmaxf(M, *cluster.map_shared_rank(&sPm[g], r));
+        float L = 0.0f, O = 0.0f;
+        if (M != -INFINITY) {
+            for (int r = 0; r < CS; r++) {
+                const float mr = *cluster.map_shared_rank(&sPm[g], r);
+                if (mr == -INFINITY) continue;
+                const float f = exp2f(mr - M);
+                L = fmaf(*cluster.map_shared_rank(&sPl[g], r), f, L);
+                O = fmaf(*cluster.map_shared_rank(&sPo[t], r), f, O);
+            }
+        }
+        a.out[((size_t)b * a.Hq + (size_t)hk * G + g) * D + dim] = (L > 0.0f) ? O / L : 0.0f;
     }
-    cp_async_commit();
-
-    // query heads of the group, pre-multiplied by scale * log2(e)
-    const T *qg = static_cast<const T *>(a.q) + ((int64_t)b * a.Hq + (int64_t)h * G) * D;
-    for (int i = tid; i < G * D; i += blockDim.x) sQ[i] = to_f32(qg[i]) * a.scale_log2;
-    for (int i = tid; i < G; i += blockDim.x) {
-        sM[i] = -INFINITY;
-        sL[i] = 0.0f;
-    }
-    cp_async_wait_all();
     __syncthreads();
-
-    const int dim = tid % D, hg = tid / D;
-    float acc[MAXH];
-#pragma unroll
-    for (int i = 0; i < MAXH; i++) acc[i] = 0.0f;
-
-    for (int t0 = 0; t0 < ntok; t0 += kTile) {
-        // logits: thread -> (head, token) pairs; a warp shares one head
-        for (int jd = tid; jd < G * kTile; jd += blockDim.x) {
-            const int hh = jd / kTile, tt = jd % kTile;
-            float lg = -INFINITY;
-            if (t0 + tt < ntok && sTok[t0 + tt] >= 0) {
-                const uint8_t *row = sK + (size_t)(t0 + tt) * SM::kRowStride;
-                const float *qh = sQ + hh * D;
-                float dot = 0.0f;
-#pragma unroll
-                for (int ch = 0; ch < SM::kChunks; ch++) {
-                    float kv[E];
-                    widen<E>(reinterpret_cast<const T *>(row + ch * 16), kv);
-#pragma unroll
-                    for (int e2 = 0; e2 < E; e2++) dot = fmaf(qh[ch * E + e2], kv[e2], dot);
-                }
-                lg = dot;
-            }
-            sLogit[jd] = lg;
-        }
-        __syncthreads();
-        // online softmax update, one warp per head
-        for (int hh = warp; hh < G; hh += blockDim.x / 32) {
-            const float x = sLogit[hh * kTile + lane];
-            float mt = x;
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, o));
-            const float m_old = sM[hh];
-            const float m_new = fmaxf(m_old, mt);
-            const float p = (x == -INFINITY) ? 0.0f : exp2f(x - m_new);
-            const float alpha = (m_old == -INFINITY) ? 0.0f : exp2f(m_old - m_new);
-            float ps = p;
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) ps += __shfl_xor_sync(kFull, ps, o);
-            sP[hh * kTile + lane] = p;
-            __syncwarp();
-            if (lane == 0) {
-                sL[hh] = sL[hh] * alpha + ps;
-                sM[hh] = m_new;
-                sAlpha[hh] = alpha;
-            }
-        }
-        __syncthreads();
-        // o += p * v; this thread owns dim `dim` of heads hg, hg + HG, ...
-        const int tmax = min(kTile, ntok - t0);
-#pragma unroll
-        for (int i = 0; i < MAXH; i++) {
-            const int hh = hg + i * HG;
-            if (hh < G) acc[i] *= sAlpha[hh];
-        }
-        for (int tt = 0; tt < tmax; tt++) {
-            const T *vrow = reinterpret_cast<const T *>(sV + (size_t)(t0 + tt) * SM::kRowStride);
-            const float v = to_f32(vrow[dim]);
-#pragma unroll
-            for (int i = 0; i < MAXH; i++) {
-                const int hh = hg + i * HG;
-                if (hh < G) acc[i] = fmaf(sP[hh * kTile + tt], v, acc[i]);
-            }
-        }
-        __syncthreads();
-    }
-    for (int i = tid; i < G; i += blockDim.x) {
-        a.part_m[pbase + i] = sM[i];
-        a.part_l[pbase + i] = sL[i];
-    }
-#pragma unroll
-    for (int i = 0; i < MAXH; i++) {
-        const int hh = hg + i * HG;
-        if (hh < G) a.part_o[(pbase + hh) * D + dim] = acc[i];
-    }
+    cluster.sync();  // no CTA leaves while another may read its shared memory
 }
 
-// Merge the nsplit partials of each (unit, head): out = sum_s 2^(m_s - M) o_s /
-// sum_s 2^(m_s - M) l_s, M = max_s m_s; an empty unit gives zeros.
-template <int D>
-__global__ void __launch_bounds__(D) combine_kernel(AttArgs a)
+int attend_cluster_size(int U, int64_t most_tokens)
 {
-    const int u = blockIdx.y, hh = blockIdx.x, dim = threadIdx.x;
-    const int G = a.G;
-    const int b = u / a.Hkv, h = u % a.Hkv;
-    float M = -INFINITY;
-    for (int s = 0; s < a.nsplit; s++)
-        M = fmaxf(M, a.part_m[((size_t)u * a.nsplit + s) * G + hh]);
-    float L = 0.0f, o = 0.0f;
-    if (M != -INFINITY) {
-        for (int s = 0; s < a.nsplit; s++) {
-            const size_t pi = ((size_t)u * a.nsplit + s) * G + hh;
-            const float m = a.part_m[pi];
-            if (m == -INFINITY) continue;
-            const float f = exp2f(m - M);
-            L = fmaf(a.part_l[pi], f, L);
-            o = fmaf(a.part_o[pi * D + dim], f, o);
-        }
-    }
-    a.out[((size_t)b * a.Hq + (size_t)h * G + hh) * D + dim] = (L > 0.0f) ? o / L : 0.0f;
+    int cs = 16;
+    while (cs > 1 && (int64_t)U * cs > 2 * 152) cs >>= 1;
+    while (cs > 1 && most_tokens < (int64_t)cs * 32) cs >>= 1;  // >= 32 tokens per CTA
+    return cs;
+}
+
+template <int D, typename T, int G>
+static kvr_status launch_attend_g(const LaunchCtx &c, const AttArgs &a, int cs)
+{
+    auto kern = attend_kernel<D, T, G>;
+    const int smem = AttCfg<D, T, G>::bytes;
+    kvr_status st = prepare_cluster_kernel(reinterpret_cast<const void *>(kern), smem);
+    if (st != KVR_OK) return st;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs, c.shape.B * c.shape.Hkv, 1);
+    cfg.blockDim = dim3(kAttThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return KVR_ERR_CUDA;
+    return check_launch();
 }
 
 template <int D, typename T>
-static kvr_status launch_attend(const LaunchCtx &c, AttArgs &a)
+static kvr_status launch_attend(const LaunchCtx &c, const AttArgs &a, int cs, int G)
 {
-    const int U = c.shape.B * c.shape.Hkv;
-    const size_t smem = AttSmem<D, T>::bytes(a.G);
-    if (smem > 48 * 1024) {
-        kvr_status st = raise_smem_limit(reinterpret_cast<const void *>(attend_partial_kernel<D, T>),
-                                         (int)AttSmem<D, T>::bytes(16));
-        if (st != KVR_OK) return st;
+    switch (G) {
+    case 1: return launch_attend_g<D, T, 1>(c, a, cs);
+    case 2: return launch_attend_g<D, T, 2>(c, a, cs);
+    case 4: return launch_attend_g<D, T, 4>(c, a, cs);
+    case 8: return launch_attend_g<D, T, 8>(c, a, cs);
+    case 16: return launch_attend_g<D, T, 16>(c, a, cs);
     }
-    attend_partial_kernel<D, T><<<dim3(a.nsplit, U), kAttThreads, smem, c.stream>>>(a);
-    combine_kernel<D><<<dim3(a.G, U), D, 0, c.stream>>>(a);
-    return check_launch();
+    return KVR_ERR_UNSUPPORTED;
 }
 
 kvr_status attend_dispatch(const LaunchCtx &c, const AttendPlan &plan, const void *q,
@@ -280,14 +365,14 @@ kvr_status attend_dispatch(const LaunchCtx &c, const AttendPlan &plan, const voi
                            const int32_t *count, const int32_t *seq_len, int W, float scale,
                            float *out, uint8_t *ws, int32_t *err)
 {
+    (void)plan;
+    (void)ws;
     AttArgs a;
     a.Hq = c.shape.Hq;
     a.Hkv = c.shape.Hkv;
-    a.G = c.shape.Hq / c.shape.Hkv;
     a.cap = c.shape.cap;
     a.W = W;
     a.kmax = kmax;
-    a.nsplit = plan.nsplit;
     a.scale_log2 = scale * kLog2e;
     a.q = q;
     a.K = K;
@@ -296,14 +381,15 @@ kvr_status attend_dispatch(const LaunchCtx &c, const AttendPlan &plan, const voi
     a.count = count;
     a.seq_len = seq_len;
     a.out = out;
-    a.part_m = reinterpret_cast<float *>(ws + plan.off_m);
-    a.part_l = reinterpret_cast<float *>(ws + plan.off_l);
-    a.part_o = reinterpret_cast<float *>(ws + plan.off_o);
     a.err = err;
+    const int G = c.shape.Hq / c.shape.Hkv;
+    const int cs = attend_cluster_size(c.shape.B * c.shape.Hkv, (int64_t)kmax + W);
     const bool bf = c.shape.dtype == KVR_BF16;
     if (c.shape.d == 128)
-        return bf ? launch_attend<128, __nv_bfloat16>(c, a) : launch_attend<128, float>(c, a);
-    return bf ? launch_attend<64, __nv_bfloat16>(c, a) : launch_attend<64, float>(c, a);
+        return bf ? launch_attend<128, __nv_bfloat16>(c, a, cs, G)
+                  : launch_attend<128, float>(c, a, cs, G);
+    return bf ? launch_attend<64, __nv_bfloat16>(c, a, cs, G)
+              : launch_attend<64, float>(c, a, cs, G);
 }
 
 }  // namespace kvr

@@ -107,7 +107,41 @@ __device__ __forceinline__ uint32_t sign_word(const float (&x)[E], int gl)
     return v;
 }
 
-// ---------------------------------------------------------------- scans
+// ---------------------------------------------------------------- warp scans
+
+__device__ __forceinline__ int warp_sum(int x)
+{
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+    return x;
+}
+
+// Exclusive prefix sum over the lanes of a warp.
+__device__ __forceinline__ int warp_exclusive_scan(int x)
+{
+    const int lane = threadIdx.x & 31;
+    int s = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, s, o);
+        if (lane >= o) s += y;
+    }
+    return s - x;
+}
+
+// Inclusive suffix sum over the lanes: lane l gets x[l] + x[l+1] + ... + x[31].
+__device__ __forceinline__ int warp_suffix_sum(int x)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_down_sync(kFull, x, o);
+        if (lane + o < 32) x += y;
+    }
+    return x;
+}
+
+// ---------------------------------------------------------------- block scans
 
 // Exclusive prefix sum over the block of one value per thread; *total gets
 // the block sum. blockDim.x must be a multiple of 32, <= 1024. scratch holds

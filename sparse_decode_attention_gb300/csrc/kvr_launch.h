@@ -44,10 +44,7 @@ struct SelectPlan {
 SelectPlan plan_select(const kvr_shape &s, const kvr_select_params &p);
 
 struct AttendPlan {
-    int tpc;     // tokens per CTA
-    int nsplit;  // CTAs per unit
-    size_t off_m, off_l, off_o;
-    size_t bytes;
+    size_t bytes;  // workspace bytes (0: partials merge on chip)
 };
 AttendPlan plan_attend(const kvr_shape &s, int kmax, int W);
 

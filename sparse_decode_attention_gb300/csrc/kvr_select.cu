@@ -348,22 +348,23 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         sAll[r * 16 + v] = *cluster.map_shared_rank(&sH1[v], r);
     }
     __syncthreads();
-    if (tid == 0) {
-        int u1 = -1, rem = Cp, cum = 0;
+    if (warp == 0) {
+        // lane v: cluster-wide count of bucket v; the C'-th key sits in the
+        // highest bucket whose suffix count reaches C'
+        int tot = 0;
+        if (lane < NL1)
+            for (int r = 0; r < CS; r++) tot += sAll[r * 16 + lane];
+        const int suf = warp_suffix_sum(tot);
+        int u1 = -1, rem = Cp;
         if (Cp > 0) {
-            for (int v = NL1 - 1; v >= 0; v--) {
-                int tot = 0;
-                for (int r = 0; r < CS; r++) tot += sAll[r * 16 + v];
-                if (cum + tot >= Cp) {
-                    u1 = v;
-                    rem = Cp - cum;
-                    break;
-                }
-                cum += tot;
-            }
+            const unsigned ok = __ballot_sync(kFull, lane < NL1 && suf >= Cp);
+            u1 = __popc(ok) - 1;
+            rem = Cp - __shfl_sync(kFull, suf - tot, u1);
         }
-        sMisc[M_U1] = u1;
-        sMisc[M_REM1] = rem;
+        if (lane == 0) {
+            sMisc[M_U1] = u1;
+            sMisc[M_REM1] = rem;
+        }
     }
     __syncthreads();
     const int u1 = sMisc[M_U1];
@@ -402,41 +403,37 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         sAll[256 + r * 16 + v] = *cluster.map_shared_rank(&sH2[v], r);
     }
     __syncthreads();
-    if (tid == 0) {
+    if (warp == 0) {
         int Tthr = 1 << 30, take = 0, off = 0;
         if (u1 >= 0) {
             const int rem = sMisc[M_REM1];
-            int cum = 0, v2 = 0;
-            for (int v = NL2 - 1; v >= 0; v--) {
-                int tot = 0;
-                for (int r = 0; r < CS; r++) tot += sAll[256 + r * 16 + v];
-                if (cum + tot >= rem) {
-                    v2 = v;
-                    break;
-                }
-                cum += tot;
-            }
-            const int quota = rem - cum;  // ties at T taken, lowest indices first
+            int tot = 0;
+            if (lane < NL2)
+                for (int r = 0; r < CS; r++) tot += sAll[256 + r * 16 + lane];
+            const int suf = warp_suffix_sum(tot);
+            const unsigned ok = __ballot_sync(kFull, lane < NL2 && suf >= rem);
+            const int v2 = __popc(ok) - 1;
+            const int quota = rem - __shfl_sync(kFull, suf - tot, v2);  // ties at T taken
             Tthr = (u1 << LOWB) | v2;
-            int eq_before = 0, sel_before = 0;
-            for (int r = 0; r < CS; r++) {
-                int gt = 0;
-                for (int v = u1 + 1; v < NL1; v++) gt += sAll[r * 16 + v];
-                for (int v = v2 + 1; v < NL2; v++) gt += sAll[256 + r * 16 + v];
-                const int eq = sAll[256 + r * 16 + v2];
-                const int tk = max(0, min(quota - eq_before, eq));
-                if (r == rank) {
-                    take = tk;
-                    off = sel_before;
-                }
-                eq_before += eq;
-                sel_before += gt + tk;
+            // lane r: CTA r's keys above T and ties at T; ties go to the lowest indices
+            int gt = 0, eq = 0;
+            if (lane < CS) {
+                for (int v = u1 + 1; v < NL1; v++) gt += sAll[lane * 16 + v];
+                for (int v = v2 + 1; v < NL2; v++) gt += sAll[256 + lane * 16 + v];
+                eq = sAll[256 + lane * 16 + v2];
             }
+            const int eq_before = warp_exclusive_scan(eq);
+            const int tk = (lane < CS) ? max(0, min(quota - eq_before, eq)) : 0;
+            const int sel_before = warp_exclusive_scan(gt + tk);
+            take = __shfl_sync(kFull, tk, rank);
+            off = __shfl_sync(kFull, sel_before, rank);
         }
-        sMisc[M_T] = Tthr;
-        sMisc[M_TAKE] = take;
-        sMisc[M_OFF] = off;
-        if (rank == 0) a.cand_count[u] = Cp;
+        if (lane == 0) {
+            sMisc[M_T] = Tthr;
+            sMisc[M_TAKE] = take;
+            sMisc[M_OFF] = off;
+            if (rank == 0) a.cand_count[u] = Cp;
+        }
     }
     __syncthreads();
 
@@ -564,7 +561,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     uint32_t prefix = 0, mask = 0;
     int rem = kp;
     if (tid < 16) sMisc[M_ABOVE + tid] = 0;
-    int *scratch = reinterpret_cast<int *>(ring);  // [CS][256] copy of every CTA's histogram
+    int *sCol = reinterpret_cast<int *>(ring);  // [256] cluster-wide histogram of a pass
+    static_assert(kSelThreads == 256, "one radix bin per thread");
     for (int pass = 0; pass < 4; pass++) {
         const int shift = 24 - 8 * pass;
         int *hist = sRad + (pass & 1) * 256;
@@ -591,18 +589,21 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         __syncthreads();
         cluster.sync();  // #4..#7: this pass's histograms published
         if (kp > 0) {
-            for (int t = tid; t < CS * 256; t += kSelThreads)
-                scratch[t] = *cluster.map_shared_rank(&hist[t & 255], t >> 8);
+            // thread t = bin t: CTA r's count in vr[r], the cluster's in sCol[t]
+            int vr[16], col = 0;
+#pragma unroll
+            for (int r = 0; r < 16; r++) {
+                vr[r] = (r < CS) ? *cluster.map_shared_rank(&hist[tid], r) : 0;
+                col += vr[r];
+            }
+            sCol[tid] = col;
             __syncthreads();
             if (warp == 0) {
                 int cnt[8], sum = 0;
 #pragma unroll
                 for (int r = 0; r < 8; r++) {
-                    const int bin = 255 - (lane * 8 + r);
-                    int c = 0;
-                    for (int x = 0; x < CS; x++) c += scratch[x * 256 + bin];
-                    cnt[r] = c;
-                    sum += c;
+                    cnt[r] = sCol[255 - (lane * 8 + r)];
+                    sum += cnt[r];
                 }
                 int incl = sum;
 #pragma unroll
@@ -624,11 +625,16 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
             }
             __syncthreads();
             const int digit = sMisc[M_DIGIT];
-            if (tid < CS) {
-                int above = 0;
-                for (int bin = digit + 1; bin < 256; bin++) above += scratch[tid * 256 + bin];
-                sMisc[M_ABOVE + tid] += above;
-                if (pass == 3) sAll[tid] = scratch[tid * 256 + digit];  // ties per CTA
+            // per CTA r: keys in bins above the digit are above the final key
+#pragma unroll
+            for (int r = 0; r < 16; r++) {
+                const int c = warp_sum(tid > digit ? vr[r] : 0);
+                if (lane == 0 && c) atomicAdd(&sMisc[M_ABOVE + r], c);
+            }
+            if (pass == 3 && tid == digit) {
+#pragma unroll
+                for (int r = 0; r < 16; r++)
+                    if (r < CS) sAll[r] = vr[r];  // ties per CTA
             }
             rem -= sMisc[M_BEFORE];
             prefix |= (uint32_t)digit << shift;
@@ -639,19 +645,17 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
 
     // ---------------------------------------------------------------- P6
     if (kp > 0) {
-        if (tid == 0) {
-            int eq_before = 0, sel_before = 0, take = 0, off = 0;
-            for (int r = 0; r < CS; r++) {
-                const int tk = max(0, min(rem - eq_before, sAll[r]));
-                if (r == rank) {
-                    take = tk;
-                    off = sel_before;
-                }
-                eq_before += sAll[r];
-                sel_before += sMisc[M_ABOVE + r] + tk;
+        if (warp == 0) {
+            // lane r: CTA r's winners above the final key, then its share of the ties
+            const int eq = (lane < CS) ? sAll[lane] : 0;
+            const int above = (lane < CS) ? sMisc[M_ABOVE + lane] : 0;
+            const int eq_before = warp_exclusive_scan(eq);
+            const int tk = (lane < CS) ? max(0, min(rem - eq_before, eq)) : 0;
+            const int sel_before = warp_exclusive_scan(above + tk);
+            if (lane == rank) {
+                sMisc[M_KTAKE] = tk;
+                sMisc[M_KOFF] = sel_before;
             }
-            sMisc[M_KTAKE] = take;
-            sMisc[M_KOFF] = off;
         }
         __syncthreads();
         const uint32_t keyT = prefix;
