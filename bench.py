@@ -248,20 +248,33 @@ def run_gpu(args, w):
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     scale = 1.0 / math.sqrt(w.d)
 
+    side = torch.cuda.Stream(device=dev)
+    fork, join = torch.cuda.Event(), torch.cuda.Event()
+
     def step(L, ev=None):
+        # The appended key's code is not read by this step's selection (the
+        # newest W tokens are the local window), so its encode runs on a side
+        # stream next to kvr_select; the step ends when both are done.
+        main = torch.cuda.current_stream()
+        fork.record(main)
+        side.wait_event(fork)
         if ev:
-            ev[0].record()
-        kvr.kvr_encode_keys(L.K, pos_new, 1, sgn, L.codes, err)
+            ev[0].record(side)
+        kvr.kvr_encode_keys(L.K, pos_new, 1, sgn, L.codes, err, stream=side)
         if ev:
-            ev[1].record()
+            ev[1].record(side)
+        join.record(side)
+        if ev:
+            ev[2].record(main)
         kvr.kvr_select(L.q, L.K, L.codes, seq, sgn, params, idx, cnt, ws_s, err)
         if ev:
-            ev[2].record()
+            ev[3].record(main)
         kvr.kvr_sparse_attend(L.q, L.K, L.V, idx, cnt, seq, w.W, scale, L.out, ws_a, err)
         if ev:
-            ev[3].record()
+            ev[4].record(main)
+        main.wait_event(join)
 
-    launches_per_step = 1 + 1 + 2  # encode, select, attend partial + combine
+    launches_per_step = 3  # encode, select, attend
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
     # eager warm-up on the capture stream, then one graph per layer
@@ -280,7 +293,7 @@ def run_gpu(args, w):
     graphs, evs = [], []
     for L in layers:
         g = torch.cuda.CUDAGraph()
-        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)] \
+        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)] \
             if external else None
         with torch.cuda.graph(g, stream=stream):
             step(L, ev)
@@ -319,8 +332,8 @@ def run_gpu(args, w):
         for i in sorted(last):
             ev = evs[i % LAYERS]
             per["encode"].append(ev[0].elapsed_time(ev[1]))
-            per["select"].append(ev[1].elapsed_time(ev[2]))
-            per["attend"].append(ev[2].elapsed_time(ev[3]))
+            per["select"].append(ev[2].elapsed_time(ev[3]))
+            per["attend"].append(ev[3].elapsed_time(ev[4]))
     avg = {k: (sum(v) / len(v) if v else None) for k, v in per.items()}
 
     # end to end through the public API with pinned host buffers

@@ -91,7 +91,7 @@ typedef struct kvr_shape {
 
 /* Selection parameters. */
 typedef struct kvr_select_params {
-    int C;       /* candidate budget of the coarse stage, 0 <= C <= 32768 */
+    int C;       /* candidate budget of the coarse stage, 0 <= C <= 16384 */
     int k;       /* final top-k, 0 <= k <= C */
     int W;       /* local window: tokens [N-W, N) are always attended and never
                     selected; the pool is [0, max(0, N-W)) */

@@ -12,7 +12,7 @@ namespace kvr {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxC = 32768;
+constexpr int kMaxC = 16384;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

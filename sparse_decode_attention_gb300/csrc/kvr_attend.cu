@@ -7,8 +7,8 @@
 //
 // One thread-block cluster per (batch, kv head) unit. The unit's token list
 // (selected indices, then the window) is cut into equal slices, one per CTA.
-// A CTA bulk-copies the K and V rows of its slice, in batches of 32 KB, into
-// double-buffered shared memory (mbarrier completion, bounded waits). Each
+// A CTA copies the K and V rows of its slice, in batches of 32 KB, into
+// double-buffered shared memory with 16-byte cp.async pieces. Each
 // warp takes a strided share of a batch: a token's K row is spread over the
 // 32 lanes (d/32 dims each), the G per-head partial dots are reduced with a
 // butterfly that hands head h to lanes [h*32/G, (h+1)*32/G), the softmax
@@ -118,7 +118,6 @@ __global__ void __launch_bounds__(kAttThreads, (G >= 16) ? 1 : 2) attend_kernel(
     float *sPm = reinterpret_cast<float *>(smem + CF::oPm);
     float *sPl = reinterpret_cast<float *>(smem + CF::oPl);
     float *sPo = reinterpret_cast<float *>(smem + CF::oPo);
-    uint64_t *sBar = reinterpret_cast<uint64_t *>(smem + CF::oBar);
 
     cg::cluster_group cluster = cg::this_cluster();
     const int CS = (int)cluster.num_blocks();
@@ -139,21 +138,16 @@ __global__ void __launch_bounds__(kAttThreads, (G >= 16) ? 1 : 2) attend_kernel(
     const int n = (int)(hi - lo);
     const int nbatch = (n + TOK - 1) / TOK;
 
-    if (tid == 0) {
-        mbar_init(&sBar[0], 1);
-        mbar_init(&sBar[1], 1);
-        mbar_fence_init();
-    }
-    __syncthreads();
-
     const uint8_t *Ku = static_cast<const uint8_t *>(a.K) + (size_t)u * a.cap * RB;
     const uint8_t *Vu = static_cast<const uint8_t *>(a.V) + (size_t)u * a.cap * RB;
-    // token ids of batch bi, then the bulk copies of their K and V rows
+    // token ids of batch bi, then 16-byte cp.async copies of their K and V rows
+    // (one commit group per batch; skipped slots are zero-filled)
+    constexpr int PPR = RB / 16;
     auto issue = [&](int bi) {
         int32_t *tok = sTok + (bi & 1) * TOK;
         uint8_t *buf = smem + (bi & 1) * CF::kBatchBytes;
-        int32_t t = -1;
         if (tid < TOK) {
+            int32_t t = -1;
             const int64_t p = lo + (int64_t)bi * TOK + tid;
             if (p < hi) {
                 if (p < cnt) {
@@ -168,13 +162,16 @@ __global__ void __launch_bounds__(kAttThreads, (G >= 16) ? 1 : 2) attend_kernel(
             }
             tok[tid] = t;
         }
-        const int nvalid = __syncthreads_count(t >= 0);
-        if (tid == 0) mbar_arrive_expect_tx(&sBar[bi & 1], (uint32_t)(nvalid * 2 * RB));
         __syncthreads();
-        if (t >= 0) {
-            bulk_g2s(buf + tid * RB, Ku + (size_t)t * RB, RB, &sBar[bi & 1]);
-            bulk_g2s(buf + (TOK + tid) * RB, Vu + (size_t)t * RB, RB, &sBar[bi & 1]);
+        const int rows = min(TOK, n - bi * TOK);
+        for (int pc = tid; pc < 2 * rows * PPR; pc += kAttThreads) {
+            const int kv = pc / (rows * PPR), rem = pc % (rows * PPR);
+            const int j = rem / PPR, part = rem % PPR;
+            const int32_t t = tok[j];
+            const uint8_t *src = (kv ? Vu : Ku) + (t >= 0 ? (size_t)t * RB : 0) + part * 16;
+            cp_async16(buf + (kv * TOK + j) * RB + part * 16, src, t >= 0 ? 16 : 0);
         }
+        cp_async_commit();
     };
     if (nbatch > 0) issue(0);
     if (nbatch > 1) issue(1);
@@ -196,7 +193,9 @@ __global__ void __launch_bounds__(kAttThreads, (G >= 16) ? 1 : 2) attend_kernel(
     float m = -INFINITY, l = 0.0f;  // softmax state of head lane / LPH
 
     for (int bi = 0; bi < nbatch; bi++) {
-        mbar_wait(&sBar[bi & 1], (uint32_t)((bi >> 1) & 1), a.err);
+        if (bi + 1 < nbatch) cp_async_wait<1>();
+        else cp_async_wait<0>();
+        __syncthreads();
         const int32_t *tok = sTok + (bi & 1) * TOK;
         const uint8_t *buf = smem + (bi & 1) * CF::kBatchBytes;
         const int rows = min(TOK, n - bi * TOK);
@@ -252,7 +251,6 @@ __global__ void __launch_bounds__(kAttThreads, (G >= 16) ? 1 : 2) attend_kernel(
                 }
             }
         }
-        fence_proxy_async();
         __syncthreads();
         if (bi + 2 < nbatch) issue(bi + 2);
     }
@@ -298,16 +296,25 @@ __global__ void __launch_bounds__(kAttThreads, (G >= 16) ? 1 : 2) attend_kernel(
     const int e0 = rank * (G * D) / CS, e1 = (rank + 1) * (G * D) / CS;
     for (int t = e0 + tid; t < e1; t += kAttThreads) {
         const int g = t / D, dim = t % D;
+        // all remote loads first (independent), then the arithmetic
+        float mr[16], lr[16], orr[16];
+#pragma unroll
+        for (int r = 0; r < 16; r++) {
+            mr[r] = (r < CS) ? *cluster.map_shared_rank(&sPm[g], r) : -INFINITY;
+            lr[r] = (r < CS) ? *cluster.map_shared_rank(&sPl[g], r) : 0.0f;
+            orr[r] = (r < CS) ? *cluster.map_shared_rank(&sPo[t], r) : 0.0f;
+        }
         float M = -INFINITY;
-        for (int r = 0; r < CS; r++) M = fmaxf(M, *cluster.map_shared_rank(&sPm[g], r));
+#pragma unroll
+        for (int r = 0; r < 16; r++) M = fmaxf(M, mr[r]);
         float L = 0.0f, O = 0.0f;
         if (M != -INFINITY) {
-            for (int r = 0; r < CS; r++) {
-                const float mr = *cluster.map_shared_rank(&sPm[g], r);
-                if (mr == -INFINITY) continue;
-                const float f = exp2f(mr - M);
-                L = fmaf(*cluster.map_shared_rank(&sPl[g], r), f, L);
-                O = fmaf(*cluster.map_shared_rank(&sPo[t], r), f, O);
+#pragma unroll
+            for (int r = 0; r < 16; r++) {
+                if (mr[r] == -INFINITY) continue;
+                const float f = exp2f(mr[r] - M);
+                L = fmaf(lr[r], f, L);
+                O = fmaf(orr[r], f, O);
             }
         }
         a.out[((size_t)b * a.Hq + (size_t)hk * G + g) * D + dim] = (L > 0.0f) ? O / L : 0.0f;

@@ -248,6 +248,23 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// 16-byte asynchronous global -> shared copy (L2 only); src_bytes < 16 zero-fills.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes = 16)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+// Wait until at most `n` of this thread's committed groups are still in flight.
+template <int n> __device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(n) : "memory");
+}
+
 // Programmatic dependent launch: wait until the preceding grid's memory is
 // visible (no-op when the launch was not programmatic).
 __device__ __forceinline__ void grid_dependency_wait()
@@ -265,6 +282,12 @@ __device__ __forceinline__ uint32_t order_key(float s)
     uint32_t u = __float_as_uint(s);
     if (u == 0x80000000u) u = 0u;
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Inverse of order_key (-0 comes back as +0).
+__device__ __forceinline__ float key_float(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
 }  // namespace kvr

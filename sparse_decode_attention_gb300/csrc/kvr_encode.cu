@@ -52,6 +52,12 @@ encode_kernel(const T *__restrict__ K, int Hkv, int64_t cap, int64_t tiles,
     if (blk * 32 >= hi) return;  // whole warp
     const int64_t t_lane = blk * 32 + lane;
     const uint32_t inmask = __ballot_sync(kFull, t_lane >= lo && t_lane < hi);
+    uint4 *dst = reinterpret_cast<uint4 *>(codes + ((size_t)unit * tiles + (size_t)(blk >> 5)) *
+                                                       (D * 128)) +
+                 ((size_t)lane * 32 + (size_t)(blk & 31));
+    // a partly covered block keeps its other tokens' bits: fetch them early
+    uint4 old = make_uint4(0u, 0u, 0u, 0u);
+    if (inmask != 0xffffffffu && lane < NCH) old = *dst;
 
     const T *Ku = K + (size_t)unit * cap * D;
     for (int s0 = 0; s0 < 32; s0 += KPW) {
@@ -75,24 +81,33 @@ encode_kernel(const T *__restrict__ K, int Hkv, int64_t cap, int64_t tiles,
     }
     __syncwarp();
 
-    // transpose: plane p = ballot over tokens of code bit p; lane c keeps chunk c
+    // transpose into planes; lane c builds chunk c (planes 4c..4c+3)
     uint32_t mine[4] = {0u, 0u, 0u, 0u};
-    const bool have = (inmask >> lane) & 1u;
-    for (int c = 0; c < NCH; c++) {
+    if (__popc(inmask) <= 4) {
+        // few tokens (the decode-time append): insert their bits directly
+        if (lane < NCH)
+            for (uint32_t m = inmask; m; m &= m - 1) {
+                const int i = __ffs(m) - 1;
 #pragma unroll
-        for (int w4 = 0; w4 < 4; w4++) {
-            const int p = 4 * c + w4;
-            const uint32_t bit = have ? (s_code[wib][lane][p >> 5] >> (p & 31)) & 1u : 0u;
-            const uint32_t word = __ballot_sync(kFull, bit);
-            if (lane == c) mine[w4] = word;
+                for (int w4 = 0; w4 < 4; w4++) {
+                    const int p = 4 * lane + w4;
+                    mine[w4] |= ((s_code[wib][i][p >> 5] >> (p & 31)) & 1u) << i;
+                }
+            }
+    } else {
+        // plane p = ballot over the tokens of code bit p
+        const bool have = (inmask >> lane) & 1u;
+        for (int c = 0; c < NCH; c++) {
+#pragma unroll
+            for (int w4 = 0; w4 < 4; w4++) {
+                const int p = 4 * c + w4;
+                const uint32_t bit = have ? (s_code[wib][lane][p >> 5] >> (p & 31)) & 1u : 0u;
+                const uint32_t word = __ballot_sync(kFull, bit);
+                if (lane == c) mine[w4] = word;
+            }
         }
     }
     if (lane < NCH) {
-        uint4 *dst = reinterpret_cast<uint4 *>(codes + ((size_t)unit * tiles + (size_t)(blk >> 5)) *
-                                                          (D * 128)) +
-                     ((size_t)lane * 32 + (size_t)(blk & 31));
-        uint4 old = make_uint4(0u, 0u, 0u, 0u);
-        if (inmask != 0xffffffffu) old = *dst;
         const uint32_t keep = ~inmask;
         *dst = make_uint4((old.x & keep) | (mine[0] & inmask), (old.y & keep) | (mine[1] & inmask),
                           (old.z & keep) | (mine[2] & inmask), (old.w & keep) | (mine[3] & inmask));

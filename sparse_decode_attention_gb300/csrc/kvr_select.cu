@@ -11,23 +11,27 @@
 // CTAs exchange histograms through distributed shared memory, so the whole
 // step needs no second launch and no global synchronisation:
 //   P1 each CTA streams its share of the unit's code tiles into shared memory
-//      with 1-D bulk copies (one mbarrier-tracked slot per warp) and scores 32
+//      with 16-byte cp.async copies (one 512-token slot per warp; per-copy
+//      overhead of 256-byte bulk copies was measured to dominate) and scores 32
 //      keys at a time on bit-planes: XOR with the query planes, a carry-save
 //      popcount of each 8-bit sub-block, the vote table as a mux tree, a
 //      ripple adder into the score planes; a histogram of the top score bits
 //      is kept in registers.
 //   P2 two cluster exchanges of 16-bin histograms fix the threshold score T,
 //      the tie quota and every CTA's output offset (ties by lowest index).
-//   P3 candidates are compacted in index order into the workspace.
+//   P3 candidates are compacted in index order into the workspace and, via
+//      distributed shared memory, into the CTA that rescores them.
 //   P4 after a cluster barrier every CTA takes an equal slice of the candidate
-//      list, bulk-copies the K rows into double-buffered shared memory and
-//      computes the canonical fp32 dot q_bar . k (half-warp per row).
-//   P5 four 8-bit radix passes over the exact scores, one cluster exchange of
-//      256-bin histograms each, find the k'-th largest (score, index) pair.
+//      list, copies the K rows (cp.async, 16 threads per 256-byte row) into
+//      double-buffered shared memory and computes the canonical fp32 dot
+//      q_bar . k (half-warp per row).
+//   P5 after one more cluster barrier every CTA gathers all C' exact scores
+//      (order-preserving uint32 keys) and runs the same four 8-bit radix
+//      passes on them to find the k'-th largest (score, index) pair and its
+//      own output offset.
 //   P6 winners are written ascending by index.
 // Every cluster barrier is reached by every CTA on every path (control flow
-// around them depends only on per-unit values), and every bulk-copy wait is
-// bounded.
+// around them depends only on per-unit values).
 #include <cooperative_groups.h>
 
 #include "kvr_device.cuh"
@@ -156,7 +160,9 @@ __device__ __forceinline__ uint32_t pool_mask(int64_t blk, int64_t pool)
 template <int D, typename T> struct SelSmem {
     static constexpr int kChunks = D / 4;             // 16-byte chunks (4 planes) per block
     static constexpr int kHalfBytes = kChunks * 256;  // 16 blocks = 512 tokens
-    static constexpr int kRingBytes = kSelWarps * kHalfBytes;
+    // P1 code slots, P4 row buffers, P5 order keys of up to 16384 candidates
+    static constexpr int kRingBytes =
+        (kSelWarps * kHalfBytes > 16384 * 4) ? kSelWarps * kHalfBytes : 16384 * 4;
     static constexpr int kRowBytes = D * (int)sizeof(T);
     static constexpr int kRowsPerBuf = kRingBytes / 2 / kRowBytes;
     static constexpr int oS = kRingBytes;
@@ -170,14 +176,17 @@ template <int D, typename T> struct SelSmem {
     static constexpr int oAll = oRad + 512 * 4;  // [16][16] level 1, [16][16] level 2
     static constexpr int oScan = oAll + 512 * 4;
     static constexpr int oMisc = oScan + 40 * 4;
-    static constexpr int oBar = oMisc + 64 * 4;  // kSelWarps + 2 mbarriers
-    static constexpr int bytes = oBar + (kSelWarps + 2) * 8;
+    static constexpr int oWH = oMisc + 64 * 4;  // [kSelWarps][256] per-warp histograms
+    static constexpr int bytes = oWH + kSelWarps * 256 * 4;
     static_assert(16 * 256 * 4 <= kRingBytes, "radix exchange scratch must fit the ring");
 };
 
 enum {
-    M_U1 = 0, M_REM1, M_T, M_TAKE, M_OFF, M_KTAKE, M_KOFF, M_DIGIT, M_BEFORE,
-    M_ABOVE = 16,  // [16] per-CTA count of keys above the radix prefix
+    M_U1 = 0, M_REM1, M_T, M_TAKE, M_OFF, M_KTAKE, M_KOFF, M_DIGIT, M_BEFORE, M_KEYT, M_QUOTA,
+    M_CNT, M_ABOVEB,
+    M_BOUND = 16,  // [17] first candidate position of each CTA's P4 slice, then C'
+    M_KMIN = 33, M_KMAX, M_GMIN, M_GMAX, M_AOWN,
+    M_SEG = 40,    // [17] first boundary-key position of each CTA, then the total
 };
 
 template <int D, typename T, int VB>
@@ -206,7 +215,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     int *sAll = reinterpret_cast<int *>(smem + SM::oAll);
     int *sScan = reinterpret_cast<int *>(smem + SM::oScan);
     int *sMisc = reinterpret_cast<int *>(smem + SM::oMisc);
-    uint64_t *sBar = reinterpret_cast<uint64_t *>(smem + SM::oBar);
 
     cg::cluster_group cluster = cg::this_cluster();
     const int CS = (int)cluster.num_blocks();
@@ -229,28 +237,36 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     const int64_t blk0 = min(h0 * 16, nb_pool), blk1 = min(h1 * 16, nb_pool);
     const uint8_t *codes_u = a.codes + (size_t)u * a.tiles * (D * 128);
 
-    if (tid == 0) {
-        for (int i = 0; i < kSelWarps + 2; i++) mbar_init(&sBar[i], 1);
-        mbar_fence_init();
-    }
     for (int i = tid; i < 16; i += kSelThreads) {
         sH1[i] = 0;
         sH2[i] = 0;
     }
+    // P4 slices: CTA r rescores candidate positions [bound[r], bound[r+1])
+    if (tid <= CS) sMisc[M_BOUND + tid] = (int)((int64_t)tid * Cp / CS);
     __syncthreads();
+    // the CTA whose P4 slice holds candidate position pos (bounds are monotone)
+    auto slice_owner = [&](int pos) {
+        int r = 0;
+#pragma unroll
+        for (int s = 8; s >= 1; s >>= 1)
+            if (r + s < CS && sMisc[M_BOUND + r + s] <= pos) r += s;
+        return r;
+    };
 
-    // Issue the first code half-tile of every warp before anything else.
-    uint32_t parity = 0;
+    // Issue the first code half-tile of every warp before anything else: the
+    // warp's 32 lanes copy its NCH chunks of 256 bytes (16 blocks x 16 B) as
+    // 16-byte pieces, consecutive lanes on consecutive pieces.
     int64_t hh = (Cp > 0 || a.coarse != nullptr) ? h0 + warp : h1;
     uint8_t *slot = ring + warp * SM::kHalfBytes;
     auto issue_half = [&](int64_t half) {
-        if (lane == 0) mbar_arrive_expect_tx(&sBar[warp], SM::kHalfBytes);
-        __syncwarp();
-        if (lane < NCH) {
-            const uint8_t *src = codes_u + (size_t)(half >> 1) * (D * 128) +
-                                 ((size_t)lane * 32 + (size_t)(half & 1) * 16) * 16;
-            bulk_g2s(slot + lane * 256, src, 256, &sBar[warp]);
+        const uint8_t *tile = codes_u + (size_t)(half >> 1) * (D * 128) + (size_t)(half & 1) * 256;
+#pragma unroll
+        for (int i = 0; i < NCH / 2; i++) {
+            const int piece = i * 32 + lane;  // chunk piece / 16, 16-byte part piece % 16
+            const int c = piece >> 4, part = piece & 15;
+            cp_async16(slot + c * 256 + part * 16, tile + (size_t)c * 512 + part * 16);
         }
+        cp_async_commit();
     };
     if (hh < h1) issue_half(hh);
 
@@ -291,8 +307,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     const int jb = lane & 15, sh = lane >> 4;  // block within the half-tile, sub-block half
     uint32_t *planes_u = a.planes + (size_t)u * 8 * a.nblk;
     for (; hh < h1; hh += kSelWarps) {
-        mbar_wait(&sBar[warp], parity, a.err);
-        parity ^= 1u;
+        cp_async_wait<0>();
+        __syncwarp();  // every lane's pieces of the half-tile have landed
         uint32_t acc[ACC];
 #pragma unroll
         for (int j = 0; j < ACC; j++) acc[j] = 0u;
@@ -316,7 +332,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         add_planes<ACC, ACC>(acc, other);
         // every lane has read the slot: refill it
         __syncwarp();
-        fence_proxy_async();
         const int64_t blk = hh * 16 + jb;
         if (hh + kSelWarps < h1) issue_half(hh + kSelWarps);
         if (sh == 0 && blk < nb_pool) {
@@ -482,8 +497,15 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
                 eq &= vm;
                 uint32_t te = 0;
                 for (uint32_t m = eq; m && allow > 0; m &= m - 1, allow--) te |= m & (0u - m);
-                for (uint32_t m = gt | te; m; m &= m - 1)
-                    cidx[pos++] = (int32_t)(blk * 32 + __ffs(m) - 1);
+                for (uint32_t m = gt | te; m; m &= m - 1) {
+                    const int32_t id = (int32_t)(blk * 32 + __ffs(m) - 1);
+                    cidx[pos] = id;
+                    // straight into the shared memory of the CTA whose P4
+                    // slice [r*C'/CS, (r+1)*C'/CS) holds list position pos
+                    const int r2 = slice_owner(pos);
+                    *cluster.map_shared_rank(&sI[pos - sMisc[M_BOUND + r2]], r2) = id;
+                    pos++;
+                }
             }
             if (a.coarse) {
                 uint8_t *co = a.coarse + (size_t)u * a.cap_pad + blk * 32;
@@ -502,40 +524,56 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
 
     // ---------------------------------------------------------------- P4
     const int lo = (int)((int64_t)rank * Cp / CS), hi = (int)((int64_t)(rank + 1) * Cp / CS);
-    const int n = hi - lo;  // <= kMaxSlice (the host picks CS so)
-    for (int j = tid; j < n; j += kSelThreads) sI[j] = cidx[lo + j];
+    const int n = hi - lo;  // <= kMaxSlice (the host picks CS so); sI filled in P3
     {
         float qv[P];
 #pragma unroll
         for (int e = 0; e < P; e++) qv[e] = sQbar[(tid & 15) * P + e];
-        const uint8_t *Ku = static_cast<const uint8_t *>(a.K) + (size_t)u * a.cap * RB;
-        const int nbatch = (n + SM::kRowsPerBuf - 1) / SM::kRowsPerBuf;
-        auto issue_rows = [&](int bi) {
-            uint8_t *buf = ring + (bi & 1) * (SM::kRingBytes / 2);
-            const int r0 = bi * SM::kRowsPerBuf, rn = min(SM::kRowsPerBuf, n - r0);
-            if (tid == 0) mbar_arrive_expect_tx(&sBar[kSelWarps + (bi & 1)], (uint32_t)(rn * RB));
-            __syncthreads();
-            for (int j = tid; j < rn; j += kSelThreads)
-                bulk_g2s(buf + j * RB, Ku + (size_t)sI[r0 + j] * RB, RB,
-                         &sBar[kSelWarps + (bi & 1)]);
-        };
-        fence_proxy_async();
-        __syncthreads();
-        if (nbatch > 0) issue_rows(0);
-        if (nbatch > 1) issue_rows(1);
+        // Rows go straight into registers: lane gl of a half-warp loads the
+        // 16-byte-aligned dims [gl*P, gl*P+P) of its row (16 lanes = one
+        // coalesced row), R rows in flight per half-warp (64 registers).
+        constexpr int WPR = P * (int)sizeof(T) / 4;  // 32-bit words per lane per row
+        constexpr int R = 64 / WPR;
+        constexpr int NHW = kSelThreads / 16;
+        const uint32_t *Kw = reinterpret_cast<const uint32_t *>(static_cast<const uint8_t *>(a.K) +
+                                                               (size_t)u * a.cap * RB);
         const int hw = tid >> 4, gl = tid & 15;
-        for (int bi = 0; bi < nbatch; bi++) {
-            mbar_wait(&sBar[kSelWarps + (bi & 1)], (uint32_t)((bi >> 1) & 1), a.err);
-            const uint8_t *buf = ring + (bi & 1) * (SM::kRingBytes / 2);
-            const int r0 = bi * SM::kRowsPerBuf, rn = min(SM::kRowsPerBuf, n - r0);
-            for (int base = 0; base < rn; base += kSelThreads / 16) {
-                const int j = base + hw;
-                float kv[P];
-                if (j < rn) {
-                    widen<P>(reinterpret_cast<const T *>(buf + j * RB) + gl * P, kv);
+        __syncthreads();  // sI complete (filled by the cluster in P3)
+        for (int base = 0; base < n; base += NHW * R) {
+            uint32_t raw[R][WPR];
+#pragma unroll
+            for (int r = 0; r < R; r++) {
+                const int j = base + r * NHW + hw;
+                if (j < n) {
+                    const uint32_t *src = Kw + (size_t)sI[j] * (RB / 4) + gl * WPR;
+#pragma unroll
+                    for (int w = 0; w < WPR; w += (WPR >= 4 ? 4 : 2)) {
+                        if constexpr (WPR >= 4) {
+                            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + w));
+                            raw[r][w] = v.x;
+                            raw[r][w + 1] = v.y;
+                            raw[r][w + 2] = v.z;
+                            raw[r][w + 3] = v.w;
+                        } else {
+                            const uint2 v = __ldg(reinterpret_cast<const uint2 *>(src + w));
+                            raw[r][w] = v.x;
+                            raw[r][w + 1] = v.y;
+                        }
+                    }
                 } else {
 #pragma unroll
-                    for (int e = 0; e < P; e++) kv[e] = 0.0f;
+                    for (int w = 0; w < WPR; w++) raw[r][w] = 0u;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < R; r++) {
+                float kv[P];
+#pragma unroll
+                for (int e = 0; e < P; e++) {
+                    if constexpr (sizeof(T) == 2)
+                        kv[e] = (e & 1) ? bf16_hi(raw[r][e >> 1]) : bf16_lo(raw[r][e >> 1]);
+                    else
+                        kv[e] = __uint_as_float(raw[r][e]);
                 }
                 float acc = 0.0f;
 #pragma unroll
@@ -543,122 +581,316 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
 #pragma unroll
                 for (int span = 8; span >= 1; span >>= 1)
                     acc = acc + __shfl_xor_sync(kFull, acc, span);
-                if (gl == 0 && j < rn) {
+                const int j = base + r * NHW + hw;
+                if (gl == 0 && j < n) {
                     if (acc != acc) set_err(a.err, KVR_DEVERR_NONFINITE);
-                    sS[r0 + j] = acc;
-                    a.cand_score[(size_t)u * a.C + lo + r0 + j] = acc;
+                    sS[j] = acc;
+                    a.cand_score[(size_t)u * a.C + lo + j] = acc;
                 }
             }
-            fence_proxy_async();
-            __syncthreads();
-            if (bi + 2 < nbatch) issue_rows(bi + 2);
         }
     }
     __syncthreads();
 
     // ---------------------------------------------------------------- P5
-    // radix select of the kp-th largest order key over the cluster's slices
-    uint32_t prefix = 0, mask = 0;
-    int rem = kp;
-    if (tid < 16) sMisc[M_ABOVE + tid] = 0;
-    int *sCol = reinterpret_cast<int *>(ring);  // [256] cluster-wide histogram of a pass
-    static_assert(kSelThreads == 256, "one radix bin per thread");
-    for (int pass = 0; pass < 4; pass++) {
-        const int shift = 24 - 8 * pass;
-        int *hist = sRad + (pass & 1) * 256;
-        for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0;
+    // Top-k over the cluster in three small exchanges: (1) the score range;
+    // (2) a 256-bin linear histogram of every slice over that range (the bin
+    // map is monotone, so the k'-th largest key sits in one boundary bin);
+    // (3) the boundary bin's keys, among which one warp finds the exact key
+    // with 8-bit radix passes. A boundary bin too large to gather (massive
+    // ties) falls back to every CTA gathering all C' keys.
+    static_assert(kSelThreads == 256, "one histogram bin per thread");
+    int *sWH = reinterpret_cast<int *>(smem + SM::oWH);
+    uint32_t *sPub = reinterpret_cast<uint32_t *>(ring);  // own boundary keys, published
+    // 256-bin histogram of `bin(i)` over the items i < n with `take(i)`:
+    // per-warp counters, then thread b sums bin b into sRad[b]
+    auto histogram = [&](int nitems, auto &&take, auto &&bin) {
+        for (int i = tid; i < kSelWarps * 256; i += kSelThreads) sWH[i] = 0;
         __syncthreads();
-        if (kp > 0) {
-            const int iters = (n + kSelThreads - 1) / kSelThreads;
-            for (int it = 0; it < iters; it++) {
-                const int j = it * kSelThreads + tid;
-                uint32_t key = 0;
-                bool part = false;
-                if (j < n) {
-                    key = order_key(sS[j]);
-                    part = (key & mask) == prefix;
+#pragma unroll 4
+        for (int i = tid; i < nitems; i += kSelThreads)
+            if (take(i)) atomicAdd(&sWH[warp * 256 + bin(i)], 1);
+        __syncthreads();
+        int c = 0;
+#pragma unroll
+        for (int w = 0; w < kSelWarps; w++) c += sWH[w * 256 + tid];
+        sRad[tid] = c;
+        __syncthreads();
+    };
+    // the bin of hist[256] holding the rem-th largest item, and how many lie
+    // above it (computed by every calling warp alike, no barrier needed)
+    auto find_bin_in = [&](const int *hist, int rem, int &bin, int &before) {
+        int cnt[8], sum = 0;
+#pragma unroll
+        for (int r = 0; r < 8; r++) {
+            cnt[r] = hist[255 - (lane * 8 + r)];
+            sum += cnt[r];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int run0 = incl - sum;
+        const bool mine = run0 < rem && rem <= incl;
+        int bn = 0, bf = 0;
+        if (mine) {
+            int run = run0;
+#pragma unroll
+            for (int r = 0; r < 8; r++) {
+                if (run + cnt[r] >= rem) {
+                    bn = 255 - (lane * 8 + r);
+                    bf = run;
+                    break;
                 }
-                const unsigned act = __ballot_sync(kFull, part);
-                if (part) {
-                    const uint32_t bin = (key >> shift) & 255u;
-                    const unsigned peers = __match_any_sync(act, bin);
-                    if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
-                }
+                run += cnt[r];
             }
         }
-        __syncthreads();
-        cluster.sync();  // #4..#7: this pass's histograms published
-        if (kp > 0) {
-            // thread t = bin t: CTA r's count in vr[r], the cluster's in sCol[t]
-            int vr[16], col = 0;
-#pragma unroll
-            for (int r = 0; r < 16; r++) {
-                vr[r] = (r < CS) ? *cluster.map_shared_rank(&hist[tid], r) : 0;
-                col += vr[r];
+        const int src = __ffs(__ballot_sync(kFull, mine)) - 1;
+        bin = __shfl_sync(kFull, bn, src);
+        before = __shfl_sync(kFull, bf, src);
+    };
+    // warp 0 only: the rem-th largest of keys[0..nk) by four 8-bit passes;
+    // writes the key and how many copies of it are taken (ties) to sMisc
+    auto radix_warp = [&](const uint32_t *keys, int nk, int rem) {
+        int *wh = sRad + 256;
+        uint32_t prefix = 0, mask = 0;
+        for (int pass = 0; pass < 4; pass++) {
+            const int shift = 24 - 8 * pass;
+            for (int i = lane; i < 256; i += 32) wh[i] = 0;
+            __syncwarp();
+            for (int i = lane; i < nk; i += 32) {
+                const uint32_t k = keys[i];
+                if ((k & mask) == prefix) atomicAdd(&wh[(k >> shift) & 255u], 1);
             }
-            sCol[tid] = col;
-            __syncthreads();
-            if (warp == 0) {
-                int cnt[8], sum = 0;
+            __syncwarp();
+            int dg, before;
+            find_bin_in(wh, rem, dg, before);
+            rem -= before;
+            prefix |= (uint32_t)dg << shift;
+            mask |= 255u << shift;
+            __syncwarp();
+        }
+        if (lane == 0) {
+            sMisc[M_KEYT] = (int)prefix;
+            sMisc[M_QUOTA] = rem;
+        }
+    };
+
+    // (1) the score range of this slice, then of the unit
+    {
+        uint32_t lmin = 0xffffffffu, lmax = 0u;
+        for (int j = tid; j < n; j += kSelThreads) {
+            const uint32_t k = order_key(sS[j]);
+            lmin = min(lmin, k);
+            lmax = max(lmax, k);
+        }
+        lmin = __reduce_min_sync(kFull, lmin);
+        lmax = __reduce_max_sync(kFull, lmax);
+        if (lane == 0) {
+            sScan[warp] = (int)lmin;
+            sScan[16 + warp] = (int)lmax;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            uint32_t a0 = 0xffffffffu, a1 = 0u;
+            for (int w = 0; w < kSelWarps; w++) {
+                a0 = min(a0, (uint32_t)sScan[w]);
+                a1 = max(a1, (uint32_t)sScan[16 + w]);
+            }
+            sMisc[M_KMIN] = (int)a0;
+            sMisc[M_KMAX] = (int)a1;
+        }
+    }
+    __syncthreads();
+    cluster.sync();  // #4: slice ranges published
+    if (warp == 0) {
+        uint32_t g0 = 0xffffffffu, g1 = 0u;
+        if (lane < CS) {
+            g0 = (uint32_t)*cluster.map_shared_rank(&sMisc[M_KMIN], lane);
+            g1 = (uint32_t)*cluster.map_shared_rank(&sMisc[M_KMAX], lane);
+        }
+        g0 = __reduce_min_sync(kFull, g0);
+        g1 = __reduce_max_sync(kFull, g1);
+        if (lane == 0) {
+            sMisc[M_GMIN] = (int)g0;
+            sMisc[M_GMAX] = (int)g1;
+        }
+    }
+    sRad[tid] = 0;
+    __syncthreads();
+    const float fmin = key_float((uint32_t)sMisc[M_GMIN]);
+    float scale = 256.0f / (key_float((uint32_t)sMisc[M_GMAX]) - fmin);
+    if (!(scale < INFINITY) || !(scale > 0.0f)) scale = 0.0f;  // one value, or no spread
+    auto lin_bin = [&](uint32_t key) {
+        const int x = (int)((key_float(key) - fmin) * scale);
+        return min(255, max(0, x));
+    };
+    // (2) this slice's linear histogram
+    if (kp > 0)
+        for (int j = tid; j < n; j += kSelThreads) atomicAdd(&sRad[lin_bin(order_key(sS[j]))], 1);
+    __syncthreads();
+    cluster.sync();  // #5: slice histograms published
+    int b_lin = 0, rem = 0;
+    if (kp > 0) {
+        int col = 0;
 #pragma unroll
-                for (int r = 0; r < 8; r++) {
-                    cnt[r] = sCol[255 - (lane * 8 + r)];
-                    sum += cnt[r];
-                }
-                int incl = sum;
+        for (int r = 0; r < 16; r++)
+            if (r < CS) col += *cluster.map_shared_rank(&sRad[tid], r);
+        sRad[256 + tid] = col;
+    }
+    if (tid == 0) sMisc[M_CNT] = 0;
+    __syncthreads();
+    if (kp > 0) {
+        int above;
+        find_bin_in(sRad + 256, kp, b_lin, above);
+        rem = kp - above;  // rank of the k'-th key inside the boundary bin
+    }
+    // this slice's keys above the boundary bin, and its boundary keys
+    int a_own = 0;
+    if (kp > 0)
+        for (int j = tid; j < n; j += kSelThreads) {
+            const uint32_t k = order_key(sS[j]);
+            const int bn = lin_bin(k);
+            if (bn > b_lin) a_own++;
+            else if (bn == b_lin) sPub[atomicAdd(&sMisc[M_CNT], 1)] = k;
+        }
+    int a_tot;
+    block_exclusive_scan(a_own, sScan, &a_tot);
+    if (tid == 0) sMisc[M_AOWN] = a_tot;
+    __syncthreads();
+    cluster.sync();  // #6: above counts and boundary keys published
+
+    uint32_t keyT = 0;
+    if (kp > 0) {
+        // boundary segments in cluster (= index) order
+        if (warp == 0) {
+            int ab = 0, nb = 0;
+            if (lane < CS) {
+                ab = *cluster.map_shared_rank(&sMisc[M_AOWN], lane);
+                nb = *cluster.map_shared_rank(&sMisc[M_CNT], lane);
+            }
+            const int ab_before = warp_exclusive_scan(ab);
+            const int nb_before = warp_exclusive_scan(nb);
+            if (lane <= CS) sMisc[M_SEG + lane] = nb_before;  // lane CS: the total
+            if (lane == rank) sMisc[M_ABOVEB] = ab_before;
+        }
+        __syncthreads();
+        const int NB = sMisc[M_SEG + CS];
+        uint32_t *sB = reinterpret_cast<uint32_t *>(sWH);
+        if (NB <= kSelWarps * 256) {
+            auto seg_owner = [&](int t) {
+                int r = 0;
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(kFull, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                int run = incl - sum;
-                if (run < rem && rem <= incl) {
-                    for (int r = 0; r < 8; r++) {
-                        if (run + cnt[r] >= rem) {
-                            sMisc[M_DIGIT] = 255 - (lane * 8 + r);
-                            sMisc[M_BEFORE] = run;
-                            break;
-                        }
-                        run += cnt[r];
+                for (int s2 = 8; s2 >= 1; s2 >>= 1)
+                    if (r + s2 < CS && sMisc[M_SEG + r + s2] <= t) r += s2;
+                return r;
+            };
+            for (int base = 0; base < NB; base += 8 * kSelThreads) {
+                uint32_t v[8];
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    const int t = base + i * kSelThreads + tid;
+                    v[i] = 0u;
+                    if (t < NB) {
+                        const int r2 = seg_owner(t);
+                        v[i] = *cluster.map_shared_rank(&sPub[t - sMisc[M_SEG + r2]], r2);
                     }
                 }
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    const int t = base + i * kSelThreads + tid;
+                    if (t < NB) sB[t] = v[i];
+                }
             }
             __syncthreads();
-            const int digit = sMisc[M_DIGIT];
-            // per CTA r: keys in bins above the digit are above the final key
-#pragma unroll
-            for (int r = 0; r < 16; r++) {
-                const int c = warp_sum(tid > digit ? vr[r] : 0);
-                if (lane == 0 && c) atomicAdd(&sMisc[M_ABOVE + r], c);
+            if (warp == 0) radix_warp(sB, NB, rem);
+            __syncthreads();
+            keyT = (uint32_t)sMisc[M_KEYT];
+            const int quota = sMisc[M_QUOTA];
+            // ties at keyT go to the lowest indices: boundary keys of earlier slices
+            int gt_b = 0, eq_b = 0, eq_m = 0;
+            for (int t = tid; t < NB; t += kSelThreads) {
+                const int r2 = seg_owner(t);
+                const uint32_t k = sB[t];
+                if (r2 < rank) {
+                    gt_b += k > keyT;
+                    eq_b += k == keyT;
+                } else if (r2 == rank) {
+                    eq_m += k == keyT;
+                }
             }
-            if (pass == 3 && tid == digit) {
-#pragma unroll
-                for (int r = 0; r < 16; r++)
-                    if (r < CS) sAll[r] = vr[r];  // ties per CTA
+            int gt_before, eq_before, eq_mine;
+            block_exclusive_scan(gt_b, sScan, &gt_before);
+            block_exclusive_scan(eq_b, sScan, &eq_before);
+            block_exclusive_scan(eq_m, sScan, &eq_mine);
+            if (tid == 0) {
+                sMisc[M_KTAKE] = max(0, min(quota - eq_before, eq_mine));
+                sMisc[M_KOFF] = sMisc[M_ABOVEB] + gt_before + min(eq_before, quota);
             }
-            rem -= sMisc[M_BEFORE];
-            prefix |= (uint32_t)digit << shift;
-            mask |= 255u << shift;
+            __syncthreads();
+        } else {
+            // fallback: every CTA gathers all C' keys and selects within the bin
+            uint32_t *sKey = reinterpret_cast<uint32_t *>(ring);
+            const int per = (Cp + kSelThreads - 1) / kSelThreads;
+            for (int base = 0; base < per; base += 8) {
+                float v[8];
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    const int t = (base + i) * kSelThreads + tid;
+                    v[i] = 0.0f;
+                    if (base + i < per && t < Cp) {
+                        const int r2 = slice_owner(t);
+                        v[i] = *cluster.map_shared_rank(&sS[t - sMisc[M_BOUND + r2]], r2);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    const int t = (base + i) * kSelThreads + tid;
+                    if (base + i < per && t < Cp) sKey[t] = order_key(v[i]);
+                }
+            }
+            __syncthreads();
+            uint32_t prefix = 0, mask = 0;
+            for (int pass = 0; pass < 4; pass++) {
+                const int shift = 24 - 8 * pass;
+                histogram(Cp,
+                          [&](int t) {
+                              return lin_bin(sKey[t]) == b_lin && (sKey[t] & mask) == prefix;
+                          },
+                          [&](int t) { return (int)((sKey[t] >> shift) & 255u); });
+                int dg, before;
+                find_bin_in(sRad, rem, dg, before);
+                rem -= before;
+                prefix |= (uint32_t)dg << shift;
+                mask |= 255u << shift;
+            }
+            keyT = prefix;
+            int gt_b = 0, eq_b = 0, eq_m = 0;
+            for (int t = tid; t < hi; t += kSelThreads) {
+                const uint32_t key = sKey[t];
+                if (t < lo) {
+                    gt_b += key > keyT;
+                    eq_b += key == keyT;
+                } else {
+                    eq_m += key == keyT;
+                }
+            }
+            int gt_before, eq_before, eq_mine;
+            block_exclusive_scan(gt_b, sScan, &gt_before);
+            block_exclusive_scan(eq_b, sScan, &eq_before);
+            block_exclusive_scan(eq_m, sScan, &eq_mine);
+            if (tid == 0) {
+                sMisc[M_KTAKE] = max(0, min(rem - eq_before, eq_mine));
+                sMisc[M_KOFF] = gt_before + min(eq_before, rem);
+            }
             __syncthreads();
         }
     }
 
     // ---------------------------------------------------------------- P6
     if (kp > 0) {
-        if (warp == 0) {
-            // lane r: CTA r's winners above the final key, then its share of the ties
-            const int eq = (lane < CS) ? sAll[lane] : 0;
-            const int above = (lane < CS) ? sMisc[M_ABOVE + lane] : 0;
-            const int eq_before = warp_exclusive_scan(eq);
-            const int tk = (lane < CS) ? max(0, min(rem - eq_before, eq)) : 0;
-            const int sel_before = warp_exclusive_scan(above + tk);
-            if (lane == rank) {
-                sMisc[M_KTAKE] = tk;
-                sMisc[M_KOFF] = sel_before;
-            }
-        }
-        __syncthreads();
-        const uint32_t keyT = prefix;
         const int spt = (n + kSelThreads - 1) / kSelThreads;
         const int j0 = min(tid * spt, n), j1 = min(j0 + spt, n);
         int n_eq = 0;
@@ -695,7 +927,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         if (tid == 0) a.out_count[u] = kp;
     }
     __syncthreads();
-    cluster.sync();  // #8: no CTA leaves while another may read its shared memory
+    cluster.sync();  // #5: no CTA leaves while another may read its shared memory
 }
 
 // ------------------------------------------------------------------ host side
