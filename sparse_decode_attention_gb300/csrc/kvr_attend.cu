@@ -46,19 +46,19 @@ struct AttArgs {
 
 template <int D, typename T, int G> struct AttCfg {
     static constexpr int kRowBytes = D * (int)sizeof(T);
-    static constexpr int kTok = 16384 / kRowBytes;  // tokens per batch (K + V = 32 KB)
+    static constexpr int kTok = 24576 / kRowBytes;  // tokens per batch (K + V = 48 KB)
     static constexpr int kBatchBytes = 2 * kTok * kRowBytes;
     static constexpr int kE = D / 32;  // dims per lane
     static constexpr int kWarpPart = kAttWarps * G * (D + 2) * 4;
     static constexpr int kBufBytes =
         (2 * kBatchBytes > kWarpPart) ? 2 * kBatchBytes : kWarpPart;
-    static constexpr int oTok = kBufBytes;             // [2][kTok] int32
-    static constexpr int oPm = oTok + 2 * kTok * 4;    // [G]
-    static constexpr int oPl = oPm + 16 * 4;           // [G]
-    static constexpr int oPo = oPl + 16 * 4;           // [G][D]
-    static constexpr int oBar = oPo + G * D * 4;       // 2 mbarriers
-    static constexpr int bytes = oBar + 16;
-    static_assert(kTok % kAttWarps == 0 && kTok <= kAttThreads, "batch split");
+    static constexpr int kChunk = 8 * kTok;                // token ids loaded at once
+    static constexpr int oTok = kBufBytes;                // [kChunk] int32
+    static constexpr int oPm = oTok + kChunk * 4;         // [G]
+    static constexpr int oPl = oPm + 16 * 4;              // [G]
+    static constexpr int oPo = oPl + 16 * 4;              // [G][D]
+    static constexpr int bytes = oPo + G * D * 4;
+    static_assert(kTok % kAttWarps == 0, "batch split");
 };
 
 template <int E, typename T>
@@ -120,6 +120,10 @@ __global__ void __launch_bounds__(kAttThreads, (G >= 16) ? 1 : 2) attend_kernel(
     float *sPo = reinterpret_cast<float *>(smem + CF::oPo);
 
     cg::cluster_group cluster = cg::this_cluster();
+    // programmatic dependent launch: this grid may start while the previous one
+    // drains; nothing is read before the previous grid's writes are visible
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int CS = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -140,41 +144,47 @@ __global__ void __launch_bounds__(kAttThreads, (G >= 16) ? 1 : 2) attend_kernel(
 
     const uint8_t *Ku = static_cast<const uint8_t *>(a.K) + (size_t)u * a.cap * RB;
     const uint8_t *Vu = static_cast<const uint8_t *>(a.V) + (size_t)u * a.cap * RB;
-    // token ids of batch bi, then 16-byte cp.async copies of their K and V rows
-    // (one commit group per batch; skipped slots are zero-filled)
     constexpr int PPR = RB / 16;
-    auto issue = [&](int bi) {
-        int32_t *tok = sTok + (bi & 1) * TOK;
-        uint8_t *buf = smem + (bi & 1) * CF::kBatchBytes;
-        if (tid < TOK) {
-            int32_t t = -1;
-            const int64_t p = lo + (int64_t)bi * TOK + tid;
-            if (p < hi) {
-                if (p < cnt) {
-                    t = a.idx[(size_t)u * a.kmax + p];
-                    if (t < 0 || t >= w0) {
-                        set_err(a.err, KVR_DEVERR_INDEX);
-                        t = -1;
-                    }
-                } else {
-                    t = (int32_t)(w0 + (p - cnt));
+    constexpr int CH = CF::kChunk;
+    // token ids of the slice positions [c0, c0 + CH), loaded at once (-1 = skip)
+    auto load_ids = [&](int c0) {
+        const int cn = min(CH, n - c0);
+        for (int j = tid; j < cn; j += kAttThreads) {
+            const int64_t p = lo + c0 + j;
+            int32_t t;
+            if (p < cnt) {
+                t = a.idx[(size_t)u * a.kmax + p];
+                if (t < 0 || t >= w0) {
+                    set_err(a.err, KVR_DEVERR_INDEX);
+                    t = -1;
                 }
+            } else {
+                t = (int32_t)(w0 + (p - cnt));
             }
-            tok[tid] = t;
+            sTok[j] = t;
         }
-        __syncthreads();
+    };
+    // 16-byte cp.async copies of the K and V rows of batch bi (one commit
+    // group per batch; skipped slots are zero-filled)
+    auto issue = [&](int bi, int c0) {
+        uint8_t *buf = smem + (bi & 1) * CF::kBatchBytes;
+        const int32_t *tok = sTok + (bi * TOK - c0);
         const int rows = min(TOK, n - bi * TOK);
-        for (int pc = tid; pc < 2 * rows * PPR; pc += kAttThreads) {
-            const int kv = pc / (rows * PPR), rem = pc % (rows * PPR);
-            const int j = rem / PPR, part = rem % PPR;
-            const int32_t t = tok[j];
-            const uint8_t *src = (kv ? Vu : Ku) + (t >= 0 ? (size_t)t * RB : 0) + part * 16;
-            cp_async16(buf + (kv * TOK + j) * RB + part * 16, src, t >= 0 ? 16 : 0);
+        static_assert((PPR & (PPR - 1)) == 0, "pieces per row: a power of two");
+#pragma unroll
+        for (int kv = 0; kv < 2; kv++) {
+            const uint8_t *base = kv ? Vu : Ku;
+            uint8_t *dst = buf + kv * TOK * RB;
+#pragma unroll 4
+            for (int pc = tid; pc < rows * PPR; pc += kAttThreads) {
+                const int j = pc / PPR, part = pc % PPR;  // shifts: PPR is a power of two
+                const int32_t t = tok[j];
+                cp_async16(dst + j * RB + part * 16, base + (t >= 0 ? (size_t)t * RB : 0) + part * 16,
+                           t >= 0 ? 16 : 0);
+            }
         }
         cp_async_commit();
     };
-    if (nbatch > 0) issue(0);
-    if (nbatch > 1) issue(1);
 
     // the group's query heads, pre-scaled into the log2 domain
     float qr[G][E];
@@ -192,67 +202,74 @@ __global__ void __launch_bounds__(kAttThreads, (G >= 16) ? 1 : 2) attend_kernel(
         for (int e = 0; e < E; e++) acc[g][e] = 0.0f;
     float m = -INFINITY, l = 0.0f;  // softmax state of head lane / LPH
 
-    for (int bi = 0; bi < nbatch; bi++) {
-        if (bi + 1 < nbatch) cp_async_wait<1>();
-        else cp_async_wait<0>();
+    for (int c0 = 0; c0 < n; c0 += CH) {
+        load_ids(c0);
         __syncthreads();
-        const int32_t *tok = sTok + (bi & 1) * TOK;
-        const uint8_t *buf = smem + (bi & 1) * CF::kBatchBytes;
-        const int rows = min(TOK, n - bi * TOK);
-        float s[TPW];
+        const int b0 = c0 / TOK, b1 = min(nbatch, (c0 + CH) / TOK);
+        issue(b0, c0);
+        if (b0 + 1 < b1) issue(b0 + 1, c0);
+        for (int bi = b0; bi < b1; bi++) {
+            if (bi + 1 < b1) cp_async_wait<1>();
+            else cp_async_wait<0>();
+            __syncthreads();
+            const int32_t *tok = sTok + (bi * TOK - c0);
+            const uint8_t *buf = smem + (bi & 1) * CF::kBatchBytes;
+            const int rows = min(TOK, n - bi * TOK);
+            float s[TPW];
 #pragma unroll
-        for (int jj = 0; jj < TPW; jj++) {
-            const int j = warp + jj * kAttWarps;
-            s[jj] = -INFINITY;
-            if (j < rows && tok[j] >= 0) {  // warp-uniform
-                float kv[E];
-                load_lane<E, T>(buf + j * RB, lane, kv);
-                float part[G];
+            for (int jj = 0; jj < TPW; jj++) {
+                const int j = warp + jj * kAttWarps;
+                s[jj] = -INFINITY;
+                if (j < rows && tok[j] >= 0) {  // warp-uniform
+                    float kv[E];
+                    load_lane<E, T>(buf + j * RB, lane, kv);
+                    float part[G];
 #pragma unroll
-                for (int g = 0; g < G; g++) {
-                    float d = 0.0f;
+                    for (int g = 0; g < G; g++) {
+                        float d = 0.0f;
 #pragma unroll
-                    for (int e = 0; e < E; e++) d = fmaf(qr[g][e], kv[e], d);
-                    part[g] = d;
-                }
-                s[jj] = reduce_heads<G>(part, lane);
-            }
-        }
-        float mb = -INFINITY;
-#pragma unroll
-        for (int jj = 0; jj < TPW; jj++) mb = fmaxf(mb, s[jj]);
-        const float m_new = fmaxf(m, mb);
-        const float alpha = (m == -INFINITY) ? 0.0f : exp2f(m - m_new);
-        float p[TPW], ps = 0.0f;
-#pragma unroll
-        for (int jj = 0; jj < TPW; jj++) {
-            p[jj] = (s[jj] == -INFINITY) ? 0.0f : exp2f(s[jj] - m_new);
-            ps += p[jj];
-        }
-        l = l * alpha + ps;
-        m = m_new;
-#pragma unroll
-        for (int g = 0; g < G; g++) {
-            const float ag = __shfl_sync(kFull, alpha, g * LPH);
-#pragma unroll
-            for (int e = 0; e < E; e++) acc[g][e] *= ag;
-        }
-#pragma unroll
-        for (int jj = 0; jj < TPW; jj++) {
-            const int j = warp + jj * kAttWarps;
-            if (j < rows && tok[j] >= 0) {
-                float vv[E];
-                load_lane<E, T>(buf + (TOK + j) * RB, lane, vv);
-#pragma unroll
-                for (int g = 0; g < G; g++) {
-                    const float pg = __shfl_sync(kFull, p[jj], g * LPH);
-#pragma unroll
-                    for (int e = 0; e < E; e++) acc[g][e] = fmaf(pg, vv[e], acc[g][e]);
+                        for (int e = 0; e < E; e++) d = fmaf(qr[g][e], kv[e], d);
+                        part[g] = d;
+                    }
+                    s[jj] = reduce_heads<G>(part, lane);
                 }
             }
+            float mb = -INFINITY;
+#pragma unroll
+            for (int jj = 0; jj < TPW; jj++) mb = fmaxf(mb, s[jj]);
+            const float m_new = fmaxf(m, mb);
+            const float alpha = (m == -INFINITY) ? 0.0f : exp2f(m - m_new);
+            float p[TPW], ps = 0.0f;
+#pragma unroll
+            for (int jj = 0; jj < TPW; jj++) {
+                p[jj] = (s[jj] == -INFINITY) ? 0.0f : exp2f(s[jj] - m_new);
+                ps += p[jj];
+            }
+            l = l * alpha + ps;
+            m = m_new;
+#pragma unroll
+            for (int g = 0; g < G; g++) {
+                const float ag = __shfl_sync(kFull, alpha, g * LPH);
+#pragma unroll
+                for (int e = 0; e < E; e++) acc[g][e] *= ag;
+            }
+#pragma unroll
+            for (int jj = 0; jj < TPW; jj++) {
+                const int j = warp + jj * kAttWarps;
+                if (j < rows && tok[j] >= 0) {
+                    float vv[E];
+                    load_lane<E, T>(buf + (TOK + j) * RB, lane, vv);
+#pragma unroll
+                    for (int g = 0; g < G; g++) {
+                        const float pg = __shfl_sync(kFull, p[jj], g * LPH);
+#pragma unroll
+                        for (int e = 0; e < E; e++) acc[g][e] = fmaf(pg, vv[e], acc[g][e]);
+                    }
+                }
+            }
+            __syncthreads();
+            if (bi + 2 < b1) issue(bi + 2, c0);
         }
-        __syncthreads();
-        if (bi + 2 < nbatch) issue(bi + 2);
     }
 
     // merge the warps (their partials reuse the batch buffers)
@@ -343,13 +360,15 @@ static kvr_status launch_attend_g(const LaunchCtx &c, const AttArgs &a, int cs)
     cfg.blockDim = dim3(kAttThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = c.stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return KVR_ERR_CUDA;
     return check_launch();
 }

@@ -116,6 +116,32 @@ __device__ __forceinline__ int warp_sum(int x)
     return x;
 }
 
+// Sum N per-lane values over the warp (N a power of two <= 32); lane l gets
+// the total of value l / (32 / N). Partner lanes split the value set in half
+// at each of the first log2(N) steps: N - 1 + 5 - log2(N) shuffles in all.
+template <int N, typename V>
+__device__ __forceinline__ V warp_reduce_split(V (&v)[N])
+{
+    const int lane = threadIdx.x & 31;
+    constexpr int LG = (N >= 32) ? 5 : (N >= 16) ? 4 : (N >= 8) ? 3 : (N >= 4) ? 2 : (N >= 2) ? 1 : 0;
+#pragma unroll
+    for (int s = 0; s < LG; s++) {
+        const int o = 16 >> s;
+        const int half = N >> (s + 1);
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < half; i++) {
+            const V send = upper ? v[i] : v[i + half];
+            const V keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(kFull, send, o);
+        }
+    }
+    V x = v[0];
+#pragma unroll
+    for (int o = 16 >> LG; o >= 1; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+    return x;
+}
+
 // Exclusive prefix sum over the lanes of a warp.
 __device__ __forceinline__ int warp_exclusive_scan(int x)
 {

@@ -44,6 +44,7 @@ namespace kvr {
 constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kMaxSlice = 2048;  // candidates per CTA in P4-P6
+constexpr int kPlaneCap = 512;   // 32-token blocks per CTA whose score planes stay on chip
 
 struct SelArgs {
     int Hq, Hkv, G;
@@ -177,7 +178,8 @@ template <int D, typename T> struct SelSmem {
     static constexpr int oScan = oAll + 512 * 4;
     static constexpr int oMisc = oScan + 40 * 4;
     static constexpr int oWH = oMisc + 64 * 4;  // [kSelWarps][256] per-warp histograms
-    static constexpr int bytes = oWH + kSelWarps * 256 * 4;
+    static constexpr int oPl = oWH + kSelWarps * 256 * 4;  // [8][kPlaneCap] score planes
+    static constexpr int bytes = oPl + 8 * kPlaneCap * 4;
     static_assert(16 * 256 * 4 <= kRingBytes, "radix exchange scratch must fit the ring");
 };
 
@@ -217,6 +219,10 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     int *sMisc = reinterpret_cast<int *>(smem + SM::oMisc);
 
     cg::cluster_group cluster = cg::this_cluster();
+    // programmatic dependent launch: this grid may start while the previous one
+    // drains; nothing is read before the previous grid's writes are visible
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int CS = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -306,6 +312,12 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     for (int i = 0; i < NL1; i++) cnt1[i] = 0;
     const int jb = lane & 15, sh = lane >> 4;  // block within the half-tile, sub-block half
     uint32_t *planes_u = a.planes + (size_t)u * 8 * a.nblk;
+    // score plane j of block blk: on chip for this CTA's first kPlaneCap blocks
+    uint32_t *sPl = reinterpret_cast<uint32_t *>(smem + SM::oPl);
+    auto plane = [&](int j, int64_t blk) -> uint32_t & {
+        const int64_t lb = blk - blk0;
+        return (lb < kPlaneCap) ? sPl[j * kPlaneCap + lb] : planes_u[(size_t)j * a.nblk + blk];
+    };
     for (; hh < h1; hh += kSelWarps) {
         cp_async_wait<0>();
         __syncwarp();  // every lane's pieces of the half-tile have landed
@@ -337,7 +349,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         if (sh == 0 && blk < nb_pool) {
             const uint32_t vm = pool_mask(blk, pool);
 #pragma unroll
-            for (int j = 0; j < ACC; j++) planes_u[(size_t)j * a.nblk + blk] = acc[j];
+            for (int j = 0; j < ACC; j++) plane(j, blk) = acc[j];
 #pragma unroll
             for (int v = 0; v < NL1; v++) {
                 uint32_t m = vm;
@@ -347,12 +359,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
             }
         }
     }
-#pragma unroll
-    for (int v = 0; v < NL1; v++) {
-        int s = cnt1[v];
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
-        if (lane == 0 && s) atomicAdd(&sH1[v], s);
+    {
+        const int s = warp_reduce_split<NL1>(cnt1);  // lane l: bucket l / (32 / NL1)
+        if ((lane % (32 / NL1)) == 0 && s) atomicAdd(&sH1[lane / (32 / NL1)], s);
     }
     __syncthreads();
     cluster.sync();  // #1: level-1 histograms published
@@ -390,7 +399,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         for (int64_t blk = blk0 + tid; blk < blk1; blk += kSelThreads) {
             uint32_t p[ACC];
 #pragma unroll
-            for (int j = 0; j < ACC; j++) p[j] = planes_u[(size_t)j * a.nblk + blk];
+            for (int j = 0; j < ACC; j++) p[j] = plane(j, blk);
             uint32_t inb = pool_mask(blk, pool);
 #pragma unroll
             for (int j = 0; j < H1; j++) inb &= ((u1 >> j) & 1) ? p[LOWB + j] : ~p[LOWB + j];
@@ -402,13 +411,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
                 cnt2[v] += __popc(m);
             }
         }
-#pragma unroll
-        for (int v = 0; v < NL2; v++) {
-            int s = cnt2[v];
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
-            if (lane == 0 && s) atomicAdd(&sH2[v], s);
-        }
+        const int s = warp_reduce_split<NL2>(cnt2);  // lane l: value l / (32 / NL2)
+        if ((lane % (32 / NL2)) == 0 && s) atomicAdd(&sH2[lane / (32 / NL2)], s);
     }
     __syncthreads();
     cluster.sync();  // #2: level-2 histograms published
@@ -460,36 +464,26 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         const int64_t bpt = (nbc + kSelThreads - 1) / kSelThreads;
         const int64_t my0 = blk0 + min((int64_t)tid * bpt, nbc);
         const int64_t my1 = blk0 + min((int64_t)(tid + 1) * bpt, nbc);
-        int n_eq = 0;
+        int n_eq = 0, n_gt = 0;
         if (u1 >= 0)
             for (int64_t blk = my0; blk < my1; blk++) {
                 uint32_t p[ACC], gt, eq;
 #pragma unroll
-                for (int j = 0; j < ACC; j++) p[j] = planes_u[(size_t)j * a.nblk + blk];
+                for (int j = 0; j < ACC; j++) p[j] = plane(j, blk);
                 compare_planes<ACC>(p, Tthr, gt, eq);
-                n_eq += __popc(eq & pool_mask(blk, pool));
+                const uint32_t vm = pool_mask(blk, pool);
+                n_eq += __popc(eq & vm);
+                n_gt += __popc(gt & vm);
             }
         int tot;
         const int eq_before = block_exclusive_scan(n_eq, sScan, &tot);
-        const int allow0 = max(0, min(sMisc[M_TAKE] - eq_before, n_eq));
-        int n_sel = 0, allow = allow0;
-        if (u1 >= 0)
-            for (int64_t blk = my0; blk < my1; blk++) {
-                uint32_t p[ACC], gt, eq;
-#pragma unroll
-                for (int j = 0; j < ACC; j++) p[j] = planes_u[(size_t)j * a.nblk + blk];
-                compare_planes<ACC>(p, Tthr, gt, eq);
-                const uint32_t vm = pool_mask(blk, pool);
-                const int ne = __popc(eq & vm);
-                n_sel += __popc(gt & vm) + min(allow, ne);
-                allow -= min(allow, ne);
-            }
-        int pos = block_exclusive_scan(n_sel, sScan, &tot) + sMisc[M_OFF];
-        allow = allow0;
+        // this thread's ties that are taken: the first `allow` of them in order
+        int allow = max(0, min(sMisc[M_TAKE] - eq_before, n_eq));
+        int pos = block_exclusive_scan(n_gt + allow, sScan, &tot) + sMisc[M_OFF];
         for (int64_t blk = my0; blk < my1; blk++) {
             uint32_t p[ACC], gt = 0, eq = 0;
 #pragma unroll
-            for (int j = 0; j < ACC; j++) p[j] = planes_u[(size_t)j * a.nblk + blk];
+            for (int j = 0; j < ACC; j++) p[j] = plane(j, blk);
             const uint32_t vm = pool_mask(blk, pool);
             if (u1 >= 0) {
                 compare_planes<ACC>(p, Tthr, gt, eq);
@@ -804,8 +798,26 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
                     if (t < NB) sB[t] = v[i];
                 }
             }
+            if (tid < 3) sScan[tid] = 0;
             __syncthreads();
-            if (warp == 0) radix_warp(sB, NB, rem);
+            if (NB <= kSelThreads) {
+                // rank by counting: thread t ranks key t against all NB keys
+                if (tid < NB) {
+                    const uint32_t k = sB[tid];
+                    int gt = 0, eq = 0;
+                    for (int j = 0; j < NB; j++) {
+                        const uint32_t kj = sB[j];
+                        gt += kj > k;
+                        eq += kj == k;
+                    }
+                    if (gt < rem && rem <= gt + eq) {  // every copy of the key agrees
+                        sMisc[M_KEYT] = (int)k;
+                        sMisc[M_QUOTA] = rem - gt;
+                    }
+                }
+            } else if (warp == 0) {
+                radix_warp(sB, NB, rem);
+            }
             __syncthreads();
             keyT = (uint32_t)sMisc[M_KEYT];
             const int quota = sMisc[M_QUOTA];
@@ -821,11 +833,17 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
                     eq_m += k == keyT;
                 }
             }
-            int gt_before, eq_before, eq_mine;
-            block_exclusive_scan(gt_b, sScan, &gt_before);
-            block_exclusive_scan(eq_b, sScan, &eq_before);
-            block_exclusive_scan(eq_m, sScan, &eq_mine);
+            gt_b = warp_sum(gt_b);
+            eq_b = warp_sum(eq_b);
+            eq_m = warp_sum(eq_m);
+            if (lane == 0) {
+                if (gt_b) atomicAdd(&sScan[0], gt_b);
+                if (eq_b) atomicAdd(&sScan[1], eq_b);
+                if (eq_m) atomicAdd(&sScan[2], eq_m);
+            }
+            __syncthreads();
             if (tid == 0) {
+                const int gt_before = sScan[0], eq_before = sScan[1], eq_mine = sScan[2];
                 sMisc[M_KTAKE] = max(0, min(quota - eq_before, eq_mine));
                 sMisc[M_KOFF] = sMisc[M_ABOVEB] + gt_before + min(eq_before, quota);
             }
@@ -952,13 +970,15 @@ static kvr_status launch_select_t(const LaunchCtx &c, const SelArgs &a, int cs)
     cfg.blockDim = dim3(kSelThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = c.stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return KVR_ERR_CUDA;
     return check_launch();
 }
