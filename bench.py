@@ -41,6 +41,23 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def measured_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the ncu capture recorded in
+    profiles/traffic.json, or None when the kernel's sources have changed
+    since that capture (the counters then describe another kernel)."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[kernel]
+        m = hashlib.sha256()
+        for name in rec["sources"]:
+            with open(os.path.join(ROOT, "sparse_decode_attention_gb300", "csrc", name), "rb") as f:
+                m.update(f.read())
+    except (OSError, KeyError, ValueError):
+        return None
+    return int(rec["dram_bytes_per_launch"]) if m.hexdigest() == rec["sources_sha256"] else None
+
+
 def algorithmic_bytes(w):
     """Bytes the hot path must read per step per unit (batch x kv head)."""
     N = w.N
@@ -351,7 +368,7 @@ def run_gpu(args, w):
         ach = ab["select"] / (avg["select"] * 1e-3) / 1e9
         roof = {"bound": "hbm", "kernel": "select_kernel (kvr_select, one launch)",
                 "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-                "peak_kind": peak_kind, "traffic": None,
+                "peak_kind": peak_kind, "traffic": measured_traffic("select_kernel"),
                 "algorithmic_bytes": ab["select"], "avg_ms": avg["select"]}
     path = None
     if avg["select"] and avg["attend"]:
@@ -360,6 +377,10 @@ def run_gpu(args, w):
         path = {"calls": "kvr_select + kvr_sparse_attend", "achieved": ach, "peak": peak,
                 "unit": "GB/s", "frac": ach / peak, "frac_of_8TBs": ach / 8000.0,
                 "us": tsum * 1e6, "algorithmic_bytes": ab["select"] + ab["attend"],
+                "traffic": (None if None in (measured_traffic("select_kernel"),
+                                             measured_traffic("attend_kernel"))
+                            else measured_traffic("select_kernel")
+                            + measured_traffic("attend_kernel")),
                 "attend_us": avg["attend"] * 1e3, "encode_us": avg["encode"] * 1e3}
     cpu = None
     if not args.no_cpu_baseline and world == 1:

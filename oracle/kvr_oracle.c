@@ -13,8 +13,8 @@
  * fast-math, so every fp32 operation below is one IEEE-754 round-to-nearest-
  * even operation, evaluated in the order written. Where an fp32 result
  * decides an integer (a sign bit, a rank), the order written here is the
- * canonical order that the GPU path must reproduce; the readings behind each
- * order are listed in the design doc.
+ * canonical order that the GPU path must reproduce; each function states the
+ * reading of the pages that fixes its order.
  *
  * Sources (page title, section):
  *   [P-rot]   ParisKV, "Centroidi Analitici Robusti al Drift": l2
