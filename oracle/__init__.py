@@ -68,23 +68,34 @@ def lib():
 
 
 def _tier_signatures(L):
-    if not hasattr(L, "orc_int2_quantize_group"):
-        return
+    u16 = ctypes.c_uint16
     L.orc_f32_to_f16_rd.argtypes = [ctypes.c_float]
-    L.orc_f32_to_f16_rd.restype = ctypes.c_uint16
+    L.orc_f32_to_f16_rd.restype = u16
     L.orc_f32_to_f16_ru.argtypes = [ctypes.c_float]
-    L.orc_f32_to_f16_ru.restype = ctypes.c_uint16
-    L.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
+    L.orc_f32_to_f16_ru.restype = u16
+    L.orc_f16_to_f32.argtypes = [u16]
     L.orc_f16_to_f32.restype = ctypes.c_float
+    L.orc_f16_next_up.argtypes = [u16]
+    L.orc_f16_next_up.restype = u16
+    L.orc_bf16_round.argtypes = [ctypes.c_float]
+    L.orc_bf16_round.restype = ctypes.c_float
+    L.orc_f32_to_f16_array.argtypes = [_P, _I64, _I32, _P]
+    L.orc_bf16_round_array.argtypes = [_P, _I64, _P]
     L.orc_int2_quantize_group.argtypes = [_P, _P, _P, _P]
-    L.orc_int2_dequantize_group.argtypes = [_P, ctypes.c_uint16, ctypes.c_uint16, _P]
-    L.orc_ledger_write_window.argtypes = [_P, _P, _P]
-    L.orc_ledger_read_window.argtypes = [_P, _P, _P]
-    L.orc_tiered_attend_unit.argtypes = [_P, _I32, _P, _P, _P, _P, _I64, _P, _I64, _I64,
+    L.orc_int2_quantize_group.restype = _I32
+    L.orc_int2_dequantize_group.argtypes = [_P, u16, u16, _P]
+    L.orc_ledger_bytes.argtypes = [_I32]
+    L.orc_ledger_bytes.restype = _I64
+    L.orc_ledger_write_window.argtypes = [_P, _P, _I32, _P]
+    L.orc_ledger_write_window.restype = _I32
+    L.orc_ledger_read_window.argtypes = [_P, _I32, _P, _P]
+    L.orc_tiered_attend_unit.argtypes = [_P, _I32, _P, _P, _P, _P, _I64, _I32,
                                          ctypes.c_float, _P, _P]
     L.orc_tiered_attend_unit.restype = _I32
-    L.orc_tier_route_unit.argtypes = [_P, _P, _P, _I64, _I64, _I64, _I64, _P]
-    L.orc_tier_route_unit.restype = _I32
+    L.orc_tier_init_unit.argtypes = [_P, _P, _P, _I64, _I32, _I64, _P, _P, _P, _P, _P, _P]
+    L.orc_tier_init_unit.restype = _I32
+    L.orc_tier_update_unit.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I64, _I32, _I32, _I64, _P]
+    L.orc_tier_update_unit.restype = _I32
 
 
 # --------------------------------------------------------------------------
@@ -279,3 +290,145 @@ def attend(q, K, V, idx, count, seq_len, W, scale, units=None):
         out[b, h * G:(h + 1) * G] = attend_unit(q[b, h * G:(h + 1) * G], K[b, h, :N],
                                                 V[b, h, :N], N, idx[b, h, :c], c, W, scale)
     return out
+
+
+# --------------------------------------------------------------------------
+# tiered window cache (kvr_tiers_oracle.c)
+# --------------------------------------------------------------------------
+
+WINDOW = 64
+BF16, INT2, EVICTED = 0, 1, 2
+
+
+def f16_round(x, direction: str) -> np.ndarray:
+    """fp16 bit patterns (uint16) of x rounded 'down' (toward -inf) or 'up'."""
+    a = f32(x).ravel()
+    out = np.zeros(a.size, dtype=np.uint16)
+    lib().orc_f32_to_f16_array(_p(a), a.size, -1 if direction == "down" else 1, _p(out))
+    return out.reshape(np.shape(x))
+
+
+def f16_value(h) -> np.ndarray:
+    """fp32 values of fp16 bit patterns."""
+    a = _c(h, np.uint16).ravel()
+    return np.array([lib().orc_f16_to_f32(int(v)) for v in a], dtype=np.float32).reshape(
+        np.shape(h))
+
+
+def bf16_round(x) -> np.ndarray:
+    """Nearest bfloat16 (ties to even) of each fp32 value, as fp32."""
+    a = f32(x).ravel()
+    out = np.zeros(a.size, dtype=np.float32)
+    lib().orc_bf16_round_array(_p(a), a.size, _p(out))
+    return out.reshape(np.shape(x))
+
+
+def int2_quantize_group(x):
+    """(codes uint8[8], scale fp16 bits, zero fp16 bits, ok) of 32 values."""
+    a = f32(x)
+    assert a.size == 32
+    codes = np.zeros(8, dtype=np.uint8)
+    s = np.zeros(1, dtype=np.uint16)
+    z = np.zeros(1, dtype=np.uint16)
+    rc = lib().orc_int2_quantize_group(_p(a), _p(codes), _p(s), _p(z))
+    return codes, int(s[0]), int(z[0]), rc == 0
+
+
+def int2_dequantize_group(codes, scale: int, zero: int) -> np.ndarray:
+    c = _c(codes, np.uint8)
+    out = np.zeros(32, dtype=np.float32)
+    lib().orc_int2_dequantize_group(_p(c), scale, zero, _p(out))
+    return out
+
+
+def ledger_bytes(d: int) -> int:
+    return int(lib().orc_ledger_bytes(d))
+
+
+def ledger_write_window(Kw, Vw) -> np.ndarray:
+    """Ledger bytes of one window from its [64, d] K and V rows."""
+    K = f32(Kw)
+    V = f32(Vw)
+    d = K.shape[-1]
+    out = np.zeros(ledger_bytes(d), dtype=np.uint8)
+    lib().orc_ledger_write_window(_p(K), _p(V), d, _p(out))
+    return out
+
+
+def ledger_read_window(ledger, d: int):
+    """Dequantised fp32 (K [64, d], V [64, d]) of one window's ledger."""
+    lg = _c(ledger, np.uint8)
+    K = np.zeros((WINDOW, d), dtype=np.float32)
+    V = np.zeros((WINDOW, d), dtype=np.float32)
+    lib().orc_ledger_read_window(_p(lg), d, _p(K), _p(V))
+    return K, V
+
+
+class TierUnit:
+    """Tier state of one (batch, kv-head) unit, with its own fp32 copy of the
+    unit's K and V rows (bf16 values), which promotions overwrite."""
+
+    def __init__(self, init_tiers, K_unit, V_unit, N: int, n_win: int):
+        self.K = f32(K_unit).copy()
+        self.V = f32(V_unit).copy()
+        self.d = self.K.shape[-1]
+        assert self.K.shape[0] >= n_win * WINDOW or self.K.shape[0] >= N
+        self.n_win = n_win
+        self.tier = np.zeros(n_win, dtype=np.int8)
+        self.score = np.zeros(n_win, dtype=np.int64)
+        self.has_ledger = np.zeros(n_win, dtype=np.uint8)
+        self.ledger = np.zeros((n_win, ledger_bytes(self.d)), dtype=np.uint8)
+        init = np.zeros(n_win, dtype=np.int8)
+        it = _c(init_tiers, np.int8)
+        init[:min(n_win, it.size)] = it[:n_win]
+        q = np.zeros(1, dtype=np.int32)
+        b = np.zeros(1, dtype=np.int64)
+        self._pad()
+        rc = lib().orc_tier_init_unit(_p(init), _p(self.K), _p(self.V), N, self.d, n_win,
+                                      _p(self.tier), _p(self.score), _p(self.has_ledger),
+                                      _p(self.ledger), _p(q), _p(b))
+        if rc < 0:
+            raise ValueError("bad initial tier value")
+        self.quota = int(q[0])
+        self.budget = int(b[0])
+
+    def _pad(self):
+        rows = self.n_win * WINDOW
+        if self.K.shape[0] < rows:
+            pad = np.zeros((rows - self.K.shape[0], self.d), dtype=np.float32)
+            self.K = np.ascontiguousarray(np.concatenate([self.K, pad]))
+            self.V = np.ascontiguousarray(np.concatenate([self.V, pad]))
+
+    def attend(self, q_group, N: int, scale: float):
+        """(out [G, d] fp64, mass [ceil(N/64)] fp64) of the tiered attention."""
+        q = f32(q_group)
+        G, d = q.shape
+        nw = -(-N // WINDOW)
+        out = np.zeros((G, d), dtype=np.float64)
+        mass = np.zeros(max(nw, 1), dtype=np.float64)
+        rc = lib().orc_tiered_attend_unit(_p(q), G, _p(self.K), _p(self.V), _p(self.ledger),
+                                          _p(self.tier), N, d, float(scale), _p(out), _p(mass))
+        if rc != 0:
+            raise ValueError("bad tier value")
+        return out, mass[:nw]
+
+    def update(self, mass, N: int):
+        """One routing step from fp32 window masses; returns [promotions,
+        demotions, evictions]."""
+        nw = -(-N // WINDOW)
+        m = np.zeros(self.n_win, dtype=np.float32)
+        mm = f32(mass).ravel()
+        m[:min(nw, mm.size)] = mm[:nw]
+        stats = np.zeros(3, dtype=np.int32)
+        rc = lib().orc_tier_update_unit(_p(self.tier), _p(self.score), _p(self.has_ledger),
+                                        _p(self.ledger), _p(self.K), _p(self.V), _p(m), N,
+                                        self.d, self.quota, self.budget, _p(stats))
+        if rc < 0:
+            raise ValueError("bad tier value")
+        return stats
+
+    def tier_bytes(self, N: int) -> int:
+        closed = N // WINDOW
+        t = self.tier[:closed]
+        return int((t == BF16).sum()) * WINDOW * 4 * self.d + int((t == INT2).sum()) * \
+            ledger_bytes(self.d)
