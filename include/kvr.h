@@ -250,6 +250,116 @@ kvr_status kvr_sparse_attend(const kvr_shape *shape, const void *q, const void *
                              float scale, float *out, void *workspace, size_t workspace_bytes,
                              int32_t *err_word, void *stream);
 
+/* ======================================================================== *
+ * Tiered window cache.
+ * Source: QEvict, "Metodologia: QEvict" (contiguous windows routed between a
+ * full-precision tier, a recoverable INT2 tier and an evicted tier under a
+ * fixed memory budget) and "Meccanismi Chiave" (per-window routing,
+ * cumulative attention scores, demotion / promotion, write-once quantisation
+ * ledger, GQA).
+ *
+ * Windows are KVR_WINDOW = 64 tokens: window w of a unit holds tokens
+ * [64w, 64w + 64). With N = seq_len[b], windows w < N/64 are closed and carry
+ * a tier; the newest partial window (if N % 64 != 0) is open, bf16 and always
+ * attended. K and V must be bf16.
+ *
+ * INT2 form, per token and per group of 32 contiguous channels, for K and V:
+ *   z    = the fp16 value rounded toward -inf from the group minimum,
+ *   s    = the smallest fp16 >= fl((max - z) / 3) with fmaf(3, s, z) >= max,
+ *   code = clamp(rint((x - z) / s), 0, 3), 0 when s == 0,
+ *   value = fmaf(code, s, z) (fp32); a promoted window stores the bf16
+ *   nearest to each value in K, V.
+ * Ledger of one window: kvr_ledger_bytes(d) = 48 d bytes laid out as
+ *   [K codes: token t < 64, group g < d/32, 8 bytes, element j of the group at
+ *   byte j/4, bits 2 (j%4)][K params: t, g, (fp16 scale, fp16 zero), little
+ *   endian][V codes][V params].
+ * ======================================================================== */
+
+#define KVR_WINDOW 64
+#define KVR_TIER_BF16 0
+#define KVR_TIER_INT2 1
+#define KVR_TIER_EVICTED 2
+
+#define KVR_DEVERR_TIER 0x20   /* tier value outside {0, 1, 2}: window treated as evicted */
+#define KVR_DEVERR_RANGE 0x40  /* an INT2 group's range does not fit fp16: its ledger
+                                  entry is unspecified */
+
+/* Device state of the tiered cache. Every array is caller-allocated device
+   memory; "unit" u = b * Hkv + h. */
+typedef struct kvr_tier_state {
+    int64_t n_win;       /* windows per unit, >= ceil(cap / 64), <= 16384 */
+    int8_t *tier;        /* [U, n_win] KVR_TIER_*; entries of non-closed windows are 0 */
+    int64_t *score;      /* [U, n_win] cumulative score, sum of llrint(mass * 2^32) */
+    uint8_t *has_ledger; /* [U, n_win] 1 once the window's ledger holds its INT2 form */
+    uint8_t *ledger;     /* [U, n_win, kvr_ledger_bytes(d)], 16-byte aligned */
+    int32_t *quota;      /* [U] bf16 windows kept (set by kvr_tier_init) */
+    int64_t *budget;     /* [U] byte budget of the closed windows (set by kvr_tier_init) */
+} kvr_tier_state;
+
+/* Bytes of one window's ledger (48 d), 0 for an unsupported d. */
+size_t kvr_ledger_bytes(int d);
+
+/*
+ * kvr_tier_init -- set up the tiers of every unit.
+ * For each unit with N = seq_len[b]: windows w < N/64 take initial_tier[u, w]
+ * (KVR_TIER_*), later windows bf16; scores 0; every closed INT2 window gets its
+ * ledger quantised from its current K, V rows (has_ledger 1), the others
+ * has_ledger 0; quota[u] = the number of closed bf16 windows and budget[u] =
+ * quota * 64 * 2 * 2d + (closed INT2 windows) * kvr_ledger_bytes(d).
+ *   initial_tier device int8 [U, n_win]; K, V device bf16 [B, Hkv, cap, d].
+ *   err_word     KVR_DEVERR_TIER, KVR_DEVERR_RANGE, KVR_DEVERR_SEQ_LEN (unit
+ *                left with every window bf16 and budget 0).
+ */
+kvr_status kvr_tier_init(const kvr_shape *shape, const kvr_tier_state *state,
+                         const int8_t *initial_tier, const void *K, const void *V,
+                         const int32_t *seq_len, int32_t *err_word, void *stream);
+
+/* Bytes of device workspace kvr_sparse_attend_tiered needs. */
+size_t kvr_tiered_attend_workspace_size(const kvr_shape *shape, int64_t n_win);
+
+/*
+ * kvr_sparse_attend_tiered -- attention over the bf16 and INT2 windows, with
+ * the attention mass of every window (the tiered form of kvr_sparse_attend).
+ *
+ * Per unit and query head g of the group, over T = tokens of closed bf16
+ * windows (from K, V) U tokens of closed INT2 windows (their ledger values,
+ * dequantised in registers) U the open window's tokens:
+ *   out[b, g, :] = sum_{t in T} softmax_t(scale * q_g . k_t) v_t   (fp32);
+ *   window_mass[u, w] = sum over the group's heads g and tokens t of window w
+ *   of that softmax probability (0 for evicted windows and w >= ceil(N/64)).
+ *   q  device [B, Hq, d] bf16;  K, V device bf16 [B, Hkv, cap, d];
+ *   out device float [B, Hq, d];  window_mass device float [U, n_win].
+ *   workspace >= kvr_tiered_attend_workspace_size bytes, 256-byte aligned.
+ */
+kvr_status kvr_sparse_attend_tiered(const kvr_shape *shape, const kvr_tier_state *state,
+                                    const void *q, const void *K, const void *V,
+                                    const int32_t *seq_len, float scale, float *out,
+                                    float *window_mass, void *workspace,
+                                    size_t workspace_bytes, int32_t *err_word, void *stream);
+
+/* Bytes of device workspace kvr_tier_update needs. */
+size_t kvr_tier_update_workspace_size(const kvr_shape *shape, int64_t n_win);
+
+/*
+ * kvr_tier_update -- one routing step of every unit after the attention.
+ *   1. score[u, w] += llrint(window_mass[u, w] * 2^32) for every non-evicted
+ *      window w < ceil(N/64) (evicted windows keep their score);
+ *   2. the live (not evicted) closed windows are ranked by (score desc,
+ *      window asc); the first quota[u] become bf16, the others INT2;
+ *   3. while the tier bytes (bf16: 64 * 2 * 2d, INT2: kvr_ledger_bytes(d))
+ *      exceed budget[u], the lowest-ranked INT2 window is evicted, for good;
+ *   4. data moves: bf16 -> INT2 quantises the window's K, V rows into its
+ *      ledger unless has_ledger (write-once); INT2 -> bf16 writes the bf16
+ *      values of the ledger into the window's K, V rows; evictions move nothing.
+ *   K, V        device bf16 [B, Hkv, cap, d] (read and written).
+ *   stats       device int32 [U, 3] or NULL: {promotions, demotions, evictions}.
+ *   workspace   >= kvr_tier_update_workspace_size bytes, 256-byte aligned.
+ */
+kvr_status kvr_tier_update(const kvr_shape *shape, const kvr_tier_state *state,
+                           const float *window_mass, const int32_t *seq_len, void *K, void *V,
+                           int32_t *stats, void *workspace, size_t workspace_bytes,
+                           int32_t *err_word, void *stream);
+
 /*
  * kvr_read_error -- synchronise `stream`, read the device error word into
  * *bits_out (may be NULL) and clear it. Returns KVR_ERR_DEVICE when a bit was

@@ -22,11 +22,17 @@ __all__ = [
     "kvr_select", "kvr_select_static_scratch", "kvr_attend_workspace_size",
     "kvr_sparse_attend", "kvr_read_error",
     "DEFAULT_LUT", "DEVERR", "SELECT_STORE_COARSE", "kvr_codes_bytes", "codes_buffer",
+    "WINDOW", "TIER_BF16", "TIER_INT2", "TIER_EVICTED", "TierState", "kvr_ledger_bytes",
+    "kvr_tier_init", "kvr_tiered_attend_workspace_size", "kvr_sparse_attend_tiered",
+    "kvr_tier_update_workspace_size", "kvr_tier_update",
 ]
 
 KVR_F32, KVR_BF16 = 0, 1
 DEFAULT_LUT = (3, 2, 1, 0, 0, 0, 0, 0, 0)
-DEVERR = {"seq_len": 0x1, "position": 0x2, "index": 0x4, "nonfinite": 0x8}
+DEVERR = {"seq_len": 0x1, "position": 0x2, "index": 0x4, "nonfinite": 0x8, "timeout": 0x10,
+          "tier": 0x20, "range": 0x40}
+WINDOW = 64
+TIER_BF16, TIER_INT2, TIER_EVICTED = 0, 1, 2
 
 
 class KvrError(RuntimeError):
@@ -52,6 +58,12 @@ class _Views(ctypes.Structure):
     _fields_ = [("coarse", ctypes.c_size_t), ("cand_idx", ctypes.c_size_t),
                 ("cand_score", ctypes.c_size_t), ("cand_count", ctypes.c_size_t),
                 ("qbar", ctypes.c_size_t)]
+
+
+class _TierState(ctypes.Structure):
+    _fields_ = [("n_win", ctypes.c_int64), ("tier", ctypes.c_void_p), ("score", ctypes.c_void_p),
+                ("has_ledger", ctypes.c_void_p), ("ledger", ctypes.c_void_p),
+                ("quota", ctypes.c_void_p), ("budget", ctypes.c_void_p)]
 
 
 class Shape:
@@ -119,8 +131,20 @@ def load(build_if_missing: bool = True):
     L.kvr_sparse_attend.argtypes = [S, _P, _P, _P, _P, ctypes.c_int, _P, _P, ctypes.c_int,
                                     ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P]
     L.kvr_read_error.argtypes = [_P, _P, _P]
+    T = ctypes.POINTER(_TierState)
+    L.kvr_ledger_bytes.argtypes = [ctypes.c_int]
+    L.kvr_ledger_bytes.restype = ctypes.c_size_t
+    L.kvr_tier_init.argtypes = [S, T, _P, _P, _P, _P, _P, _P]
+    L.kvr_tiered_attend_workspace_size.argtypes = [S, ctypes.c_int64]
+    L.kvr_tiered_attend_workspace_size.restype = ctypes.c_size_t
+    L.kvr_sparse_attend_tiered.argtypes = [S, T, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P,
+                                           ctypes.c_size_t, _P, _P]
+    L.kvr_tier_update_workspace_size.argtypes = [S, ctypes.c_int64]
+    L.kvr_tier_update_workspace_size.restype = ctypes.c_size_t
+    L.kvr_tier_update.argtypes = [S, T, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
     for fn in ("kvr_encode_keys", "kvr_select_workspace_views", "kvr_select",
-               "kvr_select_static_scratch",
+               "kvr_select_static_scratch", "kvr_tier_init", "kvr_sparse_attend_tiered",
+               "kvr_tier_update",
                "kvr_sparse_attend", "kvr_read_error"):
         getattr(L, fn).restype = ctypes.c_int
     _lib = L
@@ -266,6 +290,100 @@ def kvr_read_error(err, stream=None) -> int:
     if st not in (0, 5):
         _check(st, "kvr_read_error")
     return int(bits.value)
+
+
+# --------------------------------------------------------------------------
+# tiered window cache
+# --------------------------------------------------------------------------
+
+def kvr_ledger_bytes(d: int) -> int:
+    return int(load().kvr_ledger_bytes(int(d)))
+
+
+class TierState:
+    """Device arrays of the tiered cache (kvr_tier_state): for U = B * Hkv
+    units and n_win windows each, tier int8, score int64, has_ledger uint8,
+    ledger uint8 [U, n_win, 48 d], quota int32 [U], budget int64 [U]."""
+
+    def __init__(self, U: int, n_win: int, d: int, device="cuda"):
+        self.U, self.n_win, self.d = int(U), int(n_win), int(d)
+        self.tier = torch.zeros((U, n_win), dtype=torch.int8, device=device)
+        self.score = torch.zeros((U, n_win), dtype=torch.int64, device=device)
+        self.has_ledger = torch.zeros((U, n_win), dtype=torch.uint8, device=device)
+        self.ledger = torch.zeros((U, n_win, kvr_ledger_bytes(d)), dtype=torch.uint8,
+                                  device=device)
+        self.quota = torch.zeros(U, dtype=torch.int32, device=device)
+        self.budget = torch.zeros(U, dtype=torch.int64, device=device)
+
+    def c(self) -> _TierState:
+        return _TierState(self.n_win, self.tier.data_ptr(), self.score.data_ptr(),
+                          self.has_ledger.data_ptr(), self.ledger.data_ptr(),
+                          self.quota.data_ptr(), self.budget.data_ptr())
+
+
+def kvr_tier_init(state: TierState, initial_tier, K, V, seq_len, q_heads: int, err=None,
+                  stream=None):
+    """Tiers, scores, ledgers of the initially INT2 windows, quota, budget."""
+    _cuda(K, "K", torch.bfloat16)
+    _cuda(V, "V", torch.bfloat16)
+    _cuda(initial_tier, "initial_tier", torch.int8)
+    _cuda(seq_len, "seq_len", torch.int32)
+    if initial_tier.numel() < state.U * state.n_win:
+        raise ValueError("initial_tier must hold [U, n_win] entries")
+    B, Hkv, cap, d = K.shape
+    shape = Shape(B, q_heads, Hkv, d, cap, torch.bfloat16)
+    st = load().kvr_tier_init(ctypes.byref(shape.c()), ctypes.byref(state.c()),
+                              _ptr(initial_tier), _ptr(K), _ptr(V), _ptr(seq_len), _ptr(err),
+                              _stream(stream))
+    _check(st, "kvr_tier_init")
+
+
+def kvr_tiered_attend_workspace_size(shape: Shape, n_win: int) -> int:
+    return int(load().kvr_tiered_attend_workspace_size(ctypes.byref(shape.c()), int(n_win)))
+
+
+def kvr_sparse_attend_tiered(state: TierState, q, K, V, seq_len, scale, out, window_mass,
+                             workspace, err=None, stream=None):
+    """Attention over bf16 + INT2 windows + the open window; window masses."""
+    shape = Shape.of(_cuda(K, "K", torch.bfloat16), _cuda(q, "q", torch.bfloat16))
+    _cuda(V, "V", torch.bfloat16)
+    _cuda(seq_len, "seq_len", torch.int32)
+    _cuda(out, "out", torch.float32)
+    _cuda(window_mass, "window_mass", torch.float32)
+    _cuda(workspace, "workspace")
+    if window_mass.numel() < state.U * state.n_win:
+        raise ValueError("window_mass must hold [U, n_win] entries")
+    st = load().kvr_sparse_attend_tiered(ctypes.byref(shape.c()), ctypes.byref(state.c()),
+                                         _ptr(q), _ptr(K), _ptr(V), _ptr(seq_len),
+                                         float(scale), _ptr(out), _ptr(window_mass),
+                                         _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(),
+                                         _ptr(err), _stream(stream))
+    _check(st, "kvr_sparse_attend_tiered")
+
+
+def kvr_tier_update_workspace_size(shape: Shape, n_win: int) -> int:
+    return int(load().kvr_tier_update_workspace_size(ctypes.byref(shape.c()), int(n_win)))
+
+
+def kvr_tier_update(state: TierState, window_mass, seq_len, K, V, q_heads: int, stats,
+                    workspace, err=None, stream=None):
+    """One routing step: scores, ranks, tiers, ledger writes and promotions."""
+    _cuda(K, "K", torch.bfloat16)
+    _cuda(V, "V", torch.bfloat16)
+    _cuda(window_mass, "window_mass", torch.float32)
+    _cuda(seq_len, "seq_len", torch.int32)
+    _cuda(workspace, "workspace")
+    if stats is not None:
+        _cuda(stats, "stats", torch.int32)
+    B, Hkv, cap, d = K.shape
+    shape = Shape(B, q_heads, Hkv, d, cap, torch.bfloat16)
+    st = load().kvr_tier_update(ctypes.byref(shape.c()), ctypes.byref(state.c()),
+                                _ptr(window_mass), _ptr(seq_len), _ptr(K), _ptr(V),
+                                _ptr(stats), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _ptr(err),
+                                _stream(stream))
+    _check(st, "kvr_tier_update")
 
 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:

@@ -233,6 +233,102 @@ kvr_status kvr_sparse_attend(const kvr_shape *shape, const void *q, const void *
                            static_cast<uint8_t *>(workspace), err_word);
 }
 
+size_t kvr_ledger_bytes(int d)
+{
+    return (d == 64 || d == 128) ? (size_t)48 * d : 0;
+}
+
+}  // extern "C"
+
+namespace {
+
+kvr_status check_tiers(const kvr_shape *shape, const kvr_tier_state *s, bool need_ledger)
+{
+    kvr_status st = check_shape(shape);
+    if (st != KVR_OK) return st;
+    if (!s) return KVR_ERR_INVALID_ARG;
+    if (s->n_win < 1 || s->n_win * KVR_WINDOW < shape->cap) return KVR_ERR_INVALID_ARG;
+    if (!tier_shape_ok(*shape, s->n_win)) return KVR_ERR_UNSUPPORTED;
+    if (!s->tier || !s->score || !s->has_ledger || !s->quota || !s->budget)
+        return KVR_ERR_INVALID_ARG;
+    if (need_ledger && (!s->ledger || !aligned16(s->ledger))) return KVR_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(s->score) & 7u) || (reinterpret_cast<uintptr_t>(s->budget) & 7u) ||
+        (reinterpret_cast<uintptr_t>(s->quota) & 3u))
+        return KVR_ERR_INVALID_ARG;
+    return KVR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvr_status kvr_tier_init(const kvr_shape *shape, const kvr_tier_state *state,
+                         const int8_t *initial_tier, const void *K, const void *V,
+                         const int32_t *seq_len, int32_t *err_word, void *stream)
+{
+    kvr_status st = check_tiers(shape, state, true);
+    if (st != KVR_OK) return st;
+    if (!initial_tier || !K || !V || !seq_len) return KVR_ERR_INVALID_ARG;
+    if (!aligned16(K) || !aligned16(V)) return KVR_ERR_INVALID_ARG;
+    LaunchCtx c{*shape, static_cast<cudaStream_t>(stream)};
+    return tier_init_dispatch(c, *state, initial_tier, K, V, seq_len, err_word);
+}
+
+size_t kvr_tiered_attend_workspace_size(const kvr_shape *shape, int64_t n_win)
+{
+    if (check_shape(shape) != KVR_OK || n_win < 1 || n_win * KVR_WINDOW < shape->cap ||
+        !tier_shape_ok(*shape, n_win))
+        return 0;
+    return tiered_attend_ws_bytes(*shape, n_win);
+}
+
+kvr_status kvr_sparse_attend_tiered(const kvr_shape *shape, const kvr_tier_state *state,
+                                    const void *q, const void *K, const void *V,
+                                    const int32_t *seq_len, float scale, float *out,
+                                    float *window_mass, void *workspace,
+                                    size_t workspace_bytes, int32_t *err_word, void *stream)
+{
+    kvr_status st = check_tiers(shape, state, true);
+    if (st != KVR_OK) return st;
+    if (!q || !K || !V || !seq_len || !out || !window_mass || !workspace)
+        return KVR_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(window_mass) & 3u) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return KVR_ERR_INVALID_ARG;
+    if (!(scale == scale)) return KVR_ERR_INVALID_ARG;
+    if (workspace_bytes < tiered_attend_ws_bytes(*shape, state->n_win)) return KVR_ERR_WORKSPACE;
+    LaunchCtx c{*shape, static_cast<cudaStream_t>(stream)};
+    return tiered_attend_dispatch(c, *state, q, K, V, seq_len, scale, out, window_mass,
+                                  static_cast<uint8_t *>(workspace), err_word);
+}
+
+size_t kvr_tier_update_workspace_size(const kvr_shape *shape, int64_t n_win)
+{
+    if (check_shape(shape) != KVR_OK || n_win < 1 || n_win * KVR_WINDOW < shape->cap ||
+        !tier_shape_ok(*shape, n_win))
+        return 0;
+    return tier_update_ws_bytes(*shape, n_win);
+}
+
+kvr_status kvr_tier_update(const kvr_shape *shape, const kvr_tier_state *state,
+                           const float *window_mass, const int32_t *seq_len, void *K, void *V,
+                           int32_t *stats, void *workspace, size_t workspace_bytes,
+                           int32_t *err_word, void *stream)
+{
+    kvr_status st = check_tiers(shape, state, true);
+    if (st != KVR_OK) return st;
+    if (!window_mass || !seq_len || !K || !V || !workspace) return KVR_ERR_INVALID_ARG;
+    if (!aligned16(K) || !aligned16(V) || (reinterpret_cast<uintptr_t>(window_mass) & 3u) ||
+        (reinterpret_cast<uintptr_t>(stats) & 3u) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return KVR_ERR_INVALID_ARG;
+    if (workspace_bytes < tier_update_ws_bytes(*shape, state->n_win)) return KVR_ERR_WORKSPACE;
+    LaunchCtx c{*shape, static_cast<cudaStream_t>(stream)};
+    return tier_update_dispatch(c, *state, window_mass, seq_len, K, V, stats,
+                                static_cast<uint8_t *>(workspace), err_word);
+}
+
 kvr_status kvr_read_error(int32_t *err_word, int32_t *bits_out, void *stream)
 {
     if (!err_word) return KVR_ERR_INVALID_ARG;

@@ -61,4 +61,17 @@ kvr_status attend_dispatch(const LaunchCtx &c, const AttendPlan &plan, const voi
                            const int32_t *count, const int32_t *seq_len, int W, float scale,
                            float *out, uint8_t *ws, int32_t *err);
 
+// Tiered window cache (kvr_tiers.cu).
+bool tier_shape_ok(const kvr_shape &s, int64_t n_win);
+size_t tiered_attend_ws_bytes(const kvr_shape &s, int64_t n_win);
+size_t tier_update_ws_bytes(const kvr_shape &s, int64_t n_win);
+kvr_status tier_init_dispatch(const LaunchCtx &c, const kvr_tier_state &s, const int8_t *init,
+                              const void *K, const void *V, const int32_t *seq_len, int32_t *err);
+kvr_status tiered_attend_dispatch(const LaunchCtx &c, const kvr_tier_state &s, const void *q,
+                                  const void *K, const void *V, const int32_t *seq_len,
+                                  float scale, float *out, float *mass, uint8_t *ws, int32_t *err);
+kvr_status tier_update_dispatch(const LaunchCtx &c, const kvr_tier_state &s, const float *mass,
+                                const int32_t *seq_len, void *K, void *V, int32_t *stats,
+                                uint8_t *ws, int32_t *err);
+
 }  // namespace kvr

@@ -22,7 +22,8 @@ def declared_functions():
 
 def test_header_declares_the_four_calls():
     names = declared_functions()
-    for n in ("kvr_encode_keys", "kvr_select", "kvr_sparse_attend"):
+    for n in ("kvr_encode_keys", "kvr_select", "kvr_sparse_attend", "kvr_tier_update",
+              "kvr_tier_init", "kvr_sparse_attend_tiered"):
         assert n in names, n
 
 
@@ -103,3 +104,49 @@ def test_validation_before_launch(kvr_lib):
     assert att(s, -1, 8, need) == 1
     assert att(_shape(kvr, Hq=24, Hkv=8), 16, 8, need) == 2  # group of 3 heads
     assert att(s, 16, 8, need, scale=float("nan")) == 1
+
+
+def test_tier_calls_validate_before_launch(kvr_lib):
+    """The tier calls check shape, state and buffers on the host (no GPU)."""
+    kvr = kvr_lib
+    L = kvr.load()
+    fake = 1 << 20
+    s = _shape(kvr, B=4, cap=131072 + 512)
+    n_win = (131072 + 512) // 64
+    assert kvr.kvr_ledger_bytes(128) == 6144 and kvr.kvr_ledger_bytes(64) == 3072
+    assert kvr.kvr_ledger_bytes(96) == 0
+    wa = kvr.kvr_tiered_attend_workspace_size(s, n_win)
+    wu = kvr.kvr_tier_update_workspace_size(s, n_win)
+    assert wa >= 32 * n_win * 4 * 4 and wu >= 32 * n_win * 4
+    # unsupported: fp32 cache, 16-head groups, too few windows for the capacity
+    assert kvr.kvr_tiered_attend_workspace_size(_shape(kvr, dtype="f32"), 64) == 0
+    assert kvr.kvr_tiered_attend_workspace_size(_shape(kvr, Hq=128, Hkv=8), 64) == 0
+    assert kvr.kvr_tier_update_workspace_size(s, n_win - 1) == 0
+
+    def state(**kw):
+        f = dict(n_win=n_win, tier=fake, score=fake, has_ledger=fake, ledger=fake, quota=fake,
+                 budget=fake)
+        f.update(kw)
+        return kvr._TierState(**f)
+
+    def att(shp, st, ws_bytes, scale=0.1):
+        return L.kvr_sparse_attend_tiered(ctypes.byref(shp.c()), ctypes.byref(st), fake, fake,
+                                          fake, fake, scale, fake, fake, fake, ws_bytes, None,
+                                          None)
+    assert att(s, state(), wa - 1) == 3
+    assert att(s, state(ledger=None), wa) == 1
+    assert att(s, state(ledger=fake + 8), wa) == 1          # ledger not 16-byte aligned
+    assert att(s, state(score=fake + 4), wa) == 1           # int64 array misaligned
+    assert att(s, state(n_win=n_win - 1), wa) == 1          # capacity beyond the windows
+    assert att(s, state(n_win=20000), wa) == 2              # above the ranking limit
+    assert att(_shape(kvr, B=4, cap=131072 + 512, dtype="f32"), state(), wa) == 2
+    assert att(s, state(), wa, scale=float("nan")) == 1
+
+    def upd(shp, st, ws_bytes):
+        return L.kvr_tier_update(ctypes.byref(shp.c()), ctypes.byref(st), fake, fake, fake, fake,
+                                 None, fake, ws_bytes, None, None)
+    assert upd(s, state(), wu - 1) == 3
+    assert upd(s, state(tier=None), wu) == 1
+    assert L.kvr_tier_init(ctypes.byref(s.c()), ctypes.byref(state()), None, fake, fake, fake,
+                           None, None) == 1
+    assert L.kvr_tier_init(ctypes.byref(s.c()), None, fake, fake, fake, fake, None, None) == 1
