@@ -435,6 +435,163 @@ def run_e2e(args, w, layers, kvr, torch, sgn, params, ws_s, ws_a, idx, cnt, seq,
             "d2h_bytes_per_step": d2h, "steps": n, "mode": "eager C-ABI calls, sync per step"}
 
 
+# --------------------------------------------------------------------------
+# tiered window cache workload (--workload tiered_window_cache)
+# --------------------------------------------------------------------------
+
+def tiered_bytes(w, n_bf, n_q, open_rows):
+    """Algorithmic bytes of one tiered attention step: the bf16 windows' K and
+    V rows, the INT2 windows' ledgers, the open window's rows and the query."""
+    row = 2 * w.d
+    return n_bf * 64 * 2 * row + n_q * 48 * w.d + open_rows * 2 * row + w.Hq * w.d * 2 // w.Hkv
+
+
+def run_gpu_tiered(args, w):
+    import numpy as np
+    import torch
+    import sparse_decode_attention_gb300 as kvr
+    import workloads as wl
+
+    rank, local, world = dist_setup(args)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    kvr.load()
+    n_e2e = min(args.steps, 64)
+    total = args.warmup + args.steps + n_e2e + 8   # every appended token fits the cache
+    cap = w.N + total
+    n_win = -(-cap // 64)
+    U = w.B * w.Hkv
+    K, V, qb = wl.make_cache(w, device=dev, cap=cap)
+    closed = w.N // 64
+    plan = np.zeros((U, n_win), dtype=np.int8)
+    for u in range(U):
+        plan[u, :closed] = wl.random_tier_plan(closed, seed=w.seed + u).numpy()
+    st = kvr.TierState(U, n_win, w.d, dev)
+    seq = torch.full((w.B,), w.N, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    kvr.kvr_tier_init(st, torch.from_numpy(plan).to(dev), K, V, seq, w.Hq, err)
+    shape = kvr.Shape.of(K, qb)
+    ws_a = kvr.workspace(kvr.kvr_tiered_attend_workspace_size(shape, n_win), dev)
+    ws_u = kvr.workspace(kvr.kvr_tier_update_workspace_size(shape, n_win), dev)
+    mass = torch.zeros((U, n_win), dtype=torch.float32, device=dev)
+    out = torch.empty((w.B, w.Hq, w.d), dtype=torch.float32, device=dev)
+    stats = torch.zeros((U, 3), dtype=torch.int32, device=dev)
+    NQ = 8
+    qs = [wl.step_query(w, qb, t).contiguous() for t in range(NQ)]
+    scale = 1.0 / math.sqrt(w.d)
+    torch.cuda.synchronize()
+    if kvr.kvr_read_error(err):
+        raise RuntimeError("device error bits during the tier set-up")
+
+    def step(q, ev=None):
+        # the appended token's K / V rows are already in the cache: the step
+        # advances the length by one, attends, and routes
+        seq.add_(1)
+        if ev:
+            ev[0].record()
+        kvr.kvr_sparse_attend_tiered(st, q, K, V, seq, scale, out, mass, ws_a, err)
+        if ev:
+            ev[1].record()
+        kvr.kvr_tier_update(st, mass, seq, K, V, w.Hq, stats, ws_u, err)
+        if ev:
+            ev[2].record()
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        step(qs[0])
+        seq.sub_(1)
+    stream.synchronize()
+    graphs, evs = [], []
+    for q in qs:
+        g = torch.cuda.CUDAGraph()
+        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
+        with torch.cuda.graph(g, stream=stream):
+            step(q, ev)
+        graphs.append(g)
+        evs.append(ev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % NQ].replay()
+    stream.synchronize()
+    n0 = int(seq[0].item())
+    tiers = st.tier.cpu().numpy()
+    c0 = n0 // 64
+    n_bf = int((tiers[:, :c0] == 0).sum()) // U
+    n_q = int((tiers[:, :c0] == 1).sum()) // U
+
+    clocks = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.25 if clocks else 0)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    per = {"attend": [], "update": []}
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t_start.record()
+        for i in range(args.steps):
+            graphs[i % NQ].replay()
+        t_end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    for ev in evs:
+        per["attend"].append(ev[0].elapsed_time(ev[1]))
+        per["update"].append(ev[1].elapsed_time(ev[2]))
+    if kvr.kvr_read_error(err):
+        raise RuntimeError("device error bits during the timed region")
+    att_ms = sum(per["attend"]) / len(per["attend"])
+    upd_ms = sum(per["update"]) / len(per["update"])
+    st_tot = stats.sum(0).tolist()
+
+    # end to end: query in from pinned memory, output out, synchronised per step
+    n = n_e2e
+    hq = [q.cpu().pin_memory() for q in qs]
+    hout = torch.empty((w.B, w.Hq, w.d), dtype=torch.float32).pin_memory()
+    qd = torch.empty_like(qs[0])
+    t0 = time.perf_counter()
+    for i in range(n):
+        qd.copy_(hq[i % NQ], non_blocking=True)
+        seq.add_(1)
+        kvr.kvr_sparse_attend_tiered(st, qd, K, V, seq, scale, out, mass, ws_a, err)
+        kvr.kvr_tier_update(st, mass, seq, K, V, w.Hq, stats, ws_u, err)
+        hout.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    el = max_over_ranks(time.perf_counter() - t0, world)
+    e2e = {"value": n * world / el, "unit": "steps/s",
+           "h2d_bytes_per_step": hq[0].numel() * hq[0].element_size(),
+           "d2h_bytes_per_step": hout.numel() * hout.element_size(), "steps": n,
+           "mode": "eager C-ABI calls, sync per step"}
+    if kvr.kvr_read_error(err):
+        raise RuntimeError("device error bits during the end-to-end steps")
+    if rank != 0:
+        return
+    ab = U * tiered_bytes(w, n_bf, n_q, 32)
+    peak, peak_kind = peaks()
+    ach = ab / (att_ms * 1e-3) / 1e9
+    line = {
+        "metric": "tiered decode steps/s (B4, 131072 tokens in 64-token windows)",
+        "value": args.steps * world / (ms / 1000.0), "unit": "steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.d,
+                   "context": w.N, "window": 64, "initial_tiers": "25% bf16 / 50% INT2 / 25% "
+                   "evicted", "windows_per_unit": closed,
+                   "l2": "inputs larger than L2: each step reads %.0f MB" % (ab / 1e6)},
+        "roofline": {"bound": "hbm", "kernel": "tiered_attend_kernel + tiered_combine_kernel "
+                     "(kvr_sparse_attend_tiered)", "achieved": ach, "peak": peak,
+                     "unit": "GB/s", "frac": ach / peak, "peak_kind": peak_kind,
+                     "traffic": measured_traffic("tiered_attend_kernel"),
+                     "algorithmic_bytes": ab, "avg_ms": att_ms},
+        "tier_update_us": upd_ms * 1e3, "windows_bf16_int2_per_unit": [n_bf, n_q],
+        "moves_last_step": {"promotions": st_tot[0], "demotions": st_tot[1],
+                            "evictions": st_tot[2]},
+        "cpu_baseline": None, "e2e": e2e, "gpu_launches": 4 * args.steps, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -447,11 +604,21 @@ def main():
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layer caches rotated (fewer = a small case for profiling; the "
                          "default keeps every step's inputs cold in L2)")
+    ap.add_argument("--workload", choices=["llama3_8b_128k", "tiered_window_cache"],
+                    default="llama3_8b_128k",
+                    help="the timed workload (the 128K decode layer is the headline)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     globals()["LAYERS"] = max(1, args.layers)
     import workloads as wl
+    if args.workload == "tiered_window_cache":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the tiered workload has no "
+                              "reference line; the oracle arm covers the 128K workload"}))
+            return
+        run_gpu_tiered(args, wl.TIERED)
+        return
     w = wl.LLAMA_128K
     if args.impl == "reference":
         run_reference(args, w)
