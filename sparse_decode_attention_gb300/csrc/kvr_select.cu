@@ -25,10 +25,12 @@
 //      list, copies the K rows (cp.async, 16 threads per 256-byte row) into
 //      double-buffered shared memory and computes the canonical fp32 dot
 //      q_bar . k (half-warp per row).
-//   P5 after one more cluster barrier every CTA gathers all C' exact scores
-//      (order-preserving uint32 keys) and runs the same four 8-bit radix
-//      passes on them to find the k'-th largest (score, index) pair and its
-//      own output offset.
+//   P5 the k'-th largest exact score (order-preserving uint32 keys) in three
+//      small cluster exchanges: the score range, a 256-bin linear histogram
+//      of every CTA's slice over that range, then the keys of the one
+//      boundary bin, ranked by one warp (8-bit radix passes); a boundary bin
+//      too large to gather (massive ties) falls back to every CTA gathering
+//      all C' keys. Each CTA also gets its output offset.
 //   P6 winners are written ascending by index.
 // Every cluster barrier is reached by every CTA on every path (control flow
 // around them depends only on per-unit values).
@@ -945,7 +947,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         if (tid == 0) a.out_count[u] = kp;
     }
     __syncthreads();
-    cluster.sync();  // #5: no CTA leaves while another may read its shared memory
+    cluster.sync();  // exit: no CTA leaves while another may read its shared memory
 }
 
 // ------------------------------------------------------------------ host side
