@@ -13,9 +13,10 @@ Recipes (all seeded, torch.Generator on the requested device):
     Planted keys sit at seeded pool positions with cosine 0.9 to the group's
     mean query direction q_hat: k = med||k|| (0.9 q_hat + sqrt(0.19) u_perp).
   * per-step queries: q_t = q_base + 0.1 N(0, 1).
-  * drift: the key appended at step t has mean 1.5 sigma_u (t+1)/T * u along a
-    seeded unit direction u (sigma_u = std of the prefill keys along u); the
-    step's query is drawn from the same drifting law.
+  * drift: the key appended at step t is a draw of the prefill's law plus the
+    mean 1.5 sigma_u (t+1)/T * u along a seeded unit direction u (sigma_u = std
+    of the prefill keys along u); the step's queries are draws of the same
+    low-rank law plus the same mean.
 """
 from __future__ import annotations
 
@@ -163,23 +164,31 @@ def drift_direction(w: Workload, K: torch.Tensor, n_prefill: int, seed: int | No
     return u, proj.std(dim=-1)
 
 
-def drift_step(w: Workload, u, sigma, step: int, total: int, seed: int | None = None,
-               device="cpu"):
-    """The drifting key [B, Hkv, d] and query [B, Hq, d] of decode step `step`."""
+def drift_inputs(w: Workload, K: torch.Tensor, n_prefill: int, total: int,
+                 seed: int | None = None):
+    """Keys appended and queries of the drifting decode steps t = 0..total-1.
+
+    K must hold rows [n_prefill, n_prefill + total) drawn by make_cache (the
+    prefill's law); the key appended at step t is that row plus the drift mean
+    1.5 sigma_u (t+1)/total u. The step's G queries per KV head are fresh draws
+    of the same low-rank law plus the same mean. Returns k_new [B, Hkv, total,
+    d] and q [total, B, Hq, d] in the workload's dtype.
+    """
     seed = w.seed if seed is None else seed
-    g = gen(device, seed * 104729 + step)
-    B, Hkv, d = u.shape
-    shift = (1.5 * sigma * (step + 1) / total)[..., None] * u
-    k = torch.stack([torch.stack([_low_rank(1, d, w.rank, g, device)[0]
-                                  for _ in range(Hkv)]) for _ in range(B)]) + shift
-    qs = []
-    for b in range(B):
-        row = []
-        for h in range(Hkv):
-            for _ in range(w.G):
-                row.append(_low_rank(1, d, w.rank, g, device)[0] + shift[b, h])
-        qs.append(torch.stack(row))
-    return k.to(w.torch_dtype()), torch.stack(qs).to(w.torch_dtype())
+    u, sigma = drift_direction(w, K, n_prefill, seed)
+    dev = K.device
+    B, Hkv, _, d = K.shape
+    G, r = w.G, w.rank
+    frac = torch.arange(1, total + 1, device=dev, dtype=torch.float32) / total
+    shift = 1.5 * sigma[:, :, None, None] * frac[None, None, :, None] * u[:, :, None, :]
+    k_new = (K[:, :, n_prefill:n_prefill + total].float() + shift).to(K.dtype)
+    g = gen(dev, seed * 104729 + 1)
+    Uq = _normal((B, Hkv, d, r), g, dev) / math.sqrt(r)
+    q = _normal((B, Hkv, total * G, r), g, dev) @ Uq.transpose(-1, -2)
+    q = q + 0.1 * _normal((B, Hkv, total * G, d), g, dev)
+    q = q.view(B, Hkv, total, G, d) + shift[:, :, :, None, :]
+    q = q.permute(2, 0, 1, 3, 4).reshape(total, B, Hkv * G, d)
+    return k_new, q.to(w.torch_dtype()).contiguous()
 
 
 def random_tier_plan(n_windows: int, frac=(0.25, 0.5, 0.25), seed: int = 0):
