@@ -241,6 +241,8 @@ class Layer:
         kvr.kvr_encode_keys(K, torch.zeros(w.B, dtype=torch.int32, device=dev), w.N, sgn,
                             self.codes)
         self.out = torch.empty((w.B, w.Hq, w.d), dtype=torch.float32, device=dev)
+        # the V cache as an L2-prefetch hint for the attention that follows
+        self.params = kvr.SelectParams(w.C, w.k, w.W, w.lut, V_prefetch=V)
 
 
 def run_gpu(args, w):
@@ -283,7 +285,7 @@ def run_gpu(args, w):
         join.record(side)
         if ev:
             ev[2].record(main)
-        kvr.kvr_select(L.q, L.K, L.codes, seq, sgn, params, idx, cnt, ws_s, err)
+        kvr.kvr_select(L.q, L.K, L.codes, seq, sgn, L.params, idx, cnt, ws_s, err)
         if ev:
             ev[3].record(main)
         kvr.kvr_sparse_attend(L.q, L.K, L.V, idx, cnt, seq, w.W, scale, L.out, ws_a, err)
@@ -326,10 +328,21 @@ def run_gpu(args, w):
                 step(L, ev)
             graphs_ev.append(ge)
             evs.append(ev)
+    # the decode iteration: the appended keys' encodes form one chain on the
+    # side stream, joined once at the end (a key's code is first read when it
+    # leaves the window, W steps later), so the main stream is a chain of
+    # select -> attend kernels linked by programmatic dependent launch
     g_iter = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_iter, stream=stream):
+        main = torch.cuda.current_stream()
+        fork.record(main)
+        side.wait_event(fork)
         for L in layers:
-            step(L)
+            kvr.kvr_encode_keys(L.K, pos_new, 1, sgn, L.codes, err, stream=side)
+            kvr.kvr_select(L.q, L.K, L.codes, seq, sgn, L.params, idx, cnt, ws_s, err)
+            kvr.kvr_sparse_attend(L.q, L.K, L.V, idx, cnt, seq, w.W, scale, L.out, ws_a, err)
+        join.record(side)
+        main.wait_event(join)
     torch.cuda.synchronize()
 
     def run_steps(n):
@@ -442,7 +455,7 @@ def run_e2e(args, w, layers, kvr, torch, sgn, params, ws_s, ws_a, idx, cnt, seq,
         L.K[:, :, w.N - 1].copy_(hk[i % LAYERS], non_blocking=True)
         L.V[:, :, w.N - 1].copy_(hv[i % LAYERS], non_blocking=True)
         kvr.kvr_encode_keys(L.K, pos_new, 1, sgn, L.codes, err)
-        kvr.kvr_select(L.q, L.K, L.codes, seq, sgn, params, idx, cnt, ws_s, err)
+        kvr.kvr_select(L.q, L.K, L.codes, seq, sgn, L.params, idx, cnt, ws_s, err)
         kvr.kvr_sparse_attend(L.q, L.K, L.V, idx, cnt, seq, w.W, scale, L.out, ws_a, err)
         hout.copy_(L.out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
@@ -640,7 +653,7 @@ def run_gpu_drift(args, w):
     del k_new
     sgn = wl.srht_signs(w.d, device=dev)
     shape = kvr.Shape.of(K, qb)
-    params = kvr.SelectParams(w.C, w.k, w.W, w.lut)
+    params = kvr.SelectParams(w.C, w.k, w.W, w.lut, V_prefetch=V)
     ws_s = kvr.workspace(kvr.kvr_select_workspace_size(shape, params), dev)
     ws_a = kvr.workspace(kvr.kvr_attend_workspace_size(shape, w.k, w.W), dev)
     codes = kvr.codes_buffer(shape, dev)

@@ -98,6 +98,11 @@ typedef struct kvr_select_params {
     int lut[9];  /* vote weight by Hamming distance 0..8 between a key's and
                     the query's sub-block codes; each in [0, 15] */
     int flags;   /* KVR_SELECT_* bits, 0 for none */
+    const void *V_prefetch; /* optional hint, or NULL: the device V cache [B, Hkv, cap, d]
+                               (shape->dtype, 16-byte aligned) of a kvr_sparse_attend
+                               that follows; the selected tokens' V rows and the local
+                               window's K and V rows are then prefetched into L2 as soon
+                               as they are known. Results are unchanged. */
 } kvr_select_params;
 
 /* Byte offsets of the inspectable parts of the select workspace after a

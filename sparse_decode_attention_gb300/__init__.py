@@ -48,7 +48,8 @@ class _Shape(ctypes.Structure):
 
 class _Params(ctypes.Structure):
     _fields_ = [("C", ctypes.c_int), ("k", ctypes.c_int), ("W", ctypes.c_int),
-                ("lut", ctypes.c_int * 9), ("flags", ctypes.c_int)]
+                ("lut", ctypes.c_int * 9), ("flags", ctypes.c_int),
+                ("V_prefetch", ctypes.c_void_p)]
 
 
 SELECT_STORE_COARSE = 0x1
@@ -89,15 +90,23 @@ class Shape:
 
 
 class SelectParams:
-    def __init__(self, C, k, W, lut=DEFAULT_LUT, flags=0):
+    """kvr_select_params. ``V_prefetch``: optional V cache tensor of a
+    kvr_sparse_attend that follows (an L2 prefetch hint; results unchanged)."""
+
+    def __init__(self, C, k, W, lut=DEFAULT_LUT, flags=0, V_prefetch=None):
         self.C, self.k, self.W = int(C), int(k), int(W)
         self.lut = tuple(int(v) for v in lut)
         self.flags = int(flags)
         if len(self.lut) != 9:
             raise ValueError("lut needs 9 entries (Hamming distance 0..8)")
+        if V_prefetch is not None and (not isinstance(V_prefetch, torch.Tensor)
+                                       or not V_prefetch.is_cuda):
+            raise TypeError("V_prefetch must be a CUDA tensor or None")
+        self.V_prefetch = V_prefetch
 
     def c(self) -> _Params:
-        return _Params(self.C, self.k, self.W, (ctypes.c_int * 9)(*self.lut), self.flags)
+        vp = None if self.V_prefetch is None else self.V_prefetch.data_ptr()
+        return _Params(self.C, self.k, self.W, (ctypes.c_int * 9)(*self.lut), self.flags, vp)
 
 
 _lib = None

@@ -274,6 +274,16 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Prefetch of the 128-byte lines of [p, p + bytes) into L2 (p 128-byte
+// aligned, bytes a multiple of 128); nothing waits for it, nothing is written.
+// Per-thread line prefetches issue in parallel across the warp; bulk-copy
+// prefetches were measured slower (one copy engine per SM serialises them).
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
+{
+    for (uint32_t o = 0; o < bytes; o += 128)
+        asm volatile("prefetch.global.L2 [%0];\n" ::"l"(static_cast<const char *>(p) + o) : "memory");
+}
+
 // 16-byte asynchronous global -> shared copy (L2 only); src_bytes < 16 zero-fills.
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes = 16)
 {

@@ -55,6 +55,7 @@ struct SelArgs {
     uint32_t leaf[4];  // bit m of leaf[j] = bit j of lut[m], m = 0..8
     const void *q;
     const void *K;
+    const void *V;  // optional: prefetch the winners' V rows and the window's rows
     const uint8_t *codes;
     const int32_t *seq_len;
     const int8_t *sgn;
@@ -244,6 +245,15 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     const int64_t nb_pool = (pool + 31) / 32;
     const int64_t blk0 = min(h0 * 16, nb_pool), blk1 = min(h1 * 16, nb_pool);
     const uint8_t *codes_u = a.codes + (size_t)u * a.tiles * (D * 128);
+    if (a.V) {
+        // the local window's K and V rows, read by the attention that follows
+        const uint8_t *Kb = static_cast<const uint8_t *>(a.K) + (size_t)u * a.cap * RB;
+        const uint8_t *Vb = static_cast<const uint8_t *>(a.V) + (size_t)u * a.cap * RB;
+        for (int64_t t = pool + rank + (int64_t)CS * tid; t < N; t += (int64_t)CS * kSelThreads) {
+            prefetch_l2(Kb + (size_t)t * RB, RB);
+            prefetch_l2(Vb + (size_t)t * RB, RB);
+        }
+    }
 
     for (int i = tid; i < 16; i += kSelThreads) {
         sH1[i] = 0;
@@ -495,6 +505,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
                 for (uint32_t m = eq; m && allow > 0; m &= m - 1, allow--) te |= m & (0u - m);
                 for (uint32_t m = gt | te; m; m &= m - 1) {
                     const int32_t id = (int32_t)(blk * 32 + __ffs(m) - 1);
+                    // the row is gathered in P4, a cluster barrier later: start it now
+                    prefetch_l2(static_cast<const uint8_t *>(a.K) + ((size_t)u * a.cap + id) * RB, RB);
                     cidx[pos] = id;
                     // straight into the shared memory of the CTA whose P4
                     // slice [r*C'/CS, (r+1)*C'/CS) holds list position pos
@@ -938,7 +950,12 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
                 take = true;
                 allow--;
             }
-            if (take) orow[pos++] = sI[j];
+            if (take) {
+                orow[pos++] = sI[j];
+                if (a.V)
+                    prefetch_l2(static_cast<const uint8_t *>(a.V) + ((size_t)u * a.cap + sI[j]) * RB,
+                                RB);
+            }
         }
     }
     if (rank == 0) {
@@ -1019,6 +1036,7 @@ kvr_status select_dispatch(const LaunchCtx &c, const kvr_select_params &p, const
     }
     a.q = q;
     a.K = K;
+    a.V = p.V_prefetch;
     a.codes = codes;
     a.seq_len = seq_len;
     a.sgn = sgn;

@@ -96,6 +96,10 @@ def test_validation_before_launch(kvr_lib):
     assert sel(s, kvr.SelectParams(40000, 16, 8), need) == 1
     assert sel(s, kvr.SelectParams(64, 16, 8, lut=(16, 0, 0, 0, 0, 0, 0, 0, 0)), need) == 1
     assert sel(s, p, need, ws=ctypes.c_void_p((1 << 20) + 16)) == 1  # ws not 256-aligned
+    pv = p.c()
+    pv.V_prefetch = (1 << 20) + 8                                   # misaligned V hint
+    assert L.kvr_select(ctypes.byref(s.c()), ctypes.byref(pv), fake, fake, fake, fake, fake,
+                        fake, fake, fake, need, None, None) == 1
 
     def att(shp, kmax, W, ws_bytes, scale=0.1):
         return L.kvr_sparse_attend(ctypes.byref(shp.c()), fake, fake, fake, fake, kmax, fake,

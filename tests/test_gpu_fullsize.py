@@ -39,7 +39,7 @@ class Path:
         self.K, self.V, self.qb = wl.make_cache(w, device=DEV, cap=cap)
         self.sgn = wl.srht_signs(w.d, device=DEV)
         self.shape = kvr.Shape.of(self.K, self.qb)
-        self.params = kvr.SelectParams(w.C, w.k, w.W, w.lut)
+        self.params = kvr.SelectParams(w.C, w.k, w.W, w.lut, V_prefetch=self.V)
         self.ws_s = kvr.workspace(kvr.kvr_select_workspace_size(self.shape, self.params))
         self.ws_a = kvr.workspace(kvr.kvr_attend_workspace_size(self.shape, w.k, w.W))
         self.codes = kvr.codes_buffer(self.shape, DEV)
