@@ -44,46 +44,56 @@ kvr_status check_params(const kvr_select_params *p)
 
 }  // namespace
 
-kvr_status raise_smem_limit(const void *kernel, int bytes)
+namespace {
+
+// Per device: kernels opted into more dynamic shared memory, and how much.
+struct SmemTable {
+    std::mutex mu;
+    const void *kernel[kMaxDevices][64];
+    int bytes[kMaxDevices][64];
+};
+
+// Raise `kernel`'s dynamic shared-memory limit on the current device to at
+// least `bytes` (a call asking for more than an earlier one raises it again).
+kvr_status raise_in(SmemTable &t, const void *kernel, int bytes, bool cluster)
 {
-    static std::mutex mu;
-    static const void *done[kMaxDevices][64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVR_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < 64; i++)
-        if (done[dev][i] == kernel) return KVR_OK;
+    std::lock_guard<std::mutex> lock(t.mu);
+    int slot = -1;
+    for (int i = 0; i < 64; i++) {
+        if (t.kernel[dev][i] == kernel) {
+            if (t.bytes[dev][i] >= bytes) return KVR_OK;
+            slot = i;
+            break;
+        }
+        if (!t.kernel[dev][i] && slot < 0) slot = i;
+    }
+    if (slot < 0) return KVR_ERR_CUDA;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
         cudaSuccess)
         return KVR_ERR_CUDA;
-    for (int i = 0; i < 64; i++)
-        if (!done[dev][i]) {
-            done[dev][i] = kernel;
-            break;
-        }
+    if (cluster &&
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess)
+        return KVR_ERR_CUDA;
+    t.kernel[dev][slot] = kernel;
+    t.bytes[dev][slot] = bytes;
     return KVR_OK;
+}
+
+SmemTable g_plain, g_cluster;
+
+}  // namespace
+
+kvr_status raise_smem_limit(const void *kernel, int bytes)
+{
+    return raise_in(g_plain, kernel, bytes, false);
 }
 
 kvr_status prepare_cluster_kernel(const void *kernel, int smem_bytes)
 {
-    static std::mutex mu;
-    static const void *done[kMaxDevices][64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVR_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < 64; i++)
-        if (done[dev][i] == kernel) return KVR_OK;
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-            cudaSuccess)
-        return KVR_ERR_CUDA;
-    for (int i = 0; i < 64; i++)
-        if (!done[dev][i]) {
-            done[dev][i] = kernel;
-            break;
-        }
-    return KVR_OK;
+    return raise_in(g_cluster, kernel, smem_bytes, true);
 }
 
 SelectPlan plan_select(const kvr_shape &s, const kvr_select_params &p)

@@ -266,28 +266,76 @@ struct TieredArgs {
     int32_t *err;
 };
 
+// ---- warp-level tensor-core helpers: mma.sync m16n8k16, bf16 in, fp32 accumulate.
+// Fragment layouts (g = lane / 4, c = lane % 4): A (16x16, row-major) holds
+// (g, 2c..2c+1), (g+8, 2c..), (g, 2c+8..), (g+8, 2c+8..); B (16x8, k-major
+// columns) holds (k = 2c..2c+1, n = g), (k = 2c+8.., n = g); C (16x8) holds
+// (g, 2c..2c+1), (g+8, 2c..2c+1).
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *p)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two 2-bit codes as the bf16 pair (ca, cb) of their values 0..3 (ca in the
+// low half). bf16 of 0, 1, 2, 3 is 0x0000, 0x3f80, 0x4000, 0x4040: a byte
+// permute picks the low bytes from 0x40008000 and the high bytes from
+// 0x40403f00.
+__device__ __forceinline__ uint32_t codes2_bf16(uint32_t ca, uint32_t cb)
+{
+    const uint32_t sel = ca * 0x11u + cb * 0x1100u + 0x4040u;
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(0x40008000u), "r"(0x40403f00u), "r"(sel));
+    return r;
+}
+
 template <int D, int G> struct TieredCfg {
     static constexpr int RB = 2 * D;                   // bf16 row bytes
     static constexpr int RS = RB + 16;                 // padded row stride in shared memory
     static constexpr int NG = D / kQG;                 // INT2 groups per row
     static constexpr int LB = ledger_bytes_of(D);
     static constexpr int CB = kWin * NG * 8, PB = kWin * NG * 4;
-    static constexpr int BUF = (2 * kWin * RS > LB ? 2 * kWin * RS : LB);
-    static constexpr int DG = D / 4;                   // 4-dim groups (PV)
-    static constexpr int TS = kThreads / DG;           // token subsets (PV)
-    static constexpr int TPT = kWin / TS;              // tokens per thread per window (PV)
-    static constexpr int PART = D / 4;                 // dims per QK part (4 parts)
-    static constexpr int GP = G < 4 ? 4 : G;           // padded head count of the P rows
-    // shared memory: two staging buffers, then q, partial scores, P, softmax state
-    static constexpr int oBuf = 0;
-    static constexpr int oQ = 2 * BUF;                       // float [G][D]
-    static constexpr int oSp = oQ + G * D * 4;               // float [4][G][kWin]
-    static constexpr int oP = oSp + 4 * G * kWin * 4;        // float [kWin][GP]
-    static constexpr int oSt = oP + kWin * GP * 4;           // float m[G], l[G], alpha[G]
-    static constexpr int oWin = oSt + 3 * 16 * 4;            // int32 [2] window of each buffer
-    static constexpr int bytes = oWin + 64;
-    static_assert(TS * DG == kThreads && kWin % TS == 0, "PV thread layout");
-    static_assert(TS * D * G * 4 <= 2 * BUF, "the final reduction reuses the staging buffers");
+    // staging ring: a slot holds the 64 K (or V) rows of a bf16 window, or an
+    // INT2 window's ledger; slots are filled ahead in window order
+    static constexpr int SLOT = kWin * RS;
+    static constexpr int NS = (D >= 128) ? 5 : 8;
+    static_assert(LB <= SLOT, "a ledger fits a slot");
+    static constexpr int KS = D / 16;                  // k-steps of the score product
+    static constexpr int MT = D / 16;                  // 16-dim tiles of the output
+    static constexpr int PST = kWin + 8;               // bf16 stride of a P row (no bank conflicts)
+    // shared memory: the staging ring, partial scores, P (hi, lo), the
+    // scale-weighted P of each INT2 group (hi, lo), z terms, softmax state
+    static constexpr int oSp = NS * SLOT;                      // float [2][kWin][8]
+    static constexpr int oP = oSp + 2 * kWin * 8 * 4;          // bf16 [2][8][PST]
+    static constexpr int oSP = oP + 2 * 8 * PST * 2;           // bf16 [NG][2][8][PST]
+    static constexpr int oZt = oSP + NG * 2 * 8 * PST * 2;     // float [NG][8]
+    static constexpr int oQs = oZt + NG * 8 * 4;               // float [NG][8]
+    static constexpr int oSt = oQs + NG * 8 * 4;               // float m[8], l[8], alpha[8]
+    static constexpr int LMAX = 1024;                          // windows per listing pass
+    static constexpr int oLive = oSt + 3 * 8 * 4;              // int32 [LMAX] live windows
+    static constexpr int oCnt = oLive + LMAX * 4;              // int [8] per-warp counts
+    static constexpr int bytes = oCnt + 8 * 4;
+    static_assert(G <= 8, "one 8-column tile of heads");
+    static_assert(8 * 16 * 8 * 4 <= NS * SLOT, "the d=64 token-half reduction fits the ring");
 };
 
 template <int D, int G>
@@ -295,14 +343,16 @@ __global__ void __launch_bounds__(kThreads, 2) tiered_attend_kernel(TieredArgs a
 {
     using C = TieredCfg<D, G>;
     extern __shared__ __align__(16) uint8_t smem[];
-    float *q_s = reinterpret_cast<float *>(smem + C::oQ);
-    float *sp = reinterpret_cast<float *>(smem + C::oSp);
-    float *P = reinterpret_cast<float *>(smem + C::oP);
+    float *sSp = reinterpret_cast<float *>(smem + C::oSp);
+    __nv_bfloat16 *sP = reinterpret_cast<__nv_bfloat16 *>(smem + C::oP);    // [hi/lo][8][PST]
+    __nv_bfloat16 *sSP = reinterpret_cast<__nv_bfloat16 *>(smem + C::oSP);  // [g][hi/lo][8][PST]
+    float *sZt = reinterpret_cast<float *>(smem + C::oZt);
+    float *sQs = reinterpret_cast<float *>(smem + C::oQs);
     float *st_m = reinterpret_cast<float *>(smem + C::oSt);
-    float *st_l = st_m + 16, *st_a = st_m + 32;
-    int *buf_win = reinterpret_cast<int *>(smem + C::oWin);
+    float *st_l = st_m + 8, *st_a = st_m + 16;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gq = lane >> 2, cq = lane & 3;  // fragment row group, column pair
     const int x = blockIdx.x, u = blockIdx.y, b = u / a.Hkv, h = u % a.Hkv;
     int64_t N = a.seq_len[b];
     if (N < 0 || N > a.cap) {
@@ -313,137 +363,205 @@ __global__ void __launch_bounds__(kThreads, 2) tiered_attend_kernel(TieredArgs a
     const int64_t w_begin = nw * x / a.S, w_end = nw * (x + 1) / a.S;
     const size_t uw = (size_t)u * a.n_win;
     const int8_t *tier = a.tier + uw;
+    const __nv_bfloat16 *qg = a.q + ((size_t)b * a.Hkv * G + (size_t)h * G) * D;
 
-    // q of the group, scaled into the log2 domain
-    for (int i = tid; i < G * D; i += kThreads)
-        q_s[i] = __bfloat162float(a.q[((size_t)b * a.Hkv * G + (size_t)h * G) * D + i]) *
-                 a.scale_log2;
-    if (tid < G) {
+    // q as B fragments (column n = head gq; heads >= G are zero)
+    uint32_t qf[C::KS][2];
+#pragma unroll
+    for (int ks = 0; ks < C::KS; ks++) {
+        qf[ks][0] = qf[ks][1] = 0u;
+        if (gq < G) {
+            const uint32_t *row = reinterpret_cast<const uint32_t *>(qg + (size_t)gq * D);
+            qf[ks][0] = row[(16 * ks + 2 * cq) / 2];
+            qf[ks][1] = row[(16 * ks + 8 + 2 * cq) / 2];
+        }
+    }
+    // per-group sums of q (the zero's share of an INT2 score); zero P rows of
+    // the padding heads; softmax state
+    if (tid < C::NG * 8) {
+        const int g = tid / 8, hh = tid % 8;
+        float sum = 0.0f;
+        if (hh < G)
+            for (int j = 0; j < kQG; j++) sum += __bfloat162float(qg[(size_t)hh * D + g * kQG + j]);
+        sQs[tid] = sum;
+    }
+    for (int i = tid; i < (2 + 2 * C::NG) * 8 * C::PST; i += kThreads) {
+        const int row = (i / C::PST) % 8;
+        if (row >= G) sP[i] = __float2bfloat16_rn(0.0f);  // sP and sSP are contiguous
+    }
+    if (tid < 8) {
         st_m[tid] = -CUDART_INF_F;
         st_l[tid] = 0.0f;
     }
-    // lse of evicted windows in the range: -inf (no mass)
-    for (int64_t w = w_begin + tid; w < w_end; w += kThreads) {
-        const int8_t t = w < closed ? tier[w] : KVR_TIER_BF16;
-        if (w < closed && checked_tier(t, a.err) == KVR_TIER_EVICTED) {
-#pragma unroll
-            for (int g = 0; g < G; g++) a.lse[(uw + w) * G + g] = -CUDART_INF_F;
-        }
-    }
-
     const uint8_t *Ku = reinterpret_cast<const uint8_t *>(a.K + (size_t)u * a.cap * D);
     const uint8_t *Vu = reinterpret_cast<const uint8_t *>(a.V + (size_t)u * a.cap * D);
     const uint8_t *Lu = a.ledger + uw * (size_t)C::LB;
 
-    // next live window at or after w (w_end if none)
-    auto next_live = [&](int64_t w) {
-        while (w < w_end && w < closed) {
-            const int8_t t = tier[w];
-            if (t == KVR_TIER_BF16 || t == KVR_TIER_INT2) break;
-            w++;
+    int32_t *sLive = reinterpret_cast<int32_t *>(smem + C::oLive);
+    int *sCnt = reinterpret_cast<int *>(smem + C::oCnt);
+
+    // output accumulators: O^T tile (16 dims x 8 heads) of warp `warp`
+    // (d=128: dims 16*warp.., all tokens; d=64: dims 16*(warp%4).., token half warp/4)
+    constexpr int PV_MT = (C::MT >= 8) ? 8 : C::MT;
+    const int mt_d = warp % PV_MT;
+    const int th = warp / PV_MT;                   // token half (d=64) or 0
+    constexpr int PV_KS = (C::MT >= 8) ? 4 : 2;    // 16-token k-steps per window per warp
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+
+    // wait until at most `pending` of this thread's newest commit groups are in flight
+    auto wait_pending = [&](int pending) {
+        switch (pending) {
+        case 0: cp_async_wait<0>(); break;
+        case 1: cp_async_wait<1>(); break;
+        case 2: cp_async_wait<2>(); break;
+        case 3: cp_async_wait<3>(); break;
+        case 4: cp_async_wait<4>(); break;
+        case 5: cp_async_wait<5>(); break;
+        case 6: cp_async_wait<6>(); break;
+        default: cp_async_wait<7>(); break;
         }
-        return w;
     };
-    // stage window w into buffer `bi`
-    auto issue = [&](int64_t w, int bi) {
-        uint8_t *buf = smem + C::oBuf + bi * C::BUF;
-        const bool int2 = w < closed && tier[w] == KVR_TIER_INT2;
-        if (int2) {
-            const uint8_t *src = Lu + (size_t)w * C::LB;
-            for (int i = tid; i < C::LB / 16; i += kThreads) cp_async16(buf + i * 16, src + i * 16);
-        } else {
-            const int64_t t0 = w * kWin;
-            const int n = (int)(N - t0 < kWin ? N - t0 : kWin);
-            constexpr int PPR = C::RB / 16;  // 16-byte pieces per row
+    static_assert(C::NS <= 8, "wait_pending covers up to 7 newer groups");
+
+    for (int64_t p0 = w_begin; p0 < w_end; p0 += C::LMAX) {
+        const int64_t p1 = (p0 + C::LMAX < w_end) ? p0 + C::LMAX : w_end;
+        // the live windows of [p0, p1) in order, bit 30 set for INT2 ones (read
+        // once here, so the pipeline below never waits on the tier array);
+        // evicted windows get no mass (log2-sum-exp -inf)
+        int nlive = 0;
+        for (int64_t r0 = p0; r0 < p1; r0 += kThreads) {
+            const int64_t w = r0 + tid;
+            int code = -1;
+            if (w < p1) {
+                if (w >= closed) {
+                    code = 0;  // the open window: bf16
+                } else {
+                    const int8_t t = checked_tier(tier[w], a.err);
+                    if (t == KVR_TIER_EVICTED) {
 #pragma unroll
-            for (int kv = 0; kv < 2; kv++) {
-                const uint8_t *base = (kv ? Vu : Ku) + (size_t)t0 * C::RB;
-                uint8_t *dst = buf + kv * kWin * C::RS;
-                for (int i = tid; i < kWin * PPR; i += kThreads) {
-                    const int r = i / PPR, pc = i % PPR;
-                    const bool in = r < n;
-                    cp_async16(dst + r * C::RS + pc * 16, base + (in ? (size_t)r * C::RB : 0) + pc * 16,
-                               in ? 16 : 0);
+                        for (int g = 0; g < G; g++) a.lse[(uw + w) * G + g] = -CUDART_INF_F;
+                    } else {
+                        code = (t == KVR_TIER_INT2) ? 1 : 0;
+                    }
                 }
             }
+            const unsigned bal = __ballot_sync(kFull, code >= 0);
+            if (lane == 0) sCnt[warp] = __popc(bal);
+            __syncthreads();
+            int before = nlive, total = nlive;
+#pragma unroll
+            for (int ww = 0; ww < kThreads / 32; ww++) {
+                before += (ww < warp) ? sCnt[ww] : 0;
+                total += sCnt[ww];
+            }
+            if (code >= 0)
+                sLive[before + __popc(bal & ((1u << lane) - 1u))] = (int32_t)w | (code << 30);
+            nlive = total;
+            __syncthreads();
         }
-        if (tid == 0) buf_win[bi] = (int)(int2 ? -(w + 1) : (w + 1));
-    };
 
-    // PV accumulators: 4 dims x G heads over the token subset ts
-    const int dg = tid % C::DG, ts = tid / C::DG;
-    float acc[G][4];
-#pragma unroll
-    for (int g = 0; g < G; g++)
-#pragma unroll
-        for (int j = 0; j < 4; j++) acc[g][j] = 0.0f;
+        // Loads in list order: a bf16 (or the open) window is two loads (K
+        // rows, then V rows), an INT2 window one (its ledger); load L goes to
+        // slot L % NS and is one cp.async commit group. The producer runs up
+        // to NS loads ahead of the consumer.
+        int pi = 0, ppart = 0;  // producer: list position, next part (0 K / ledger, 1 V)
+        int li = 0, lc = 0;     // loads issued, loads consumed (block-uniform)
+        auto issue_ahead = [&]() {
+            while (li - lc < C::NS && pi < nlive) {
+                const int32_t e = sLive[pi];
+                const int64_t pw = e & 0x3fffffff;
+                uint8_t *dst = smem + (li % C::NS) * C::SLOT;
+                if ((e >> 30) & 1) {
+                    const uint8_t *src = Lu + (size_t)pw * C::LB;
+                    for (int i = tid; i < C::LB / 16; i += kThreads) cp_async16(dst + i * 16, src + i * 16);
+                    pi++;
+                } else {
+                    const int64_t t0 = pw * kWin;
+                    const int n = (int)(N - t0 < kWin ? N - t0 : kWin);
+                    constexpr int PPR = C::RB / 16;
+                    const uint8_t *base = (ppart ? Vu : Ku) + (size_t)t0 * C::RB;
+                    for (int i = tid; i < kWin * PPR; i += kThreads) {
+                        const int r = i / PPR, pc = i % PPR;
+                        const bool in = r < n;
+                        cp_async16(dst + r * C::RS + pc * 16,
+                                   base + (in ? (size_t)r * C::RB : 0) + pc * 16, in ? 16 : 0);
+                    }
+                    if (ppart) {
+                        ppart = 0;
+                        pi++;
+                    } else {
+                        ppart = 1;
+                    }
+                }
+                cp_async_commit();
+                li++;
+            }
+        };
 
-    int64_t cur = next_live(w_begin);
-    if (cur < w_end) issue(cur, 0);
-    cp_async_commit();
-    int bi = 0;
-    while (cur < w_end) {
-        const int64_t nxt = next_live(cur + 1);
-        if (nxt < w_end) issue(nxt, bi ^ 1);
-        cp_async_commit();
-        cp_async_wait<1>();
+        for (int ci = 0; ci < nlive; ci++) {
+        const int32_t ce = sLive[ci];
+        const int64_t cur = ce & 0x3fffffff;
+        const bool int2 = (ce >> 30) & 1;
+        const int need = int2 ? 1 : 2;
+        issue_ahead();
+        wait_pending(li - lc - need);
         __syncthreads();
 
-        const uint8_t *buf = smem + C::oBuf + bi * C::BUF;
-        const bool int2 = buf_win[bi] < 0;
+        const uint8_t *buf = smem + (lc % C::NS) * C::SLOT;         // K rows or the ledger
+        const uint8_t *vbuf = smem + ((lc + 1) % C::NS) * C::SLOT;  // V rows (bf16 windows)
         const int n = (int)(N - cur * kWin < kWin ? N - cur * kWin : kWin);
 
-        // ---- scores: token t = tid % 64, part p = tid / 64 (D/4 dims)
+        // ---- scores: warp -> 16 tokens (mt), half of the dims (kh)
         {
-            const int t = tid % kWin, p = tid / kWin;
-            float s[G];
-#pragma unroll
-            for (int g = 0; g < G; g++) s[g] = 0.0f;
+            const int mt = warp & 3, kh = warp >> 2;
+            float c4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             if (!int2) {
-                const uint8_t *row = buf + t * C::RS + p * C::PART * 2;
+                const int lm = lane >> 3, lr = lane & 7;  // ldmatrix: matrix, row
+                const uint8_t *rowp = buf + (16 * mt + lr + ((lm & 1) ? 8 : 0)) * C::RS +
+                                      ((lm & 2) ? 16 : 0);
 #pragma unroll
-                for (int c = 0; c < C::PART; c += 8) {
-                    const uint4 kv4 = *reinterpret_cast<const uint4 *>(row + c * 2);
-                    const uint32_t w4[4] = {kv4.x, kv4.y, kv4.z, kv4.w};
-                    float k8[8];
-#pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        k8[2 * i] = bf16_lo(w4[i]);
-                        k8[2 * i + 1] = bf16_hi(w4[i]);
-                    }
-#pragma unroll
-                    for (int g = 0; g < G; g++) {
-                        const float4 qa = *reinterpret_cast<const float4 *>(q_s + g * D + p * C::PART + c);
-                        const float4 qb = *reinterpret_cast<const float4 *>(q_s + g * D + p * C::PART + c + 4);
-                        s[g] = fmaf(qa.x, k8[0], s[g]);
-                        s[g] = fmaf(qa.y, k8[1], s[g]);
-                        s[g] = fmaf(qa.z, k8[2], s[g]);
-                        s[g] = fmaf(qa.w, k8[3], s[g]);
-                        s[g] = fmaf(qb.x, k8[4], s[g]);
-                        s[g] = fmaf(qb.y, k8[5], s[g]);
-                        s[g] = fmaf(qb.z, k8[6], s[g]);
-                        s[g] = fmaf(qb.w, k8[7], s[g]);
-                    }
+                for (int ks = 0; ks < C::KS; ks++) {
+                    if (ks / (C::KS / 2) != kh) continue;  // warp-uniform; ks stays a constant
+                    uint32_t af[4];
+                    ldsm_x4(af, rowp + ks * 32);
+                    mma16816(c4, af, qf[ks][0], qf[ks][1]);
                 }
             } else {
-                // dims [p*PART, (p+1)*PART) of group (p*PART)/32
-                const int d0 = p * C::PART, grp = d0 / kQG, e0 = d0 % kQG;
-                const uint8_t *cb = buf + (t * C::NG + grp) * 8;
-                const uint32_t params = *reinterpret_cast<const uint32_t *>(buf + C::CB + (t * C::NG + grp) * 4);
-                const float sc = __half2float(__ushort_as_half((unsigned short)(params & 0xffffu)));
-                const float zz = __half2float(__ushort_as_half((unsigned short)(params >> 16)));
-                const uint2 cw = *reinterpret_cast<const uint2 *>(cb);
+                const int r0 = 16 * mt + gq, r1 = r0 + 8;
 #pragma unroll
-                for (int c = 0; c < C::PART; c++) {
-                    const int e = e0 + c;
-                    const uint32_t wd = e < 16 ? cw.x : cw.y;
-                    const float kx = fmaf((float)((wd >> (2 * (e & 15))) & 3u), sc, zz);
+                for (int g = 0; g < C::NG; g++) {
+                    if (g / (C::NG / 2) != kh) continue;  // warp-uniform; g stays a constant
+                    const uint2 w0 = *reinterpret_cast<const uint2 *>(buf + (r0 * C::NG + g) * 8);
+                    const uint2 w1 = *reinterpret_cast<const uint2 *>(buf + (r1 * C::NG + g) * 8);
+                    float cg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                    for (int g = 0; g < G; g++) s[g] = fmaf(q_s[g * D + d0 + c], kx, s[g]);
+                    for (int j = 0; j < 2; j++) {
+                        const uint32_t x0 = j ? w0.y : w0.x, x1 = j ? w1.y : w1.x;
+                        const int s0 = 4 * cq, s1 = 4 * cq + 16;
+                        uint32_t af[4];
+                        af[0] = codes2_bf16((x0 >> s0) & 3u, (x0 >> (s0 + 2)) & 3u);
+                        af[1] = codes2_bf16((x1 >> s0) & 3u, (x1 >> (s0 + 2)) & 3u);
+                        af[2] = codes2_bf16((x0 >> s1) & 3u, (x0 >> (s1 + 2)) & 3u);
+                        af[3] = codes2_bf16((x1 >> s1) & 3u, (x1 >> (s1 + 2)) & 3u);
+                        mma16816(cg, af, qf[2 * g + j][0], qf[2 * g + j][1]);
+                    }
+                    // value = code * s + z: score = s * (codes . q) + z * sum(q)
+                    const uint32_t p0 = *reinterpret_cast<const uint32_t *>(buf + C::CB + (r0 * C::NG + g) * 4);
+                    const uint32_t p1 = *reinterpret_cast<const uint32_t *>(buf + C::CB + (r1 * C::NG + g) * 4);
+                    const float s0f = __half2float(__ushort_as_half((unsigned short)(p0 & 0xffffu)));
+                    const float z0f = __half2float(__ushort_as_half((unsigned short)(p0 >> 16)));
+                    const float s1f = __half2float(__ushort_as_half((unsigned short)(p1 & 0xffffu)));
+                    const float z1f = __half2float(__ushort_as_half((unsigned short)(p1 >> 16)));
+                    const float qa = sQs[g * 8 + 2 * cq], qb = sQs[g * 8 + 2 * cq + 1];
+                    c4[0] += fmaf(s0f, cg[0], z0f * qa);
+                    c4[1] += fmaf(s0f, cg[1], z0f * qb);
+                    c4[2] += fmaf(s1f, cg[2], z1f * qa);
+                    c4[3] += fmaf(s1f, cg[3], z1f * qb);
                 }
             }
-#pragma unroll
-            for (int g = 0; g < G; g++) sp[(p * G + g) * kWin + t] = s[g];
+            float *sp = sSp + (size_t)kh * kWin * 8;
+            *reinterpret_cast<float2 *>(sp + (16 * mt + gq) * 8 + 2 * cq) = make_float2(c4[0], c4[1]);
+            *reinterpret_cast<float2 *>(sp + (16 * mt + gq + 8) * 8 + 2 * cq) = make_float2(c4[2], c4[3]);
         }
         __syncthreads();
 
@@ -451,12 +569,9 @@ __global__ void __launch_bounds__(kThreads, 2) tiered_attend_kernel(TieredArgs a
         if (warp < G) {
             const int g = warp;
             float s0 = -CUDART_INF_F, s1 = -CUDART_INF_F;
-            if (lane < n)
-                s0 = ((sp[(0 * G + g) * kWin + lane] + sp[(1 * G + g) * kWin + lane]) +
-                      sp[(2 * G + g) * kWin + lane]) + sp[(3 * G + g) * kWin + lane];
+            if (lane < n) s0 = (sSp[lane * 8 + g] + sSp[(kWin + lane) * 8 + g]) * a.scale_log2;
             if (lane + 32 < n)
-                s1 = ((sp[(0 * G + g) * kWin + lane + 32] + sp[(1 * G + g) * kWin + lane + 32]) +
-                      sp[(2 * G + g) * kWin + lane + 32]) + sp[(3 * G + g) * kWin + lane + 32];
+                s1 = (sSp[(lane + 32) * 8 + g] + sSp[(kWin + lane + 32) * 8 + g]) * a.scale_log2;
             float wm = fmaxf(s0, s1);
 #pragma unroll
             for (int o = 16; o; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(kFull, wm, o));
@@ -466,8 +581,37 @@ __global__ void __launch_bounds__(kThreads, 2) tiered_attend_kernel(TieredArgs a
             float ls = p0 + p1;
 #pragma unroll
             for (int o = 16; o; o >>= 1) ls += __shfl_xor_sync(kFull, ls, o);
-            P[lane * C::GP + g] = p0;
-            P[(lane + 32) * C::GP + g] = p1;
+            // P split into bf16 hi + lo (about 16 bits kept)
+            const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
+            sP[g * C::PST + lane] = h0;
+            sP[g * C::PST + lane + 32] = h1;
+            sP[(8 + g) * C::PST + lane] = __float2bfloat16_rn(p0 - __bfloat162float(h0));
+            sP[(8 + g) * C::PST + lane + 32] = __float2bfloat16_rn(p1 - __bfloat162float(h1));
+            if (int2) {
+                // V values = code * s + z: P weighted by each group's scale, and
+                // the zero's share sum_t z p per group
+                const uint8_t *vp = buf + 2 * C::CB + C::PB;  // V params
+#pragma unroll
+                for (int gg = 0; gg < C::NG; gg++) {
+                    const uint32_t q0 = *reinterpret_cast<const uint32_t *>(vp + (lane * C::NG + gg) * 4);
+                    const uint32_t q1 = *reinterpret_cast<const uint32_t *>(vp + ((lane + 32) * C::NG + gg) * 4);
+                    const float sa = __half2float(__ushort_as_half((unsigned short)(q0 & 0xffffu)));
+                    const float za = __half2float(__ushort_as_half((unsigned short)(q0 >> 16)));
+                    const float sb = __half2float(__ushort_as_half((unsigned short)(q1 & 0xffffu)));
+                    const float zb = __half2float(__ushort_as_half((unsigned short)(q1 >> 16)));
+                    const float w0 = sa * p0, w1 = sb * p1;
+                    const __nv_bfloat16 k0 = __float2bfloat16_rn(w0), k1 = __float2bfloat16_rn(w1);
+                    __nv_bfloat16 *spg = sSP + (size_t)gg * 2 * 8 * C::PST;
+                    spg[g * C::PST + lane] = k0;
+                    spg[g * C::PST + lane + 32] = k1;
+                    spg[(8 + g) * C::PST + lane] = __float2bfloat16_rn(w0 - __bfloat162float(k0));
+                    spg[(8 + g) * C::PST + lane + 32] = __float2bfloat16_rn(w1 - __bfloat162float(k1));
+                    float zs = za * p0 + zb * p1;
+#pragma unroll
+                    for (int o = 16; o; o >>= 1) zs += __shfl_xor_sync(kFull, zs, o);
+                    if (lane == 0) sZt[gg * 8 + g] = zs;
+                }
+            }
             if (lane == 0) {
                 const float al = exp2f(m_old - m_new);
                 st_a[g] = al;
@@ -478,85 +622,99 @@ __global__ void __launch_bounds__(kThreads, 2) tiered_attend_kernel(TieredArgs a
         }
         __syncthreads();
 
-        // ---- PV: 4 dims (dg) x G heads over tokens ts, ts + TS, ...
+        // ---- output: O^T (dims x heads) += V^T P^T for this warp's 16 dims
         {
-            float al[G];
-#pragma unroll
-            for (int g = 0; g < G; g++) al[g] = st_a[g];
-#pragma unroll
-            for (int g = 0; g < G; g++)
-#pragma unroll
-                for (int j = 0; j < 4; j++) acc[g][j] *= al[g];
+            const float al0 = (2 * cq < G) ? st_a[2 * cq] : 0.0f;
+            const float al1 = (2 * cq + 1 < G) ? st_a[2 * cq + 1] : 0.0f;
+            acc[0] *= al0;
+            acc[1] *= al1;
+            acc[2] *= al0;
+            acc[3] *= al1;
             if (!int2) {
-                const uint8_t *vbase = buf + kWin * C::RS + dg * 8;
+                const int lm = lane >> 3, lr = lane & 7;  // ldmatrix: matrix, row
+                const uint8_t *vrow = vbuf + (lr + ((lm & 2) ? 8 : 0)) * C::RS +
+                                      (16 * mt_d + ((lm & 1) ? 8 : 0)) * 2;
 #pragma unroll
-                for (int i = 0; i < C::TPT; i++) {
-                    const int t = ts + i * C::TS;
-                    const uint2 vv = *reinterpret_cast<const uint2 *>(vbase + t * C::RS);
-                    const float v4[4] = {bf16_lo(vv.x), bf16_hi(vv.x), bf16_lo(vv.y), bf16_hi(vv.y)};
-                    float pg[C::GP];
-#pragma unroll
-                    for (int g = 0; g < C::GP; g += 4) {
-                        const float4 pp = *reinterpret_cast<const float4 *>(P + t * C::GP + g);
-                        pg[g] = pp.x;
-                        pg[g + 1] = pp.y;
-                        pg[g + 2] = pp.z;
-                        pg[g + 3] = pp.w;
-                    }
-#pragma unroll
-                    for (int g = 0; g < G; g++)
-#pragma unroll
-                        for (int j = 0; j < 4; j++) acc[g][j] = fmaf(pg[g], v4[j], acc[g][j]);
+                for (int j = 0; j < PV_KS; j++) {
+                    const int t0 = 16 * (th * PV_KS + j);
+                    uint32_t af[4];
+                    ldsm_x4_t(af, vrow + t0 * C::RS);
+                    const __nv_bfloat16 *ph = sP + gq * C::PST + t0 + 2 * cq;
+                    const __nv_bfloat16 *pl = sP + (8 + gq) * C::PST + t0 + 2 * cq;
+                    mma16816(acc, af, *reinterpret_cast<const uint32_t *>(ph),
+                             *reinterpret_cast<const uint32_t *>(ph + 8));
+                    mma16816(acc, af, *reinterpret_cast<const uint32_t *>(pl),
+                             *reinterpret_cast<const uint32_t *>(pl + 8));
                 }
             } else {
+                const int g = (16 * mt_d) / kQG, wsel = ((16 * mt_d) % kQG) / 16;
                 const uint8_t *vc = buf + C::CB + C::PB;  // V codes
-                const uint8_t *vp = vc + C::CB;           // V params
-                const int grp = (4 * dg) / kQG, e0 = (4 * dg) % kQG;
+                const __nv_bfloat16 *spg = sSP + (size_t)g * 2 * 8 * C::PST;
 #pragma unroll
-                for (int i = 0; i < C::TPT; i++) {
-                    const int t = ts + i * C::TS;
-                    const uint32_t byte = vc[(t * C::NG + grp) * 8 + e0 / 4];
-                    const uint32_t params = *reinterpret_cast<const uint32_t *>(vp + (t * C::NG + grp) * 4);
-                    const float sc = __half2float(__ushort_as_half((unsigned short)(params & 0xffffu)));
-                    const float zz = __half2float(__ushort_as_half((unsigned short)(params >> 16)));
-                    float v4[4];
-#pragma unroll
-                    for (int j = 0; j < 4; j++) v4[j] = fmaf((float)((byte >> (2 * j)) & 3u), sc, zz);
-                    float pg[C::GP];
-#pragma unroll
-                    for (int g = 0; g < C::GP; g += 4) {
-                        const float4 pp = *reinterpret_cast<const float4 *>(P + t * C::GP + g);
-                        pg[g] = pp.x;
-                        pg[g + 1] = pp.y;
-                        pg[g + 2] = pp.z;
-                        pg[g + 3] = pp.w;
-                    }
-#pragma unroll
-                    for (int g = 0; g < G; g++)
-#pragma unroll
-                        for (int j = 0; j < 4; j++) acc[g][j] = fmaf(pg[g], v4[j], acc[g][j]);
+                for (int j = 0; j < PV_KS; j++) {
+                    const int t0 = 16 * (th * PV_KS + j);
+                    const int ta = t0 + 2 * cq;
+                    const uint32_t wa = *reinterpret_cast<const uint32_t *>(vc + (ta * C::NG + g) * 8 + 4 * wsel);
+                    const uint32_t wb = *reinterpret_cast<const uint32_t *>(vc + ((ta + 1) * C::NG + g) * 8 + 4 * wsel);
+                    const uint32_t wc = *reinterpret_cast<const uint32_t *>(vc + ((ta + 8) * C::NG + g) * 8 + 4 * wsel);
+                    const uint32_t wd = *reinterpret_cast<const uint32_t *>(vc + ((ta + 9) * C::NG + g) * 8 + 4 * wsel);
+                    const int e0 = 2 * gq, e1 = 2 * (gq + 8);
+                    uint32_t af[4];
+                    af[0] = codes2_bf16((wa >> e0) & 3u, (wb >> e0) & 3u);
+                    af[1] = codes2_bf16((wa >> e1) & 3u, (wb >> e1) & 3u);
+                    af[2] = codes2_bf16((wc >> e0) & 3u, (wd >> e0) & 3u);
+                    af[3] = codes2_bf16((wc >> e1) & 3u, (wd >> e1) & 3u);
+                    const __nv_bfloat16 *ph = spg + gq * C::PST + t0 + 2 * cq;
+                    const __nv_bfloat16 *pl = spg + (8 + gq) * C::PST + t0 + 2 * cq;
+                    mma16816(acc, af, *reinterpret_cast<const uint32_t *>(ph),
+                             *reinterpret_cast<const uint32_t *>(ph + 8));
+                    mma16816(acc, af, *reinterpret_cast<const uint32_t *>(pl),
+                             *reinterpret_cast<const uint32_t *>(pl + 8));
+                }
+                if (th == 0) {
+                    const float za = (2 * cq < G) ? sZt[g * 8 + 2 * cq] : 0.0f;
+                    const float zb = (2 * cq + 1 < G) ? sZt[g * 8 + 2 * cq + 1] : 0.0f;
+                    acc[0] += za;
+                    acc[1] += zb;
+                    acc[2] += za;
+                    acc[3] += zb;
                 }
             }
         }
-        __syncthreads();  // buffer bi and P are reused next
-        cur = nxt;
-        bi ^= 1;
+        __syncthreads();  // the window's slots, P and the partial scores are reused next
+        lc += need;
+        }
     }
     cp_async_wait<0>();
     __syncthreads();
 
-    // ---- reduce the token subsets: red[ts][g][D] in the staging buffers
-    float *red = reinterpret_cast<float *>(smem + C::oBuf);
-#pragma unroll
-    for (int g = 0; g < G; g++)
-        *reinterpret_cast<float4 *>(red + ((size_t)ts * G + g) * D + 4 * dg) =
-            make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
-    __syncthreads();
+    // ---- this CTA's partial: o[head][dim] unnormalised, m, l per head
     float *part = a.part + ((size_t)u * a.S + x) * (2 * G + G * D);
-    for (int i = tid; i < G * D; i += kThreads) {
-        float o = 0.0f;
-        for (int r = 0; r < C::TS; r++) o += red[(size_t)r * G * D + i];
-        part[2 * G + i] = o;
+    if constexpr (PV_MT < 8) {
+        // d = 64: add the two token halves
+        float *red = reinterpret_cast<float *>(smem);
+        if (th == 1)
+            *reinterpret_cast<float4 *>(red + (mt_d * 32 + lane) * 4) =
+                make_float4(acc[0], acc[1], acc[2], acc[3]);
+        __syncthreads();
+        if (th == 0) {
+            const float4 o = *reinterpret_cast<const float4 *>(red + (mt_d * 32 + lane) * 4);
+            acc[0] += o.x;
+            acc[1] += o.y;
+            acc[2] += o.z;
+            acc[3] += o.w;
+        }
+    }
+    if (th == 0) {
+        const int d0 = 16 * mt_d + gq;
+        if (2 * cq < G) {
+            part[2 * G + (2 * cq) * D + d0] = acc[0];
+            part[2 * G + (2 * cq) * D + d0 + 8] = acc[2];
+        }
+        if (2 * cq + 1 < G) {
+            part[2 * G + (2 * cq + 1) * D + d0] = acc[1];
+            part[2 * G + (2 * cq + 1) * D + d0 + 8] = acc[3];
+        }
     }
     if (tid < G) {
         part[tid] = st_m[tid];
@@ -660,29 +818,44 @@ __global__ void __launch_bounds__(kRankThreads) tier_rank_kernel(RankArgs r)
         s_moves = 0;
     }
     __syncthreads();
-    // 1. scores; 2. collect the live closed windows
-    for (int64_t w = tid; w < nw; w += kRankThreads) {
-        const int8_t t = checked_tier(a.tier[uw + w], r.err);
-        if (t == KVR_TIER_EVICTED) continue;
-        const int64_t sc = a.score[uw + w] + __float2ll_rn(r.mass[uw + w] * 4294967296.0f);
-        a.score[uw + w] = sc;
-        if (w < closed) {
-            const int i = atomicAdd(&s_live, 1);
+    // 1. scores; 2. collect the live closed windows (one shared-memory
+    // atomic per warp and round: ballot, then each lane's rank in the warp)
+    const int lane = tid & 31;
+    for (int64_t w0 = 0; w0 < nw; w0 += kRankThreads) {
+        const int64_t w = w0 + tid;
+        bool take = false;
+        int64_t sc = 0;
+        if (w < nw) {
+            const int8_t t = checked_tier(a.tier[uw + w], r.err);
+            if (t != KVR_TIER_EVICTED) {
+                sc = a.score[uw + w] + __float2ll_rn(r.mass[uw + w] * 4294967296.0f);
+                a.score[uw + w] = sc;
+                take = w < closed;
+            }
+        }
+        const unsigned bal = __ballot_sync(kFull, take);
+        int base = 0;
+        if (lane == 0 && bal) base = atomicAdd(&s_live, __popc(bal));
+        base = __shfl_sync(kFull, base, 0);
+        if (take) {
+            const int i = base + __popc(bal & ((1u << lane) - 1u));
             key[i] = sc;
             win[i] = (int32_t)w;
         }
     }
     __syncthreads();
     const int live = s_live;
-    for (int i = live + tid; i < r.P; i += kRankThreads) {
+    int P = 2;  // sort length: the next power of two of the live count
+    while (P < live) P <<= 1;
+    for (int i = live + tid; i < P; i += kRankThreads) {
         key[i] = INT64_MIN;
         win[i] = INT32_MAX;
     }
     __syncthreads();
     // bitonic sort of [0, P) into rank order
-    for (int k = 2; k <= r.P; k <<= 1) {
+    for (int k = 2; k <= P; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = tid; i < r.P; i += kRankThreads) {
+            for (int i = tid; i < P; i += kRankThreads) {
                 const int l = i ^ j;
                 if (l > i) {
                     const bool up = (i & k) == 0;  // this block in rank order
@@ -749,10 +922,14 @@ __global__ void __launch_bounds__(kThreads) tier_move_kernel(TierArgs a, const i
 {
     const int u = blockIdx.y;
     const size_t uw = (size_t)u * a.n_win;
-    const int n = n_moves[u];
+    const int n = min(max(n_moves[u], 0), (int)a.n_win);
     for (int i = blockIdx.x; i < n; i += gridDim.x) {
         const int32_t e = moves[uw + i];
         const int64_t w = e & ((1 << 30) - 1);
+        if (e < 0 || (w + 1) * kWin > a.cap) {  // never written by the ranking
+            if (threadIdx.x == 0) set_err(err, KVR_DEVERR_INDEX);
+            continue;
+        }
         const size_t row = (size_t)u * a.cap + (size_t)w * kWin;
         uint8_t *lg = a.ledger + (uw + w) * (size_t)ledger_bytes_of(D);
         if (e >> 30) dequantize_window<D>(lg, K + row * D, V + row * D);
@@ -813,6 +990,7 @@ kvr_status tier_init_dispatch(const LaunchCtx &c, const kvr_tier_state &s, const
         tier_init_kernel<128><<<grid, kThreads, 0, c.stream>>>(a, init, Kb, Vb, seq_len, err);
     else
         tier_init_kernel<64><<<grid, kThreads, 0, c.stream>>>(a, init, Kb, Vb, seq_len, err);
+    if (check_launch() != KVR_OK) return KVR_ERR_CUDA;
     tier_count_kernel<<<U, kThreads, 0, c.stream>>>(a, seq_len);
     return check_launch();
 }
@@ -826,6 +1004,7 @@ static kvr_status tiered_launch(const LaunchCtx &c, TieredArgs a, float *out, fl
     if (st != KVR_OK) return st;
     const int U = c.shape.B * c.shape.Hkv;
     tiered_attend_kernel<D, G><<<dim3(a.S, U), kThreads, C::bytes, c.stream>>>(a);
+    if (check_launch() != KVR_OK) return KVR_ERR_CUDA;  // the combine reads its partials
     tiered_combine_kernel<D, G><<<U, kThreads, 0, c.stream>>>(a, out, mass);
     return check_launch();
 }
@@ -891,6 +1070,9 @@ kvr_status tier_update_dispatch(const LaunchCtx &c, const kvr_tier_state &s, con
     kvr_status st = raise_smem_limit(reinterpret_cast<const void *>(&tier_rank_kernel), smem);
     if (st != KVR_OK) return st;
     tier_rank_kernel<<<U, kRankThreads, smem, c.stream>>>(r);
+    // the move kernel reads the lists the ranking writes: never launch it
+    // after a ranking that did not launch
+    if (check_launch() != KVR_OK) return KVR_ERR_CUDA;
     const dim3 grid(kMoveX, (unsigned)U);
     auto *Kb = static_cast<__nv_bfloat16 *>(K);
     auto *Vb = static_cast<__nv_bfloat16 *>(V);
