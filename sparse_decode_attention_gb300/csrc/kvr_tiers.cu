@@ -26,6 +26,10 @@
 //                        ledger, dequantise promoted windows into K, V
 #include <algorithm>
 
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math_constants.h>
@@ -308,23 +312,37 @@ __device__ __forceinline__ uint32_t codes2_bf16(uint32_t ca, uint32_t cb)
     return r;
 }
 
+// 2-D tensor-map copy of one box into shared memory, completing on `bar`
+// (x: innermost coordinate in elements, a multiple of 8 for 2-byte elements).
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+        "{%2, %3}], [%4];\n" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
 template <int D, int G> struct TieredCfg {
     static constexpr int RB = 2 * D;                   // bf16 row bytes
-    static constexpr int RS = RB + 16;                 // padded row stride in shared memory
     static constexpr int NG = D / kQG;                 // INT2 groups per row
     static constexpr int LB = ledger_bytes_of(D);
     static constexpr int CB = kWin * NG * 8, PB = kWin * NG * 4;
-    // staging ring: a slot holds the 64 K (or V) rows of a bf16 window, or an
-    // INT2 window's ledger; slots are filled ahead in window order
-    static constexpr int SLOT = kWin * RS;
+    // staging ring: a slot holds the 64 K (or V) rows of a bf16 window as
+    // 128-byte-swizzled boxes of 64 rows x 64 dims (TMA), or an INT2 window's
+    // ledger (bulk copy); slots are filled ahead in window order
+    static constexpr int SLOT = kWin * RB;
     static constexpr int NS = (D >= 128) ? 5 : 8;
+    static constexpr int BOXES = D / 64;                 // 128-byte column boxes per row
     static_assert(LB <= SLOT, "a ledger fits a slot");
     static constexpr int KS = D / 16;                  // k-steps of the score product
     static constexpr int MT = D / 16;                  // 16-dim tiles of the output
     static constexpr int PST = kWin + 8;               // bf16 stride of a P row (no bank conflicts)
     // shared memory: the staging ring, partial scores, P (hi, lo), the
     // scale-weighted P of each INT2 group (hi, lo), z terms, softmax state
-    static constexpr int oSp = NS * SLOT;                      // float [2][kWin][8]
+    static constexpr int oBar = NS * SLOT;                     // uint64 [NS] slot barriers
+    static constexpr int oSp = oBar + 64;                      // float [2][kWin][8]
     static constexpr int oP = oSp + 2 * kWin * 8 * 4;          // bf16 [2][8][PST]
     static constexpr int oSP = oP + 2 * 8 * PST * 2;           // bf16 [NG][2][8][PST]
     static constexpr int oZt = oSP + NG * 2 * 8 * PST * 2;     // float [NG][8]
@@ -333,16 +351,21 @@ template <int D, int G> struct TieredCfg {
     static constexpr int LMAX = 1024;                          // windows per listing pass
     static constexpr int oLive = oSt + 3 * 8 * 4;              // int32 [LMAX] live windows
     static constexpr int oCnt = oLive + LMAX * 4;              // int [8] per-warp counts
-    static constexpr int bytes = oCnt + 8 * 4;
+    static constexpr int bytes = oCnt + 8 * 4 + 1024;         // + alignment of the ring to 1 KB
     static_assert(G <= 8, "one 8-column tile of heads");
     static_assert(8 * 16 * 8 * 4 <= NS * SLOT, "the d=64 token-half reduction fits the ring");
 };
 
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 2) tiered_attend_kernel(TieredArgs a)
+__global__ void __launch_bounds__(kThreads, 2)
+    tiered_attend_kernel(TieredArgs a, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV)
 {
     using C = TieredCfg<D, G>;
-    extern __shared__ __align__(16) uint8_t smem[];
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    // the ring's 128-byte swizzle repeats every 1 KB: align its base to 1 KB
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t *sBar = reinterpret_cast<uint64_t *>(smem + C::oBar);
     float *sSp = reinterpret_cast<float *>(smem + C::oSp);
     __nv_bfloat16 *sP = reinterpret_cast<__nv_bfloat16 *>(smem + C::oP);    // [hi/lo][8][PST]
     __nv_bfloat16 *sSP = reinterpret_cast<__nv_bfloat16 *>(smem + C::oSP);  // [g][hi/lo][8][PST]
@@ -393,8 +416,11 @@ __global__ void __launch_bounds__(kThreads, 2) tiered_attend_kernel(TieredArgs a
         st_m[tid] = -CUDART_INF_F;
         st_l[tid] = 0.0f;
     }
-    const uint8_t *Ku = reinterpret_cast<const uint8_t *>(a.K + (size_t)u * a.cap * D);
-    const uint8_t *Vu = reinterpret_cast<const uint8_t *>(a.V + (size_t)u * a.cap * D);
+    if (tid == 0) {
+        for (int i = 0; i < C::NS; i++) mbar_init(&sBar[i], 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
     const uint8_t *Lu = a.ledger + uw * (size_t)C::LB;
 
     int32_t *sLive = reinterpret_cast<int32_t *>(smem + C::oLive);
@@ -408,21 +434,7 @@ __global__ void __launch_bounds__(kThreads, 2) tiered_attend_kernel(TieredArgs a
     constexpr int PV_KS = (C::MT >= 8) ? 4 : 2;    // 16-token k-steps per window per warp
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 
-    // wait until at most `pending` of this thread's newest commit groups are in flight
-    auto wait_pending = [&](int pending) {
-        switch (pending) {
-        case 0: cp_async_wait<0>(); break;
-        case 1: cp_async_wait<1>(); break;
-        case 2: cp_async_wait<2>(); break;
-        case 3: cp_async_wait<3>(); break;
-        case 4: cp_async_wait<4>(); break;
-        case 5: cp_async_wait<5>(); break;
-        case 6: cp_async_wait<6>(); break;
-        default: cp_async_wait<7>(); break;
-        }
-    };
-    static_assert(C::NS <= 8, "wait_pending covers up to 7 newer groups");
-
+    int li = 0, lc = 0;  // loads issued, loads consumed (block-uniform, across passes)
     for (int64_t p0 = w_begin; p0 < w_end; p0 += C::LMAX) {
         const int64_t p1 = (p0 + C::LMAX < w_end) ? p0 + C::LMAX : w_end;
         // the live windows of [p0, p1) in order, bit 30 set for INT2 ones (read
@@ -460,40 +472,41 @@ __global__ void __launch_bounds__(kThreads, 2) tiered_attend_kernel(TieredArgs a
             __syncthreads();
         }
 
-        // Loads in list order: a bf16 (or the open) window is two loads (K
-        // rows, then V rows), an INT2 window one (its ledger); load L goes to
-        // slot L % NS and is one cp.async commit group. The producer runs up
-        // to NS loads ahead of the consumer.
+        // Loads in list order: a bf16 (or the open) window is two loads (its 64
+        // K rows, then its 64 V rows, as 128-byte-swizzled tensor-map boxes),
+        // an INT2 window one (its ledger, one bulk copy). Load L fills slot
+        // L % NS and completes phase (L / NS) & 1 of that slot's barrier; one
+        // thread issues, up to NS loads ahead of the consumer.
         int pi = 0, ppart = 0;  // producer: list position, next part (0 K / ledger, 1 V)
-        int li = 0, lc = 0;     // loads issued, loads consumed (block-uniform)
         auto issue_ahead = [&]() {
             while (li - lc < C::NS && pi < nlive) {
                 const int32_t e = sLive[pi];
                 const int64_t pw = e & 0x3fffffff;
-                uint8_t *dst = smem + (li % C::NS) * C::SLOT;
-                if ((e >> 30) & 1) {
-                    const uint8_t *src = Lu + (size_t)pw * C::LB;
-                    for (int i = tid; i < C::LB / 16; i += kThreads) cp_async16(dst + i * 16, src + i * 16);
-                    pi++;
-                } else {
-                    const int64_t t0 = pw * kWin;
-                    const int n = (int)(N - t0 < kWin ? N - t0 : kWin);
-                    constexpr int PPR = C::RB / 16;
-                    const uint8_t *base = (ppart ? Vu : Ku) + (size_t)t0 * C::RB;
-                    for (int i = tid; i < kWin * PPR; i += kThreads) {
-                        const int r = i / PPR, pc = i % PPR;
-                        const bool in = r < n;
-                        cp_async16(dst + r * C::RS + pc * 16,
-                                   base + (in ? (size_t)r * C::RB : 0) + pc * 16, in ? 16 : 0);
-                    }
-                    if (ppart) {
-                        ppart = 0;
-                        pi++;
+                const int slot = li % C::NS;
+                uint8_t *dst = smem + slot * C::SLOT;
+                const bool q2 = (e >> 30) & 1;
+                if (tid == 0) {
+                    fence_proxy_async();  // earlier reads of the slot before the async writes
+                    if (q2) {
+                        mbar_arrive_expect_tx(&sBar[slot], C::LB);
+                        bulk_g2s(dst, Lu + (size_t)pw * C::LB, C::LB, &sBar[slot]);
                     } else {
-                        ppart = 1;
+                        mbar_arrive_expect_tx(&sBar[slot], C::SLOT);
+                        const int y = (int)((int64_t)u * a.cap + pw * kWin);
+#pragma unroll
+                        for (int bx = 0; bx < C::BOXES; bx++)
+                            tma_load_2d(dst + bx * kWin * 128, ppart ? &tmV : &tmK, 64 * bx, y,
+                                        &sBar[slot]);
                     }
                 }
-                cp_async_commit();
+                if (q2) {
+                    pi++;
+                } else if (ppart) {
+                    ppart = 0;
+                    pi++;
+                } else {
+                    ppart = 1;
+                }
                 li++;
             }
         };
@@ -504,12 +517,22 @@ __global__ void __launch_bounds__(kThreads, 2) tiered_attend_kernel(TieredArgs a
         const bool int2 = (ce >> 30) & 1;
         const int need = int2 ? 1 : 2;
         issue_ahead();
-        wait_pending(li - lc - need);
-        __syncthreads();
-
-        const uint8_t *buf = smem + (lc % C::NS) * C::SLOT;         // K rows or the ledger
-        const uint8_t *vbuf = smem + ((lc + 1) % C::NS) * C::SLOT;  // V rows (bf16 windows)
+        const uint8_t *buf = smem + (lc % C::NS) * C::SLOT;   // K rows or the ledger
+        uint8_t *vbuf = smem + ((lc + 1) % C::NS) * C::SLOT;  // V rows (bf16 windows)
         const int n = (int)(N - cur * kWin < kWin ? N - cur * kWin : kWin);
+        mbar_wait(&sBar[lc % C::NS], (uint32_t)((lc / C::NS) & 1), a.err);
+        if (!int2) {
+            mbar_wait(&sBar[(lc + 1) % C::NS], (uint32_t)(((lc + 1) / C::NS) & 1), a.err);
+            // rows past the sequence in the open window: whatever the cache holds
+            // there must not reach the sum (0 * NaN), so zero them
+            if (n < kWin)
+                for (int i = tid; i < C::BOXES * (kWin - n) * 8; i += kThreads) {
+                    const int bx = i / ((kWin - n) * 8), rem = i % ((kWin - n) * 8);
+                    *reinterpret_cast<uint4 *>(vbuf + bx * kWin * 128 + (n + rem / 8) * 128 +
+                                               (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+        }
+        __syncthreads();
 
         // ---- scores: warp -> 16 tokens (mt), half of the dims (kh)
         {
@@ -517,13 +540,14 @@ __global__ void __launch_bounds__(kThreads, 2) tiered_attend_kernel(TieredArgs a
             float c4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             if (!int2) {
                 const int lm = lane >> 3, lr = lane & 7;  // ldmatrix: matrix, row
-                const uint8_t *rowp = buf + (16 * mt + lr + ((lm & 1) ? 8 : 0)) * C::RS +
-                                      ((lm & 2) ? 16 : 0);
+                // row r, 16-byte chunk c of a box sits at r*128 + ((c ^ (r % 8)) * 16)
+                const uint8_t *rowp = buf + (16 * mt + lr + ((lm & 1) ? 8 : 0)) * 128;
 #pragma unroll
                 for (int ks = 0; ks < C::KS; ks++) {
                     if (ks / (C::KS / 2) != kh) continue;  // warp-uniform; ks stays a constant
+                    const int ch = 2 * ks + ((lm & 2) ? 1 : 0);
                     uint32_t af[4];
-                    ldsm_x4(af, rowp + ks * 32);
+                    ldsm_x4(af, rowp + (ch >> 3) * kWin * 128 + (((ch & 7) ^ lr) << 4));
                     mma16816(c4, af, qf[ks][0], qf[ks][1]);
                 }
             } else {
@@ -632,13 +656,14 @@ __global__ void __launch_bounds__(kThreads, 2) tiered_attend_kernel(TieredArgs a
             acc[3] *= al1;
             if (!int2) {
                 const int lm = lane >> 3, lr = lane & 7;  // ldmatrix: matrix, row
-                const uint8_t *vrow = vbuf + (lr + ((lm & 2) ? 8 : 0)) * C::RS +
-                                      (16 * mt_d + ((lm & 1) ? 8 : 0)) * 2;
+                const int ch = 2 * mt_d + ((lm & 1) ? 1 : 0);
+                const uint8_t *vrow = vbuf + (ch >> 3) * kWin * 128 +
+                                      (lr + ((lm & 2) ? 8 : 0)) * 128 + (((ch & 7) ^ lr) << 4);
 #pragma unroll
                 for (int j = 0; j < PV_KS; j++) {
                     const int t0 = 16 * (th * PV_KS + j);
                     uint32_t af[4];
-                    ldsm_x4_t(af, vrow + t0 * C::RS);
+                    ldsm_x4_t(af, vrow + t0 * 128);
                     const __nv_bfloat16 *ph = sP + gq * C::PST + t0 + 2 * cq;
                     const __nv_bfloat16 *pl = sP + (8 + gq) * C::PST + t0 + 2 * cq;
                     mma16816(acc, af, *reinterpret_cast<const uint32_t *>(ph),
@@ -681,11 +706,11 @@ __global__ void __launch_bounds__(kThreads, 2) tiered_attend_kernel(TieredArgs a
                 }
             }
         }
-        __syncthreads();  // the window's slots, P and the partial scores are reused next
+        fence_proxy_async();  // this thread's slot accesses before the next copies into it
+        __syncthreads();      // the window's slots, P and the partial scores are reused next
         lc += need;
         }
     }
-    cp_async_wait<0>();
     __syncthreads();
 
     // ---- this CTA's partial: o[head][dim] unnormalised, m, l per head
@@ -995,6 +1020,36 @@ kvr_status tier_init_dispatch(const LaunchCtx &c, const kvr_tier_state &s, const
     return check_launch();
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// Tensor map of a bf16 cache viewed as rows x d elements: boxes of 64 rows x
+// 64 dims (128 bytes) with the 128-byte swizzle; rows past the end read as zero.
+static bool rows_map(CUtensorMap *m, const void *base, int d, uint64_t rows)
+{
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kWin};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D, int G>
 static kvr_status tiered_launch(const LaunchCtx &c, TieredArgs a, float *out, float *mass)
 {
@@ -1003,7 +1058,10 @@ static kvr_status tiered_launch(const LaunchCtx &c, TieredArgs a, float *out, fl
     kvr_status st = raise_smem_limit(k, C::bytes);
     if (st != KVR_OK) return st;
     const int U = c.shape.B * c.shape.Hkv;
-    tiered_attend_kernel<D, G><<<dim3(a.S, U), kThreads, C::bytes, c.stream>>>(a);
+    CUtensorMap tmK, tmV;
+    const uint64_t rows = (uint64_t)U * (uint64_t)c.shape.cap;
+    if (!rows_map(&tmK, a.K, D, rows) || !rows_map(&tmV, a.V, D, rows)) return KVR_ERR_CUDA;
+    tiered_attend_kernel<D, G><<<dim3(a.S, U), kThreads, C::bytes, c.stream>>>(a, tmK, tmV);
     if (check_launch() != KVR_OK) return KVR_ERR_CUDA;  // the combine reads its partials
     tiered_combine_kernel<D, G><<<U, kThreads, 0, c.stream>>>(a, out, mass);
     return check_launch();
@@ -1086,7 +1144,9 @@ kvr_status tier_update_dispatch(const LaunchCtx &c, const kvr_tier_state &s, con
 bool tier_shape_ok(const kvr_shape &s, int64_t n_win)
 {
     const int G = s.Hq / s.Hkv;
-    return s.dtype == KVR_BF16 && G <= 8 && n_win <= kMaxWin && n_win * kWin >= s.cap;
+    // tensor-map row coordinates are int32
+    return s.dtype == KVR_BF16 && G <= 8 && n_win <= kMaxWin && n_win * kWin >= s.cap &&
+           (int64_t)s.B * s.Hkv * s.cap < ((int64_t)1 << 31);
 }
 
 }  // namespace kvr
