@@ -334,26 +334,29 @@ template <int D, int G> struct TieredCfg {
     // ledger (bulk copy); slots are filled ahead in window order
     static constexpr int SLOT = kWin * RB;
     static constexpr int NS = (D >= 128) ? 5 : 8;
-    static constexpr int BOXES = D / 64;                 // 128-byte column boxes per row
+    static constexpr int BOXES = D / 64;               // 128-byte column boxes per row
     static_assert(LB <= SLOT, "a ledger fits a slot");
     static constexpr int KS = D / 16;                  // k-steps of the score product
     static constexpr int MT = D / 16;                  // 16-dim tiles of the output
     static constexpr int PST = kWin + 8;               // bf16 stride of a P row (no bank conflicts)
-    // shared memory: the staging ring, partial scores, P (hi, lo), the
-    // scale-weighted P of each INT2 group (hi, lo), z terms, softmax state
-    static constexpr int oBar = NS * SLOT;                     // uint64 [NS] slot barriers
-    static constexpr int oSp = oBar + 64;                      // float [2][kWin][8]
-    static constexpr int oP = oSp + 2 * kWin * 8 * 4;          // bf16 [2][8][PST]
-    static constexpr int oSP = oP + 2 * 8 * PST * 2;           // bf16 [NG][2][8][PST]
-    static constexpr int oZt = oSP + NG * 2 * 8 * PST * 2;     // float [NG][8]
-    static constexpr int oQs = oZt + NG * 8 * 4;               // float [NG][8]
-    static constexpr int oSt = oQs + NG * 8 * 4;               // float m[8], l[8], alpha[8]
-    static constexpr int LMAX = 1024;                          // windows per listing pass
-    static constexpr int oLive = oSt + 3 * 8 * 4;              // int32 [LMAX] live windows
-    static constexpr int oCnt = oLive + LMAX * 4;              // int [8] per-warp counts
-    static constexpr int bytes = oCnt + 8 * 4 + 1024;         // + alignment of the ring to 1 KB
+    static constexpr int NSTR = 2;                     // softmax streams: even / odd windows
+    // shared memory after the ring: slot barriers, scores, P (hi, lo), the
+    // scale-weighted P of each INT2 group (hi, lo), z terms, q sums, stream
+    // states, the live-window list
+    static constexpr int oBar = NS * SLOT;                        // uint64 [NS]
+    static constexpr int oSp = oBar + 64;                         // float [NSTR][kWin][8]
+    static constexpr int oP = oSp + NSTR * kWin * 8 * 4;          // bf16 [NSTR][2][8][PST]
+    static constexpr int oSP = oP + NSTR * 2 * 8 * PST * 2;       // bf16 [NSTR][NG][2][8][PST]
+    static constexpr int oZt = oSP + NSTR * NG * 2 * 8 * PST * 2; // float [NSTR][NG][8]
+    static constexpr int oQs = oZt + NSTR * NG * 8 * 4;           // float [NG][8]
+    static constexpr int oSt = oQs + NG * 8 * 4;                  // float [NSTR][m, l, alpha][8]
+    static constexpr int LMAX = 1024;                             // windows per listing pass
+    static constexpr int oLive = oSt + NSTR * 3 * 8 * 4;          // int32 [LMAX]
+    static constexpr int oCnt = oLive + LMAX * 4;                 // int [8]
+    static constexpr int bytes = oCnt + 8 * 4 + 1024;             // + alignment of the ring
     static_assert(G <= 8, "one 8-column tile of heads");
-    static_assert(8 * 16 * 8 * 4 <= NS * SLOT, "the d=64 token-half reduction fits the ring");
+    static_assert(NS >= 4, "a pair of bf16 windows takes four slots");
+    static_assert(8 * 32 * 4 * 4 <= NS * SLOT, "the d=64 stream merge fits the ring");
 };
 
 template <int D, int G>
@@ -367,12 +370,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *sBar = reinterpret_cast<uint64_t *>(smem + C::oBar);
     float *sSp = reinterpret_cast<float *>(smem + C::oSp);
-    __nv_bfloat16 *sP = reinterpret_cast<__nv_bfloat16 *>(smem + C::oP);    // [hi/lo][8][PST]
-    __nv_bfloat16 *sSP = reinterpret_cast<__nv_bfloat16 *>(smem + C::oSP);  // [g][hi/lo][8][PST]
+    __nv_bfloat16 *sP = reinterpret_cast<__nv_bfloat16 *>(smem + C::oP);
+    __nv_bfloat16 *sSP = reinterpret_cast<__nv_bfloat16 *>(smem + C::oSP);
     float *sZt = reinterpret_cast<float *>(smem + C::oZt);
     float *sQs = reinterpret_cast<float *>(smem + C::oQs);
-    float *st_m = reinterpret_cast<float *>(smem + C::oSt);
-    float *st_l = st_m + 8, *st_a = st_m + 16;
+    float *sSt = reinterpret_cast<float *>(smem + C::oSt);  // stream st: m at st*24, l +8, alpha +16
+    int32_t *sLive = reinterpret_cast<int32_t *>(smem + C::oLive);
+    int *sCnt = reinterpret_cast<int *>(smem + C::oCnt);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gq = lane >> 2, cq = lane & 3;  // fragment row group, column pair
@@ -387,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const size_t uw = (size_t)u * a.n_win;
     const int8_t *tier = a.tier + uw;
     const __nv_bfloat16 *qg = a.q + ((size_t)b * a.Hkv * G + (size_t)h * G) * D;
+    const uint8_t *Lu = a.ledger + uw * (size_t)C::LB;
 
     // q as B fragments (column n = head gq; heads >= G are zero)
     uint32_t qf[C::KS][2];
@@ -400,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     }
     // per-group sums of q (the zero's share of an INT2 score); zero P rows of
-    // the padding heads; softmax state
+    // the padding heads; stream states; slot barriers
     if (tid < C::NG * 8) {
         const int g = tid / 8, hh = tid % 8;
         float sum = 0.0f;
@@ -408,37 +413,32 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int j = 0; j < kQG; j++) sum += __bfloat162float(qg[(size_t)hh * D + g * kQG + j]);
         sQs[tid] = sum;
     }
-    for (int i = tid; i < (2 + 2 * C::NG) * 8 * C::PST; i += kThreads) {
+    for (int i = tid; i < C::NSTR * (2 + 2 * C::NG) * 8 * C::PST; i += kThreads) {
         const int row = (i / C::PST) % 8;
         if (row >= G) sP[i] = __float2bfloat16_rn(0.0f);  // sP and sSP are contiguous
     }
-    if (tid < 8) {
-        st_m[tid] = -CUDART_INF_F;
-        st_l[tid] = 0.0f;
+    if (tid < C::NSTR * 8) {
+        sSt[(tid / 8) * 24 + tid % 8] = -CUDART_INF_F;
+        sSt[(tid / 8) * 24 + 8 + tid % 8] = 0.0f;
     }
     if (tid == 0) {
         for (int i = 0; i < C::NS; i++) mbar_init(&sBar[i], 1);
         mbar_fence_init();
     }
     __syncthreads();
-    const uint8_t *Lu = a.ledger + uw * (size_t)C::LB;
 
-    int32_t *sLive = reinterpret_cast<int32_t *>(smem + C::oLive);
-    int *sCnt = reinterpret_cast<int *>(smem + C::oCnt);
-
-    // output accumulators: O^T tile (16 dims x 8 heads) of warp `warp`
-    // (d=128: dims 16*warp.., all tokens; d=64: dims 16*(warp%4).., token half warp/4)
-    constexpr int PV_MT = (C::MT >= 8) ? 8 : C::MT;
-    const int mt_d = warp % PV_MT;
-    const int th = warp / PV_MT;                   // token half (d=64) or 0
-    constexpr int PV_KS = (C::MT >= 8) ? 4 : 2;    // 16-token k-steps per window per warp
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    // output accumulators O^T (16 dims x 8 heads) per stream: d=128, warp w
+    // owns dims 16w.. of both streams; d=64, warp w owns dims 16(w%4).. of
+    // stream w/4
+    constexpr bool BOTH = C::MT >= 8;
+    const int mt_d = BOTH ? warp : (warp & 3);
+    const int my_st = BOTH ? 0 : (warp >> 2);
+    float acc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 
     int li = 0, lc = 0;  // loads issued, loads consumed (block-uniform, across passes)
     for (int64_t p0 = w_begin; p0 < w_end; p0 += C::LMAX) {
         const int64_t p1 = (p0 + C::LMAX < w_end) ? p0 + C::LMAX : w_end;
-        // the live windows of [p0, p1) in order, bit 30 set for INT2 ones (read
-        // once here, so the pipeline below never waits on the tier array);
+        // the live windows of [p0, p1) in order, bit 30 set for INT2 ones;
         // evicted windows get no mass (log2-sum-exp -inf)
         int nlive = 0;
         for (int64_t r0 = p0; r0 < p1; r0 += kThreads) {
@@ -511,239 +511,285 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         };
 
-        for (int ci = 0; ci < nlive; ci++) {
-        const int32_t ce = sLive[ci];
-        const int64_t cur = ce & 0x3fffffff;
-        const bool int2 = (ce >> 30) & 1;
-        const int need = int2 ? 1 : 2;
-        issue_ahead();
-        const uint8_t *buf = smem + (lc % C::NS) * C::SLOT;   // K rows or the ledger
-        uint8_t *vbuf = smem + ((lc + 1) % C::NS) * C::SLOT;  // V rows (bf16 windows)
-        const int n = (int)(N - cur * kWin < kWin ? N - cur * kWin : kWin);
-        mbar_wait(&sBar[lc % C::NS], (uint32_t)((lc / C::NS) & 1), a.err);
-        if (!int2) {
-            mbar_wait(&sBar[(lc + 1) % C::NS], (uint32_t)(((lc + 1) / C::NS) & 1), a.err);
-            // rows past the sequence in the open window: whatever the cache holds
-            // there must not reach the sum (0 * NaN), so zero them
-            if (n < kWin)
-                for (int i = tid; i < C::BOXES * (kWin - n) * 8; i += kThreads) {
-                    const int bx = i / ((kWin - n) * 8), rem = i % ((kWin - n) * 8);
-                    *reinterpret_cast<uint4 *>(vbuf + bx * kWin * 128 + (n + rem / 8) * 128 +
-                                               (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
-                }
-        }
-        __syncthreads();
-
-        // ---- scores: warp -> 16 tokens (mt), half of the dims (kh)
-        {
-            const int mt = warp & 3, kh = warp >> 2;
-            float c4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if (!int2) {
-                const int lm = lane >> 3, lr = lane & 7;  // ldmatrix: matrix, row
-                // row r, 16-byte chunk c of a box sits at r*128 + ((c ^ (r % 8)) * 16)
-                const uint8_t *rowp = buf + (16 * mt + lr + ((lm & 1) ? 8 : 0)) * 128;
+        // windows in pairs: window ci feeds stream 0, ci + 1 stream 1
+        for (int ci = 0; ci < nlive; ci += 2) {
+            const bool hasB = ci + 1 < nlive;
+            // per window (A: stream 0, B: stream 1) as scalars, picked with
+            // selects: an array indexed by a warp-dependent stream would live
+            // in local memory
+            const int32_t eA = sLive[ci], eB = hasB ? sLive[ci + 1] : 0;
+            const bool q2A = ((eA >> 30) & 1) != 0, q2B = hasB && ((eB >> 30) & 1) != 0;
+            const int64_t cwA = eA & 0x3fffffff, cwB = eB & 0x3fffffff;
+            const int needA = q2A ? 1 : 2;
+            const int needB = hasB ? (q2B ? 1 : 2) : 0;
+            const int slA = lc, slB = lc + needA;  // first load of each window
+            const int nvA = (int)(N - cwA * kWin < kWin ? N - cwA * kWin : kWin);
+            const int nvB = (int)(N - cwB * kWin < kWin ? N - cwB * kWin : kWin);
+            issue_ahead();
+            for (int L = lc; L < lc + needA + needB; L++)
+                mbar_wait(&sBar[L % C::NS], (uint32_t)((L / C::NS) & 1), a.err);
 #pragma unroll
-                for (int ks = 0; ks < C::KS; ks++) {
-                    if (ks / (C::KS / 2) != kh) continue;  // warp-uniform; ks stays a constant
-                    const int ch = 2 * ks + ((lm & 2) ? 1 : 0);
-                    uint32_t af[4];
-                    ldsm_x4(af, rowp + (ch >> 3) * kWin * 128 + (((ch & 7) ^ lr) << 4));
-                    mma16816(c4, af, qf[ks][0], qf[ks][1]);
-                }
-            } else {
-                const int r0 = 16 * mt + gq, r1 = r0 + 8;
-#pragma unroll
-                for (int g = 0; g < C::NG; g++) {
-                    if (g / (C::NG / 2) != kh) continue;  // warp-uniform; g stays a constant
-                    const uint2 w0 = *reinterpret_cast<const uint2 *>(buf + (r0 * C::NG + g) * 8);
-                    const uint2 w1 = *reinterpret_cast<const uint2 *>(buf + (r1 * C::NG + g) * 8);
-                    float cg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                    for (int j = 0; j < 2; j++) {
-                        const uint32_t x0 = j ? w0.y : w0.x, x1 = j ? w1.y : w1.x;
-                        const int s0 = 4 * cq, s1 = 4 * cq + 16;
-                        uint32_t af[4];
-                        af[0] = codes2_bf16((x0 >> s0) & 3u, (x0 >> (s0 + 2)) & 3u);
-                        af[1] = codes2_bf16((x1 >> s0) & 3u, (x1 >> (s0 + 2)) & 3u);
-                        af[2] = codes2_bf16((x0 >> s1) & 3u, (x0 >> (s1 + 2)) & 3u);
-                        af[3] = codes2_bf16((x1 >> s1) & 3u, (x1 >> (s1 + 2)) & 3u);
-                        mma16816(cg, af, qf[2 * g + j][0], qf[2 * g + j][1]);
+            for (int st = 0; st < 2; st++) {
+                const bool q2s = st ? q2B : q2A;
+                const int nvs = st ? nvB : nvA, sls = st ? slB : slA;
+                // rows past the sequence in the open window: whatever the cache
+                // holds there must not reach the sum (0 * NaN), so zero them
+                if ((st == 0 || hasB) && !q2s && nvs < kWin) {
+                    uint8_t *vb = smem + ((sls + 1) % C::NS) * C::SLOT;
+                    const int nz = kWin - nvs;
+                    for (int i = tid; i < C::BOXES * nz * 8; i += kThreads) {
+                        const int bx = i / (nz * 8), rem = i % (nz * 8);
+                        *reinterpret_cast<uint4 *>(vb + bx * kWin * 128 + (nvs + rem / 8) * 128 +
+                                                   (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
                     }
-                    // value = code * s + z: score = s * (codes . q) + z * sum(q)
-                    const uint32_t p0 = *reinterpret_cast<const uint32_t *>(buf + C::CB + (r0 * C::NG + g) * 4);
-                    const uint32_t p1 = *reinterpret_cast<const uint32_t *>(buf + C::CB + (r1 * C::NG + g) * 4);
-                    const float s0f = __half2float(__ushort_as_half((unsigned short)(p0 & 0xffffu)));
-                    const float z0f = __half2float(__ushort_as_half((unsigned short)(p0 >> 16)));
-                    const float s1f = __half2float(__ushort_as_half((unsigned short)(p1 & 0xffffu)));
-                    const float z1f = __half2float(__ushort_as_half((unsigned short)(p1 >> 16)));
-                    const float qa = sQs[g * 8 + 2 * cq], qb = sQs[g * 8 + 2 * cq + 1];
-                    c4[0] += fmaf(s0f, cg[0], z0f * qa);
-                    c4[1] += fmaf(s0f, cg[1], z0f * qb);
-                    c4[2] += fmaf(s1f, cg[2], z1f * qa);
-                    c4[3] += fmaf(s1f, cg[3], z1f * qb);
                 }
             }
-            float *sp = sSp + (size_t)kh * kWin * 8;
-            *reinterpret_cast<float2 *>(sp + (16 * mt + gq) * 8 + 2 * cq) = make_float2(c4[0], c4[1]);
-            *reinterpret_cast<float2 *>(sp + (16 * mt + gq + 8) * 8 + 2 * cq) = make_float2(c4[2], c4[3]);
-        }
-        __syncthreads();
+            __syncthreads();
 
-        // ---- softmax state: warp g < G handles head g (two tokens per lane)
-        if (warp < G) {
-            const int g = warp;
-            float s0 = -CUDART_INF_F, s1 = -CUDART_INF_F;
-            if (lane < n) s0 = (sSp[lane * 8 + g] + sSp[(kWin + lane) * 8 + g]) * a.scale_log2;
-            if (lane + 32 < n)
-                s1 = (sSp[(lane + 32) * 8 + g] + sSp[(kWin + lane + 32) * 8 + g]) * a.scale_log2;
-            float wm = fmaxf(s0, s1);
+            // ---- scores: warp -> window (warp / 4), 16 tokens (warp % 4), all dims
+            {
+                const int st = warp >> 2, mt = warp & 3;
+                if (st == 0 || hasB) {
+                    const uint8_t *buf = smem + ((st ? slB : slA) % C::NS) * C::SLOT;
+                    float c4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    if (!(st ? q2B : q2A)) {
+                        const int lm = lane >> 3, lr = lane & 7;  // ldmatrix: matrix, row
+                        // row r, 16-byte chunk c of a box sits at r*128 + ((c ^ (r % 8)) * 16)
+                        const uint8_t *rowp = buf + (16 * mt + lr + ((lm & 1) ? 8 : 0)) * 128;
 #pragma unroll
-            for (int o = 16; o; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(kFull, wm, o));
-            const float m_old = st_m[g];
-            const float m_new = fmaxf(m_old, wm);
-            const float p0 = exp2f(s0 - m_new), p1 = exp2f(s1 - m_new);
-            float ls = p0 + p1;
+                        for (int ks = 0; ks < C::KS; ks++) {
+                            const int ch = 2 * ks + ((lm & 2) ? 1 : 0);
+                            uint32_t af[4];
+                            ldsm_x4(af, rowp + (ch >> 3) * kWin * 128 + (((ch & 7) ^ lr) << 4));
+                            mma16816(c4, af, qf[ks][0], qf[ks][1]);
+                        }
+                    } else {
+                        const int r0 = 16 * mt + gq, r1 = r0 + 8;
 #pragma unroll
-            for (int o = 16; o; o >>= 1) ls += __shfl_xor_sync(kFull, ls, o);
-            // P split into bf16 hi + lo (about 16 bits kept)
-            const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
-            sP[g * C::PST + lane] = h0;
-            sP[g * C::PST + lane + 32] = h1;
-            sP[(8 + g) * C::PST + lane] = __float2bfloat16_rn(p0 - __bfloat162float(h0));
-            sP[(8 + g) * C::PST + lane + 32] = __float2bfloat16_rn(p1 - __bfloat162float(h1));
-            if (int2) {
-                // V values = code * s + z: P weighted by each group's scale, and
-                // the zero's share sum_t z p per group
-                const uint8_t *vp = buf + 2 * C::CB + C::PB;  // V params
+                        for (int g = 0; g < C::NG; g++) {
+                            const uint2 w0 = *reinterpret_cast<const uint2 *>(buf + (r0 * C::NG + g) * 8);
+                            const uint2 w1 = *reinterpret_cast<const uint2 *>(buf + (r1 * C::NG + g) * 8);
+                            float cg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                for (int gg = 0; gg < C::NG; gg++) {
-                    const uint32_t q0 = *reinterpret_cast<const uint32_t *>(vp + (lane * C::NG + gg) * 4);
-                    const uint32_t q1 = *reinterpret_cast<const uint32_t *>(vp + ((lane + 32) * C::NG + gg) * 4);
-                    const float sa = __half2float(__ushort_as_half((unsigned short)(q0 & 0xffffu)));
-                    const float za = __half2float(__ushort_as_half((unsigned short)(q0 >> 16)));
-                    const float sb = __half2float(__ushort_as_half((unsigned short)(q1 & 0xffffu)));
-                    const float zb = __half2float(__ushort_as_half((unsigned short)(q1 >> 16)));
-                    const float w0 = sa * p0, w1 = sb * p1;
-                    const __nv_bfloat16 k0 = __float2bfloat16_rn(w0), k1 = __float2bfloat16_rn(w1);
-                    __nv_bfloat16 *spg = sSP + (size_t)gg * 2 * 8 * C::PST;
-                    spg[g * C::PST + lane] = k0;
-                    spg[g * C::PST + lane + 32] = k1;
-                    spg[(8 + g) * C::PST + lane] = __float2bfloat16_rn(w0 - __bfloat162float(k0));
-                    spg[(8 + g) * C::PST + lane + 32] = __float2bfloat16_rn(w1 - __bfloat162float(k1));
-                    float zs = za * p0 + zb * p1;
-#pragma unroll
-                    for (int o = 16; o; o >>= 1) zs += __shfl_xor_sync(kFull, zs, o);
-                    if (lane == 0) sZt[gg * 8 + g] = zs;
+                            for (int j = 0; j < 2; j++) {
+                                const uint32_t x0 = j ? w0.y : w0.x, x1 = j ? w1.y : w1.x;
+                                const int s0 = 4 * cq, s1 = 4 * cq + 16;
+                                uint32_t af[4];
+                                af[0] = codes2_bf16((x0 >> s0) & 3u, (x0 >> (s0 + 2)) & 3u);
+                                af[1] = codes2_bf16((x1 >> s0) & 3u, (x1 >> (s0 + 2)) & 3u);
+                                af[2] = codes2_bf16((x0 >> s1) & 3u, (x0 >> (s1 + 2)) & 3u);
+                                af[3] = codes2_bf16((x1 >> s1) & 3u, (x1 >> (s1 + 2)) & 3u);
+                                mma16816(cg, af, qf[2 * g + j][0], qf[2 * g + j][1]);
+                            }
+                            // value = code * s + z: score = s * (codes . q) + z * sum(q)
+                            const uint32_t pa = *reinterpret_cast<const uint32_t *>(buf + C::CB + (r0 * C::NG + g) * 4);
+                            const uint32_t pb = *reinterpret_cast<const uint32_t *>(buf + C::CB + (r1 * C::NG + g) * 4);
+                            const float s0f = __half2float(__ushort_as_half((unsigned short)(pa & 0xffffu)));
+                            const float z0f = __half2float(__ushort_as_half((unsigned short)(pa >> 16)));
+                            const float s1f = __half2float(__ushort_as_half((unsigned short)(pb & 0xffffu)));
+                            const float z1f = __half2float(__ushort_as_half((unsigned short)(pb >> 16)));
+                            const float qa = sQs[g * 8 + 2 * cq], qb = sQs[g * 8 + 2 * cq + 1];
+                            c4[0] += fmaf(s0f, cg[0], z0f * qa);
+                            c4[1] += fmaf(s0f, cg[1], z0f * qb);
+                            c4[2] += fmaf(s1f, cg[2], z1f * qa);
+                            c4[3] += fmaf(s1f, cg[3], z1f * qb);
+                        }
+                    }
+                    float *sp = sSp + (size_t)st * kWin * 8;
+                    *reinterpret_cast<float2 *>(sp + (16 * mt + gq) * 8 + 2 * cq) = make_float2(c4[0], c4[1]);
+                    *reinterpret_cast<float2 *>(sp + (16 * mt + gq + 8) * 8 + 2 * cq) = make_float2(c4[2], c4[3]);
                 }
             }
-            if (lane == 0) {
-                const float al = exp2f(m_old - m_new);
-                st_a[g] = al;
-                st_l[g] = st_l[g] * al + ls;
-                st_m[g] = m_new;
-                a.lse[(uw + cur) * G + g] = m_new + log2f(ls);
-            }
-        }
-        __syncthreads();
+            __syncthreads();
 
-        // ---- output: O^T (dims x heads) += V^T P^T for this warp's 16 dims
-        {
-            const float al0 = (2 * cq < G) ? st_a[2 * cq] : 0.0f;
-            const float al1 = (2 * cq + 1 < G) ? st_a[2 * cq + 1] : 0.0f;
-            acc[0] *= al0;
-            acc[1] *= al1;
-            acc[2] *= al0;
-            acc[3] *= al1;
-            if (!int2) {
-                const int lm = lane >> 3, lr = lane & 7;  // ldmatrix: matrix, row
-                const int ch = 2 * mt_d + ((lm & 1) ? 1 : 0);
-                const uint8_t *vrow = vbuf + (ch >> 3) * kWin * 128 +
-                                      (lr + ((lm & 2) ? 8 : 0)) * 128 + (((ch & 7) ^ lr) << 4);
+            // ---- softmax: warp -> stream (warp / 4), heads warp % 4, + 4
+            {
+                const int st = warp >> 2;
+                if (st == 0 || hasB) {
+                    const float *sp = sSp + (size_t)st * kWin * 8;
+                    __nv_bfloat16 *pst = sP + (size_t)st * 2 * 8 * C::PST;
+                    __nv_bfloat16 *sps = sSP + (size_t)st * C::NG * 2 * 8 * C::PST;
+                    float *zts = sZt + st * C::NG * 8;
+                    float *stt = sSt + st * 24;
+                    const uint8_t *buf = smem + ((st ? slB : slA) % C::NS) * C::SLOT;
+                    const int nvs = st ? nvB : nvA;
+                    const bool q2s = st ? q2B : q2A;
+                    const int64_t cws = st ? cwB : cwA;
+                    for (int g = warp & 3; g < G; g += 4) {
+                        float s0 = -CUDART_INF_F, s1 = -CUDART_INF_F;
+                        if (lane < nvs) s0 = sp[lane * 8 + g] * a.scale_log2;
+                        if (lane + 32 < nvs) s1 = sp[(lane + 32) * 8 + g] * a.scale_log2;
+                        float wm = fmaxf(s0, s1);
 #pragma unroll
-                for (int j = 0; j < PV_KS; j++) {
-                    const int t0 = 16 * (th * PV_KS + j);
-                    uint32_t af[4];
-                    ldsm_x4_t(af, vrow + t0 * 128);
-                    const __nv_bfloat16 *ph = sP + gq * C::PST + t0 + 2 * cq;
-                    const __nv_bfloat16 *pl = sP + (8 + gq) * C::PST + t0 + 2 * cq;
-                    mma16816(acc, af, *reinterpret_cast<const uint32_t *>(ph),
-                             *reinterpret_cast<const uint32_t *>(ph + 8));
-                    mma16816(acc, af, *reinterpret_cast<const uint32_t *>(pl),
-                             *reinterpret_cast<const uint32_t *>(pl + 8));
-                }
-            } else {
-                const int g = (16 * mt_d) / kQG, wsel = ((16 * mt_d) % kQG) / 16;
-                const uint8_t *vc = buf + C::CB + C::PB;  // V codes
-                const __nv_bfloat16 *spg = sSP + (size_t)g * 2 * 8 * C::PST;
+                        for (int o = 16; o; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(kFull, wm, o));
+                        const float m_old = stt[g];
+                        const float m_new = fmaxf(m_old, wm);
+                        const float p0 = exp2f(s0 - m_new), p1 = exp2f(s1 - m_new);
+                        float ls = p0 + p1;
 #pragma unroll
-                for (int j = 0; j < PV_KS; j++) {
-                    const int t0 = 16 * (th * PV_KS + j);
-                    const int ta = t0 + 2 * cq;
-                    const uint32_t wa = *reinterpret_cast<const uint32_t *>(vc + (ta * C::NG + g) * 8 + 4 * wsel);
-                    const uint32_t wb = *reinterpret_cast<const uint32_t *>(vc + ((ta + 1) * C::NG + g) * 8 + 4 * wsel);
-                    const uint32_t wc = *reinterpret_cast<const uint32_t *>(vc + ((ta + 8) * C::NG + g) * 8 + 4 * wsel);
-                    const uint32_t wd = *reinterpret_cast<const uint32_t *>(vc + ((ta + 9) * C::NG + g) * 8 + 4 * wsel);
-                    const int e0 = 2 * gq, e1 = 2 * (gq + 8);
-                    uint32_t af[4];
-                    af[0] = codes2_bf16((wa >> e0) & 3u, (wb >> e0) & 3u);
-                    af[1] = codes2_bf16((wa >> e1) & 3u, (wb >> e1) & 3u);
-                    af[2] = codes2_bf16((wc >> e0) & 3u, (wd >> e0) & 3u);
-                    af[3] = codes2_bf16((wc >> e1) & 3u, (wd >> e1) & 3u);
-                    const __nv_bfloat16 *ph = spg + gq * C::PST + t0 + 2 * cq;
-                    const __nv_bfloat16 *pl = spg + (8 + gq) * C::PST + t0 + 2 * cq;
-                    mma16816(acc, af, *reinterpret_cast<const uint32_t *>(ph),
-                             *reinterpret_cast<const uint32_t *>(ph + 8));
-                    mma16816(acc, af, *reinterpret_cast<const uint32_t *>(pl),
-                             *reinterpret_cast<const uint32_t *>(pl + 8));
-                }
-                if (th == 0) {
-                    const float za = (2 * cq < G) ? sZt[g * 8 + 2 * cq] : 0.0f;
-                    const float zb = (2 * cq + 1 < G) ? sZt[g * 8 + 2 * cq + 1] : 0.0f;
-                    acc[0] += za;
-                    acc[1] += zb;
-                    acc[2] += za;
-                    acc[3] += zb;
+                        for (int o = 16; o; o >>= 1) ls += __shfl_xor_sync(kFull, ls, o);
+                        // P split into bf16 hi + lo (about 16 bits kept)
+                        const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
+                        pst[g * C::PST + lane] = h0;
+                        pst[g * C::PST + lane + 32] = h1;
+                        pst[(8 + g) * C::PST + lane] = __float2bfloat16_rn(p0 - __bfloat162float(h0));
+                        pst[(8 + g) * C::PST + lane + 32] = __float2bfloat16_rn(p1 - __bfloat162float(h1));
+                        if (q2s) {
+                            // V values = code * s + z: P weighted by each group's
+                            // scale, and the zero's share sum_t z p per group
+                            const uint8_t *vp = buf + 2 * C::CB + C::PB;  // V params
+#pragma unroll
+                            for (int gg = 0; gg < C::NG; gg++) {
+                                const uint32_t q0 = *reinterpret_cast<const uint32_t *>(vp + (lane * C::NG + gg) * 4);
+                                const uint32_t q1 = *reinterpret_cast<const uint32_t *>(vp + ((lane + 32) * C::NG + gg) * 4);
+                                const float sa = __half2float(__ushort_as_half((unsigned short)(q0 & 0xffffu)));
+                                const float za = __half2float(__ushort_as_half((unsigned short)(q0 >> 16)));
+                                const float sb = __half2float(__ushort_as_half((unsigned short)(q1 & 0xffffu)));
+                                const float zb = __half2float(__ushort_as_half((unsigned short)(q1 >> 16)));
+                                const float w0 = sa * p0, w1 = sb * p1;
+                                const __nv_bfloat16 k0 = __float2bfloat16_rn(w0), k1 = __float2bfloat16_rn(w1);
+                                __nv_bfloat16 *spg = sps + (size_t)gg * 2 * 8 * C::PST;
+                                spg[g * C::PST + lane] = k0;
+                                spg[g * C::PST + lane + 32] = k1;
+                                spg[(8 + g) * C::PST + lane] = __float2bfloat16_rn(w0 - __bfloat162float(k0));
+                                spg[(8 + g) * C::PST + lane + 32] = __float2bfloat16_rn(w1 - __bfloat162float(k1));
+                                float zs = za * p0 + zb * p1;
+#pragma unroll
+                                for (int o = 16; o; o >>= 1) zs += __shfl_xor_sync(kFull, zs, o);
+                                if (lane == 0) zts[gg * 8 + g] = zs;
+                            }
+                        }
+                        if (lane == 0) {
+                            const float al = exp2f(m_old - m_new);
+                            stt[16 + g] = al;
+                            stt[8 + g] = stt[8 + g] * al + ls;
+                            stt[g] = m_new;
+                            a.lse[(uw + cws) * G + g] = m_new + log2f(ls);
+                        }
+                    }
                 }
             }
-        }
-        fence_proxy_async();  // this thread's slot accesses before the next copies into it
-        __syncthreads();      // the window's slots, P and the partial scores are reused next
-        lc += need;
+            __syncthreads();
+
+            // ---- output: O^T (dims x heads) += V^T P^T, per stream
+#pragma unroll
+            for (int st = 0; st < 2; st++) {
+                if (!BOTH && st != my_st) continue;
+                if (st == 1 && !hasB) continue;
+                float *ac = acc[BOTH ? st : 0];
+                const float *stt = sSt + st * 24;
+                const float al0 = (2 * cq < G) ? stt[16 + 2 * cq] : 0.0f;
+                const float al1 = (2 * cq + 1 < G) ? stt[16 + 2 * cq + 1] : 0.0f;
+                ac[0] *= al0;
+                ac[1] *= al1;
+                ac[2] *= al0;
+                ac[3] *= al1;
+                const __nv_bfloat16 *pst = sP + (size_t)st * 2 * 8 * C::PST;
+                const int sls = st ? slB : slA;
+                if (!(st ? q2B : q2A)) {
+                    const uint8_t *vbuf = smem + ((sls + 1) % C::NS) * C::SLOT;
+                    const int lm = lane >> 3, lr = lane & 7;  // ldmatrix: matrix, row
+                    const int ch = 2 * mt_d + ((lm & 1) ? 1 : 0);
+                    const uint8_t *vrow = vbuf + (ch >> 3) * kWin * 128 +
+                                          (lr + ((lm & 2) ? 8 : 0)) * 128 + (((ch & 7) ^ lr) << 4);
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        const int t0 = 16 * j;
+                        uint32_t af[4];
+                        ldsm_x4_t(af, vrow + t0 * 128);
+                        const __nv_bfloat16 *ph = pst + gq * C::PST + t0 + 2 * cq;
+                        const __nv_bfloat16 *pl = pst + (8 + gq) * C::PST + t0 + 2 * cq;
+                        mma16816(*reinterpret_cast<float(*)[4]>(ac), af,
+                                 *reinterpret_cast<const uint32_t *>(ph),
+                                 *reinterpret_cast<const uint32_t *>(ph + 8));
+                        mma16816(*reinterpret_cast<float(*)[4]>(ac), af,
+                                 *reinterpret_cast<const uint32_t *>(pl),
+                                 *reinterpret_cast<const uint32_t *>(pl + 8));
+                    }
+                } else {
+                    const uint8_t *buf = smem + (sls % C::NS) * C::SLOT;
+                    const int g = (16 * mt_d) / kQG, wsel = ((16 * mt_d) % kQG) / 16;
+                    const uint8_t *vc = buf + C::CB + C::PB;  // V codes
+                    const __nv_bfloat16 *spg = sSP + ((size_t)st * C::NG + g) * 2 * 8 * C::PST;
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        const int t0 = 16 * j;
+                        const int ta = t0 + 2 * cq;
+                        const uint32_t wa = *reinterpret_cast<const uint32_t *>(vc + (ta * C::NG + g) * 8 + 4 * wsel);
+                        const uint32_t wb = *reinterpret_cast<const uint32_t *>(vc + ((ta + 1) * C::NG + g) * 8 + 4 * wsel);
+                        const uint32_t wc = *reinterpret_cast<const uint32_t *>(vc + ((ta + 8) * C::NG + g) * 8 + 4 * wsel);
+                        const uint32_t wd = *reinterpret_cast<const uint32_t *>(vc + ((ta + 9) * C::NG + g) * 8 + 4 * wsel);
+                        const int e0 = 2 * gq, e1 = 2 * (gq + 8);
+                        uint32_t af[4];
+                        af[0] = codes2_bf16((wa >> e0) & 3u, (wb >> e0) & 3u);
+                        af[1] = codes2_bf16((wa >> e1) & 3u, (wb >> e1) & 3u);
+                        af[2] = codes2_bf16((wc >> e0) & 3u, (wd >> e0) & 3u);
+                        af[3] = codes2_bf16((wc >> e1) & 3u, (wd >> e1) & 3u);
+                        const __nv_bfloat16 *ph = spg + gq * C::PST + t0 + 2 * cq;
+                        const __nv_bfloat16 *pl = spg + (8 + gq) * C::PST + t0 + 2 * cq;
+                        mma16816(*reinterpret_cast<float(*)[4]>(ac), af,
+                                 *reinterpret_cast<const uint32_t *>(ph),
+                                 *reinterpret_cast<const uint32_t *>(ph + 8));
+                        mma16816(*reinterpret_cast<float(*)[4]>(ac), af,
+                                 *reinterpret_cast<const uint32_t *>(pl),
+                                 *reinterpret_cast<const uint32_t *>(pl + 8));
+                    }
+                    const float *zts = sZt + st * C::NG * 8;
+                    const float za = (2 * cq < G) ? zts[g * 8 + 2 * cq] : 0.0f;
+                    const float zb = (2 * cq + 1 < G) ? zts[g * 8 + 2 * cq + 1] : 0.0f;
+                    ac[0] += za;
+                    ac[1] += zb;
+                    ac[2] += za;
+                    ac[3] += zb;
+                }
+            }
+            fence_proxy_async();  // this thread's slot accesses before the next copies into it
+            __syncthreads();      // the pair's slots, P and the scores are reused next
+            lc += needA + needB;
         }
     }
     __syncthreads();
 
-    // ---- this CTA's partial: o[head][dim] unnormalised, m, l per head
+    // ---- merge the two streams into this CTA's partial: o[head][dim]
+    // (unnormalised), m, l per head
     float *part = a.part + ((size_t)u * a.S + x) * (2 * G + G * D);
-    if constexpr (PV_MT < 8) {
-        // d = 64: add the two token halves
+    auto factor = [&](int st, int hh) {  // weight of stream st's head hh in the merge
+        const float m0 = sSt[hh], m1 = sSt[24 + hh];
+        const float M = fmaxf(m0, m1);
+        const float m = st ? m1 : m0;
+        return (m == -CUDART_INF_F) ? 0.0f : exp2f(m - M);
+    };
+    if (!BOTH) {
+        // d = 64: stream 1's warps hand their tiles to stream 0's warps
         float *red = reinterpret_cast<float *>(smem);
-        if (th == 1)
+        if (my_st == 1)
             *reinterpret_cast<float4 *>(red + (mt_d * 32 + lane) * 4) =
-                make_float4(acc[0], acc[1], acc[2], acc[3]);
+                make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
         __syncthreads();
-        if (th == 0) {
+        if (my_st == 0) {
             const float4 o = *reinterpret_cast<const float4 *>(red + (mt_d * 32 + lane) * 4);
-            acc[0] += o.x;
-            acc[1] += o.y;
-            acc[2] += o.z;
-            acc[3] += o.w;
+            acc[1][0] = o.x;
+            acc[1][1] = o.y;
+            acc[1][2] = o.z;
+            acc[1][3] = o.w;
         }
     }
-    if (th == 0) {
+    if (my_st == 0) {
         const int d0 = 16 * mt_d + gq;
-        if (2 * cq < G) {
-            part[2 * G + (2 * cq) * D + d0] = acc[0];
-            part[2 * G + (2 * cq) * D + d0 + 8] = acc[2];
-        }
-        if (2 * cq + 1 < G) {
-            part[2 * G + (2 * cq + 1) * D + d0] = acc[1];
-            part[2 * G + (2 * cq + 1) * D + d0 + 8] = acc[3];
+#pragma unroll
+        for (int e = 0; e < 2; e++) {
+            const int hh = 2 * cq + e;
+            if (hh < G) {
+                const float f0 = factor(0, hh), f1 = factor(1, hh);
+                part[2 * G + hh * D + d0] = acc[0][e] * f0 + acc[1][e] * f1;
+                part[2 * G + hh * D + d0 + 8] = acc[0][2 + e] * f0 + acc[1][2 + e] * f1;
+            }
         }
     }
     if (tid < G) {
-        part[tid] = st_m[tid];
-        part[G + tid] = st_l[tid];
+        const float m0 = sSt[tid], m1 = sSt[24 + tid];
+        part[tid] = fmaxf(m0, m1);
+        part[G + tid] = sSt[8 + tid] * factor(0, tid) + sSt[32 + tid] * factor(1, tid);
     }
 }
 
