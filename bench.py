@@ -419,6 +419,14 @@ def run_gpu(args, w):
                             else measured_traffic("select_kernel")
                             + measured_traffic("attend_kernel")),
                 "attend_us": avg["attend"] * 1e3, "encode_us": avg["encode"] * 1e3}
+    # the whole step against its measured time: every byte the step must read
+    # (codes, candidate rows, selected K / V, query, the appended key) over
+    # ms_per_step; select and attend overlap across their launch boundary, so
+    # this is the path's effective fraction
+    step_bytes = ab["select"] + ab["attend"] + ab["encode"]
+    step_ach = step_bytes / (ms / args.steps * 1e-3) / 1e9
+    step_roof = {"bytes": step_bytes, "achieved": step_ach, "peak": peak, "unit": "GB/s",
+                 "frac": step_ach / peak, "us": ms / args.steps * 1e3}
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         v, el, done = time_oracle(w, args.cpu_seconds, "cuda")
@@ -430,6 +438,7 @@ def run_gpu(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config_of(w), "roofline": roof, "path_roofline": path,
+        "step_roofline": step_roof,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
