@@ -241,8 +241,12 @@ class Layer:
         kvr.kvr_encode_keys(K, torch.zeros(w.B, dtype=torch.int32, device=dev), w.N, sgn,
                             self.codes)
         self.out = torch.empty((w.B, w.Hq, w.d), dtype=torch.float32, device=dev)
-        # the V cache as an L2-prefetch hint for the attention that follows
-        self.params = kvr.SelectParams(w.C, w.k, w.W, w.lut, V_prefetch=V)
+        # the V cache as an L2-prefetch hint for the attention that follows;
+        # the codes, K, V and lengths are never written by the kernel before a
+        # selection in the step chain (the previous layer's attention), so it
+        # may start on them early
+        self.params = kvr.SelectParams(w.C, w.k, w.W, w.lut, flags=kvr.SELECT_EARLY_INPUTS,
+                                       V_prefetch=V)
 
 
 def run_gpu(args, w):

@@ -78,6 +78,11 @@ typedef enum kvr_dtype { KVR_F32 = 0, KVR_BF16 = 1 } kvr_dtype;
 /* kvr_select_params.flags */
 #define KVR_SELECT_STORE_COARSE 0x1 /* also write every pool key's coarse score to the
                                        workspace (diagnostics; costs time) */
+#define KVR_SELECT_EARLY_INPUTS 0x2 /* the caller asserts that codes, K, V_prefetch, seq_len
+                                       and srht_sign were complete before the previous kernel
+                                       on the stream was launched (only q may come from that
+                                       kernel): the call then starts reading them while that
+                                       kernel still runs (programmatic dependent launch) */
 
 /* Shape of one layer's cache and query. */
 typedef struct kvr_shape {

@@ -37,7 +37,7 @@ kvr_status check_params(const kvr_select_params *p)
         return KVR_ERR_INVALID_ARG;
     for (int i = 0; i < 9; i++)
         if (p->lut[i] < 0 || p->lut[i] > 15) return KVR_ERR_INVALID_ARG;
-    if (p->flags & ~KVR_SELECT_STORE_COARSE) return KVR_ERR_INVALID_ARG;
+    if (p->flags & ~(KVR_SELECT_STORE_COARSE | KVR_SELECT_EARLY_INPUTS)) return KVR_ERR_INVALID_ARG;
     if (!aligned16(p->V_prefetch)) return KVR_ERR_INVALID_ARG;
     return KVR_OK;
 }

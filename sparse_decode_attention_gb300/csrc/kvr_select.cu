@@ -56,6 +56,7 @@ struct SelArgs {
     const void *q;
     const void *K;
     const void *V;  // optional: prefetch the winners' V rows and the window's rows
+    bool early;     // KVR_SELECT_EARLY_INPUTS
     const uint8_t *codes;
     const int32_t *seq_len;
     const int8_t *sgn;
@@ -224,7 +225,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     cg::cluster_group cluster = cg::this_cluster();
     // programmatic dependent launch: this grid may start while the previous one
     // drains; nothing is read before the previous grid's writes are visible
-    grid_dependency_wait();
+    // with KVR_SELECT_EARLY_INPUTS only q is waited for: the length, the code
+    // copies and the row prefetches below start while the previous grid runs
+    if (!a.early) grid_dependency_wait();
     grid_launch_dependents();
     const int CS = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
@@ -287,6 +290,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         cp_async_commit();
     };
     if (hh < h1) issue_half(hh);
+    if (a.early) grid_dependency_wait();  // q may come from the previous grid
 
     // q_bar and its code (every CTA of the cluster computes them)
     if (warp == 0) {
@@ -1037,6 +1041,7 @@ kvr_status select_dispatch(const LaunchCtx &c, const kvr_select_params &p, const
     a.q = q;
     a.K = K;
     a.V = p.V_prefetch;
+    a.early = (p.flags & KVR_SELECT_EARLY_INPUTS) != 0;
     a.codes = codes;
     a.seq_len = seq_len;
     a.sgn = sgn;

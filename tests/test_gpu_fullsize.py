@@ -63,6 +63,20 @@ class Path:
         kvr.kvr_sparse_attend(q, self.K, self.V, self.idx, self.cnt, self.seq, self.w.W,
                               1.0 / math.sqrt(self.w.d), self.out, self.ws_a, self.err)
 
+    def step_chain(self, q, N):
+        """The benchmark's decode chain: selection with early inputs (the
+        previous kernel on the stream is the last attention, which writes none
+        of its inputs but q), then attention. The caller synchronises after any
+        kernel that wrote codes, K or lengths."""
+        self.seq.fill_(N)
+        torch.cuda.synchronize()
+        early = kvr.SelectParams(self.w.C, self.w.k, self.w.W, self.w.lut,
+                                 flags=kvr.SELECT_EARLY_INPUTS, V_prefetch=self.V)
+        kvr.kvr_select(q, self.K, self.codes, self.seq, self.sgn, early, self.idx, self.cnt,
+                       self.ws_s, self.err)
+        kvr.kvr_sparse_attend(q, self.K, self.V, self.idx, self.cnt, self.seq, self.w.W,
+                              1.0 / math.sqrt(self.w.d), self.out, self.ws_a, self.err)
+
     def check_units(self, q, N, units, check_codes=True):
         w = self.w
         idx = self.idx.cpu().numpy()
@@ -96,10 +110,19 @@ def test_llama_128k_layer_full_size():
     w = wl.LLAMA_128K
     p = Path(w, cap=w.N)
     p.encode(0, w.N)
-    for t in range(2):
-        q = wl.step_query(w, p.qb, t).contiguous()
-        p.step(q, w.N)
+    q = wl.step_query(w, p.qb, 0).contiguous()
+    p.step(q, w.N)
     p.check_units(q, w.N, [(0, h) for h in range(w.Hkv)])
+    # the benchmark's chain: after one synchronisation, select (early inputs)
+    # -> attend -> select -> attend -> ..., no host sync in between
+    early = kvr.SelectParams(w.C, w.k, w.W, w.lut, flags=kvr.SELECT_EARLY_INPUTS, V_prefetch=p.V)
+    torch.cuda.synchronize()
+    for t in range(1, 4):
+        q = wl.step_query(w, p.qb, t).contiguous()
+        kvr.kvr_select(q, p.K, p.codes, p.seq, p.sgn, early, p.idx, p.cnt, p.ws_s, p.err)
+        kvr.kvr_sparse_attend(q, p.K, p.V, p.idx, p.cnt, p.seq, w.W, 1.0 / math.sqrt(w.d),
+                              p.out, p.ws_a, p.err)
+    p.check_units(q, w.N, [(0, h) for h in range(w.Hkv)], check_codes=False)
     assert kvr.kvr_read_error(p.err) == 0
 
 
@@ -126,6 +149,9 @@ def test_million_token_context_full_size():
     q = wl.step_query(w, p.qb, 0).contiguous()
     p.step(q, w.N)
     p.check_units(q, w.N, [(0, 0), (0, 5)])
+    q = wl.step_query(w, p.qb, 1).contiguous()
+    p.step_chain(q, w.N)
+    p.check_units(q, w.N, [(0, 2), (0, 7)], check_codes=False)
     assert kvr.kvr_read_error(p.err) == 0
 
 
