@@ -19,7 +19,8 @@ import subprocess
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = [os.path.join(_HERE, "kvr_oracle.c"), os.path.join(_HERE, "kvr_tiers_oracle.c")]
+_SRC = [os.path.join(_HERE, "kvr_oracle.c"), os.path.join(_HERE, "kvr_tiers_oracle.c"),
+        os.path.join(_HERE, "kvr_rsq_oracle.c")]
 _LIB = os.path.join(_HERE, "libkvr_oracle.so")
 _lib = None
 
@@ -63,8 +64,25 @@ def lib():
         L.orc_attend_unit.argtypes = [_P, _I32, _P, _P, _I64, _I32, _P, _I64, _I64,
                                       ctypes.c_float, _P]
         _tier_signatures(L)
+        _rsq_signatures(L)
         _lib = L
     return _lib
+
+
+def _rsq_signatures(L):
+    L.orc_rsq_table.argtypes = [_I32, _P, _P]
+    L.orc_rsq_table.restype = _I32
+    L.orc_rsq_float_tables.argtypes = [_I32, _P, _P]
+    L.orc_rsq_float_tables.restype = _I32
+    L.orc_rsq_record_bytes.argtypes = [_I32]
+    L.orc_rsq_record_bytes.restype = _I64
+    L.orc_rsq_encode.argtypes = [_P, _I64, _I32, _P, _P]
+    L.orc_rsq_encode.restype = _I32
+    L.orc_rsq_score.argtypes = [_P, _P, _I32]
+    L.orc_rsq_score.restype = ctypes.c_float
+    L.orc_select_unit_rsq.argtypes = [_P, _I32, _P, _P, _I64, _I32, _P, _I64, _I64, _I64, _P,
+                                      _P, _P, _P, _P]
+    L.orc_select_unit_rsq.restype = _I32
 
 
 def _tier_signatures(L):
@@ -432,3 +450,69 @@ class TierUnit:
         t = self.tier[:closed]
         return int((t == BF16).sum()) * WINDOW * 4 * self.d + int((t == INT2).sum()) * \
             ledger_bytes(self.d)
+
+
+# --------------------------------------------------------------------------
+# calibrated inner-product reranker (kvr_rsq_oracle.c)
+# --------------------------------------------------------------------------
+
+def rsq_table(m: int = 8):
+    """(bin edges [9], levels [8]) of the 3-bit magnitude quantiser, fp64."""
+    bound = np.zeros(9, dtype=np.float64)
+    level = np.zeros(8, dtype=np.float64)
+    if lib().orc_rsq_table(m, _p(bound), _p(level)):
+        raise ValueError("m must be >= 3")
+    return bound, level
+
+
+def rsq_float_tables(m: int = 8):
+    """(fl(edge^2) [8] with entry 0 = 0, fl(level) [8]): the fp32 tables."""
+    bsq = np.zeros(8, dtype=np.float32)
+    lev = np.zeros(8, dtype=np.float32)
+    lib().orc_rsq_float_tables(m, _p(bsq), _p(lev))
+    return bsq, lev
+
+
+def rsq_record_bytes(d: int) -> int:
+    return int(lib().orc_rsq_record_bytes(d))
+
+
+def rsq_encode(x, sgn) -> np.ndarray:
+    """Records [..., 6 d/8] uint8 of the rows x [..., d]."""
+    a = f32(x)
+    d = a.shape[-1]
+    n = a.size // d
+    s = _c(sgn, np.int8)
+    out = np.zeros(a.shape[:-1] + (rsq_record_bytes(d),), dtype=np.uint8)
+    if lib().orc_rsq_encode(_p(a), n, d, _p(s), _p(out)):
+        raise ValueError("unsupported head_dim %d" % d)
+    return out
+
+
+def rsq_score(record, zq) -> np.float32:
+    r = _c(record, np.uint8)
+    z = f32(zq)
+    return np.float32(lib().orc_rsq_score(_p(r), _p(z), z.shape[-1]))
+
+
+def select_unit_rsq(q_group, codes_unit, rec_unit, N, sgn, C, k, W, lut, diagnostics=False):
+    """Selection of one unit with the reranker; (idx[k] padded -1, count[, diag])."""
+    q = f32(q_group)
+    G, d = q.shape
+    cd = _c(codes_unit, np.uint8)
+    rc_ = _c(rec_unit, np.uint8)
+    s = _c(sgn, np.int8)
+    lt = _c(lut, np.int32)
+    idx = np.full(max(k, 1), -1, dtype=np.int32)
+    cnt = np.zeros(1, dtype=np.int32)
+    pool = max(0, N - W)
+    nc = max(0, min(C, pool))
+    cand = np.full(max(nc, 1), -1, dtype=np.int32)
+    candS = np.zeros(max(nc, 1), dtype=np.float32)
+    rc = lib().orc_select_unit_rsq(_p(q), G, _p(cd), _p(rc_), N, d, _p(s), C, k, W, _p(lt),
+                                   _p(idx), _p(cnt), _p(cand), _p(candS))
+    if rc != 0:
+        raise ValueError("oracle selection failed")
+    if not diagnostics:
+        return idx[:k], int(cnt[0])
+    return idx[:k], int(cnt[0]), dict(cand=cand[:nc], cand_S=candS[:nc])
