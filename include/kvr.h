@@ -78,8 +78,8 @@ typedef enum kvr_dtype { KVR_F32 = 0, KVR_BF16 = 1 } kvr_dtype;
 /* kvr_select_params.flags */
 #define KVR_SELECT_STORE_COARSE 0x1 /* also write every pool key's coarse score to the
                                        workspace (diagnostics; costs time) */
-#define KVR_SELECT_EARLY_INPUTS 0x2 /* the caller asserts that codes, K, V_prefetch, seq_len
-                                       and srht_sign were complete before the previous kernel
+#define KVR_SELECT_EARLY_INPUTS 0x2 /* the caller asserts that codes, K, V_prefetch,
+                                       rsq_records, seq_len and srht_sign were complete before the previous kernel
                                        on the stream was launched (only q may come from that
                                        kernel): the call then starts reading them while that
                                        kernel still runs (programmatic dependent launch) */
@@ -108,6 +108,11 @@ typedef struct kvr_select_params {
                                that follows; the selected tokens' V rows and the local
                                window's K and V rows are then prefetched into L2 as soon
                                as they are known. Results are unchanged. */
+    const uint8_t *rsq_records; /* optional, or NULL: the device records [B, Hkv, cap,
+                               kvr_rsq_record_bytes(d)] of the pool keys (kvr_encode_rsq);
+                               when set, the candidates are ranked by the calibrated
+                               estimate from the records instead of exact q_bar . k, and
+                               K is not read (cand_score then holds the estimates) */
 } kvr_select_params;
 
 /* Byte offsets of the inspectable parts of the select workspace after a
@@ -154,6 +159,46 @@ size_t kvr_codes_bytes(const kvr_shape *shape);
 kvr_status kvr_encode_keys(const kvr_shape *shape, const void *K, const int32_t *pos0,
                            int n_new, const int8_t *srht_sign, uint8_t *codes,
                            int32_t *err_word, void *stream);
+
+/*
+ * Calibrated inner-product reranking (an alternative to exact rescoring).
+ * Source: ParisKV, "Pipeline di Recupero Nativa su GPU in Due Stadi",
+ * candidate reranking: each sub-space direction of a rotated key is coded
+ * with a sign bit and 3 magnitude bits from the Beta prior the rotation
+ * induces, a per-key, per-sub-space scale corrects the quantisation, and the
+ * score is estimated without the full-precision key.
+ *
+ * Record of a key (kvr_rsq_record_bytes(d) = 6 d/8 bytes): with z = FWHT(D k)
+ * and per sub-block b of 8 coordinates z_b:
+ *   d/8 little-endian words [sign bits, magnitude bit 0, bit 1, bit 2], bit j
+ *   of each byte for coordinate j; the magnitude mag_j = #{i in 1..7 :
+ *   fl(z_j^2) >= fl(bsq[i] s)} with s = fma chain of z_j^2 over j ascending;
+ *   then d/8 bf16 scales w_b = bf16(s / c), c = fma chain of |z_j| lev[mag_j]
+ *   (0 when c = 0).
+ * bsq / lev (kvr_rsq_tables): fl of the squared edges of the 8 equal-
+ * probability bins of |u_j| for a uniformly random unit vector in R^8 (u_j^2 ~
+ * Beta(1/2, 7/2)) and fl of each bin's conditional mean of |u_j|.
+ * Estimate of a record against zq = FWHT(D q_bar): per block e_b = fma chain
+ * over j ascending of (+-lev[mag_j]) zq_j from +0, t_b = w_b e_b, then
+ * butterfly sums over 16 block slots (empty slots +0) with spans 8, 4, 2, 1.
+ * ======================================================================== */
+
+/* Bytes of one key's record, 0 for an unsupported d. */
+size_t kvr_rsq_record_bytes(int d);
+
+/* The quantiser tables (host): bsq[8] (bsq[0] = 0) and lev[8]. */
+kvr_status kvr_rsq_tables(float *bsq, float *lev);
+
+/*
+ * kvr_encode_rsq -- records of rows [pos0[b], pos0[b] + n_new) of every unit
+ * (append time, next to kvr_encode_keys).
+ *   K        device [B, Hkv, cap, d] of shape->dtype.
+ *   records  device [B, Hkv, cap, kvr_rsq_record_bytes(d)] bytes, 16-byte aligned.
+ *   err_word KVR_DEVERR_POSITION for rows outside [0, cap) (skipped).
+ */
+kvr_status kvr_encode_rsq(const kvr_shape *shape, const void *K, const int32_t *pos0, int n_new,
+                          const int8_t *srht_sign, uint8_t *records, int32_t *err_word,
+                          void *stream);
 
 /* Bytes of device workspace kvr_select needs for this shape and params. */
 size_t kvr_select_workspace_size(const kvr_shape *shape, const kvr_select_params *p);

@@ -26,6 +26,7 @@ __all__ = [
     "WINDOW", "TIER_BF16", "TIER_INT2", "TIER_EVICTED", "TierState", "kvr_ledger_bytes",
     "kvr_tier_init", "kvr_tiered_attend_workspace_size", "kvr_sparse_attend_tiered",
     "kvr_tier_update_workspace_size", "kvr_tier_update",
+    "kvr_rsq_record_bytes", "kvr_rsq_tables", "kvr_encode_rsq", "rsq_buffer",
 ]
 
 KVR_F32, KVR_BF16 = 0, 1
@@ -50,7 +51,7 @@ class _Shape(ctypes.Structure):
 class _Params(ctypes.Structure):
     _fields_ = [("C", ctypes.c_int), ("k", ctypes.c_int), ("W", ctypes.c_int),
                 ("lut", ctypes.c_int * 9), ("flags", ctypes.c_int),
-                ("V_prefetch", ctypes.c_void_p)]
+                ("V_prefetch", ctypes.c_void_p), ("rsq_records", ctypes.c_void_p)]
 
 
 SELECT_STORE_COARSE = 0x1
@@ -93,9 +94,11 @@ class Shape:
 
 class SelectParams:
     """kvr_select_params. ``V_prefetch``: optional V cache tensor of a
-    kvr_sparse_attend that follows (an L2 prefetch hint; results unchanged)."""
+    kvr_sparse_attend that follows (an L2 prefetch hint; results unchanged).
+    ``rsq_records``: optional uint8 records of the pool keys (kvr_encode_rsq);
+    when given, candidates are ranked by the calibrated estimate."""
 
-    def __init__(self, C, k, W, lut=DEFAULT_LUT, flags=0, V_prefetch=None):
+    def __init__(self, C, k, W, lut=DEFAULT_LUT, flags=0, V_prefetch=None, rsq_records=None):
         self.C, self.k, self.W = int(C), int(k), int(W)
         self.lut = tuple(int(v) for v in lut)
         self.flags = int(flags)
@@ -105,10 +108,14 @@ class SelectParams:
                                        or not V_prefetch.is_cuda):
             raise TypeError("V_prefetch must be a CUDA tensor or None")
         self.V_prefetch = V_prefetch
+        if rsq_records is not None:
+            _cuda(rsq_records, "rsq_records", torch.uint8)
+        self.rsq_records = rsq_records
 
     def c(self) -> _Params:
         vp = None if self.V_prefetch is None else self.V_prefetch.data_ptr()
-        return _Params(self.C, self.k, self.W, (ctypes.c_int * 9)(*self.lut), self.flags, vp)
+        rp = None if self.rsq_records is None else self.rsq_records.data_ptr()
+        return _Params(self.C, self.k, self.W, (ctypes.c_int * 9)(*self.lut), self.flags, vp, rp)
 
 
 _lib = None
@@ -153,9 +160,13 @@ def load(build_if_missing: bool = True):
     L.kvr_tier_update_workspace_size.argtypes = [S, ctypes.c_int64]
     L.kvr_tier_update_workspace_size.restype = ctypes.c_size_t
     L.kvr_tier_update.argtypes = [S, T, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
+    L.kvr_rsq_record_bytes.argtypes = [ctypes.c_int]
+    L.kvr_rsq_record_bytes.restype = ctypes.c_size_t
+    L.kvr_rsq_tables.argtypes = [_P, _P]
+    L.kvr_encode_rsq.argtypes = [S, _P, _P, ctypes.c_int, _P, _P, _P, _P]
     for fn in ("kvr_encode_keys", "kvr_select_workspace_views", "kvr_select",
                "kvr_select_static_scratch", "kvr_tier_init", "kvr_sparse_attend_tiered",
-               "kvr_tier_update",
+               "kvr_tier_update", "kvr_rsq_tables", "kvr_encode_rsq",
                "kvr_sparse_attend", "kvr_read_error"):
         getattr(L, fn).restype = ctypes.c_int
     _lib = L
@@ -246,6 +257,9 @@ def kvr_select(q, K, codes, seq_len, srht_sign, params: SelectParams, out_idx, o
     _cuda(out_idx, "out_idx", torch.int32)
     _cuda(out_count, "out_count", torch.int32)
     _cuda(workspace, "workspace")
+    if params.rsq_records is not None and (
+            params.rsq_records.numel() < shape.B * shape.Hkv * shape.cap * kvr_rsq_record_bytes(shape.d)):
+        raise ValueError("rsq_records buffer too small")
     st = load().kvr_select(ctypes.byref(shape.c()), ctypes.byref(params.c()), _ptr(q), _ptr(K),
                            _ptr(codes), _ptr(seq_len), _ptr(srht_sign), _ptr(out_idx),
                            _ptr(out_count), _ptr(workspace),
@@ -400,3 +414,41 @@ def kvr_tier_update(state: TierState, window_mass, seq_len, K, V, q_heads: int, 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:
     """A 256-byte aligned device buffer of at least nbytes (torch allocation)."""
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def kvr_rsq_record_bytes(d: int) -> int:
+    """Bytes of one key's reranker record (0 for an unsupported d)."""
+    return int(load().kvr_rsq_record_bytes(int(d)))
+
+
+def kvr_rsq_tables():
+    """(bsq, lev): the float32 squared bin edges and levels of the 3-bit
+    magnitude quantiser, as the library computed them."""
+    bsq = (ctypes.c_float * 8)()
+    lev = (ctypes.c_float * 8)()
+    _check(load().kvr_rsq_tables(ctypes.cast(bsq, ctypes.c_void_p),
+                                 ctypes.cast(lev, ctypes.c_void_p)), "kvr_rsq_tables")
+    return list(bsq), list(lev)
+
+
+def rsq_buffer(K, device=None):
+    """Zeroed uint8 records [B, Hkv, cap, record bytes] for a K cache [B, Hkv, cap, d]."""
+    B, Hkv, cap, d = K.shape
+    rb = kvr_rsq_record_bytes(d)
+    if rb == 0:
+        raise ValueError("the reranker supports d = 64 or 128")
+    return torch.zeros((B, Hkv, cap, rb), dtype=torch.uint8, device=device or K.device)
+
+
+def kvr_encode_rsq(K, pos0, n_new, srht_sign, records, err=None, stream=None):
+    """Reranker records of rows [pos0[b], pos0[b] + n_new) of every unit of K."""
+    _cuda(K, "K")
+    shape = Shape(K.shape[0], K.shape[1], K.shape[1], K.shape[3], K.shape[2], K.dtype)
+    _cuda(pos0, "pos0", torch.int32)
+    _cuda(srht_sign, "srht_sign", torch.int8)
+    _cuda(records, "records", torch.uint8)
+    if records.numel() < K.shape[0] * K.shape[1] * K.shape[2] * kvr_rsq_record_bytes(K.shape[3]):
+        raise ValueError("records buffer too small")
+    st = load().kvr_encode_rsq(ctypes.byref(shape.c()), _ptr(K), _ptr(pos0), int(n_new),
+                               _ptr(srht_sign), _ptr(records), _ptr(err), _stream(stream))
+    _check(st, "kvr_encode_rsq")

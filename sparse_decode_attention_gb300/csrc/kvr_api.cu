@@ -38,7 +38,7 @@ kvr_status check_params(const kvr_select_params *p)
     for (int i = 0; i < 9; i++)
         if (p->lut[i] < 0 || p->lut[i] > 15) return KVR_ERR_INVALID_ARG;
     if (p->flags & ~(KVR_SELECT_STORE_COARSE | KVR_SELECT_EARLY_INPUTS)) return KVR_ERR_INVALID_ARG;
-    if (!aligned16(p->V_prefetch)) return KVR_ERR_INVALID_ARG;
+    if (!aligned16(p->V_prefetch) || !aligned16(p->rsq_records)) return KVR_ERR_INVALID_ARG;
     return KVR_OK;
 }
 
@@ -171,6 +171,35 @@ kvr_status kvr_encode_keys(const kvr_shape *shape, const void *K, const int32_t 
     if ((int64_t)shape->B * shape->Hkv * n_new > ((int64_t)1 << 40)) return KVR_ERR_INVALID_ARG;
     LaunchCtx c{*shape, static_cast<cudaStream_t>(stream)};
     return encode_dispatch(c, K, pos0, n_new, srht_sign, codes, err_word);
+}
+
+size_t kvr_rsq_record_bytes(int d)
+{
+    return (d == 64 || d == 128) ? (size_t)6 * (d / 8) : 0;
+}
+
+kvr_status kvr_rsq_tables(float *bsq, float *lev)
+{
+    if (!bsq || !lev) return KVR_ERR_INVALID_ARG;
+    const RsqTables &t = rsq_tables();
+    std::memcpy(bsq, t.bsq, sizeof(t.bsq));
+    std::memcpy(lev, t.lev, sizeof(t.lev));
+    return KVR_OK;
+}
+
+kvr_status kvr_encode_rsq(const kvr_shape *shape, const void *K, const int32_t *pos0, int n_new,
+                          const int8_t *srht_sign, uint8_t *records, int32_t *err_word,
+                          void *stream)
+{
+    kvr_status st = check_shape(shape);
+    if (st != KVR_OK) return st;
+    if (n_new < 0) return KVR_ERR_INVALID_ARG;
+    if (!K || !pos0 || !srht_sign || !records) return KVR_ERR_INVALID_ARG;
+    if (!aligned16(K) || !aligned16(records)) return KVR_ERR_INVALID_ARG;
+    if (n_new == 0) return KVR_OK;
+    if ((int64_t)shape->B * shape->Hkv * n_new > ((int64_t)1 << 40)) return KVR_ERR_INVALID_ARG;
+    LaunchCtx c{*shape, static_cast<cudaStream_t>(stream)};
+    return rsq_encode_dispatch(c, K, pos0, n_new, srht_sign, records, err_word);
 }
 
 size_t kvr_select_workspace_size(const kvr_shape *shape, const kvr_select_params *p)

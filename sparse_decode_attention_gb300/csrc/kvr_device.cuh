@@ -284,6 +284,12 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
         asm volatile("prefetch.global.L2 [%0];\n" ::"l"(static_cast<const char *>(p) + o) : "memory");
 }
 
+// Prefetch of the one 128-byte line that holds p into L2.
+__device__ __forceinline__ void prefetch_l2_line(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p) : "memory");
+}
+
 // 16-byte asynchronous global -> shared copy (L2 only); src_bytes < 16 zero-fills.
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes = 16)
 {

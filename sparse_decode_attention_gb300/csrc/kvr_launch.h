@@ -61,6 +61,17 @@ kvr_status attend_dispatch(const LaunchCtx &c, const AttendPlan &plan, const voi
                            const int32_t *count, const int32_t *seq_len, int W, float scale,
                            float *out, uint8_t *ws, int32_t *err);
 
+// Calibrated inner-product reranker (kvr_rsq.cu): fp32 tables of the
+// 3-bit magnitude quantiser (bsq[i] = squared bin edge, bsq[0] = 0; lev[i] =
+// level of bin i).
+struct RsqTables {
+    float bsq[8];
+    float lev[8];
+};
+const RsqTables &rsq_tables();
+kvr_status rsq_encode_dispatch(const LaunchCtx &c, const void *K, const int32_t *pos0, int n_new,
+                               const int8_t *sgn, uint8_t *rec, int32_t *err);
+
 // Tiered window cache (kvr_tiers.cu).
 bool tier_shape_ok(const kvr_shape &s, int64_t n_win);
 size_t tiered_attend_ws_bytes(const kvr_shape &s, int64_t n_win);

@@ -57,6 +57,8 @@ struct SelArgs {
     const void *K;
     const void *V;  // optional: prefetch the winners' V rows and the window's rows
     bool early;     // KVR_SELECT_EARLY_INPUTS
+    const uint8_t *rsq;  // reranker records, or null: exact rescoring
+    float lev[8];        // reranker magnitude levels
     const uint8_t *codes;
     const int32_t *seq_len;
     const int8_t *sgn;
@@ -183,7 +185,8 @@ template <int D, typename T> struct SelSmem {
     static constexpr int oMisc = oScan + 40 * 4;
     static constexpr int oWH = oMisc + 64 * 4;  // [kSelWarps][256] per-warp histograms
     static constexpr int oPl = oWH + kSelWarps * 256 * 4;  // [8][kPlaneCap] score planes
-    static constexpr int bytes = oPl + 8 * kPlaneCap * 4;
+    static constexpr int oLev = oPl + 8 * kPlaneCap * 4;  // float [8] reranker levels
+    static constexpr int bytes = oLev + 8 * 4;
     static_assert(16 * 256 * 4 <= kRingBytes, "radix exchange scratch must fit the ring");
 };
 
@@ -310,7 +313,12 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         fwht_lanes<E, 32>(x, lane);
 #pragma unroll
         for (int r = 0; r < E; r++) sQsgn[lane * E + r] = x[r] < 0.0f ? -1 : 0;
+        // the reranker scores against zq = FWHT(D q_bar) itself, q_bar is not needed
+        if (a.rsq)
+#pragma unroll
+            for (int r = 0; r < E; r++) sQbar[lane * E + r] = x[r];
     }
+    if (tid < 8) reinterpret_cast<float *>(smem + SM::oLev)[tid] = a.lev[tid];
     __syncthreads();
     for (int c = tid; c < NCH; c += kSelThreads)
         sQm[c] = make_uint4((uint32_t)sQsgn[4 * c], (uint32_t)sQsgn[4 * c + 1],
@@ -509,8 +517,15 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
                 for (uint32_t m = eq; m && allow > 0; m &= m - 1, allow--) te |= m & (0u - m);
                 for (uint32_t m = gt | te; m; m &= m - 1) {
                     const int32_t id = (int32_t)(blk * 32 + __ffs(m) - 1);
-                    // the row is gathered in P4, a cluster barrier later: start it now
-                    prefetch_l2(static_cast<const uint8_t *>(a.K) + ((size_t)u * a.cap + id) * RB, RB);
+                    // the row (or record) is read in P4, a cluster barrier later: start it now
+                    if (a.rsq) {
+                        constexpr int RBQ = 6 * (D / 8);
+                        const uint8_t *rp = a.rsq + ((size_t)u * a.cap + id) * RBQ;
+                        prefetch_l2_line(rp);
+                        prefetch_l2_line(rp + RBQ - 1);
+                    } else {
+                        prefetch_l2(static_cast<const uint8_t *>(a.K) + ((size_t)u * a.cap + id) * RB, RB);
+                    }
                     cidx[pos] = id;
                     // straight into the shared memory of the CTA whose P4
                     // slice [r*C'/CS, (r+1)*C'/CS) holds list position pos
@@ -537,7 +552,55 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     // ---------------------------------------------------------------- P4
     const int lo = (int)((int64_t)rank * Cp / CS), hi = (int)((int64_t)(rank + 1) * Cp / CS);
     const int n = hi - lo;  // <= kMaxSlice (the host picks CS so); sI filled in P3
-    {
+    if (a.rsq) {
+        // Calibrated estimate from the records, no K rows: lane gl of a
+        // half-warp is block slot gl (slots past d/8 add +0), zq of its block
+        // is in sQbar; e = fma chain over the block's 8 coordinates of
+        // (+-level) * zq, t = w * e, then butterfly sums over spans 8..1.
+        constexpr int NB = D / 8, RBQ = 6 * NB, NHW = kSelThreads / 16, RR = 8;
+        const int hw = tid >> 4, gl = tid & 15;
+        const float *sLev = reinterpret_cast<const float *>(smem + SM::oLev);
+        float zqv[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) zqv[e] = (gl < NB) ? sQbar[gl * 8 + e] : 0.0f;
+        const uint8_t *recu = a.rsq + (size_t)u * a.cap * RBQ;
+        __syncthreads();  // sI complete (filled by the cluster in P3)
+        for (int base = 0; base < n; base += NHW * RR) {
+            uint32_t wd[RR];
+            uint32_t ws[RR];
+#pragma unroll
+            for (int r = 0; r < RR; r++) {
+                const int j = base + r * NHW + hw;
+                wd[r] = 0u;
+                ws[r] = 0u;
+                if (j < n && gl < NB) {
+                    const uint8_t *rp = recu + (size_t)sI[j] * RBQ;
+                    wd[r] = *reinterpret_cast<const uint32_t *>(rp + 4 * gl);
+                    ws[r] = *reinterpret_cast<const uint16_t *>(rp + 4 * NB + 2 * gl);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < RR; r++) {
+                float e = 0.0f;
+#pragma unroll
+                for (int jj = 0; jj < 8; jj++) {
+                    const uint32_t m = ((wd[r] >> (8 + jj)) & 1u) | (((wd[r] >> (16 + jj)) & 1u) << 1) |
+                                       (((wd[r] >> (24 + jj)) & 1u) << 2);
+                    const float lv = sLev[m];
+                    e = __fmaf_rn(((wd[r] >> jj) & 1u) ? -lv : lv, zqv[jj], e);
+                }
+                float t = (gl < NB) ? __uint_as_float(ws[r] << 16) * e : 0.0f;
+#pragma unroll
+                for (int span = 8; span >= 1; span >>= 1) t = t + __shfl_xor_sync(kFull, t, span);
+                const int j = base + r * NHW + hw;
+                if (gl == 0 && j < n) {
+                    if (t != t) set_err(a.err, KVR_DEVERR_NONFINITE);
+                    sS[j] = t;
+                    a.cand_score[(size_t)u * a.C + lo + j] = t;
+                }
+            }
+        }
+    } else {
         float qv[P];
 #pragma unroll
         for (int e = 0; e < P; e++) qv[e] = sQbar[(tid & 15) * P + e];
@@ -1045,6 +1108,8 @@ kvr_status select_dispatch(const LaunchCtx &c, const kvr_select_params &p, const
     a.K = K;
     a.V = p.V_prefetch;
     a.early = (p.flags & KVR_SELECT_EARLY_INPUTS) != 0;
+    a.rsq = p.rsq_records;
+    for (int i = 0; i < 8; i++) a.lev[i] = rsq_tables().lev[i];
     a.codes = codes;
     a.seq_len = seq_len;
     a.sgn = sgn;

@@ -154,3 +154,31 @@ def test_tier_calls_validate_before_launch(kvr_lib):
     assert L.kvr_tier_init(ctypes.byref(s.c()), ctypes.byref(state()), None, fake, fake, fake,
                            None, None) == 1
     assert L.kvr_tier_init(ctypes.byref(s.c()), None, fake, fake, fake, fake, None, None) == 1
+
+
+def test_reranker_calls_validate_before_launch(kvr_lib):
+    """kvr_encode_rsq and the records field of kvr_select_params are checked
+    on the host (no GPU)."""
+    kvr = kvr_lib
+    L = kvr.load()
+    fake = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    s = _shape(kvr)
+    assert kvr.kvr_rsq_record_bytes(128) == 96 and kvr.kvr_rsq_record_bytes(64) == 48
+    assert kvr.kvr_rsq_record_bytes(96) == 0
+
+    def enc(shp, K, n, rec):
+        return L.kvr_encode_rsq(ctypes.byref(shp.c()), K, fake, n, fake, rec, None, None)
+    assert enc(s, None, 1, fake) == 1
+    assert enc(s, fake, 1, None) == 1
+    assert enc(s, fake, 1, odd) == 1                  # records not 16-byte aligned
+    assert enc(s, fake, -1, fake) == 1
+    assert enc(_shape(kvr, d=96), fake, 1, fake) == 2
+    assert enc(s, fake, 0, fake) == 0                 # nothing to do
+    assert L.kvr_rsq_tables(None, None) == 1
+    p = kvr.SelectParams(64, 16, 8)
+    need = kvr.kvr_select_workspace_size(s, p)
+    pv = p.c()
+    pv.rsq_records = (1 << 20) + 8                    # misaligned records
+    assert L.kvr_select(ctypes.byref(s.c()), ctypes.byref(pv), fake, fake, fake, fake, fake,
+                        fake, fake, fake, need, None, None) == 1

@@ -162,3 +162,13 @@ def test_selection_ranks_the_candidates_by_the_estimate():
     order = sorted(range(len(S)), key=lambda j: (-float(S[j]), int(dg["cand"][j])))
     ref = np.sort(dg["cand"][order[:w.k]])
     assert cnt == min(w.k, len(S)) and np.array_equal(idx[:cnt], ref)
+
+
+def test_library_tables_equal_the_oracle_tables(kvr_lib):
+    """The CUDA library builds its quantiser tables on the host from its own
+    incomplete-beta code; they must round to the same fp32 values (host call,
+    no GPU)."""
+    bsq, lev = kvr_lib.kvr_rsq_tables()
+    obsq, olev = oracle.rsq_float_tables(M)
+    assert np.array_equal(np.array(bsq, dtype=np.float32), obsq)
+    assert np.array_equal(np.array(lev, dtype=np.float32), olev)
