@@ -58,20 +58,24 @@ def measured_traffic(kernel):
     return int(rec["dram_bytes_per_launch"]) if m.hexdigest() == rec["sources_sha256"] else None
 
 
-def algorithmic_bytes(w):
-    """Bytes the hot path must read per step per unit (batch x kv head)."""
+def algorithmic_bytes(w, rerank="exact"):
+    """Bytes the hot path must read or write per step per unit (batch x kv
+    head). With the reranker, a candidate costs its record (6 d/8 bytes)
+    instead of its K row, and the appended key also gets a record."""
     N = w.N
     pool = N - w.W
     Cp = min(w.C, pool)
     kp = min(w.k, Cp)
     row = w.d * 2  # bf16 row
+    rec = 6 * w.d // 8
     codes = pool * (w.d // 8)
-    cand_rows = Cp * row
+    cand_rows = Cp * (rec if rerank == "rsq" else row)
     sel_kv = (kp + w.W) * 2 * row
     q = w.G * w.d * 2
     units = w.B * w.Hkv
+    enc = row + w.d // 8 + (rec if rerank == "rsq" else 0)
     return dict(select=units * (codes + cand_rows + q), attend=units * (sel_kv + q),
-                encode=units * (row + w.d // 8), units=units)
+                encode=units * enc, units=units)
 
 
 class ClockSampler:
@@ -232,7 +236,7 @@ def config_of(w):
 # --------------------------------------------------------------------------
 
 class Layer:
-    def __init__(self, w, l, kvr, wl, torch, sgn):
+    def __init__(self, w, l, kvr, wl, torch, sgn, rerank="exact"):
         dev = "cuda"
         K, V, qb = wl.make_cache(w, device=dev, cap=w.N, seed=w.seed + 1000 * l)
         self.K, self.V = K, V
@@ -245,8 +249,20 @@ class Layer:
         # the codes, K, V and lengths are never written by the kernel before a
         # selection in the step chain (the previous layer's attention), so it
         # may start on them early
+        self.rec = None
+        if rerank == "rsq":
+            # reranker records of every key, kept beside the codes
+            self.rec = kvr.rsq_buffer(K)
+            kvr.kvr_encode_rsq(K, torch.zeros(w.B, dtype=torch.int32, device=dev), w.N, sgn,
+                               self.rec)
         self.params = kvr.SelectParams(w.C, w.k, w.W, w.lut, flags=kvr.SELECT_EARLY_INPUTS,
-                                       V_prefetch=V)
+                                       V_prefetch=V, rsq_records=self.rec)
+
+    def encode_new(self, kvr, pos_new, sgn, err, stream=None):
+        """Code (and record) of the appended key."""
+        kvr.kvr_encode_keys(self.K, pos_new, 1, sgn, self.codes, err, stream=stream)
+        if self.rec is not None:
+            kvr.kvr_encode_rsq(self.K, pos_new, 1, sgn, self.rec, err, stream=stream)
 
 
 def run_gpu(args, w):
@@ -259,7 +275,8 @@ def run_gpu(args, w):
     dev = torch.device("cuda", torch.cuda.current_device())
     kvr.load()
     sgn = wl.srht_signs(w.d, device=dev)
-    layers = [Layer(w, l, kvr, wl, torch, sgn) for l in range(LAYERS)]
+    rerank = args.rerank
+    layers = [Layer(w, l, kvr, wl, torch, sgn, rerank) for l in range(LAYERS)]
     shape = kvr.Shape.of(layers[0].K, layers[0].q)
     params = kvr.SelectParams(w.C, w.k, w.W, w.lut)
     ws_s = kvr.workspace(kvr.kvr_select_workspace_size(shape, params), dev)
@@ -283,7 +300,7 @@ def run_gpu(args, w):
         side.wait_event(fork)
         if ev:
             ev[0].record(side)
-        kvr.kvr_encode_keys(L.K, pos_new, 1, sgn, L.codes, err, stream=side)
+        L.encode_new(kvr, pos_new, sgn, err, stream=side)
         if ev:
             ev[1].record(side)
         join.record(side)
@@ -297,7 +314,7 @@ def run_gpu(args, w):
             ev[4].record(main)
         main.wait_event(join)
 
-    launches_per_step = 3  # encode, select, attend
+    launches_per_step = 4 if rerank == "rsq" else 3  # encode(s), select, attend
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
     # eager warm-up on the capture stream, then one graph per layer
@@ -342,7 +359,7 @@ def run_gpu(args, w):
         fork.record(main)
         side.wait_event(fork)
         for L in layers:
-            kvr.kvr_encode_keys(L.K, pos_new, 1, sgn, L.codes, err, stream=side)
+            L.encode_new(kvr, pos_new, sgn, err, stream=side)
             kvr.kvr_select(L.q, L.K, L.codes, seq, sgn, L.params, idx, cnt, ws_s, err)
             kvr.kvr_sparse_attend(L.q, L.K, L.V, idx, cnt, seq, w.W, scale, L.out, ws_a, err)
         join.record(side)
@@ -398,18 +415,22 @@ def run_gpu(args, w):
     e2e = run_e2e(args, w, layers, kvr, torch, sgn, params, ws_s, ws_a, idx, cnt, seq, pos_new,
                   err, scale, world)
 
+    recall = rerank_recall(w, layers[0], kvr, torch, sgn, ws_s, seq) if rerank == "rsq" else None
+
     steps_total = args.steps * world
     value = steps_total / (ms / 1000.0)
     if rank != 0:
         return
-    ab = algorithmic_bytes(w)
+    ab = algorithmic_bytes(w, rerank)
+    # the reranking select reads records, not K rows: its own counters
+    sel_key = "select_kernel_rsq" if rerank == "rsq" else "select_kernel"
     peak, peak_kind = peaks()
     roof = None
     if avg["select"]:
         ach = ab["select"] / (avg["select"] * 1e-3) / 1e9
         roof = {"bound": "hbm", "kernel": "select_kernel (kvr_select, one launch)",
                 "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-                "peak_kind": peak_kind, "traffic": measured_traffic("select_kernel"),
+                "peak_kind": peak_kind, "traffic": measured_traffic(sel_key),
                 "algorithmic_bytes": ab["select"], "avg_ms": avg["select"]}
     path = None
     if avg["select"] and avg["attend"]:
@@ -418,9 +439,9 @@ def run_gpu(args, w):
         path = {"calls": "kvr_select + kvr_sparse_attend", "achieved": ach, "peak": peak,
                 "unit": "GB/s", "frac": ach / peak, "frac_of_8TBs": ach / 8000.0,
                 "us": tsum * 1e6, "algorithmic_bytes": ab["select"] + ab["attend"],
-                "traffic": (None if None in (measured_traffic("select_kernel"),
+                "traffic": (None if None in (measured_traffic(sel_key),
                                              measured_traffic("attend_kernel"))
-                            else measured_traffic("select_kernel")
+                            else measured_traffic(sel_key)
                             + measured_traffic("attend_kernel")),
                 "attend_us": avg["attend"] * 1e3, "encode_us": avg["encode"] * 1e3}
     # the whole step against its measured time: every byte the step must read
@@ -441,12 +462,30 @@ def run_gpu(args, w):
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": config_of(w), "roofline": roof, "path_roofline": path,
+        "data": "synthetic", "config": dict(config_of(w), rerank=rerank), "roofline": roof,
+        "path_roofline": path, "rerank_recall": recall,
         "step_roofline": step_roof,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
+
+
+def rerank_recall(w, L, kvr, torch, sgn, ws_s, seq):
+    """Share of the exact path's top-k that the reranked top-k keeps, over
+    every unit of one layer (a quality figure, untimed)."""
+    exact = kvr.SelectParams(w.C, w.k, w.W, w.lut)
+    ia = torch.empty((w.B, w.Hkv, w.k), dtype=torch.int32, device=L.K.device)
+    ie = torch.empty_like(ia)
+    ca = torch.empty((w.B, w.Hkv), dtype=torch.int32, device=L.K.device)
+    ce = torch.empty_like(ca)
+    kvr.kvr_select(L.q, L.K, L.codes, seq, sgn, L.params, ia, ca, ws_s)
+    kvr.kvr_select(L.q, L.K, L.codes, seq, sgn, exact, ie, ce, ws_s)
+    a, e = ia.cpu().reshape(-1, w.k), ie.cpu().reshape(-1, w.k)
+    ca, ce = ca.cpu().reshape(-1), ce.cpu().reshape(-1)
+    kept = [len(set(a[u, :ca[u]].tolist()) & set(e[u, :ce[u]].tolist())) / max(1, int(ce[u]))
+            for u in range(a.shape[0])]
+    return {"of": "exact q_bar.k top-%d" % w.k, "mean": sum(kept) / len(kept), "min": min(kept)}
 
 
 def run_e2e(args, w, layers, kvr, torch, sgn, params, ws_s, ws_a, idx, cnt, seq, pos_new, err,
@@ -467,7 +506,7 @@ def run_e2e(args, w, layers, kvr, torch, sgn, params, ws_s, ws_a, idx, cnt, seq,
         L.q.copy_(hq[i % LAYERS], non_blocking=True)
         L.K[:, :, w.N - 1].copy_(hk[i % LAYERS], non_blocking=True)
         L.V[:, :, w.N - 1].copy_(hv[i % LAYERS], non_blocking=True)
-        kvr.kvr_encode_keys(L.K, pos_new, 1, sgn, L.codes, err)
+        L.encode_new(kvr, pos_new, sgn, err)
         kvr.kvr_select(L.q, L.K, L.codes, seq, sgn, L.params, idx, cnt, ws_s, err)
         kvr.kvr_sparse_attend(L.q, L.K, L.V, idx, cnt, seq, w.W, scale, L.out, ws_a, err)
         hout.copy_(L.out, non_blocking=True)
@@ -806,6 +845,9 @@ def main():
                                            "batched_drift"],
                     default="llama3_8b_128k",
                     help="the timed workload (the 128K decode layer is the headline)")
+    ap.add_argument("--rerank", choices=["exact", "rsq"], default="exact",
+                    help="candidate ranking of the 128K workload: exact q_bar.k from the K "
+                         "rows, or the calibrated estimate from per-key records")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -170,8 +170,9 @@ kvr_status kvr_encode_keys(const kvr_shape *shape, const void *K, const int32_t 
  *
  * Record of a key (kvr_rsq_record_bytes(d) = 6 d/8 bytes): with z = FWHT(D k)
  * and per sub-block b of 8 coordinates z_b:
- *   d/8 little-endian words [sign bits, magnitude bit 0, bit 1, bit 2], bit j
- *   of each byte for coordinate j; the magnitude mag_j = #{i in 1..7 :
+ *   d/8 little-endian 32-bit words, nibble j (bits 4j .. 4j+3) of word b
+ *   = mag_j | sign_j << 3 for coordinate 8b + j (sign_j = z_j < 0, the
+ *   code bit); the magnitude mag_j = #{i in 1..7 :
  *   fl(z_j^2) >= fl(bsq[i] s)} with s = fma chain of z_j^2 over j ascending;
  *   then d/8 bf16 scales w_b = bf16(s / c), c = fma chain of |z_j| lev[mag_j]
  *   (0 when c = 0).

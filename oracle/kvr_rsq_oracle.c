@@ -31,9 +31,9 @@
  *     8 coordinates of a block from +0, times w_b, then butterfly sums over
  *     16 block slots with spans 8, 4, 2, 1, empty slots +0).
  *
- * Record of one key (6 * d/8 bytes): d/8 little-endian 32-bit block words
- * [sign bits, magnitude bit 0, bit 1, bit 2] (bit j of each byte for
- * coordinate j of the block), then d/8 bf16 scales w_b.
+ * Record of one key (6 * d/8 bytes): d/8 little-endian 32-bit block words,
+ * nibble j (bits 4j .. 4j+3) of word b holding coordinate 8b + j as
+ * magnitude | sign << 3, then d/8 bf16 scales w_b.
  */
 #include <math.h>
 #include <stdint.h>
@@ -189,7 +189,7 @@ int orc_rsq_encode(const float *x, int64_t n, int d, const int8_t *sgn, uint8_t 
             float s = 0.0f;
             for (int j = 0; j < RSQ_M; j++)
                 s = fmaf(zb[j], zb[j], s);
-            unsigned sign = 0, p0 = 0, p1 = 0, p2 = 0;
+            uint32_t word = 0;
             float c = 0.0f;
             for (int j = 0; j < RSQ_M; j++) {
                 const float a = zb[j] * zb[j];
@@ -197,19 +197,14 @@ int orc_rsq_encode(const float *x, int64_t n, int d, const int8_t *sgn, uint8_t 
                 for (int i = 1; i < RSQ_LEVELS; i++)
                     if (a >= bsq[i] * s)
                         mag = i;
-                if (zb[j] < 0.0f)
-                    sign |= 1u << j;
-                p0 |= (unsigned)(mag & 1) << j;
-                p1 |= (unsigned)((mag >> 1) & 1) << j;
-                p2 |= (unsigned)((mag >> 2) & 1) << j;
+                const uint32_t neg = zb[j] < 0.0f ? 1u : 0u;
+                word |= ((uint32_t)mag | neg << 3) << (4 * j);
                 c = fmaf(fabsf(zb[j]), lev[mag], c);
             }
             const float w = (c > 0.0f) ? s / c : 0.0f;
             const uint16_t wb = bf16_bits(w);
-            out[4 * b + 0] = (uint8_t)sign;
-            out[4 * b + 1] = (uint8_t)p0;
-            out[4 * b + 2] = (uint8_t)p1;
-            out[4 * b + 3] = (uint8_t)p2;
+            for (int i = 0; i < 4; i++)
+                out[4 * b + i] = (uint8_t)(word >> (8 * i));
             out[4 * nb + 2 * b] = (uint8_t)(wb & 0xff);
             out[4 * nb + 2 * b + 1] = (uint8_t)(wb >> 8);
         }
@@ -227,12 +222,12 @@ float orc_rsq_score(const uint8_t *rec, const float *zq, int d)
         t[b] = 0.0f;
         if (b >= nb)
             continue;
-        const unsigned sign = rec[4 * b], p0 = rec[4 * b + 1], p1 = rec[4 * b + 2],
-                       p2 = rec[4 * b + 3];
+        const uint32_t word = (uint32_t)rec[4 * b] | (uint32_t)rec[4 * b + 1] << 8 |
+                              (uint32_t)rec[4 * b + 2] << 16 | (uint32_t)rec[4 * b + 3] << 24;
         float e = 0.0f;
         for (int j = 0; j < RSQ_M; j++) {
-            const int mag = (int)(((p0 >> j) & 1) | (((p1 >> j) & 1) << 1) | (((p2 >> j) & 1) << 2));
-            const float v = ((sign >> j) & 1) ? -lev[mag] : lev[mag];
+            const uint32_t nib = (word >> (4 * j)) & 15u;
+            const float v = (nib & 8u) ? -lev[nib & 7u] : lev[nib & 7u];
             e = fmaf(v, zq[b * RSQ_M + j], e);
         }
         const uint16_t wb = (uint16_t)(rec[4 * nb + 2 * b] | (rec[4 * nb + 2 * b + 1] << 8));

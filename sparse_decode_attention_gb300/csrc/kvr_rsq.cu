@@ -103,7 +103,8 @@ RsqTables make_tables()
 // 8 coordinates (LPB = 8 / E lanes): s = fma chain of z_j^2 over j ascending
 // from +0, mag_j = #{i : fl(z_j^2) >= fl(bsq_i s)}, c = fma chain of
 // |z_j| lev[mag_j], w = bf16(s / c) (0 when c == 0). The chains run through
-// the block's lanes in coordinate order.
+// the block's lanes in coordinate order. Word of the block: nibble j =
+// mag_j | sign_j << 3.
 template <int D, typename T>
 __global__ void __launch_bounds__(256)
 rsq_encode_kernel(const T *__restrict__ K, int Hkv, int64_t cap, const int32_t *__restrict__ pos0,
@@ -151,7 +152,7 @@ rsq_encode_kernel(const T *__restrict__ K, int Hkv, int64_t cap, const int32_t *
         s = __shfl_sync(kFull, sk, first + k);
     }
     int mag[E];
-    uint32_t sign = 0, p0 = 0, p1 = 0, p2 = 0;
+    uint32_t word = 0;
 #pragma unroll
     for (int r = 0; r < E; r++) {
         const float a2 = z[r] * z[r];
@@ -161,10 +162,7 @@ rsq_encode_kernel(const T *__restrict__ K, int Hkv, int64_t cap, const int32_t *
             if (a2 >= s_bsq[i] * s) m = i;
         mag[r] = m;
         const int j = pos * E + r;  // coordinate within the block
-        sign |= (uint32_t)(z[r] < 0.0f) << j;
-        p0 |= (uint32_t)(m & 1) << j;
-        p1 |= (uint32_t)((m >> 1) & 1) << j;
-        p2 |= (uint32_t)((m >> 2) & 1) << j;
+        word |= ((uint32_t)m | (uint32_t)(z[r] < 0.0f) << 3) << (4 * j);
     }
     float c = 0.0f;
 #pragma unroll
@@ -176,7 +174,6 @@ rsq_encode_kernel(const T *__restrict__ K, int Hkv, int64_t cap, const int32_t *
         }
         c = __shfl_sync(kFull, ck, first + k);
     }
-    uint32_t word = sign | (p0 << 8) | (p1 << 16) | (p2 << 24);
 #pragma unroll
     for (int o = 1; o < LPB; o <<= 1) word |= __shfl_xor_sync(kFull, word, o);
     if (pos == 0) {

@@ -185,8 +185,8 @@ template <int D, typename T> struct SelSmem {
     static constexpr int oMisc = oScan + 40 * 4;
     static constexpr int oWH = oMisc + 64 * 4;  // [kSelWarps][256] per-warp histograms
     static constexpr int oPl = oWH + kSelWarps * 256 * 4;  // [8][kPlaneCap] score planes
-    static constexpr int oLev = oPl + 8 * kPlaneCap * 4;  // float [8] reranker levels
-    static constexpr int bytes = oLev + 8 * 4;
+    static constexpr int oLev = oPl + 8 * kPlaneCap * 4;  // float [16] signed reranker levels
+    static constexpr int bytes = oLev + 16 * 4;
     static_assert(16 * 256 * 4 <= kRingBytes, "radix exchange scratch must fit the ring");
 };
 
@@ -318,7 +318,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
 #pragma unroll
             for (int r = 0; r < E; r++) sQbar[lane * E + r] = x[r];
     }
-    if (tid < 8) reinterpret_cast<float *>(smem + SM::oLev)[tid] = a.lev[tid];
+    // nibble code -> signed level: magnitude in bits 0..2, sign in bit 3
+    if (tid < 16) reinterpret_cast<float *>(smem + SM::oLev)[tid] = (tid & 8) ? -a.lev[tid & 7] : a.lev[tid & 7];
     __syncthreads();
     for (int c = tid; c < NCH; c += kSelThreads)
         sQm[c] = make_uint4((uint32_t)sQsgn[4 * c], (uint32_t)sQsgn[4 * c + 1],
@@ -556,7 +557,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         // Calibrated estimate from the records, no K rows: lane gl of a
         // half-warp is block slot gl (slots past d/8 add +0), zq of its block
         // is in sQbar; e = fma chain over the block's 8 coordinates of
-        // (+-level) * zq, t = w * e, then butterfly sums over spans 8..1.
+        // (+-level) * zq, the signed level looked up by the coordinate's
+        // nibble; t = w * e, then butterfly sums over spans 8..1.
         constexpr int NB = D / 8, RBQ = 6 * NB, NHW = kSelThreads / 16, RR = 8;
         const int hw = tid >> 4, gl = tid & 15;
         const float *sLev = reinterpret_cast<const float *>(smem + SM::oLev);
@@ -583,12 +585,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
             for (int r = 0; r < RR; r++) {
                 float e = 0.0f;
 #pragma unroll
-                for (int jj = 0; jj < 8; jj++) {
-                    const uint32_t m = ((wd[r] >> (8 + jj)) & 1u) | (((wd[r] >> (16 + jj)) & 1u) << 1) |
-                                       (((wd[r] >> (24 + jj)) & 1u) << 2);
-                    const float lv = sLev[m];
-                    e = __fmaf_rn(((wd[r] >> jj) & 1u) ? -lv : lv, zqv[jj], e);
-                }
+                for (int jj = 0; jj < 8; jj++) e = __fmaf_rn(sLev[(wd[r] >> (4 * jj)) & 15u], zqv[jj], e);
                 float t = (gl < NB) ? __uint_as_float(ws[r] << 16) * e : 0.0f;
 #pragma unroll
                 for (int span = 8; span >= 1; span >>= 1) t = t + __shfl_xor_sync(kFull, t, span);

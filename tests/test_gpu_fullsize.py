@@ -216,3 +216,40 @@ def test_tiered_window_cache_full_size():
             assert np.array_equal(oracle.f32(V[b, h].cpu()), o.V[:cap]), (t, u)
     assert moved > 0
     assert kvr.kvr_read_error(err) == 0
+
+
+def test_llama_128k_reranked_full_size():
+    """The 128K layer with the calibrated reranker in the benchmark's launch
+    configuration (early inputs, V hint, records): records of sampled units,
+    candidate estimates and top-k sets bit-exact, attention within 2e-3."""
+    w = wl.LLAMA_128K
+    p = Path(w, cap=w.N)
+    p.encode(0, w.N)
+    rec = kvr.rsq_buffer(p.K)
+    kvr.kvr_encode_rsq(p.K, torch.zeros(w.B, dtype=torch.int32, device=DEV), w.N, p.sgn, rec,
+                       p.err)
+    params = kvr.SelectParams(w.C, w.k, w.W, w.lut, flags=kvr.SELECT_EARLY_INPUTS,
+                              V_prefetch=p.V, rsq_records=rec)
+    sgn = p.sgn.cpu().numpy()
+    scale = np.float32(1.0 / math.sqrt(w.d))
+    for t in range(2):
+        q = wl.step_query(w, p.qb, t).contiguous()
+        torch.cuda.synchronize()
+        kvr.kvr_select(q, p.K, p.codes, p.seq, p.sgn, params, p.idx, p.cnt, p.ws_s, p.err)
+        kvr.kvr_sparse_attend(q, p.K, p.V, p.idx, p.cnt, p.seq, w.W, float(scale), p.out,
+                              p.ws_a, p.err)
+        idx, cnt, out = p.idx.cpu().numpy(), p.cnt.cpu().numpy(), p.out.cpu().numpy()
+        qn = q.float().cpu().numpy()
+        for h in ((0, 3), (5, 7))[t]:
+            Ku = oracle.f32(p.K[0, h].cpu())
+            codes = oracle.encode(Ku, sgn)
+            ref_rec = oracle.rsq_encode(Ku, sgn)
+            assert np.array_equal(rec[0, h].cpu().numpy(), ref_rec), h
+            qg = qn[0, h * w.G:(h + 1) * w.G]
+            ref_idx, ref_cnt = oracle.select_unit_rsq(qg, codes, ref_rec, w.N, sgn, w.C, w.k,
+                                                      w.W, w.lut)
+            assert cnt[0, h] == ref_cnt and np.array_equal(idx[0, h], ref_idx), h
+            ref = oracle.attend_unit(qg, Ku, oracle.f32(p.V[0, h].cpu()), w.N,
+                                     ref_idx[:ref_cnt], ref_cnt, w.W, scale)
+            assert np.abs(out[0, h * w.G:(h + 1) * w.G] - ref).max() <= ATOL, h
+    assert kvr.kvr_read_error(p.err) == 0

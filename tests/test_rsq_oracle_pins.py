@@ -56,11 +56,12 @@ def test_float_tables_round_the_fp64_ones():
 
 
 def decode(rec, d):
+    """Test-side reading of the documented record: a 32-bit word per block,
+    nibble j = magnitude | sign << 3 of coordinate j, then bf16 scales."""
     nb = d // M
-    w = rec[:4 * nb].reshape(nb, 4)
-    bits = lambda byte: np.array([(int(byte) >> j) & 1 for j in range(M)])
-    sign = np.stack([bits(w[b, 0]) for b in range(nb)])
-    mag = np.stack([bits(w[b, 1]) | (bits(w[b, 2]) << 1) | (bits(w[b, 3]) << 2) for b in range(nb)])
+    words = rec[:4 * nb].view("<u4")
+    nib = np.array([[(int(words[b]) >> (4 * j)) & 15 for j in range(M)] for b in range(nb)])
+    sign, mag = nib >> 3, nib & 7
     scale = rec[4 * nb:].view(np.uint16).astype(np.uint32) << 16
     return sign, mag, scale.view(np.float32)
 
