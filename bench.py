@@ -28,7 +28,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "sparse decode-attention steps/s at 128K ctx; achieved HBM GB/s vs peak"
+OFFLOAD_METRIC = "sparse decode-attention steps/s at 1M ctx, K/V in host memory"
 LAYERS = 32
+LAYERS_DEFAULT = LAYERS
 
 
 def peaks():
@@ -236,7 +238,7 @@ def config_of(w):
 # --------------------------------------------------------------------------
 
 class Layer:
-    def __init__(self, w, l, kvr, wl, torch, sgn, rerank="exact"):
+    def __init__(self, w, l, kvr, wl, torch, sgn, rerank="exact", host=False):
         dev = "cuda"
         K, V, qb = wl.make_cache(w, device=dev, cap=w.N, seed=w.seed + 1000 * l)
         self.K, self.V = K, V
@@ -255,8 +257,17 @@ class Layer:
             self.rec = kvr.rsq_buffer(K)
             kvr.kvr_encode_rsq(K, torch.zeros(w.B, dtype=torch.int32, device=dev), w.N, sgn,
                                self.rec)
+        if host:
+            # the full-precision cache moves to page-locked host memory; the
+            # kernels read it through the device's mapping (no copy calls)
+            self.K = torch.empty(K.shape, dtype=K.dtype, pin_memory=True)
+            self.V = torch.empty(V.shape, dtype=V.dtype, pin_memory=True)
+            self.K.copy_(K)
+            self.V.copy_(V)
+            del K, V
+            torch.cuda.empty_cache()
         self.params = kvr.SelectParams(w.C, w.k, w.W, w.lut, flags=kvr.SELECT_EARLY_INPUTS,
-                                       V_prefetch=V, rsq_records=self.rec)
+                                       V_prefetch=None if host else self.V, rsq_records=self.rec)
 
     def encode_new(self, kvr, pos_new, sgn, err, stream=None):
         """Code (and record) of the appended key."""
@@ -275,8 +286,9 @@ def run_gpu(args, w):
     dev = torch.device("cuda", torch.cuda.current_device())
     kvr.load()
     sgn = wl.srht_signs(w.d, device=dev)
-    rerank = args.rerank
-    layers = [Layer(w, l, kvr, wl, torch, sgn, rerank) for l in range(LAYERS)]
+    host = args.workload == "million_offload"
+    rerank = args.rerank or ("rsq" if host else "exact")
+    layers = [Layer(w, l, kvr, wl, torch, sgn, rerank, host) for l in range(LAYERS)]
     shape = kvr.Shape.of(layers[0].K, layers[0].q)
     params = kvr.SelectParams(w.C, w.k, w.W, w.lut)
     ws_s = kvr.workspace(kvr.kvr_select_workspace_size(shape, params), dev)
@@ -439,11 +451,21 @@ def run_gpu(args, w):
         path = {"calls": "kvr_select + kvr_sparse_attend", "achieved": ach, "peak": peak,
                 "unit": "GB/s", "frac": ach / peak, "frac_of_8TBs": ach / 8000.0,
                 "us": tsum * 1e6, "algorithmic_bytes": ab["select"] + ab["attend"],
-                "traffic": (None if None in (measured_traffic(sel_key),
-                                             measured_traffic("attend_kernel"))
+                "traffic": (None if host or None in (measured_traffic(sel_key),
+                                                     measured_traffic("attend_kernel"))
                             else measured_traffic(sel_key)
                             + measured_traffic("attend_kernel")),
                 "attend_us": avg["attend"] * 1e3, "encode_us": avg["encode"] * 1e3}
+    link = None
+    if host and avg["attend"]:
+        # the attention's gathers cross the host link: its bytes over its time
+        # against a page-locked host -> device copy measured on this machine
+        lpk = link_peak(torch)
+        ach = ab["attend"] / (avg["attend"] * 1e-3) / 1e9
+        link = {"bound": "host link", "kernel": "attend_kernel (rows gathered from host memory)",
+                "achieved": ach, "peak": lpk, "unit": "GB/s", "frac": ach / lpk,
+                "peak_kind": "measured here: 1 GiB pinned host -> device copy, best of 5",
+                "algorithmic_bytes": ab["attend"], "avg_ms": avg["attend"]}
     # the whole step against its measured time: every byte the step must read
     # (codes, candidate rows, selected K / V, query, the appended key) over
     # ms_per_step; select and attend overlap across their launch boundary, so
@@ -456,14 +478,18 @@ def run_gpu(args, w):
     if not args.no_cpu_baseline and world == 1:
         v, el, done = time_oracle(w, args.cpu_seconds, "cuda")
         cpu = {"value": v, "unit": "steps/s", "cores": 1, "kind": "oracle",
-               "sample": "%d unit-steps (batch 0, kv head 0) of the 128K workload in %.1f s, "
-                         "single-threaded; steps/s = unit-steps / %d / s" % (done, el, ab["units"])}
+               "sample": "%d unit-steps (batch 0, kv head 0) of the %s workload in %.1f s, "
+                         "single-threaded; steps/s = unit-steps / %d / s"
+                         % (done, w.name, el, ab["units"])}
+    cfg = dict(config_of(w), rerank=rerank)
+    if host:
+        cfg["kv_residency"] = "K, V in page-locked host memory read through the device mapping"
     line = {
-        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+        "metric": OFFLOAD_METRIC if host else METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": dict(config_of(w), rerank=rerank), "roofline": roof,
-        "path_roofline": path, "rerank_recall": recall,
+        "data": "synthetic", "config": cfg, "roofline": roof,
+        "path_roofline": path, "link_roofline": link, "rerank_recall": recall,
         "step_roofline": step_roof,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
@@ -471,13 +497,30 @@ def run_gpu(args, w):
     print(json.dumps(line), flush=True)
 
 
+def link_peak(torch):
+    """GB/s of a 1 GiB page-locked host -> device copy (best of 5, CUDA events)."""
+    src = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    best = None
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1)
+        best = t if best is None else min(best, t)
+    del src, dst
+    return (1 << 30) / (best * 1e-3) / 1e9
+
+
 def rerank_recall(w, L, kvr, torch, sgn, ws_s, seq):
     """Share of the exact path's top-k that the reranked top-k keeps, over
     every unit of one layer (a quality figure, untimed)."""
     exact = kvr.SelectParams(w.C, w.k, w.W, w.lut)
-    ia = torch.empty((w.B, w.Hkv, w.k), dtype=torch.int32, device=L.K.device)
+    ia = torch.empty((w.B, w.Hkv, w.k), dtype=torch.int32, device=L.codes.device)
     ie = torch.empty_like(ia)
-    ca = torch.empty((w.B, w.Hkv), dtype=torch.int32, device=L.K.device)
+    ca = torch.empty((w.B, w.Hkv), dtype=torch.int32, device=L.codes.device)
     ce = torch.empty_like(ca)
     kvr.kvr_select(L.q, L.K, L.codes, seq, sgn, L.params, ia, ca, ws_s)
     kvr.kvr_select(L.q, L.K, L.codes, seq, sgn, exact, ie, ce, ws_s)
@@ -498,7 +541,10 @@ def run_e2e(args, w, layers, kvr, torch, sgn, params, ws_s, ws_a, idx, cnt, seq,
     hk = [L.K[:, :, w.N - 1].cpu().pin_memory() for L in layers]
     hv = [L.V[:, :, w.N - 1].cpu().pin_memory() for L in layers]
     hout = torch.empty((w.B, w.Hq, w.d), dtype=torch.float32).pin_memory()
-    h2d = hq[0].numel() * hq[0].element_size() + 2 * hk[0].numel() * hk[0].element_size()
+    # a host-resident cache takes the appended K/V row by a host-side write
+    # (the kernels read it through the mapping): only q crosses to the device
+    row_h2d = 0 if not layers[0].K.is_cuda else 2 * hk[0].numel() * hk[0].element_size()
+    h2d = hq[0].numel() * hq[0].element_size() + row_h2d
     d2h = hout.numel() * hout.element_size()
 
     def one(i):
@@ -842,12 +888,13 @@ def main():
                     help="layer caches rotated (fewer = a small case for profiling; the "
                          "default keeps every step's inputs cold in L2)")
     ap.add_argument("--workload", choices=["llama3_8b_128k", "tiered_window_cache",
-                                           "batched_drift"],
+                                           "batched_drift", "million_offload"],
                     default="llama3_8b_128k",
                     help="the timed workload (the 128K decode layer is the headline)")
-    ap.add_argument("--rerank", choices=["exact", "rsq"], default="exact",
-                    help="candidate ranking of the 128K workload: exact q_bar.k from the K "
-                         "rows, or the calibrated estimate from per-key records")
+    ap.add_argument("--rerank", choices=["exact", "rsq"], default=None,
+                    help="candidate ranking: exact q_bar.k from the K rows (default for "
+                         "device caches), or the calibrated estimate from per-key records "
+                         "(default for million_offload)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -866,6 +913,17 @@ def main():
                               "reference line; the oracle arm covers the 128K workload"}))
             return
         run_gpu_drift(args, wl.DRIFT)
+        return
+    if args.workload == "million_offload":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the host-resident workload "
+                              "has no reference line; the oracle arm covers the 128K workload"}))
+            return
+        # two layers of 2^20 tokens: 8.6 GB of page-locked host cache, and the
+        # device-side codes and records (2 x 0.94 GB) exceed L2
+        if args.layers == LAYERS_DEFAULT:
+            globals()["LAYERS"] = 2
+        run_gpu(args, wl.MILLION)
         return
     w = wl.LLAMA_128K
     if args.impl == "reference":

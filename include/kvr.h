@@ -46,6 +46,18 @@
  *   seq_len   [B] int32 device: tokens 0..seq_len[b]-1 of batch b are valid.
  *   srht_sign [d] int8 device: the +-1 diagonal of the rotation.
  * All base pointers must be 16-byte aligned.
+ *
+ * Host-resident caches (ParisKV, "Offloading tramite Indirizzamento Virtuale
+ * Unificato": the full-precision KV stays in host memory and the GPU gathers
+ * only the rows it needs, with no copy call): the K and V arguments of
+ * kvr_encode_keys, kvr_encode_rsq, kvr_select and kvr_sparse_attend may point
+ * to page-locked host memory mapped into the device's address space
+ * (cudaHostAlloc, or cudaHostRegister with mapping; under unified addressing
+ * the host pointer itself). The kernels then read those rows over the
+ * host-GPU link. Pageable host memory is not allowed (the library does not
+ * query pointer kinds). With kvr_select_params.rsq_records set, kvr_select
+ * reads no K rows, so only the attention's gathers cross the link. The tier
+ * calls need device memory.
  */
 #ifndef KVR_H_
 #define KVR_H_

@@ -215,6 +215,16 @@ def _cuda(t, name, dtype=None):
     return t
 
 
+def _kv(t, name):
+    """A K or V cache: a CUDA tensor, or a page-locked host tensor that the
+    kernels read through the device's mapping of it (host-resident cache)."""
+    if not isinstance(t, torch.Tensor) or not (t.is_cuda or t.is_pinned()):
+        raise TypeError("%s must be a CUDA tensor or a page-locked (pinned) host tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t
+
+
 def _codes(codes, shape):
     _cuda(codes, "codes", torch.uint8)
     if codes.numel() < kvr_codes_bytes(shape):
@@ -224,7 +234,7 @@ def _codes(codes, shape):
 
 def kvr_encode_keys(K, pos0, n_new, srht_sign, codes, err=None, stream=None, shape=None):
     """Encode rows [pos0[b], pos0[b] + n_new) of every unit of K into codes."""
-    _cuda(K, "K")
+    _kv(K, "K")
     shape = shape or Shape(K.shape[0], K.shape[1], K.shape[1], K.shape[3], K.shape[2], K.dtype)
     _cuda(pos0, "pos0", torch.int32)
     _cuda(srht_sign, "srht_sign", torch.int8)
@@ -250,7 +260,7 @@ def kvr_select_workspace_views(shape: Shape, params: SelectParams) -> dict:
 def kvr_select(q, K, codes, seq_len, srht_sign, params: SelectParams, out_idx, out_count,
                workspace, err=None, stream=None):
     """Coarse score, candidate set, exact rescoring and top-k for every unit."""
-    shape = Shape.of(_cuda(K, "K"), _cuda(q, "q", K.dtype))
+    shape = Shape.of(_kv(K, "K"), _cuda(q, "q", K.dtype))
     _codes(codes, shape)
     _cuda(seq_len, "seq_len", torch.int32)
     _cuda(srht_sign, "srht_sign", torch.int8)
@@ -272,7 +282,7 @@ def kvr_select_static_scratch(q, K, codes, seq_len, srht_sign, params: SelectPar
                               out_count, err=None, stream=None):
     """kvr_select for callers that cannot allocate: scratch is a fixed device
     array inside the library (16 MiB per GPU), shared by every call on a device."""
-    shape = Shape.of(_cuda(K, "K"), _cuda(q, "q", K.dtype))
+    shape = Shape.of(_kv(K, "K"), _cuda(q, "q", K.dtype))
     _codes(codes, shape)
     _cuda(seq_len, "seq_len", torch.int32)
     _cuda(srht_sign, "srht_sign", torch.int8)
@@ -292,8 +302,10 @@ def kvr_attend_workspace_size(shape: Shape, kmax: int, W: int) -> int:
 def kvr_sparse_attend(q, K, V, idx, count, seq_len, W, scale, out, workspace, err=None,
                       stream=None):
     """Gather + online-softmax attention over idx[b, h, :count] plus the window."""
-    shape = Shape.of(_cuda(K, "K"), _cuda(q, "q", K.dtype))
-    _cuda(V, "V", K.dtype)
+    shape = Shape.of(_kv(K, "K"), _cuda(q, "q", K.dtype))
+    _kv(V, "V")
+    if V.dtype != K.dtype or V.shape != K.shape:
+        raise TypeError("V must have K's dtype and shape")
     _cuda(idx, "idx", torch.int32)
     _cuda(count, "count", torch.int32)
     _cuda(seq_len, "seq_len", torch.int32)
@@ -432,17 +444,21 @@ def kvr_rsq_tables():
 
 
 def rsq_buffer(K, device=None):
-    """Zeroed uint8 records [B, Hkv, cap, record bytes] for a K cache [B, Hkv, cap, d]."""
+    """Zeroed uint8 device records [B, Hkv, cap, record bytes] for a K cache
+    [B, Hkv, cap, d] (on K's device, or the current CUDA device for a
+    host-resident K)."""
     B, Hkv, cap, d = K.shape
     rb = kvr_rsq_record_bytes(d)
     if rb == 0:
         raise ValueError("the reranker supports d = 64 or 128")
-    return torch.zeros((B, Hkv, cap, rb), dtype=torch.uint8, device=device or K.device)
+    if device is None:
+        device = K.device if K.is_cuda else torch.device("cuda", torch.cuda.current_device())
+    return torch.zeros((B, Hkv, cap, rb), dtype=torch.uint8, device=device)
 
 
 def kvr_encode_rsq(K, pos0, n_new, srht_sign, records, err=None, stream=None):
     """Reranker records of rows [pos0[b], pos0[b] + n_new) of every unit of K."""
-    _cuda(K, "K")
+    _kv(K, "K")
     shape = Shape(K.shape[0], K.shape[1], K.shape[1], K.shape[3], K.shape[2], K.dtype)
     _cuda(pos0, "pos0", torch.int32)
     _cuda(srht_sign, "srht_sign", torch.int8)

@@ -182,3 +182,17 @@ def test_reranker_calls_validate_before_launch(kvr_lib):
     pv.rsq_records = (1 << 20) + 8                    # misaligned records
     assert L.kvr_select(ctypes.byref(s.c()), ctypes.byref(pv), fake, fake, fake, fake, fake,
                         fake, fake, fake, need, None, None) == 1
+
+
+def test_pageable_host_caches_are_refused(kvr_lib):
+    """K / V may be device or page-locked host memory; pageable host tensors
+    are refused by the binding before any call (no GPU)."""
+    import torch
+    kvr = kvr_lib
+    K = torch.zeros((1, 2, 64, 64), dtype=torch.bfloat16)          # pageable
+    for call in (lambda: kvr.kvr_encode_keys(K, None, 1, None, None),
+                 lambda: kvr.kvr_encode_rsq(K, None, 1, None, None),
+                 lambda: kvr.kvr_select(None, K, None, None, None, None, None, None, None),
+                 lambda: kvr.kvr_sparse_attend(None, K, K, None, None, None, 8, 0.1, None, None)):
+        with pytest.raises(TypeError, match="page-locked"):
+            call()

@@ -1,10 +1,10 @@
 """GPU parity of the calibrated inner-product reranker (ParisKV, "Pipeline di
 Recupero Nativa su GPU in Due Stadi", candidate reranking) against the oracle.
 
-Records (sign and 3-bit magnitude bit planes, bf16 calibration scales) must
-match byte for byte; the selection with records ranks the same candidate set
-as the exact path by estimates that must match bit for bit, and the top-k
-index sets must be equal; attention over those sets within 2e-3.
+Records (a sign and 3-bit magnitude nibble per coordinate, bf16 calibration
+scales) must match byte for byte; the selection with records ranks the same
+candidate set as the exact path by estimates that must match bit for bit, and
+the top-k index sets must be equal; attention over those sets within 2e-3.
 """
 import math
 
