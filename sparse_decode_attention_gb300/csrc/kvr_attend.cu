@@ -84,6 +84,7 @@ __device__ __forceinline__ void load_lane(const uint8_t *row, int lane, float (&
 template <int G>
 __device__ __forceinline__ float reduce_heads(float (&v)[G], int lane)
 {
+    __syncwarp();
     constexpr int LG = (G >= 16) ? 4 : (G >= 8) ? 3 : (G >= 4) ? 2 : (G >= 2) ? 1 : 0;
 #pragma unroll
     for (int s = 0; s < LG; s++) {

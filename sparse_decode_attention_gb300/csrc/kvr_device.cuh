@@ -68,6 +68,7 @@ __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162flo
 template <int E, int L>
 __device__ __forceinline__ void fwht_lanes(float (&x)[E], int gl)
 {
+    __syncwarp();  // reconverge first: a diverged warp runs each shuffle once per branch
 #pragma unroll
     for (int h = 1; h < E; h <<= 1) {
 #pragma unroll
@@ -96,6 +97,7 @@ __device__ __forceinline__ void fwht_lanes(float (&x)[E], int gl)
 template <int E>
 __device__ __forceinline__ uint32_t sign_word(const float (&x)[E], int gl)
 {
+    __syncwarp();
     uint32_t bits = 0;
 #pragma unroll
     for (int r = 0; r < E; r++)
@@ -111,6 +113,7 @@ __device__ __forceinline__ uint32_t sign_word(const float (&x)[E], int gl)
 
 __device__ __forceinline__ int warp_sum(int x)
 {
+    __syncwarp();
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
     return x;
@@ -122,6 +125,7 @@ __device__ __forceinline__ int warp_sum(int x)
 template <int N, typename V>
 __device__ __forceinline__ V warp_reduce_split(V (&v)[N])
 {
+    __syncwarp();
     const int lane = threadIdx.x & 31;
     constexpr int LG = (N >= 32) ? 5 : (N >= 16) ? 4 : (N >= 8) ? 3 : (N >= 4) ? 2 : (N >= 2) ? 1 : 0;
 #pragma unroll
@@ -147,10 +151,11 @@ __device__ __forceinline__ int warp_exclusive_scan(int x)
 {
     const int lane = threadIdx.x & 31;
     int s = x;
+    __syncwarp();
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(kFull, s, o);
-        if (lane >= o) s += y;
+        s += (lane >= o) ? y : 0;
     }
     return s - x;
 }
@@ -159,10 +164,11 @@ __device__ __forceinline__ int warp_exclusive_scan(int x)
 __device__ __forceinline__ int warp_suffix_sum(int x)
 {
     const int lane = threadIdx.x & 31;
+    __syncwarp();
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_down_sync(kFull, x, o);
-        if (lane + o < 32) x += y;
+        x += (lane + o < 32) ? y : 0;
     }
     return x;
 }

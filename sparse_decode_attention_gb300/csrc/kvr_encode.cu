@@ -51,6 +51,7 @@ encode_kernel(const T *__restrict__ K, int Hkv, int64_t cap, int64_t tiles,
     const int64_t blk = lo / 32 + kb;
     if (blk * 32 >= hi) return;  // whole warp
     const int64_t t_lane = blk * 32 + lane;
+    __syncwarp();
     const uint32_t inmask = __ballot_sync(kFull, t_lane >= lo && t_lane < hi);
     uint4 *dst = reinterpret_cast<uint4 *>(codes + ((size_t)unit * tiles + (size_t)(blk >> 5)) *
                                                        (D * 128)) +

@@ -149,6 +149,7 @@ rsq_encode_kernel(const T *__restrict__ K, int Hkv, int64_t cap, const int32_t *
 #pragma unroll
             for (int r = 0; r < E; r++) sk = fmaf(z[r], z[r], sk);
         }
+        __syncwarp();
         s = __shfl_sync(kFull, sk, first + k);
     }
     int mag[E];
@@ -172,6 +173,7 @@ rsq_encode_kernel(const T *__restrict__ K, int Hkv, int64_t cap, const int32_t *
 #pragma unroll
             for (int r = 0; r < E; r++) ck = fmaf(fabsf(z[r]), s_lev[mag[r]], ck);
         }
+        __syncwarp();
         c = __shfl_sync(kFull, ck, first + k);
     }
 #pragma unroll

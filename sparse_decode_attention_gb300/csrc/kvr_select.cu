@@ -226,6 +226,16 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     int *sMisc = reinterpret_cast<int *>(smem + SM::oMisc);
 
     cg::cluster_group cluster = cg::this_cluster();
+    // Warm the L2 lines (and address translations) of the query group's rows
+    // before anything waits: the loads themselves come after the dependency
+    // wait, and a prefetch into L2 cannot return data older than L2 holds.
+    {
+        const int ub = blockIdx.y / a.Hkv, uh = blockIdx.y % a.Hkv;
+        const uint8_t *qrows = static_cast<const uint8_t *>(a.q) +
+                               ((int64_t)ub * a.Hq + (int64_t)uh * a.G) * D * (int64_t)sizeof(T);
+        const int qbytes = a.G * D * (int)sizeof(T);
+        for (int o = threadIdx.x * 128; o < qbytes; o += kSelThreads * 128) prefetch_l2_line(qrows + o);
+    }
     // programmatic dependent launch: this grid may start while the previous one
     // drains; nothing is read before the previous grid's writes are visible
     // with KVR_SELECT_EARLY_INPUTS only q is waited for: the length, the code
@@ -297,18 +307,38 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
 
     // q_bar and its code (every CTA of the cluster computes them)
     if (warp == 0) {
+        // reconverge the warp (the branches above split it): its shuffles
+        // below would otherwise run once per branch
+        __syncwarp();
         constexpr int E = D / 32;
-        const T *qg = static_cast<const T *>(a.q) + ((int64_t)b * a.Hq + (int64_t)h * a.G) * D;
+        const T *qg = static_cast<const T *>(a.q) + ((int64_t)b * a.Hq + (int64_t)h * a.G) * D + lane * E;
+        // every load is issued before the first use (up to 4 heads' rows at
+        // a time), then the heads are summed left to right
+        int sg[E];
+#pragma unroll
+        for (int r = 0; r < E; r++) sg[r] = a.sgn[lane * E + r];
+        float acc[E];
+        for (int g0 = 0; g0 < a.G; g0 += 4) {
+            float v[4][E];
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+#pragma unroll
+                for (int r = 0; r < E; r++)
+                    v[i][r] = (g0 + i < a.G) ? to_f32(__ldg(qg + (int64_t)(g0 + i) * D + r)) : 0.0f;
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+#pragma unroll
+                for (int r = 0; r < E; r++)
+                    if (g0 + i < a.G) acc[r] = (g0 + i == 0) ? v[i][r] : acc[r] + v[i][r];
+        }
         float x[E];
 #pragma unroll
         for (int r = 0; r < E; r++) {
             const int j = lane * E + r;
-            float acc = to_f32(qg[j]);
-            for (int g = 1; g < a.G; g++) acc = acc + to_f32(qg[(int64_t)g * D + j]);
-            x[r] = acc / (float)a.G;
+            x[r] = acc[r] / (float)a.G;
             sQbar[j] = x[r];
             if (rank == 0) a.qbar[(int64_t)u * D + j] = x[r];
-            if (a.sgn[j] < 0) x[r] = -x[r];
+            if (sg[r] < 0) x[r] = -x[r];
         }
         fwht_lanes<E, 32>(x, lane);
 #pragma unroll
@@ -364,6 +394,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
             add_planes<ACC, VB>(acc, vote);
         }
         uint32_t other[ACC];  // the other half of the sub-blocks sits in lane ^ 16
+        __syncwarp();
 #pragma unroll
         for (int j = 0; j < ACC; j++) other[j] = __shfl_xor_sync(kFull, acc[j], 16);
         add_planes<ACC, ACC>(acc, other);
@@ -570,16 +601,18 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         for (int base = 0; base < n; base += NHW * RR) {
             uint32_t wd[RR];
             uint32_t ws[RR];
+            // branch-free (clamped index, then masked): the warp stays converged
+            // for the butterflies below
 #pragma unroll
             for (int r = 0; r < RR; r++) {
                 const int j = base + r * NHW + hw;
-                wd[r] = 0u;
-                ws[r] = 0u;
-                if (j < n && gl < NB) {
-                    const uint8_t *rp = recu + (size_t)sI[j] * RBQ;
-                    wd[r] = *reinterpret_cast<const uint32_t *>(rp + 4 * gl);
-                    ws[r] = *reinterpret_cast<const uint16_t *>(rp + 4 * NB + 2 * gl);
-                }
+                const bool live = j < n && gl < NB;
+                const uint8_t *rp = recu + (size_t)sI[j < n ? j : n - 1] * RBQ;
+                const int gs = gl < NB ? gl : 0;
+                const uint32_t w0 = *reinterpret_cast<const uint32_t *>(rp + 4 * gs);
+                const uint32_t s0 = *reinterpret_cast<const uint16_t *>(rp + 4 * NB + 2 * gs);
+                wd[r] = live ? w0 : 0u;
+                ws[r] = live ? s0 : 0u;
             }
 #pragma unroll
             for (int r = 0; r < RR; r++) {
@@ -702,10 +735,11 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
             sum += cnt[r];
         }
         int incl = sum;
+        __syncwarp();
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += y;
+            incl += (lane >= o) ? y : 0;
         }
         const int run0 = incl - sum;
         const bool mine = run0 < rem && rem <= incl;
@@ -722,6 +756,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
                 run += cnt[r];
             }
         }
+        __syncwarp();
         const int src = __ffs(__ballot_sync(kFull, mine)) - 1;
         bin = __shfl_sync(kFull, bn, src);
         before = __shfl_sync(kFull, bf, src);
@@ -761,6 +796,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
             lmin = min(lmin, k);
             lmax = max(lmax, k);
         }
+        __syncwarp();
         lmin = __reduce_min_sync(kFull, lmin);
         lmax = __reduce_max_sync(kFull, lmax);
         if (lane == 0) {

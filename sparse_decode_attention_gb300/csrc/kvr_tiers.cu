@@ -457,6 +457,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     }
                 }
             }
+            __syncwarp();
             const unsigned bal = __ballot_sync(kFull, code >= 0);
             if (lane == 0) sCnt[warp] = __popc(bal);
             __syncthreads();
@@ -620,6 +621,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         if (lane < nvs) s0 = sp[lane * 8 + g] * a.scale_log2;
                         if (lane + 32 < nvs) s1 = sp[(lane + 32) * 8 + g] * a.scale_log2;
                         float wm = fmaxf(s0, s1);
+                        __syncwarp();
 #pragma unroll
                         for (int o = 16; o; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(kFull, wm, o));
                         const float m_old = stt[g];
@@ -904,6 +906,7 @@ __global__ void __launch_bounds__(kRankThreads) tier_rank_kernel(RankArgs r)
                 take = w < closed;
             }
         }
+        __syncwarp();
         const unsigned bal = __ballot_sync(kFull, take);
         int base = 0;
         if (lane == 0 && bal) base = atomicAdd(&s_live, __popc(bal));
