@@ -25,8 +25,6 @@ namespace cg = cooperative_groups;
 
 namespace kvr {
 
-constexpr int kAttThreads = 256;
-constexpr int kAttWarps = kAttThreads / 32;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct AttArgs {
@@ -45,11 +43,16 @@ struct AttArgs {
 };
 
 template <int D, typename T, int G> struct AttCfg {
+    // 8 warps: a CTA of this kernel and one of the selection that precedes it
+    // fit on one SM together (registers and shared memory), so the attention
+    // becomes resident while the selection drains (16 warps measured slower)
+    static constexpr int kThreads = 256;
+    static constexpr int kWarps = kThreads / 32;
     static constexpr int kRowBytes = D * (int)sizeof(T);
     static constexpr int kTok = 24576 / kRowBytes;  // tokens per batch (K + V = 48 KB)
     static constexpr int kBatchBytes = 2 * kTok * kRowBytes;
     static constexpr int kE = D / 32;  // dims per lane
-    static constexpr int kWarpPart = kAttWarps * G * (D + 2) * 4;
+    static constexpr int kWarpPart = kWarps * G * (D + 2) * 4;
     static constexpr int kBufBytes =
         (2 * kBatchBytes > kWarpPart) ? 2 * kBatchBytes : kWarpPart;
     static constexpr int kChunk = 8 * kTok;                // token ids loaded at once
@@ -58,7 +61,7 @@ template <int D, typename T, int G> struct AttCfg {
     static constexpr int oPl = oPm + 16 * 4;              // [G]
     static constexpr int oPo = oPl + 16 * 4;              // [G][D]
     static constexpr int bytes = oPo + G * D * 4;
-    static_assert(kTok % kAttWarps == 0, "batch split");
+    static_assert(kTok % kWarps == 0, "batch split");
 };
 
 template <int E, typename T>
@@ -105,9 +108,11 @@ __device__ __forceinline__ float reduce_heads(float (&v)[G], int lane)
 }
 
 template <int D, typename T, int G>
-__global__ void __launch_bounds__(kAttThreads, (G >= 16) ? 1 : 2) attend_kernel(AttArgs a)
+__global__ void __launch_bounds__(AttCfg<D, T, G>::kThreads, (G >= 16) ? 1 : 2) attend_kernel(AttArgs a)
 {
     using CF = AttCfg<D, T, G>;
+    constexpr int kAttThreads = CF::kThreads;
+    constexpr int kAttWarps = CF::kWarps;
     constexpr int E = CF::kE;
     constexpr int RB = CF::kRowBytes;
     constexpr int TOK = CF::kTok;
@@ -358,7 +363,7 @@ static kvr_status launch_attend_g(const LaunchCtx &c, const AttArgs &a, int cs)
     if (st != KVR_OK) return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cs, c.shape.B * c.shape.Hkv, 1);
-    cfg.blockDim = dim3(kAttThreads, 1, 1);
+    cfg.blockDim = dim3(AttCfg<D, T, G>::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = c.stream;
     cudaLaunchAttribute attr[2];
