@@ -20,7 +20,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = [os.path.join(_HERE, "kvr_oracle.c"), os.path.join(_HERE, "kvr_tiers_oracle.c"),
-        os.path.join(_HERE, "kvr_rsq_oracle.c")]
+        os.path.join(_HERE, "kvr_rsq_oracle.c"), os.path.join(_HERE, "kvr_regions_oracle.c")]
 _LIB = os.path.join(_HERE, "libkvr_oracle.so")
 _lib = None
 
@@ -65,8 +65,22 @@ def lib():
                                       ctypes.c_float, _P]
         _tier_signatures(L)
         _rsq_signatures(L)
+        _region_signatures(L)
         _lib = L
     return _lib
+
+
+def _region_signatures(L):
+    L.orc_region_init.argtypes = [_I64, _I64, _I64]
+    L.orc_region_init.restype = _I64
+    L.orc_region_advance.argtypes = [_I64, _I64, _I64, _I64, _I64]
+    L.orc_region_advance.restype = _I64
+    L.orc_select_unit_regions.argtypes = [_P, _I32, _P, _P, _P, _I64, _I32, _P, _I64, _I64, _I64,
+                                          _I64, _P, _P, _P, _P, _P, _P]
+    L.orc_select_unit_regions.restype = _I32
+    L.orc_attend_unit_regions.argtypes = [_P, _I32, _P, _P, _I64, _I32, _I64, _I64, _P, _I64,
+                                          ctypes.c_float, _P]
+    L.orc_attend_unit_regions.restype = _I32
 
 
 def _rsq_signatures(L):
@@ -516,3 +530,62 @@ def select_unit_rsq(q_group, codes_unit, rec_unit, N, sgn, C, k, W, lut, diagnos
     if not diagnostics:
         return idx[:k], int(cnt[0])
     return idx[:k], int(cnt[0]), dict(cand=cand[:nc], cand_S=candS[:nc])
+
+
+# --------------------------------------------------------------------------
+# cache regions: sink, retrieval, local + update buffer (kvr_regions_oracle.c)
+# --------------------------------------------------------------------------
+
+def region_init(N, S, L) -> int:
+    """Retrieval end at set-up: Local holds the L newest tokens, buffer empty."""
+    return int(lib().orc_region_init(int(N), int(S), int(L)))
+
+
+def region_advance(N, R, S, L, U) -> int:
+    """Retrieval end after appends up to length N (buffer of U tokens)."""
+    return int(lib().orc_region_advance(int(N), int(R), int(S), int(L), int(U)))
+
+
+def select_unit_regions(q_group, K_unit, codes_unit, N, S, R, sgn, C, k, lut, rec_unit=None,
+                        diagnostics=False):
+    """Selection of one unit over the retrieval region [S', R'); exact scores,
+    or the reranker's estimates when rec_unit is given."""
+    q = f32(q_group)
+    G, d = q.shape
+    Kf = f32(K_unit) if K_unit is not None else np.zeros((1, d), dtype=np.float32)
+    cd = _c(codes_unit, np.uint8)
+    rc_ = None if rec_unit is None else _c(rec_unit, np.uint8)
+    s = _c(sgn, np.int8)
+    lt = _c(lut, np.int32)
+    lo = min(S, N)
+    hi = min(max(R, lo), N)
+    pool = hi - lo
+    nc = max(0, min(C, pool))
+    idx = np.full(max(k, 1), -1, dtype=np.int32)
+    cnt = np.zeros(1, dtype=np.int32)
+    cand = np.full(max(nc, 1), -1, dtype=np.int32)
+    candS = np.zeros(max(nc, 1), dtype=np.float32)
+    coarse = np.zeros(max(pool, 1), dtype=np.int32)
+    rc = lib().orc_select_unit_regions(_p(q), G, _p(Kf), _p(cd), None if rc_ is None else _p(rc_),
+                                       N, d, _p(s), C, k, S, R, _p(lt), _p(idx), _p(cnt),
+                                       _p(cand), _p(candS), _p(coarse))
+    if rc != 0:
+        raise ValueError("oracle selection failed")
+    if not diagnostics:
+        return idx[:k], int(cnt[0])
+    return idx[:k], int(cnt[0]), dict(cand=cand[:nc], cand_S=candS[:nc], coarse=coarse[:pool])
+
+
+def attend_unit_regions(q_group, K_unit, V_unit, N, S, R, idx, count, scale) -> np.ndarray:
+    """Attention over [0, S') + idx + [R', N) of one unit, fp64."""
+    q = f32(q_group)
+    G, d = q.shape
+    Kf = f32(K_unit)
+    Vf = f32(V_unit)
+    ix = _c(idx, np.int32)
+    out = np.zeros((G, d), dtype=np.float64)
+    rc = lib().orc_attend_unit_regions(_p(q), G, _p(Kf), _p(Vf), N, d, S, R, _p(ix), count,
+                                       float(scale), _p(out))
+    if rc != 0:
+        raise ValueError("selected index outside the retrieval region")
+    return out
