@@ -91,7 +91,8 @@ typedef enum kvr_dtype { KVR_F32 = 0, KVR_BF16 = 1 } kvr_dtype;
 #define KVR_SELECT_STORE_COARSE 0x1 /* also write every pool key's coarse score to the
                                        workspace (diagnostics; costs time) */
 #define KVR_SELECT_EARLY_INPUTS 0x2 /* the caller asserts that codes, K, V_prefetch,
-                                       rsq_records, seq_len and srht_sign were complete before the previous kernel
+                                       rsq_records, region_end, seq_len and srht_sign were
+                                       complete before the previous kernel
                                        on the stream was launched (only q may come from that
                                        kernel): the call then starts reading them while that
                                        kernel still runs (programmatic dependent launch) */
@@ -125,6 +126,13 @@ typedef struct kvr_select_params {
                                when set, the candidates are ranked by the calibrated
                                estimate from the records instead of exact q_bar . k, and
                                K is not read (cand_score then holds the estimates) */
+    int sink;               /* cache regions (ParisKV, "Meccanismo di Aggiornamento a
+                               Finestra Scorrevole"): the first `sink` tokens are the Sink,
+                               always attended, never candidates; 0 = none */
+    const int32_t *region_end; /* optional, or NULL: device int32 [B], the end R_b of the
+                               Retrieval region (kvr_regions_update); [R_b, N) is Local
+                               plus the Update Buffer. NULL: R_b = N - W. The pool is
+                               [S', R') with S' = min(sink, N), R' = min(max(R_b, S'), N) */
 } kvr_select_params;
 
 /* Byte offsets of the inspectable parts of the select workspace after a
@@ -290,6 +298,26 @@ kvr_status kvr_select_static_scratch(const kvr_shape *shape, const kvr_select_pa
                                      int32_t *out_idx, int32_t *out_count, int32_t *err_word,
                                      void *stream);
 
+/*
+ * Cache regions (ParisKV, "Meccanismo di Aggiornamento a Finestra
+ * Scorrevole"): for unbounded generation a unit's tokens are Sink [0, S),
+ * Retrieval [S, R) (searched by kvr_select), and Local followed by the Update
+ * Buffer [R, N) (always attended, like the Sink). New tokens enter the
+ * buffer; when it holds U tokens the U oldest local tokens move to Retrieval.
+ *
+ * kvr_regions_update -- the Retrieval end of every batch entry after appends:
+ *   init != 0: region_end[b] = max(min(S, N), N - L)   (set-up, buffer empty)
+ *   then:      R = max(region_end[b], min(S, N));
+ *              while (N - R >= L + U) R += U;  region_end[b] = R
+ * with N = seq_len[b]. One launch of one small kernel.
+ *   seq_len     device int32 [B]; a negative value sets KVR_DEVERR_SEQ_LEN and
+ *               leaves the entry unchanged.
+ *   region_end  device int32 [B] (read unless init, written).
+ *   sink, local >= 0; buffer >= 1; else KVR_ERR_INVALID_ARG.
+ */
+kvr_status kvr_regions_update(int B, const int32_t *seq_len, int sink, int local, int buffer,
+                              int init, int32_t *region_end, int32_t *err_word, void *stream);
+
 /* Bytes of device workspace kvr_sparse_attend needs (kmax = row length of idx). */
 size_t kvr_attend_workspace_size(const kvr_shape *shape, int kmax, int W);
 
@@ -317,6 +345,20 @@ kvr_status kvr_sparse_attend(const kvr_shape *shape, const void *q, const void *
                              const int32_t *count, const int32_t *seq_len, int W,
                              float scale, float *out, void *workspace, size_t workspace_bytes,
                              int32_t *err_word, void *stream);
+
+/*
+ * kvr_sparse_attend_regions -- kvr_sparse_attend over the cache regions:
+ * T = [0, S') U {idx[b,h,0..count-1]} U [R', N) with S' = min(sink, N) and
+ * R' = min(max(region_end[b], S'), N); idx entries must lie in [S', R')
+ * (others set KVR_DEVERR_INDEX and are skipped). Other arguments as in
+ * kvr_sparse_attend; region_end is required (device int32 [B]).
+ */
+kvr_status kvr_sparse_attend_regions(const kvr_shape *shape, const void *q, const void *K,
+                                     const void *V, const int32_t *idx, int kmax,
+                                     const int32_t *count, const int32_t *seq_len, int sink,
+                                     const int32_t *region_end, float scale, float *out,
+                                     void *workspace, size_t workspace_bytes, int32_t *err_word,
+                                     void *stream);
 
 /* ======================================================================== *
  * Tiered window cache.

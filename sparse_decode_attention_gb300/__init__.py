@@ -27,6 +27,7 @@ __all__ = [
     "kvr_tier_init", "kvr_tiered_attend_workspace_size", "kvr_sparse_attend_tiered",
     "kvr_tier_update_workspace_size", "kvr_tier_update",
     "kvr_rsq_record_bytes", "kvr_rsq_tables", "kvr_encode_rsq", "rsq_buffer",
+    "kvr_sparse_attend_regions", "kvr_regions_update",
 ]
 
 KVR_F32, KVR_BF16 = 0, 1
@@ -51,7 +52,8 @@ class _Shape(ctypes.Structure):
 class _Params(ctypes.Structure):
     _fields_ = [("C", ctypes.c_int), ("k", ctypes.c_int), ("W", ctypes.c_int),
                 ("lut", ctypes.c_int * 9), ("flags", ctypes.c_int),
-                ("V_prefetch", ctypes.c_void_p), ("rsq_records", ctypes.c_void_p)]
+                ("V_prefetch", ctypes.c_void_p), ("rsq_records", ctypes.c_void_p),
+                ("sink", ctypes.c_int), ("region_end", ctypes.c_void_p)]
 
 
 SELECT_STORE_COARSE = 0x1
@@ -96,9 +98,13 @@ class SelectParams:
     """kvr_select_params. ``V_prefetch``: optional V cache tensor of a
     kvr_sparse_attend that follows (an L2 prefetch hint; results unchanged).
     ``rsq_records``: optional uint8 records of the pool keys (kvr_encode_rsq);
-    when given, candidates are ranked by the calibrated estimate."""
+    when given, candidates are ranked by the calibrated estimate.
+    ``sink`` / ``region_end``: cache regions (the first ``sink`` tokens are
+    never candidates; ``region_end`` int32 [B] ends the Retrieval pool,
+    kvr_regions_update)."""
 
-    def __init__(self, C, k, W, lut=DEFAULT_LUT, flags=0, V_prefetch=None, rsq_records=None):
+    def __init__(self, C, k, W, lut=DEFAULT_LUT, flags=0, V_prefetch=None, rsq_records=None,
+                 sink=0, region_end=None):
         self.C, self.k, self.W = int(C), int(k), int(W)
         self.lut = tuple(int(v) for v in lut)
         self.flags = int(flags)
@@ -111,11 +117,17 @@ class SelectParams:
         if rsq_records is not None:
             _cuda(rsq_records, "rsq_records", torch.uint8)
         self.rsq_records = rsq_records
+        if region_end is not None:
+            _cuda(region_end, "region_end", torch.int32)
+        self.sink = int(sink)
+        self.region_end = region_end
 
     def c(self) -> _Params:
         vp = None if self.V_prefetch is None else self.V_prefetch.data_ptr()
         rp = None if self.rsq_records is None else self.rsq_records.data_ptr()
-        return _Params(self.C, self.k, self.W, (ctypes.c_int * 9)(*self.lut), self.flags, vp, rp)
+        re = None if self.region_end is None else self.region_end.data_ptr()
+        return _Params(self.C, self.k, self.W, (ctypes.c_int * 9)(*self.lut), self.flags, vp, rp,
+                       self.sink, re)
 
 
 _lib = None
@@ -164,9 +176,14 @@ def load(build_if_missing: bool = True):
     L.kvr_rsq_record_bytes.restype = ctypes.c_size_t
     L.kvr_rsq_tables.argtypes = [_P, _P]
     L.kvr_encode_rsq.argtypes = [S, _P, _P, ctypes.c_int, _P, _P, _P, _P]
+    L.kvr_sparse_attend_regions.argtypes = [S, _P, _P, _P, _P, ctypes.c_int, _P, _P, ctypes.c_int,
+                                            _P, ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P]
+    L.kvr_regions_update.argtypes = [ctypes.c_int, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, _P, _P, _P]
     for fn in ("kvr_encode_keys", "kvr_select_workspace_views", "kvr_select",
                "kvr_select_static_scratch", "kvr_tier_init", "kvr_sparse_attend_tiered",
                "kvr_tier_update", "kvr_rsq_tables", "kvr_encode_rsq",
+               "kvr_sparse_attend_regions", "kvr_regions_update",
                "kvr_sparse_attend", "kvr_read_error"):
         getattr(L, fn).restype = ctypes.c_int
     _lib = L
@@ -468,3 +485,38 @@ def kvr_encode_rsq(K, pos0, n_new, srht_sign, records, err=None, stream=None):
     st = load().kvr_encode_rsq(ctypes.byref(shape.c()), _ptr(K), _ptr(pos0), int(n_new),
                                _ptr(srht_sign), _ptr(records), _ptr(err), _stream(stream))
     _check(st, "kvr_encode_rsq")
+
+
+def kvr_sparse_attend_regions(q, K, V, idx, count, seq_len, sink, region_end, scale, out,
+                              workspace, err=None, stream=None):
+    """Attention over the Sink, idx[b, h, :count] and [region_end[b], N)."""
+    shape = Shape.of(_kv(K, "K"), _cuda(q, "q", K.dtype))
+    _kv(V, "V")
+    if V.dtype != K.dtype or V.shape != K.shape:
+        raise TypeError("V must have K's dtype and shape")
+    _cuda(idx, "idx", torch.int32)
+    _cuda(count, "count", torch.int32)
+    _cuda(seq_len, "seq_len", torch.int32)
+    _cuda(region_end, "region_end", torch.int32)
+    _cuda(out, "out", torch.float32)
+    _cuda(workspace, "workspace")
+    st = load().kvr_sparse_attend_regions(ctypes.byref(shape.c()), _ptr(q), _ptr(K), _ptr(V),
+                                          _ptr(idx), int(idx.shape[-1]), _ptr(count),
+                                          _ptr(seq_len), int(sink), _ptr(region_end),
+                                          float(scale), _ptr(out), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), _ptr(err),
+                                          _stream(stream))
+    _check(st, "kvr_sparse_attend_regions")
+
+
+def kvr_regions_update(seq_len, sink, local, buffer, region_end, init=False, err=None,
+                       stream=None):
+    """Retrieval end of every batch entry after appends (or at set-up)."""
+    _cuda(seq_len, "seq_len", torch.int32)
+    _cuda(region_end, "region_end", torch.int32)
+    if region_end.numel() < seq_len.numel():
+        raise ValueError("region_end needs one entry per batch entry")
+    st = load().kvr_regions_update(int(seq_len.numel()), _ptr(seq_len), int(sink), int(local),
+                                   int(buffer), 1 if init else 0, _ptr(region_end), _ptr(err),
+                                   _stream(stream))
+    _check(st, "kvr_regions_update")

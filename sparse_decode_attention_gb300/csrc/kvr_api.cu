@@ -39,6 +39,8 @@ kvr_status check_params(const kvr_select_params *p)
         if (p->lut[i] < 0 || p->lut[i] > 15) return KVR_ERR_INVALID_ARG;
     if (p->flags & ~(KVR_SELECT_STORE_COARSE | KVR_SELECT_EARLY_INPUTS)) return KVR_ERR_INVALID_ARG;
     if (!aligned16(p->V_prefetch) || !aligned16(p->rsq_records)) return KVR_ERR_INVALID_ARG;
+    if (p->sink < 0 || (reinterpret_cast<uintptr_t>(p->region_end) & 3u) != 0)
+        return KVR_ERR_INVALID_ARG;
     return KVR_OK;
 }
 
@@ -269,8 +271,44 @@ kvr_status kvr_sparse_attend(const kvr_shape *shape, const void *q, const void *
     const AttendPlan pl = plan_attend(*shape, kmax, W);
     if (workspace_bytes < pl.bytes) return KVR_ERR_WORKSPACE;
     LaunchCtx c{*shape, static_cast<cudaStream_t>(stream)};
-    return attend_dispatch(c, pl, q, K, V, idx, kmax, count, seq_len, W, scale, out,
+    return attend_dispatch(c, pl, q, K, V, idx, kmax, count, seq_len, W, 0, nullptr, scale, out,
                            static_cast<uint8_t *>(workspace), err_word);
+}
+
+kvr_status kvr_sparse_attend_regions(const kvr_shape *shape, const void *q, const void *K,
+                                     const void *V, const int32_t *idx, int kmax,
+                                     const int32_t *count, const int32_t *seq_len, int sink,
+                                     const int32_t *region_end, float scale, float *out,
+                                     void *workspace, size_t workspace_bytes, int32_t *err_word,
+                                     void *stream)
+{
+    kvr_status st = check_shape(shape);
+    if (st != KVR_OK) return st;
+    if (kmax < 0 || sink < 0) return KVR_ERR_INVALID_ARG;
+    if (!q || !K || !V || !count || !seq_len || !out || !region_end) return KVR_ERR_INVALID_ARG;
+    if (kmax > 0 && !idx) return KVR_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(region_end) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return KVR_ERR_INVALID_ARG;
+    if (!(scale == scale)) return KVR_ERR_INVALID_ARG;
+    const AttendPlan pl = plan_attend(*shape, kmax, 0);
+    if (workspace_bytes < pl.bytes) return KVR_ERR_WORKSPACE;
+    LaunchCtx c{*shape, static_cast<cudaStream_t>(stream)};
+    return attend_dispatch(c, pl, q, K, V, idx, kmax, count, seq_len, 0, sink, region_end, scale,
+                           out, static_cast<uint8_t *>(workspace), err_word);
+}
+
+kvr_status kvr_regions_update(int B, const int32_t *seq_len, int sink, int local, int buffer,
+                              int init, int32_t *region_end, int32_t *err_word, void *stream)
+{
+    if (B < 0 || sink < 0 || local < 0 || buffer < 1) return KVR_ERR_INVALID_ARG;
+    if (B == 0) return KVR_OK;
+    if (!seq_len || !region_end) return KVR_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(seq_len) & 3u) || (reinterpret_cast<uintptr_t>(region_end) & 3u))
+        return KVR_ERR_INVALID_ARG;
+    return regions_dispatch(static_cast<cudaStream_t>(stream), B, seq_len, sink, local, buffer,
+                            init, region_end, err_word);
 }
 
 size_t kvr_ledger_bytes(int d)

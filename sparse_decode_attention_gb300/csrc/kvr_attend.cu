@@ -31,6 +31,8 @@ struct AttArgs {
     int Hq, Hkv;
     int64_t cap;
     int W, kmax;
+    int sink;                   // Sink tokens [0, sink), always attended
+    const int32_t *region_end;  // Retrieval end per batch entry, or null: N - W
     float scale_log2;  // scale * log2(e)
     const void *q;
     const void *K;
@@ -141,9 +143,12 @@ __global__ void __launch_bounds__(AttCfg<D, T, G>::kThreads, (G >= 16) ? 1 : 2) 
         if (rank == 0 && tid == 0 && hk == 0) set_err(a.err, KVR_DEVERR_SEQ_LEN);
         N = 0;
     }
-    const int64_t w0 = N > a.W ? N - a.W : 0;
+    // T = selected tokens, then [w0, N) (Local and buffer), then the Sink [0, p0)
+    const int64_t p0 = min((int64_t)max(a.sink, 0), N);
+    int64_t w0 = a.region_end ? (int64_t)a.region_end[b] : N - a.W;
+    w0 = w0 < p0 ? p0 : (w0 > N ? N : w0);
     const int cnt = max(0, min(a.count[u], a.kmax));
-    const int64_t nT = cnt + (N - w0);
+    const int64_t nT = cnt + (N - w0) + p0;
     const int64_t lo = (int64_t)rank * nT / CS, hi = (int64_t)(rank + 1) * nT / CS;
     const int n = (int)(hi - lo);
     const int nbatch = (n + TOK - 1) / TOK;
@@ -160,12 +165,14 @@ __global__ void __launch_bounds__(AttCfg<D, T, G>::kThreads, (G >= 16) ? 1 : 2) 
             int32_t t;
             if (p < cnt) {
                 t = a.idx[(size_t)u * a.kmax + p];
-                if (t < 0 || t >= w0) {
+                if (t < p0 || t >= w0) {
                     set_err(a.err, KVR_DEVERR_INDEX);
                     t = -1;
                 }
-            } else {
+            } else if (p < cnt + (N - w0)) {
                 t = (int32_t)(w0 + (p - cnt));
+            } else {
+                t = (int32_t)(p - cnt - (N - w0));
             }
             sTok[j] = t;
         }
@@ -394,8 +401,9 @@ static kvr_status launch_attend(const LaunchCtx &c, const AttArgs &a, int cs, in
 
 kvr_status attend_dispatch(const LaunchCtx &c, const AttendPlan &plan, const void *q,
                            const void *K, const void *V, const int32_t *idx, int kmax,
-                           const int32_t *count, const int32_t *seq_len, int W, float scale,
-                           float *out, uint8_t *ws, int32_t *err)
+                           const int32_t *count, const int32_t *seq_len, int W, int sink,
+                           const int32_t *region_end, float scale, float *out, uint8_t *ws,
+                           int32_t *err)
 {
     (void)plan;
     (void)ws;
@@ -405,6 +413,8 @@ kvr_status attend_dispatch(const LaunchCtx &c, const AttendPlan &plan, const voi
     a.cap = c.shape.cap;
     a.W = W;
     a.kmax = kmax;
+    a.sink = sink;
+    a.region_end = region_end;
     a.scale_log2 = scale * kLog2e;
     a.q = q;
     a.K = K;
@@ -415,7 +425,10 @@ kvr_status attend_dispatch(const LaunchCtx &c, const AttendPlan &plan, const voi
     a.out = out;
     a.err = err;
     const int G = c.shape.Hq / c.shape.Hkv;
-    const int cs = attend_cluster_size(c.shape.B * c.shape.Hkv, (int64_t)kmax + W);
+    // tokens per unit for the cluster size (load balance only): with regions
+    // the Local + buffer length lives on the device, 256 stands in for it
+    const int64_t most = (int64_t)kmax + (region_end ? (int64_t)sink + 256 : (int64_t)W);
+    const int cs = attend_cluster_size(c.shape.B * c.shape.Hkv, most);
     const bool bf = c.shape.dtype == KVR_BF16;
     if (c.shape.d == 128)
         return bf ? launch_attend<128, __nv_bfloat16>(c, a, cs, G)

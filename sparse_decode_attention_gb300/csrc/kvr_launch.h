@@ -58,8 +58,13 @@ kvr_status select_dispatch(const LaunchCtx &c, const kvr_select_params &p, const
 
 kvr_status attend_dispatch(const LaunchCtx &c, const AttendPlan &plan, const void *q,
                            const void *K, const void *V, const int32_t *idx, int kmax,
-                           const int32_t *count, const int32_t *seq_len, int W, float scale,
-                           float *out, uint8_t *ws, int32_t *err);
+                           const int32_t *count, const int32_t *seq_len, int W, int sink,
+                           const int32_t *region_end, float scale, float *out, uint8_t *ws,
+                           int32_t *err);
+
+// Cache regions (kvr_regions.cu).
+kvr_status regions_dispatch(cudaStream_t stream, int B, const int32_t *seq_len, int sink,
+                            int local, int buffer, int init, int32_t *region_end, int32_t *err);
 
 // Calibrated inner-product reranker (kvr_rsq.cu): fp32 tables of the
 // 3-bit magnitude quantiser (bsq[i] = squared bin edge, bsq[0] = 0; lev[i] =

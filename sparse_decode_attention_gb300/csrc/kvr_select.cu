@@ -58,6 +58,8 @@ struct SelArgs {
     const void *V;  // optional: prefetch the winners' V rows and the window's rows
     bool early;     // KVR_SELECT_EARLY_INPUTS
     const uint8_t *rsq;  // reranker records, or null: exact rescoring
+    int sink;                   // Sink tokens [0, sink)
+    const int32_t *region_end;  // Retrieval end per batch entry, or null: N - W
     float lev[8];        // reranker magnitude levels
     const uint8_t *codes;
     const int32_t *seq_len;
@@ -155,13 +157,16 @@ __device__ __forceinline__ void compare_planes(const uint32_t (&p)[A], int T, ui
     }
 }
 
-// Keys of a 32-token block that lie in the pool [0, pool).
-__device__ __forceinline__ uint32_t pool_mask(int64_t blk, int64_t pool)
+// Keys of a 32-token block that lie in the pool [p0, pool).
+__device__ __forceinline__ uint32_t pool_mask(int64_t blk, int64_t p0, int64_t pool)
 {
     const int64_t lo = blk * 32;
-    if (lo + 32 <= pool) return 0xffffffffu;
-    if (lo >= pool) return 0u;
-    return (1u << (uint32_t)(pool - lo)) - 1u;
+    uint32_t m;
+    if (lo + 32 <= pool) m = 0xffffffffu;
+    else if (lo >= pool) m = 0u;
+    else m = (1u << (uint32_t)(pool - lo)) - 1u;
+    if (p0 > lo) m = (p0 >= lo + 32) ? 0u : m & (0xffffffffu << (uint32_t)(p0 - lo));
+    return m;
 }
 
 template <int D, typename T> struct SelSmem {
@@ -253,8 +258,12 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         if (rank == 0 && tid == 0 && h == 0) set_err(a.err, KVR_DEVERR_SEQ_LEN);
         N = 0;
     }
-    const int64_t pool = N > a.W ? N - a.W : 0;
-    const int Cp = (int)min((int64_t)a.C, pool);
+    // pool = the Retrieval region [p0, pool): after the Sink, before Local
+    const int64_t p0 = min((int64_t)max(a.sink, 0), N);
+    int64_t pend = a.region_end ? (int64_t)a.region_end[b] : N - a.W;
+    pend = pend < p0 ? p0 : (pend > N ? N : pend);
+    const int64_t pool = pend;
+    const int Cp = (int)min((int64_t)a.C, pool - p0);
     const int kp = min(a.k, Cp);
     const int64_t nhalf = (pool + 511) / 512;
     const int64_t h0 = (int64_t)rank * nhalf / CS, h1 = (int64_t)(rank + 1) * nhalf / CS;
@@ -266,6 +275,10 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         const uint8_t *Kb = static_cast<const uint8_t *>(a.K) + (size_t)u * a.cap * RB;
         const uint8_t *Vb = static_cast<const uint8_t *>(a.V) + (size_t)u * a.cap * RB;
         for (int64_t t = pool + rank + (int64_t)CS * tid; t < N; t += (int64_t)CS * kSelThreads) {
+            prefetch_l2(Kb + (size_t)t * RB, RB);
+            prefetch_l2(Vb + (size_t)t * RB, RB);
+        }
+        for (int64_t t = rank + (int64_t)CS * tid; t < p0; t += (int64_t)CS * kSelThreads) {  // the Sink
             prefetch_l2(Kb + (size_t)t * RB, RB);
             prefetch_l2(Vb + (size_t)t * RB, RB);
         }
@@ -403,7 +416,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         const int64_t blk = hh * 16 + jb;
         if (hh + kSelWarps < h1) issue_half(hh + kSelWarps);
         if (sh == 0 && blk < nb_pool) {
-            const uint32_t vm = pool_mask(blk, pool);
+            const uint32_t vm = pool_mask(blk, p0, pool);
 #pragma unroll
             for (int j = 0; j < ACC; j++) plane(j, blk) = acc[j];
 #pragma unroll
@@ -456,7 +469,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
             uint32_t p[ACC];
 #pragma unroll
             for (int j = 0; j < ACC; j++) p[j] = plane(j, blk);
-            uint32_t inb = pool_mask(blk, pool);
+            uint32_t inb = pool_mask(blk, p0, pool);
 #pragma unroll
             for (int j = 0; j < H1; j++) inb &= ((u1 >> j) & 1) ? p[LOWB + j] : ~p[LOWB + j];
 #pragma unroll
@@ -527,7 +540,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
 #pragma unroll
                 for (int j = 0; j < ACC; j++) p[j] = plane(j, blk);
                 compare_planes<ACC>(p, Tthr, gt, eq);
-                const uint32_t vm = pool_mask(blk, pool);
+                const uint32_t vm = pool_mask(blk, p0, pool);
                 n_eq += __popc(eq & vm);
                 n_gt += __popc(gt & vm);
             }
@@ -540,7 +553,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
             uint32_t p[ACC], gt = 0, eq = 0;
 #pragma unroll
             for (int j = 0; j < ACC; j++) p[j] = plane(j, blk);
-            const uint32_t vm = pool_mask(blk, pool);
+            const uint32_t vm = pool_mask(blk, p0, pool);
             if (u1 >= 0) {
                 compare_planes<ACC>(p, Tthr, gt, eq);
                 gt &= vm;
@@ -1142,6 +1155,8 @@ kvr_status select_dispatch(const LaunchCtx &c, const kvr_select_params &p, const
     a.V = p.V_prefetch;
     a.early = (p.flags & KVR_SELECT_EARLY_INPUTS) != 0;
     a.rsq = p.rsq_records;
+    a.sink = p.sink;
+    a.region_end = p.region_end;
     for (int i = 0; i < 8; i++) a.lev[i] = rsq_tables().lev[i];
     a.codes = codes;
     a.seq_len = seq_len;

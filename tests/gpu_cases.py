@@ -47,7 +47,8 @@ def select_gpu(q, K, codes, seq_len, sgn, params):
     B, Hkv, cap, d = K.shape
     params = kvr.SelectParams(params.C, params.k, params.W, params.lut,
                               params.flags | kvr.SELECT_STORE_COARSE,
-                              V_prefetch=params.V_prefetch, rsq_records=params.rsq_records)
+                              V_prefetch=params.V_prefetch, rsq_records=params.rsq_records,
+                              sink=params.sink, region_end=params.region_end)
     shape = kvr.Shape.of(K, q)
     ws = kvr.workspace(kvr.kvr_select_workspace_size(shape, params))
     ws.fill_(0xAB)  # stale contents must not matter

@@ -196,3 +196,37 @@ def test_pageable_host_caches_are_refused(kvr_lib):
                  lambda: kvr.kvr_sparse_attend(None, K, K, None, None, None, 8, 0.1, None, None)):
         with pytest.raises(TypeError, match="page-locked"):
             call()
+
+
+def test_region_calls_validate_before_launch(kvr_lib):
+    """kvr_regions_update, kvr_sparse_attend_regions and the region fields of
+    kvr_select_params are checked on the host (no GPU)."""
+    kvr = kvr_lib
+    L = kvr.load()
+    fake = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 2)
+    upd = lambda B, S, Lc, U, re=fake, sl=fake: L.kvr_regions_update(B, sl, S, Lc, U, 0, re, None,
+                                                                      None)
+    assert upd(0, 4, 128, 64) == 0                 # nothing to do
+    assert upd(2, -1, 128, 64) == 1
+    assert upd(2, 4, -1, 64) == 1
+    assert upd(2, 4, 128, 0) == 1                  # the buffer holds at least one token
+    assert upd(2, 4, 128, 64, re=None) == 1
+    assert upd(2, 4, 128, 64, re=odd) == 1
+    s = _shape(kvr)
+    att = lambda sink, re: L.kvr_sparse_attend_regions(ctypes.byref(s.c()), fake, fake, fake,
+                                                       fake, 16, fake, fake, sink, re, 0.1, fake,
+                                                       fake, 0, None, None)
+    assert att(4, None) == 1                       # region_end required
+    assert att(-1, fake) == 1
+    assert att(4, odd) == 1
+    p = kvr.SelectParams(64, 16, 8)
+    need = kvr.kvr_select_workspace_size(s, p)
+    pv = p.c()
+    pv.sink = -3
+    assert L.kvr_select(ctypes.byref(s.c()), ctypes.byref(pv), fake, fake, fake, fake, fake,
+                        fake, fake, fake, need, None, None) == 1
+    pv = p.c()
+    pv.region_end = (1 << 20) + 2                  # int32 array misaligned
+    assert L.kvr_select(ctypes.byref(s.c()), ctypes.byref(pv), fake, fake, fake, fake, fake,
+                        fake, fake, fake, need, None, None) == 1
