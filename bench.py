@@ -751,7 +751,15 @@ def run_gpu_drift(args, w):
     del k_new
     sgn = wl.srht_signs(w.d, device=dev)
     shape = kvr.Shape.of(K, qb)
-    params = kvr.SelectParams(w.C, w.k, w.W, w.lut, V_prefetch=V)
+    regions = None
+    if args.regions:
+        # Sink / Local / Update buffer sizes in tokens (cache regions)
+        regions = tuple(int(x) for x in args.regions.split(","))
+        S_r, L_r, U_r = regions
+        rend = torch.zeros(w.B, dtype=torch.int32, device=dev)
+        params = kvr.SelectParams(w.C, w.k, 0, w.lut, V_prefetch=V, sink=S_r, region_end=rend)
+    else:
+        params = kvr.SelectParams(w.C, w.k, w.W, w.lut, V_prefetch=V)
     ws_s = kvr.workspace(kvr.kvr_select_workspace_size(shape, params), dev)
     ws_a = kvr.workspace(kvr.kvr_attend_workspace_size(shape, w.k, w.W), dev)
     codes = kvr.codes_buffer(shape, dev)
@@ -769,6 +777,9 @@ def run_gpu_drift(args, w):
 
     def reset():
         pos.fill_(N0)
+        if regions:
+            seq.fill_(N0)
+            kvr.kvr_regions_update(seq, S_r, L_r, U_r, rend, init=True, err=err)
         seq.fill_(N0 + 1)
         tt.zero_()
 
@@ -777,12 +788,17 @@ def run_gpu_drift(args, w):
         if ev:
             ev[0].record()
         kvr.kvr_encode_keys(K, pos, 1, sgn, codes, err)
+        if regions:
+            kvr.kvr_regions_update(seq, S_r, L_r, U_r, rend, err=err)
         if ev:
             ev[1].record()
         kvr.kvr_select(q, K, codes, seq, sgn, params, idx, cnt, ws_s, err)
         if ev:
             ev[2].record()
-        kvr.kvr_sparse_attend(q, K, V, idx, cnt, seq, w.W, scale, out, ws_a, err)
+        if regions:
+            kvr.kvr_sparse_attend_regions(q, K, V, idx, cnt, seq, S_r, rend, scale, out, ws_a, err)
+        else:
+            kvr.kvr_sparse_attend(q, K, V, idx, cnt, seq, w.W, scale, out, ws_a, err)
         if ev:
             ev[3].record()
         pos.add_(1)
@@ -797,11 +813,13 @@ def run_gpu_drift(args, w):
     for t in range(T):
         step()
         N = N0 + t + 1
-        pool = N - w.W
-        kk = min(w.k, min(w.C, pool))
+        p0, pool = 0, N - w.W
+        if regions:
+            p0, pool = min(S_r, N), int(rend[0])
+        kk = min(w.k, min(w.C, pool - p0))
         qbar = qs[t].double().view(w.B, w.Hkv, G, w.d).mean(2)
-        S = torch.einsum("bhnd,bhd->bhn", K64[:, :, :pool], qbar)
-        top = torch.topk(S, kk, dim=-1).indices
+        S = torch.einsum("bhnd,bhd->bhn", K64[:, :, p0:pool], qbar)
+        top = torch.topk(S, kk, dim=-1).indices + p0
         got = idx[:, :, :kk].long()
         hit = (torch.sort(got, -1).values.unsqueeze(-1) ==
                torch.sort(top, -1).values.unsqueeze(-2)).any(-1).sum(-1)
@@ -853,12 +871,15 @@ def run_gpu_drift(args, w):
     r = recall
     line = {
         "metric": "batched drift decode steps/s (B8, 32768 prefill + %d appending steps) and "
-                  "exact-top-k recall per step" % T,
+                  "exact-top-k recall per step" % T
+                  + (", sink / local / update-buffer regions" if regions else ""),
         "value": T * world / (ms / 1000.0), "unit": "steps/s", "n_gpus": world, "steps": T,
         "warmup": args.warmup, "ms_per_step": ms / T, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.d,
                    "prefill": N0, "appending_steps": T, "C": w.C, "k": w.k, "W": w.W,
+                   "regions": None if not regions else
+                   {"sink": regions[0], "local": regions[1], "buffer": regions[2]},
                    "l2": "inputs larger than L2: each step reads %.0f MB"
                          % ((ab["select"] + ab["attend"]) / 1e6)},
         "recall": {"mean": sum(r) / len(r), "min": min(r), "first_step": r[0],
@@ -870,7 +891,7 @@ def run_gpu_drift(args, w):
                      "peak_kind": peak_kind, "traffic": None,
                      "algorithmic_bytes": ab["select"], "avg_ms": sel_ms},
         "attend_us": att_ms * 1e3, "cpu_baseline": None, "e2e": None,
-        "gpu_launches": 3 * T, "clocks": clk,
+        "gpu_launches": (4 if regions else 3) * T, "clocks": clk,
     }
     print(json.dumps(line), flush=True)
 
@@ -891,6 +912,10 @@ def main():
                                            "batched_drift", "million_offload"],
                     default="llama3_8b_128k",
                     help="the timed workload (the 128K decode layer is the headline)")
+    ap.add_argument("--regions", default=None, metavar="S,L,U",
+                    help="batched_drift only: sink, local and update-buffer sizes (tokens); "
+                         "selection over the retrieval region, attention over sink + top-k + "
+                         "local and buffer")
     ap.add_argument("--rerank", choices=["exact", "rsq"], default=None,
                     help="candidate ranking: exact q_bar.k from the K rows (default for "
                          "device caches), or the calibrated estimate from per-key records "
