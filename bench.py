@@ -724,7 +724,62 @@ def run_gpu_tiered(args, w):
                             "evictions": st_tot[2]},
         "cpu_baseline": None, "e2e": e2e, "gpu_launches": 4 * args.steps, "clocks": clk,
     }
+    if args.diagnostics:
+        del K, V, st
+        torch.cuda.empty_cache()
+        line["cache_dynamics"] = tiered_dynamics(w, args.diagnostics, dev)
     print(json.dumps(line), flush=True)
+
+
+def tiered_dynamics(w, steps, dev):
+    """Untimed: Future Missed Mass, Global LIR and selection churn of the
+    routing policy over `steps` appending steps with fresh queries. The
+    full-attention window masses come from the tiered attention over an
+    all-bf16 state and an unmodified copy of the cache."""
+    import numpy as np
+    import torch
+    import sparse_decode_attention_gb300 as kvr
+    import workloads as wl
+    from sparse_decode_attention_gb300 import diagnostics as dg
+
+    cap = w.N + steps + 8
+    n_win = -(-cap // 64)
+    U = w.B * w.Hkv
+    K, V, qb = wl.make_cache(w, device=dev, cap=cap)
+    K0, V0 = K.clone(), V.clone()
+    closed = w.N // 64
+    plan = np.zeros((U, n_win), dtype=np.int8)
+    for u in range(U):
+        plan[u, :closed] = wl.random_tier_plan(closed, seed=w.seed + u).numpy()
+    seq = torch.full((w.B,), w.N, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = kvr.TierState(U, n_win, w.d, dev)
+    kvr.kvr_tier_init(st, torch.from_numpy(plan).to(dev), K, V, seq, w.Hq, err)
+    dense = dg.full_mass_state(U, n_win, w.d, K0, V0, seq, w.Hq, err)
+    shape = kvr.Shape.of(K, qb)
+    ws_a = kvr.workspace(kvr.kvr_tiered_attend_workspace_size(shape, n_win), dev)
+    ws_u = kvr.workspace(kvr.kvr_tier_update_workspace_size(shape, n_win), dev)
+    mass = torch.zeros((U, n_win), dtype=torch.float32, device=dev)
+    full = torch.zeros((U, n_win), dtype=torch.float32, device=dev)
+    out = torch.empty((w.B, w.Hq, w.d), dtype=torch.float32, device=dev)
+    stats = torch.zeros((U, 3), dtype=torch.int32, device=dev)
+    scale = 1.0 / math.sqrt(w.d)
+    dyn = dg.CacheDynamics()
+    for t in range(steps):
+        seq.add_(1)
+        q = wl.step_query(w, qb, 1000 + t).contiguous()
+        kvr.kvr_sparse_attend_tiered(dense, q, K0, V0, seq, scale, out, full, ws_a, err)
+        before = st.tier.clone()
+        kvr.kvr_sparse_attend_tiered(st, q, K, V, seq, scale, out, mass, ws_a, err)
+        kvr.kvr_tier_update(st, mass, seq, K, V, w.Hq, stats, ws_u, err)
+        dyn.record(full, before, st.tier, w.N + t + 1)
+    if kvr.kvr_read_error(err):
+        raise RuntimeError("device error bits during the diagnostics pass")
+    res = dyn.summary()
+    res["definitions"] = ("FMM: full-attention mass on evicted windows / total, per step and "
+                          "unit; LIR: active-set leaves later reactivated / leaves; churn: "
+                          "|A_t xor A_t-1| / |A_t-1|; active = bf16 closed windows")
+    return res
 
 
 # --------------------------------------------------------------------------
@@ -912,6 +967,9 @@ def main():
                                            "batched_drift", "million_offload"],
                     default="llama3_8b_128k",
                     help="the timed workload (the 128K decode layer is the headline)")
+    ap.add_argument("--diagnostics", type=int, default=0, metavar="STEPS",
+                    help="tiered_window_cache only: also run STEPS untimed appending steps and "
+                         "report Future Missed Mass, Global LIR and selection churn")
     ap.add_argument("--regions", default=None, metavar="S,L,U",
                     help="batched_drift only: sink, local and update-buffer sizes (tokens); "
                          "selection over the retrieval region, attention over sink + top-k + "
