@@ -183,10 +183,11 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *scratch, int *to
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
     int x = v;
+    __syncwarp();
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         int y = __shfl_up_sync(kFull, x, off);
-        if (lane >= off) x += y;
+        x += (lane >= off) ? y : 0;
     }
     if (lane == 31) scratch[warp] = x;
     __syncthreads();
@@ -196,7 +197,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *scratch, int *to
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             int y = __shfl_up_sync(kFull, s, off);
-            if (lane >= off) s += y;
+            s += (lane >= off) ? y : 0;
         }
         scratch[lane] = s - w;  // exclusive warp offsets
         if (lane == 31) scratch[32] = s;
@@ -206,6 +207,47 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *scratch, int *to
     *total = scratch[32];
     __syncthreads();
     return res;
+}
+
+// Two block-wide exclusive prefix sums in one pass (one value pair per
+// thread): *ba / *bb get the sums of a / b over the lower threads. scratch
+// holds 66 ints. Contains __syncthreads: call from uniform control flow.
+__device__ __forceinline__ void block_exclusive_scan2(int a, int b, int *scratch, int *ba, int *bb)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    int x = a, y = b;
+    __syncwarp();
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int xa = __shfl_up_sync(kFull, x, off);
+        const int yb = __shfl_up_sync(kFull, y, off);
+        x += (lane >= off) ? xa : 0;
+        y += (lane >= off) ? yb : 0;
+    }
+    if (lane == 31) {
+        scratch[warp] = x;
+        scratch[33 + warp] = y;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int wa = (lane < nwarps) ? scratch[lane] : 0;
+        const int wb = (lane < nwarps) ? scratch[33 + lane] : 0;
+        int sa = wa, sb = wb;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int ta = __shfl_up_sync(kFull, sa, off);
+            const int tb = __shfl_up_sync(kFull, sb, off);
+            sa += (lane >= off) ? ta : 0;
+            sb += (lane >= off) ? tb : 0;
+        }
+        scratch[lane] = sa - wa;
+        scratch[33 + lane] = sb - wb;
+    }
+    __syncthreads();
+    *ba = scratch[warp] + x - a;
+    *bb = scratch[33 + warp] + y - b;
+    __syncthreads();
 }
 
 __device__ __forceinline__ void set_err(int32_t *err, int bit)

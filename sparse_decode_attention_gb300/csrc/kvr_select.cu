@@ -187,7 +187,7 @@ template <int D, typename T> struct SelSmem {
     static constexpr int oRad = oH2 + 16 * 4;    // [2][256]
     static constexpr int oAll = oRad + 512 * 4;  // [16][16] level 1, [16][16] level 2
     static constexpr int oScan = oAll + 512 * 4;
-    static constexpr int oMisc = oScan + 40 * 4;
+    static constexpr int oMisc = oScan + 72 * 4;
     static constexpr int oWH = oMisc + 64 * 4;  // [kSelWarps][256] per-warp histograms
     static constexpr int oPl = oWH + kSelWarps * 256 * 4;  // [8][kPlaneCap] score planes
     static constexpr int oLev = oPl + 8 * kPlaneCap * 4;  // float [16] signed reranker levels
@@ -556,11 +556,13 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
                 n_eq += __popc(eq & vm);
                 n_gt += __popc(gt & vm);
             }
-        int tot;
-        const int eq_before = block_exclusive_scan(n_eq, sScan, &tot);
-        // this thread's ties that are taken: the first `allow` of them in order
-        int allow = max(0, min(sMisc[M_TAKE] - eq_before, n_eq));
-        int pos = block_exclusive_scan(n_gt + allow, sScan, &tot) + sMisc[M_OFF];
+        // one scan of both counts: the ties taken before this thread are the
+        // first `take` ties in order, min(take, eq_before) of them
+        int eq_before, gt_before;
+        block_exclusive_scan2(n_eq, n_gt, sScan, &eq_before, &gt_before);
+        const int take = sMisc[M_TAKE];
+        int allow = max(0, min(take - eq_before, n_eq));
+        int pos = gt_before + min(take, eq_before) + sMisc[M_OFF];
         for (int64_t blk = my0; blk < my1; blk++) {
             uint32_t p[ACC], gt = 0, eq = 0;
 #pragma unroll
@@ -1053,24 +1055,21 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     if (kp > 0) {
         const int spt = (n + kSelThreads - 1) / kSelThreads;
         const int j0 = min(tid * spt, n), j1 = min(j0 + spt, n);
-        int n_eq = 0;
-        for (int j = j0; j < j1; j++) n_eq += order_key(sS[j]) == keyT;
-        int tot;
-        const int eq_before = block_exclusive_scan(n_eq, sScan, &tot);
-        const int allow0 = max(0, min(sMisc[M_KTAKE] - eq_before, n_eq));
-        int n_sel = 0, allow = allow0;
+        int n_eq = 0, n_gt = 0;
         for (int j = j0; j < j1; j++) {
             const uint32_t key = order_key(sS[j]);
-            if (key > keyT) {
-                n_sel++;
-            } else if (key == keyT && allow > 0) {
-                n_sel++;
-                allow--;
-            }
+            n_eq += key == keyT;
+            n_gt += key > keyT;
         }
-        int pos = block_exclusive_scan(n_sel, sScan, &tot) + sMisc[M_KOFF];
+        // one scan of both counts: the ties taken before this thread are the
+        // first `ktake` ties in order, min(ktake, eq_before) of them
+        int eq_before, gt_before;
+        block_exclusive_scan2(n_eq, n_gt, sScan, &eq_before, &gt_before);
+        const int ktake = sMisc[M_KTAKE];
+        const int allow0 = max(0, min(ktake - eq_before, n_eq));
+        int pos = gt_before + min(ktake, eq_before) + sMisc[M_KOFF];
         int32_t *orow = a.out_idx + (size_t)u * a.k;
-        allow = allow0;
+        int allow = allow0;
         for (int j = j0; j < j1; j++) {
             const uint32_t key = order_key(sS[j]);
             bool take = key > keyT;
