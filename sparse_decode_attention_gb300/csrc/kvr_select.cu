@@ -611,6 +611,11 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     // ---------------------------------------------------------------- P4
     const int lo = (int)((int64_t)rank * Cp / CS), hi = (int)((int64_t)(rank + 1) * Cp / CS);
     const int n = hi - lo;  // <= kMaxSlice (the host picks CS so); sI filled in P3
+    if (tid == 0) {  // P5 accumulators, ordered by the barrier below
+        sMisc[M_KMIN] = (int)0xffffffffu;
+        sMisc[M_KMAX] = 0;
+        sMisc[M_AOWN] = 0;
+    }
     if (a.rsq) {
         // Calibrated estimate from the records, no K rows: lane gl of a
         // half-warp is block slot gl (slots past d/8 add +0), zq of its block
@@ -826,19 +831,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         __syncwarp();
         lmin = __reduce_min_sync(kFull, lmin);
         lmax = __reduce_max_sync(kFull, lmax);
-        if (lane == 0) {
-            sScan[warp] = (int)lmin;
-            sScan[16 + warp] = (int)lmax;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            uint32_t a0 = 0xffffffffu, a1 = 0u;
-            for (int w = 0; w < kSelWarps; w++) {
-                a0 = min(a0, (uint32_t)sScan[w]);
-                a1 = max(a1, (uint32_t)sScan[16 + w]);
-            }
-            sMisc[M_KMIN] = (int)a0;
-            sMisc[M_KMAX] = (int)a1;
+        if (lane == 0) {  // slots set before P4
+            atomicMin(reinterpret_cast<unsigned *>(&sMisc[M_KMIN]), lmin);
+            atomicMax(reinterpret_cast<unsigned *>(&sMisc[M_KMAX]), lmax);
         }
     }
     __syncthreads();
@@ -894,9 +889,10 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
             if (bn > b_lin) a_own++;
             else if (bn == b_lin) sPub[atomicAdd(&sMisc[M_CNT], 1)] = k;
         }
-    int a_tot;
-    block_exclusive_scan(a_own, sScan, &a_tot);
-    if (tid == 0) sMisc[M_AOWN] = a_tot;
+    {
+        const int s = warp_sum(a_own);
+        if (lane == 0 && s) atomicAdd(&sMisc[M_AOWN], s);  // slot cleared before P4
+    }
     __syncthreads();
     cluster.sync();  // #6: above counts and boundary keys published
 
