@@ -534,7 +534,9 @@ def rerank_recall(w, L, kvr, torch, sgn, ws_s, seq):
 def run_e2e(args, w, layers, kvr, torch, sgn, params, ws_s, ws_a, idx, cnt, seq, pos_new, err,
             scale, world):
     """Per step: copy the query and the appended K/V row from pinned host memory,
-    run the three public calls, copy the output back, synchronise."""
+    run the step through the public API (kvr_decode_step: the appended key's
+    code, selection, attention, one library call, arguments marshalled once
+    per layer), copy the output back, synchronise."""
     dev = layers[0].K.device
     n = min(args.steps, args.e2e_steps)
     hq = [L.q.cpu().pin_memory() for L in layers]
@@ -547,14 +549,15 @@ def run_e2e(args, w, layers, kvr, torch, sgn, params, ws_s, ws_a, idx, cnt, seq,
     h2d = hq[0].numel() * hq[0].element_size() + row_h2d
     d2h = hout.numel() * hout.element_size()
 
+    steps = [kvr.DecodeStep(L.q, L.K, L.V, L.codes, seq, pos_new, sgn, L.params, idx, cnt, scale,
+                            L.out, ws_s, err) for L in layers]
+
     def one(i):
         L = layers[i % LAYERS]
         L.q.copy_(hq[i % LAYERS], non_blocking=True)
         L.K[:, :, w.N - 1].copy_(hk[i % LAYERS], non_blocking=True)
         L.V[:, :, w.N - 1].copy_(hv[i % LAYERS], non_blocking=True)
-        L.encode_new(kvr, pos_new, sgn, err)
-        kvr.kvr_select(L.q, L.K, L.codes, seq, sgn, L.params, idx, cnt, ws_s, err)
-        kvr.kvr_sparse_attend(L.q, L.K, L.V, idx, cnt, seq, w.W, scale, L.out, ws_a, err)
+        steps[i % LAYERS]()
         hout.copy_(L.out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
@@ -567,7 +570,8 @@ def run_e2e(args, w, layers, kvr, torch, sgn, params, ws_s, ws_a, idx, cnt, seq,
     el = time.perf_counter() - t0
     el = max_over_ranks(el, world)
     return {"value": n * world / el, "unit": "steps/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": n, "mode": "eager C-ABI calls, sync per step"}
+            "d2h_bytes_per_step": d2h, "steps": n,
+            "mode": "kvr_decode_step per step (one C-ABI call), sync per step"}
 
 
 # --------------------------------------------------------------------------

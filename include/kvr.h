@@ -263,6 +263,23 @@ kvr_status kvr_select(const kvr_shape *shape, const kvr_select_params *p, const 
                       void *workspace, size_t workspace_bytes, int32_t *err_word,
                       void *stream);
 
+/*
+ * kvr_decode_step -- one decode step of every unit in one call: the code
+ * (and, with p->rsq_records, the reranker record) of the appended key at row
+ * pos_new[b], then kvr_select, then the attention over its output (over the
+ * cache regions when p->region_end is set, else over the top-k and the
+ * window W), all enqueued on `stream` in that order. Arguments as in those
+ * calls; out_idx must hold p->k entries per unit; the attention needs no
+ * workspace. KVR_SELECT_EARLY_INPUTS is ignored (the selection follows the
+ * encode that writes its codes). Validation errors of any part are returned
+ * before that part is enqueued; the parts before it stay enqueued.
+ */
+kvr_status kvr_decode_step(const kvr_shape *shape, const kvr_select_params *p, const void *q,
+                           const void *K, const void *V, uint8_t *codes, const int32_t *seq_len,
+                           const int32_t *pos_new, const int8_t *srht_sign, int32_t *out_idx,
+                           int32_t *out_count, float scale, float *out, void *workspace,
+                           size_t workspace_bytes, int32_t *err_word, void *stream);
+
 /* Size of the fixed device scratch array behind kvr_select_static_scratch. */
 #define KVR_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 

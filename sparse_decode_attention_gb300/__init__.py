@@ -27,7 +27,7 @@ __all__ = [
     "kvr_tier_init", "kvr_tiered_attend_workspace_size", "kvr_sparse_attend_tiered",
     "kvr_tier_update_workspace_size", "kvr_tier_update",
     "kvr_rsq_record_bytes", "kvr_rsq_tables", "kvr_encode_rsq", "rsq_buffer",
-    "kvr_sparse_attend_regions", "kvr_regions_update",
+    "kvr_sparse_attend_regions", "kvr_regions_update", "kvr_decode_step", "DecodeStep",
 ]
 
 KVR_F32, KVR_BF16 = 0, 1
@@ -180,10 +180,12 @@ def load(build_if_missing: bool = True):
                                             _P, ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P]
     L.kvr_regions_update.argtypes = [ctypes.c_int, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, _P, _P, _P]
+    L.kvr_decode_step.argtypes = [S, Pp, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P,
+                                  _P, ctypes.c_size_t, _P, _P]
     for fn in ("kvr_encode_keys", "kvr_select_workspace_views", "kvr_select",
                "kvr_select_static_scratch", "kvr_tier_init", "kvr_sparse_attend_tiered",
                "kvr_tier_update", "kvr_rsq_tables", "kvr_encode_rsq",
-               "kvr_sparse_attend_regions", "kvr_regions_update",
+               "kvr_sparse_attend_regions", "kvr_regions_update", "kvr_decode_step",
                "kvr_sparse_attend", "kvr_read_error"):
         getattr(L, fn).restype = ctypes.c_int
     _lib = L
@@ -520,3 +522,51 @@ def kvr_regions_update(seq_len, sink, local, buffer, region_end, init=False, err
                                    int(buffer), 1 if init else 0, _ptr(region_end), _ptr(err),
                                    _stream(stream))
     _check(st, "kvr_regions_update")
+
+
+def _decode_args(q, K, V, codes, seq_len, pos_new, srht_sign, params, out_idx, out_count, scale,
+                 out, workspace, err, stream):
+    shape = Shape.of(_kv(K, "K"), _cuda(q, "q", K.dtype))
+    _kv(V, "V")
+    if V.dtype != K.dtype or V.shape != K.shape:
+        raise TypeError("V must have K's dtype and shape")
+    _codes(codes, shape)
+    for t, n, dt in ((seq_len, "seq_len", torch.int32), (pos_new, "pos_new", torch.int32),
+                     (srht_sign, "srht_sign", torch.int8), (out_idx, "out_idx", torch.int32),
+                     (out_count, "out_count", torch.int32), (out, "out", torch.float32)):
+        _cuda(t, n, dt)
+    _cuda(workspace, "workspace")
+    if out_idx.shape[-1] != params.k:
+        raise ValueError("out_idx rows must hold params.k entries")
+    return (ctypes.byref(shape.c()), ctypes.byref(params.c()), _ptr(q), _ptr(K), _ptr(V),
+            _ptr(codes), _ptr(seq_len), _ptr(pos_new), _ptr(srht_sign), _ptr(out_idx),
+            _ptr(out_count), float(scale), _ptr(out), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream))
+
+
+def kvr_decode_step(q, K, V, codes, seq_len, pos_new, srht_sign, params: SelectParams, out_idx,
+                    out_count, scale, out, workspace, err=None, stream=None):
+    """Code (and record) of the appended key at pos_new, selection and
+    attention, in one library call."""
+    _check(load().kvr_decode_step(*_decode_args(q, K, V, codes, seq_len, pos_new, srht_sign,
+                                                params, out_idx, out_count, scale, out,
+                                                workspace, err, stream)), "kvr_decode_step")
+
+
+class DecodeStep:
+    """kvr_decode_step with its arguments marshalled once: calling it enqueues
+    the step on the stream given at construction with no per-call argument
+    conversion (the tensors must stay alive and in place)."""
+
+    def __init__(self, q, K, V, codes, seq_len, pos_new, srht_sign, params: SelectParams, out_idx,
+                 out_count, scale, out, workspace, err=None, stream=None):
+        self._keep = (q, K, V, codes, seq_len, pos_new, srht_sign, params, out_idx, out_count,
+                      out, workspace, err, stream)
+        self._args = _decode_args(q, K, V, codes, seq_len, pos_new, srht_sign, params, out_idx,
+                                  out_count, scale, out, workspace, err, stream)
+        self._fn = load().kvr_decode_step
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != 0:
+            raise KvrError(st, "kvr_decode_step")

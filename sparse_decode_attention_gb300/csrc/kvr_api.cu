@@ -247,6 +247,40 @@ kvr_status kvr_select(const kvr_shape *shape, const kvr_select_params *p, const 
                            static_cast<uint8_t *>(workspace), err_word);
 }
 
+kvr_status kvr_decode_step(const kvr_shape *shape, const kvr_select_params *p, const void *q,
+                           const void *K, const void *V, uint8_t *codes, const int32_t *seq_len,
+                           const int32_t *pos_new, const int8_t *srht_sign, int32_t *out_idx,
+                           int32_t *out_count, float scale, float *out, void *workspace,
+                           size_t workspace_bytes, int32_t *err_word, void *stream)
+{
+    kvr_status st = check_shape(shape);
+    if (st != KVR_OK) return st;
+    if ((st = check_params(p)) != KVR_OK) return st;
+    if (!pos_new || !out || !(scale == scale)) return KVR_ERR_INVALID_ARG;
+    // validated before anything is enqueued: the attention's arguments too
+    if (!V || !aligned16(V) || !aligned16(out)) return KVR_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(pos_new) & 3u) != 0) return KVR_ERR_INVALID_ARG;
+    if (workspace_bytes < plan_select(*shape, *p).bytes) return KVR_ERR_WORKSPACE;
+    // the appended key's code is written by the first launch: the selection
+    // must not start on its inputs early
+    kvr_select_params ps = *p;
+    ps.flags &= ~KVR_SELECT_EARLY_INPUTS;
+    if ((st = kvr_encode_keys(shape, K, pos_new, 1, srht_sign, codes, err_word, stream)) != KVR_OK)
+        return st;
+    if (p->rsq_records &&
+        (st = kvr_encode_rsq(shape, K, pos_new, 1, srht_sign, const_cast<uint8_t *>(p->rsq_records),
+                             err_word, stream)) != KVR_OK)
+        return st;
+    if ((st = kvr_select(shape, &ps, q, K, codes, seq_len, srht_sign, out_idx, out_count, workspace,
+                         workspace_bytes, err_word, stream)) != KVR_OK)
+        return st;
+    if (p->region_end)
+        return kvr_sparse_attend_regions(shape, q, K, V, out_idx, p->k, out_count, seq_len, p->sink,
+                                         p->region_end, scale, out, nullptr, 0, err_word, stream);
+    return kvr_sparse_attend(shape, q, K, V, out_idx, p->k, out_count, seq_len, p->W, scale, out,
+                             nullptr, 0, err_word, stream);
+}
+
 size_t kvr_attend_workspace_size(const kvr_shape *shape, int kmax, int W)
 {
     if (check_shape(shape) != KVR_OK || kmax < 0 || W < 0) return 0;

@@ -230,3 +230,23 @@ def test_region_calls_validate_before_launch(kvr_lib):
     pv.region_end = (1 << 20) + 2                  # int32 array misaligned
     assert L.kvr_select(ctypes.byref(s.c()), ctypes.byref(pv), fake, fake, fake, fake, fake,
                         fake, fake, fake, need, None, None) == 1
+
+
+def test_decode_step_validates_before_launch(kvr_lib):
+    kvr = kvr_lib
+    L = kvr.load()
+    fake = ctypes.c_void_p(1 << 20)
+    s = _shape(kvr)
+    p = kvr.SelectParams(64, 16, 8)
+    need = kvr.kvr_select_workspace_size(s, p)
+
+    def step(prm, pos=fake, V=fake, out=fake, scale=0.1, ws=need):
+        return L.kvr_decode_step(ctypes.byref(s.c()), ctypes.byref(prm.c()), fake, fake, V, fake,
+                                 fake, pos, fake, fake, fake, scale, out, fake, ws, None, None)
+    assert step(p, pos=None) == 1
+    assert step(p, pos=ctypes.c_void_p((1 << 20) + 2)) == 1      # int32 array misaligned
+    assert step(p, V=None) == 1
+    assert step(p, out=ctypes.c_void_p((1 << 20) + 4)) == 1
+    assert step(p, scale=float("nan")) == 1
+    assert step(p, ws=need - 1) == 3
+    assert step(kvr.SelectParams(64, 65, 8)) == 1

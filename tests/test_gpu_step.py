@@ -1,0 +1,82 @@
+"""kvr_decode_step (encode of the appended key, selection, attention in one
+library call) gives bit-identical results to the three separate calls, with
+the plain window and with records + cache regions; and the prepared caller
+(DecodeStep) equals it."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+import sparse_decode_attention_gb300 as kvr
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    kvr.load()
+    oracle.build()
+
+
+@pytest.mark.parametrize("mode", ["window", "regions_rsq"])
+def test_decode_step_equals_the_separate_calls(mode):
+    seq0 = [9000, 6000]
+    w = wl.Workload("step", B=2, Hq=8, Hkv=2, d=128, N=max(seq0) + 1, dtype="bf16", rank=32,
+                    planted=16, seed=93)
+    K, V, qb = wl.make_cache(w, device=DEV, cap=9100)
+    sgn = wl.srht_signs(128, device=DEV)
+    shape = kvr.Shape.of(K, qb)
+    B, Hkv = 2, 2
+    runs = []
+    for how in ("separate", "fused", "prepared"):
+        codes = kvr.codes_buffer(shape, DEV)
+        kvr.kvr_encode_keys(K, torch.zeros(B, dtype=torch.int32, device=DEV), 9000, sgn, codes)
+        rec = rend = None
+        S = 0
+        if mode == "regions_rsq":
+            rec = kvr.rsq_buffer(K)
+            kvr.kvr_encode_rsq(K, torch.zeros(B, dtype=torch.int32, device=DEV), 9000, sgn, rec)
+            S = 4
+            rend = torch.tensor([8850, 5880], dtype=torch.int32, device=DEV)
+        params = kvr.SelectParams(1024, 256, 128, wl.DEFAULT_LUT, rsq_records=rec, sink=S,
+                                  region_end=rend)
+        seq = torch.tensor([n + 1 for n in seq0], dtype=torch.int32, device=DEV)
+        pos = torch.tensor(seq0, dtype=torch.int32, device=DEV)
+        ws = kvr.workspace(kvr.kvr_select_workspace_size(shape, params))
+        idx = torch.full((B, Hkv, 256), 7, dtype=torch.int32, device=DEV)
+        cnt = torch.zeros((B, Hkv), dtype=torch.int32, device=DEV)
+        out = torch.zeros((B, 8, 128), dtype=torch.float32, device=DEV)
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        q = wl.step_query(w, qb, 3).contiguous()
+        scale = 1 / math.sqrt(128)
+        if how == "separate":
+            kvr.kvr_encode_keys(K, pos, 1, sgn, codes, err)
+            if rec is not None:
+                kvr.kvr_encode_rsq(K, pos, 1, sgn, rec, err)
+            kvr.kvr_select(q, K, codes, seq, sgn, params, idx, cnt, ws, err)
+            if rend is not None:
+                kvr.kvr_sparse_attend_regions(q, K, V, idx, cnt, seq, S, rend, scale, out,
+                                              kvr.workspace(0), err)
+            else:
+                kvr.kvr_sparse_attend(q, K, V, idx, cnt, seq, 128, scale, out, kvr.workspace(0),
+                                      err)
+        elif how == "fused":
+            kvr.kvr_decode_step(q, K, V, codes, seq, pos, sgn, params, idx, cnt, scale, out, ws,
+                                err)
+        else:
+            kvr.DecodeStep(q, K, V, codes, seq, pos, sgn, params, idx, cnt, scale, out, ws, err)()
+        torch.cuda.synchronize()
+        assert kvr.kvr_read_error(err) == 0
+        runs.append((codes.cpu().numpy(), None if rec is None else rec.cpu().numpy(),
+                     idx.cpu().numpy(), cnt.cpu().numpy(), out.cpu().numpy()))
+    for other in runs[1:]:
+        for a, b in zip(runs[0], other):
+            if a is not None:
+                assert np.array_equal(a, b)
+    assert runs[0][3].min() > 0
