@@ -20,7 +20,8 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = [os.path.join(_HERE, "kvr_oracle.c"), os.path.join(_HERE, "kvr_tiers_oracle.c"),
-        os.path.join(_HERE, "kvr_rsq_oracle.c"), os.path.join(_HERE, "kvr_regions_oracle.c")]
+        os.path.join(_HERE, "kvr_rsq_oracle.c"), os.path.join(_HERE, "kvr_regions_oracle.c"),
+        os.path.join(_HERE, "kvr_votes_oracle.c")]
 _LIB = os.path.join(_HERE, "libkvr_oracle.so")
 _lib = None
 
@@ -66,6 +67,13 @@ def lib():
         _tier_signatures(L)
         _rsq_signatures(L)
         _region_signatures(L)
+        L.orc_flip_cost.argtypes = [_P, ctypes.c_uint]
+        L.orc_flip_cost.restype = ctypes.c_float
+        L.orc_mag_vote_table.argtypes = [_P, _I32, _P, _P]
+        L.orc_mag_vote_table.restype = _I32
+        L.orc_select_unit_mag.argtypes = [_P, _I32, _P, _P, _I64, _I32, _P, _I64, _I64, _I64, _P,
+                                          _P, _P, _P, _P, _P, _P]
+        L.orc_select_unit_mag.restype = _I32
         _lib = L
     return _lib
 
@@ -589,3 +597,50 @@ def attend_unit_regions(q_group, K_unit, V_unit, N, S, R, idx, count, scale) -> 
     if rc != 0:
         raise ValueError("selected index outside the retrieval region")
     return out
+
+
+# --------------------------------------------------------------------------
+# magnitude-aware coarse votes (kvr_votes_oracle.c)
+# --------------------------------------------------------------------------
+
+def flip_cost(a8, x) -> np.float32:
+    """fp32 sum of a8[j] over the set bits j of x, ascending from +0."""
+    a = f32(a8)
+    return np.float32(lib().orc_flip_cost(_p(a), int(x)))
+
+
+def mag_vote_table(zq, lut) -> np.ndarray:
+    """Vote tables [d/8, 256] int32 of the rotated query zq [d]."""
+    z = f32(zq)
+    d = z.shape[-1]
+    T = np.zeros((d // 8, 256), dtype=np.int32)
+    if lib().orc_mag_vote_table(_p(z), d, _p(_c(lut, np.int32)), _p(T)):
+        raise ValueError("unsupported head_dim %d" % d)
+    return T
+
+
+def select_unit_mag(q_group, K_unit, codes_unit, N, sgn, C, k, W, lut, diagnostics=False):
+    """Selection of one unit with magnitude-aware votes; (idx[k] padded -1,
+    count[, diag with cand, cand_S, coarse, table])."""
+    q = f32(q_group)
+    G, d = q.shape
+    Kf = f32(K_unit)
+    cd = _c(codes_unit, np.uint8)
+    s = _c(sgn, np.int8)
+    lt = _c(lut, np.int32)
+    pool = max(0, N - W)
+    nc = max(0, min(C, pool))
+    idx = np.full(max(k, 1), -1, dtype=np.int32)
+    cnt = np.zeros(1, dtype=np.int32)
+    cand = np.full(max(nc, 1), -1, dtype=np.int32)
+    candS = np.zeros(max(nc, 1), dtype=np.float32)
+    coarse = np.zeros(max(pool, 1), dtype=np.int32)
+    table = np.zeros((d // 8, 256), dtype=np.int32)
+    rc = lib().orc_select_unit_mag(_p(q), G, _p(Kf), _p(cd), N, d, _p(s), C, k, W, _p(lt),
+                                   _p(idx), _p(cnt), _p(cand), _p(candS), _p(coarse), _p(table))
+    if rc != 0:
+        raise ValueError("oracle selection failed")
+    if not diagnostics:
+        return idx[:k], int(cnt[0])
+    return idx[:k], int(cnt[0]), dict(cand=cand[:nc], cand_S=candS[:nc], coarse=coarse[:pool],
+                                      table=table)
