@@ -238,7 +238,7 @@ def config_of(w):
 # --------------------------------------------------------------------------
 
 class Layer:
-    def __init__(self, w, l, kvr, wl, torch, sgn, rerank="exact", host=False):
+    def __init__(self, w, l, kvr, wl, torch, sgn, rerank="exact", host=False, mag=False):
         dev = "cuda"
         K, V, qb = wl.make_cache(w, device=dev, cap=w.N, seed=w.seed + 1000 * l)
         self.K, self.V = K, V
@@ -266,7 +266,8 @@ class Layer:
             self.V.copy_(V)
             del K, V
             torch.cuda.empty_cache()
-        self.params = kvr.SelectParams(w.C, w.k, w.W, w.lut, flags=kvr.SELECT_EARLY_INPUTS,
+        flags = kvr.SELECT_EARLY_INPUTS | (kvr.SELECT_MAGNITUDE_VOTES if mag else 0)
+        self.params = kvr.SelectParams(w.C, w.k, w.W, w.lut, flags=flags,
                                        V_prefetch=None if host else self.V, rsq_records=self.rec)
 
     def encode_new(self, kvr, pos_new, sgn, err, stream=None):
@@ -288,9 +289,10 @@ def run_gpu(args, w):
     sgn = wl.srht_signs(w.d, device=dev)
     host = args.workload == "million_offload"
     rerank = args.rerank or ("rsq" if host else "exact")
-    layers = [Layer(w, l, kvr, wl, torch, sgn, rerank, host) for l in range(LAYERS)]
+    mag = args.votes == "magnitude"
+    layers = [Layer(w, l, kvr, wl, torch, sgn, rerank, host, mag) for l in range(LAYERS)]
     shape = kvr.Shape.of(layers[0].K, layers[0].q)
-    params = kvr.SelectParams(w.C, w.k, w.W, w.lut)
+    params = layers[0].params   # the flags of every layer's selection (workspace size)
     ws_s = kvr.workspace(kvr.kvr_select_workspace_size(shape, params), dev)
     ws_a = kvr.workspace(kvr.kvr_attend_workspace_size(shape, w.k, w.W), dev)
     idx = torch.empty((w.B, w.Hkv, w.k), dtype=torch.int32, device=dev)
@@ -326,7 +328,8 @@ def run_gpu(args, w):
             ev[4].record(main)
         main.wait_event(join)
 
-    launches_per_step = 4 if rerank == "rsq" else 3  # encode(s), select, attend
+    # encode(s), select (plus its vote lists), attend
+    launches_per_step = (4 if rerank == "rsq" else 3) + (1 if mag else 0)
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
     # eager warm-up on the capture stream, then one graph per layer
@@ -481,7 +484,7 @@ def run_gpu(args, w):
                "sample": "%d unit-steps (batch 0, kv head 0) of the %s workload in %.1f s, "
                          "single-threaded; steps/s = unit-steps / %d / s"
                          % (done, w.name, el, ab["units"])}
-    cfg = dict(config_of(w), rerank=rerank)
+    cfg = dict(config_of(w), rerank=rerank, votes=args.votes)
     if host:
         cfg["kv_residency"] = "K, V in page-locked host memory read through the device mapping"
     line = {
@@ -810,15 +813,17 @@ def run_gpu_drift(args, w):
     del k_new
     sgn = wl.srht_signs(w.d, device=dev)
     shape = kvr.Shape.of(K, qb)
+    vflags = kvr.SELECT_MAGNITUDE_VOTES if args.votes == "magnitude" else 0
     regions = None
     if args.regions:
         # Sink / Local / Update buffer sizes in tokens (cache regions)
         regions = tuple(int(x) for x in args.regions.split(","))
         S_r, L_r, U_r = regions
         rend = torch.zeros(w.B, dtype=torch.int32, device=dev)
-        params = kvr.SelectParams(w.C, w.k, 0, w.lut, V_prefetch=V, sink=S_r, region_end=rend)
+        params = kvr.SelectParams(w.C, w.k, 0, w.lut, V_prefetch=V, sink=S_r, region_end=rend,
+                                  flags=vflags)
     else:
-        params = kvr.SelectParams(w.C, w.k, w.W, w.lut, V_prefetch=V)
+        params = kvr.SelectParams(w.C, w.k, w.W, w.lut, V_prefetch=V, flags=vflags)
     ws_s = kvr.workspace(kvr.kvr_select_workspace_size(shape, params), dev)
     ws_a = kvr.workspace(kvr.kvr_attend_workspace_size(shape, w.k, w.W), dev)
     codes = kvr.codes_buffer(shape, dev)
@@ -931,12 +936,14 @@ def run_gpu_drift(args, w):
     line = {
         "metric": "batched drift decode steps/s (B8, 32768 prefill + %d appending steps) and "
                   "exact-top-k recall per step" % T
-                  + (", sink / local / update-buffer regions" if regions else ""),
+                  + (", sink / local / update-buffer regions" if regions else "")
+                  + (", magnitude-aware votes" if vflags else ""),
         "value": T * world / (ms / 1000.0), "unit": "steps/s", "n_gpus": world, "steps": T,
         "warmup": args.warmup, "ms_per_step": ms / T, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.d,
                    "prefill": N0, "appending_steps": T, "C": w.C, "k": w.k, "W": w.W,
+                   "votes": args.votes,
                    "regions": None if not regions else
                    {"sink": regions[0], "local": regions[1], "buffer": regions[2]},
                    "l2": "inputs larger than L2: each step reads %.0f MB"
@@ -950,7 +957,7 @@ def run_gpu_drift(args, w):
                      "peak_kind": peak_kind, "traffic": None,
                      "algorithmic_bytes": ab["select"], "avg_ms": sel_ms},
         "attend_us": att_ms * 1e3, "cpu_baseline": None, "e2e": None,
-        "gpu_launches": (4 if regions else 3) * T, "clocks": clk,
+        "gpu_launches": (3 + (1 if regions else 0) + (1 if vflags else 0)) * T, "clocks": clk,
     }
     print(json.dumps(line), flush=True)
 
@@ -974,6 +981,9 @@ def main():
     ap.add_argument("--diagnostics", type=int, default=0, metavar="STEPS",
                     help="tiered_window_cache only: also run STEPS untimed appending steps and "
                          "report Future Missed Mass, Global LIR and selection churn")
+    ap.add_argument("--votes", choices=["hamming", "magnitude"], default="hamming",
+                    help="coarse votes: Hamming rings of the query code (default) or centroids "
+                         "ranked by the rotated query's magnitudes")
     ap.add_argument("--regions", default=None, metavar="S,L,U",
                     help="batched_drift only: sink, local and update-buffer sizes (tokens); "
                          "selection over the retrieval region, attention over sink + top-k + "

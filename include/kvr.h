@@ -90,6 +90,16 @@ typedef enum kvr_dtype { KVR_F32 = 0, KVR_BF16 = 1 } kvr_dtype;
 /* kvr_select_params.flags */
 #define KVR_SELECT_STORE_COARSE 0x1 /* also write every pool key's coarse score to the
                                        workspace (diagnostics; costs time) */
+#define KVR_SELECT_MAGNITUDE_VOTES 0x4 /* coarse votes from the centroids ranked by their
+                                       similarity to the rotated query (ParisKV, "Pipeline di
+                                       Recupero Nativa su GPU in Due Stadi", top-rho centroids
+                                       per sub-space): with a_j = |zq_j|, zq = FWHT(D q_bar),
+                                       the flip pattern x of a key's sub-block code against the
+                                       query code costs f(x) = sum over the set bits j of x,
+                                       ascending, of a_j (fp32 from +0); patterns ordered by
+                                       (f, x) fill the tiers of sizes 1, 8, 28, 56, 70, 56, 28,
+                                       8, 1 and vote lut[tier] (instead of lut[popcount(x)]).
+                                       One more kernel launch; the scoring does more work */
 #define KVR_SELECT_EARLY_INPUTS 0x2 /* the caller asserts that codes, K, V_prefetch,
                                        rsq_records, region_end, seq_len and srht_sign were
                                        complete before the previous kernel

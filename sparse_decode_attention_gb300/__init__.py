@@ -21,7 +21,8 @@ __all__ = [
     "kvr_encode_keys", "kvr_select_workspace_size", "kvr_select_workspace_views",
     "kvr_select", "kvr_select_static_scratch", "kvr_attend_workspace_size",
     "kvr_sparse_attend", "kvr_read_error",
-    "DEFAULT_LUT", "DEVERR", "SELECT_STORE_COARSE", "SELECT_EARLY_INPUTS", "kvr_codes_bytes",
+    "DEFAULT_LUT", "DEVERR", "SELECT_STORE_COARSE", "SELECT_EARLY_INPUTS",
+    "SELECT_MAGNITUDE_VOTES", "kvr_codes_bytes",
     "codes_buffer",
     "WINDOW", "TIER_BF16", "TIER_INT2", "TIER_EVICTED", "TierState", "kvr_ledger_bytes",
     "kvr_tier_init", "kvr_tiered_attend_workspace_size", "kvr_sparse_attend_tiered",
@@ -58,6 +59,7 @@ class _Params(ctypes.Structure):
 
 SELECT_STORE_COARSE = 0x1
 SELECT_EARLY_INPUTS = 0x2
+SELECT_MAGNITUDE_VOTES = 0x4
 
 
 class _Views(ctypes.Structure):

@@ -37,7 +37,8 @@ kvr_status check_params(const kvr_select_params *p)
         return KVR_ERR_INVALID_ARG;
     for (int i = 0; i < 9; i++)
         if (p->lut[i] < 0 || p->lut[i] > 15) return KVR_ERR_INVALID_ARG;
-    if (p->flags & ~(KVR_SELECT_STORE_COARSE | KVR_SELECT_EARLY_INPUTS)) return KVR_ERR_INVALID_ARG;
+    if (p->flags & ~(KVR_SELECT_STORE_COARSE | KVR_SELECT_EARLY_INPUTS | KVR_SELECT_MAGNITUDE_VOTES))
+        return KVR_ERR_INVALID_ARG;
     if (!aligned16(p->V_prefetch) || !aligned16(p->rsq_records)) return KVR_ERR_INVALID_ARG;
     if (p->sink < 0 || (reinterpret_cast<uintptr_t>(p->region_end) & 3u) != 0)
         return KVR_ERR_INVALID_ARG;
@@ -118,6 +119,8 @@ SelectPlan plan_select(const kvr_shape &s, const kvr_select_params &p)
     pl.off_cand_count = take((size_t)U * 4);
     pl.off_qbar = take((size_t)U * s.d * 4);
     pl.off_coarse = pl.has_coarse ? take((size_t)U * pl.cap_pad) : 0;
+    pl.has_votes = (p.flags & KVR_SELECT_MAGNITUDE_VOTES) != 0;
+    pl.off_votes = pl.has_votes ? take((size_t)U * (s.d / 8) * kVoteStride * 2) : 0;
     pl.bytes = o;
     return pl;
 }

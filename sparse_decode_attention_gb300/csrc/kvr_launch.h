@@ -38,9 +38,25 @@ struct SelectPlan {
     int64_t nblk;     // 32-token blocks per unit row of the score planes
     int64_t tiles;    // 1024-token code tiles per unit
     bool has_coarse;
+    bool has_votes;   // magnitude-aware vote lists
     size_t off_planes, off_cand_idx, off_cand_score, off_cand_count, off_qbar, off_coarse;
+    size_t off_votes;
     size_t bytes;
 };
+
+// Magnitude-aware vote lists (kvr_votes.cu): per unit and sub-block,
+// kVoteStride uint16 entries: up to 256 (pattern | vote << 8), the count at
+// index 256 (16-byte aligned rows).
+constexpr int kVoteStride = 264;
+struct VoteArgs {
+    const void *q;
+    const int8_t *sgn;
+    int Hq, Hkv, G, nb;
+    int lut[9];
+    uint16_t *lists;
+};
+kvr_status vote_list_dispatch(const LaunchCtx &c, const void *q, const int8_t *sgn,
+                              const int32_t *lut, uint16_t *lists);
 SelectPlan plan_select(const kvr_shape &s, const kvr_select_params &p);
 
 struct AttendPlan {

@@ -60,6 +60,7 @@ struct SelArgs {
     const uint8_t *rsq;  // reranker records, or null: exact rescoring
     int sink;                   // Sink tokens [0, sink)
     const int32_t *region_end;  // Retrieval end per batch entry, or null: N - W
+    const uint16_t *votes;      // magnitude-aware vote lists of the units, or null
     float lev[8];        // reranker magnitude levels
     const uint8_t *codes;
     const int32_t *seq_len;
@@ -193,6 +194,7 @@ template <int D, typename T> struct SelSmem {
     static constexpr int oLev = oPl + 8 * kPlaneCap * 4;  // float [16] signed reranker levels
     static constexpr int bytes = oLev + 16 * 4;
     static_assert(16 * 256 * 4 <= kRingBytes, "radix exchange scratch must fit the ring");
+    static_assert((D / 8) * kVoteStride * 2 <= 2 * kMaxSlice * 4, "vote lists must fit sS + sI");
 };
 
 enum {
@@ -329,6 +331,13 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         }
     }
     if (a.early) grid_dependency_wait();  // q may come from the previous grid
+    if (a.votes) {
+        // this unit's vote lists (written by the previous grid) into the
+        // candidate-score area, which P1 and P2 do not use
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.votes + (size_t)u * NB * kVoteStride);
+        uint4 *dst = reinterpret_cast<uint4 *>(smem + SM::oS);
+        for (int i = tid; i < NB * kVoteStride * 2 / 16; i += kSelThreads) dst[i] = src[i];
+    }
 
     // q_bar and its code (every CTA of the cluster computes them)
     if (warp == 0) {
@@ -411,11 +420,28 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
             const uint4 q0 = sQm[2 * sb], q1 = sQm[2 * sb + 1];
             const uint32_t x[8] = {v0.x ^ q0.x, v0.y ^ q0.y, v0.z ^ q0.z, v0.w ^ q0.w,
                                    v1.x ^ q1.x, v1.y ^ q1.y, v1.z ^ q1.z, v1.w ^ q1.w};
-            uint32_t c0, c1, c2, c3;
-            count8(x, c0, c1, c2, c3);
             uint32_t vote[VB];
+            if (a.votes) {
+                // match the 32 keys' flip patterns against the voted patterns
+                const uint16_t *lst = reinterpret_cast<const uint16_t *>(smem + SM::oS) + sb * kVoteStride;
+                const int np = lst[256];
 #pragma unroll
-            for (int j = 0; j < VB; j++) vote[j] = lut_bit(c0, c1, c2, c3, L[j]);
+                for (int j = 0; j < VB; j++) vote[j] = 0u;
+#pragma unroll 2
+                for (int i = 0; i < np; i++) {
+                    const uint32_t e = lst[i];
+                    uint32_t miss = 0u;
+#pragma unroll
+                    for (int j = 0; j < 8; j++) miss |= x[j] ^ (0u - ((e >> j) & 1u));
+#pragma unroll
+                    for (int j = 0; j < VB; j++) vote[j] |= ((e >> (8 + j)) & 1u) ? ~miss : 0u;
+                }
+            } else {
+                uint32_t c0, c1, c2, c3;
+                count8(x, c0, c1, c2, c3);
+#pragma unroll
+                for (int j = 0; j < VB; j++) vote[j] = lut_bit(c0, c1, c2, c3, L[j]);
+            }
             add_planes<ACC, VB>(acc, vote);
         }
         uint32_t other[ACC];  // the other half of the sub-blocks sits in lane ^ 16
@@ -1164,6 +1190,7 @@ kvr_status select_dispatch(const LaunchCtx &c, const kvr_select_params &p, const
     a.rsq = p.rsq_records;
     a.sink = p.sink;
     a.region_end = p.region_end;
+    a.votes = plan.has_votes ? reinterpret_cast<const uint16_t *>(ws + plan.off_votes) : nullptr;
     for (int i = 0; i < 8; i++) a.lev[i] = rsq_tables().lev[i];
     a.codes = codes;
     a.seq_len = seq_len;
@@ -1180,6 +1207,11 @@ kvr_status select_dispatch(const LaunchCtx &c, const kvr_select_params &p, const
     a.cap_pad = plan.cap_pad;
     a.tiles = plan.tiles;
     a.err = err;
+    if (plan.has_votes) {
+        const kvr_status st = vote_list_dispatch(c, q, sgn, p.lut,
+                                                 reinterpret_cast<uint16_t *>(ws + plan.off_votes));
+        if (st != KVR_OK) return st;
+    }
     const int cs = select_cluster_size(c.shape.B * c.shape.Hkv, p.C);
     const bool bf = c.shape.dtype == KVR_BF16;
     if (c.shape.d == 128)

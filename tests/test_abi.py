@@ -61,7 +61,10 @@ def test_workspace_sizes(kvr_lib):
     vc = kvr.kvr_select_workspace_views(s, pc)
     assert vc["coarse"] % 256 == 0
     assert kvr.kvr_select_workspace_size(s, pc) >= n + 8 * 131072
-    assert kvr.kvr_select_workspace_size(s, kvr.SelectParams(8, 4, 0, flags=4)) == 0  # unknown flag
+    assert kvr.kvr_select_workspace_size(s, kvr.SelectParams(8, 4, 0, flags=8)) == 0  # unknown flag
+    # magnitude-aware votes: one vote-list row per unit and sub-block on top
+    pm = kvr.SelectParams(8192, 2048, 128, flags=kvr.SELECT_MAGNITUDE_VOTES)
+    assert kvr.kvr_select_workspace_size(s, pm) >= n + 8 * 16 * 264 * 2
     assert kvr.kvr_codes_bytes(s) == 8 * 128 * 128 * 128  # 128 tiles of 1024 tokens per unit
     assert kvr.kvr_codes_bytes(_shape(kvr, cap=1025, d=64)) == 8 * 2 * 64 * 128
     assert kvr.kvr_select_workspace_size(_shape(kvr, d=96), p) == 0
