@@ -214,7 +214,7 @@ def run_reference(args, w):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 / value, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w),
+        "config": dict(config_of(w), rerank="exact", votes="hamming"),
         "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle",
                          "sample": "%d unit-steps (batch 0, kv head 0 of %d units) of the 128K "
                                    "workload, %.1f s; steps/s = unit-steps / %d / s"
