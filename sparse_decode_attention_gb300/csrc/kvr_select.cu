@@ -205,7 +205,10 @@ enum {
     M_SEG = 40,    // [17] first boundary-key position of each CTA, then the total
 };
 
-template <int D, typename T, int VB>
+// EXT: the instantiation carries the optional modes (reranker records,
+// magnitude-aware votes); without it their code is compiled out, which keeps
+// the common kernel smaller (instruction fetch is its top stall).
+template <int D, typename T, int VB, bool EXT>
 __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
 {
     using SM = SelSmem<D, T>;
@@ -331,7 +334,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         }
     }
     if (a.early) grid_dependency_wait();  // q may come from the previous grid
-    if (a.votes) {
+    if (EXT && a.votes) {
         // this unit's vote lists (written by the previous grid) into the
         // candidate-score area, which P1 and P2 do not use
         const uint4 *src = reinterpret_cast<const uint4 *>(a.votes + (size_t)u * NB * kVoteStride);
@@ -378,7 +381,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
 #pragma unroll
         for (int r = 0; r < E; r++) sQsgn[lane * E + r] = x[r] < 0.0f ? -1 : 0;
         // the reranker scores against zq = FWHT(D q_bar) itself, q_bar is not needed
-        if (a.rsq)
+        if (EXT && a.rsq)
 #pragma unroll
             for (int r = 0; r < E; r++) sQbar[lane * E + r] = x[r];
     }
@@ -421,7 +424,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
             const uint32_t x[8] = {v0.x ^ q0.x, v0.y ^ q0.y, v0.z ^ q0.z, v0.w ^ q0.w,
                                    v1.x ^ q1.x, v1.y ^ q1.y, v1.z ^ q1.z, v1.w ^ q1.w};
             uint32_t vote[VB];
-            if (a.votes) {
+            if (EXT && a.votes) {
                 // match the 32 keys' flip patterns against the voted patterns
                 const uint16_t *lst = reinterpret_cast<const uint16_t *>(smem + SM::oS) + sb * kVoteStride;
                 const int np = lst[256];
@@ -603,7 +606,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
                 for (uint32_t m = gt | te; m; m &= m - 1) {
                     const int32_t id = (int32_t)(blk * 32 + __ffs(m) - 1);
                     // the row (or record) is read in P4, a cluster barrier later: start it now
-                    if (a.rsq) {
+                    if (EXT && a.rsq) {
                         constexpr int RBQ = 6 * (D / 8);
                         const uint8_t *rp = a.rsq + ((size_t)u * a.cap + id) * RBQ;
                         prefetch_l2_line(rp);
@@ -642,7 +645,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         sMisc[M_KMAX] = 0;
         sMisc[M_AOWN] = 0;
     }
-    if (a.rsq) {
+    if (EXT && a.rsq) {
         // Calibrated estimate from the records, no K rows: lane gl of a
         // half-warp is block slot gl (slots past d/8 add +0), zq of its block
         // is in sQbar; e = fma chain over the block's 8 coordinates of
@@ -1117,19 +1120,16 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
 }
 
 // ------------------------------------------------------------------ host side
+//
+// This file is compiled twice: as itself (the common kernels, EXT = false,
+// and the host code) and through kvr_select_ext.cu with KVR_SELECT_EXT_TU
+// defined (only the EXT = true kernels and their launcher), so the two sets
+// of instantiations build in parallel.
 
-int select_cluster_size(int U, int C)
-{
-    int cs = 16;
-    while (cs > 1 && (int64_t)U * cs > 2 * 152) cs >>= 1;
-    while (cs < 16 && (int64_t)cs * kMaxSlice < C) cs <<= 1;
-    return cs;
-}
-
-template <int D, typename T, int VB>
+template <int D, typename T, int VB, bool EXT>
 static kvr_status launch_select_t(const LaunchCtx &c, const SelArgs &a, int cs)
 {
-    auto kern = select_kernel<D, T, VB>;
+    auto kern = select_kernel<D, T, VB, EXT>;
     const int smem = SelSmem<D, T>::bytes;
     kvr_status st = prepare_cluster_kernel(reinterpret_cast<const void *>(kern), smem);
     if (st != KVR_OK) return st;
@@ -1151,15 +1151,46 @@ static kvr_status launch_select_t(const LaunchCtx &c, const SelArgs &a, int cs)
     return check_launch();
 }
 
-template <int D, typename T>
+template <int D, typename T, bool EXT>
 static kvr_status launch_select_vb(const LaunchCtx &c, const SelArgs &a, int cs, int vb)
 {
     switch (vb) {
-    case 1: return launch_select_t<D, T, 1>(c, a, cs);
-    case 2: return launch_select_t<D, T, 2>(c, a, cs);
-    case 3: return launch_select_t<D, T, 3>(c, a, cs);
-    default: return launch_select_t<D, T, 4>(c, a, cs);
+    case 1: return launch_select_t<D, T, 1, EXT>(c, a, cs);
+    case 2: return launch_select_t<D, T, 2, EXT>(c, a, cs);
+    case 3: return launch_select_t<D, T, 3, EXT>(c, a, cs);
+    default: return launch_select_t<D, T, 4, EXT>(c, a, cs);
     }
+}
+
+template <bool EXT>
+static kvr_status launch_select(const LaunchCtx &c, const SelArgs &a, int cs, int vb)
+{
+    const bool bf = c.shape.dtype == KVR_BF16;
+    if (c.shape.d == 128)
+        return bf ? launch_select_vb<128, __nv_bfloat16, EXT>(c, a, cs, vb)
+                  : launch_select_vb<128, float, EXT>(c, a, cs, vb);
+    return bf ? launch_select_vb<64, __nv_bfloat16, EXT>(c, a, cs, vb)
+              : launch_select_vb<64, float, EXT>(c, a, cs, vb);
+}
+
+#ifdef KVR_SELECT_EXT_TU
+
+kvr_status select_launch_ext(const LaunchCtx &c, const SelArgs &a, int cs, int vb)
+{
+    return launch_select<true>(c, a, cs, vb);
+}
+
+#else
+
+// defined in the KVR_SELECT_EXT_TU compilation of this file
+kvr_status select_launch_ext(const LaunchCtx &c, const SelArgs &a, int cs, int vb);
+
+int select_cluster_size(int U, int C)
+{
+    int cs = 16;
+    while (cs > 1 && (int64_t)U * cs > 2 * 152) cs >>= 1;
+    while (cs < 16 && (int64_t)cs * kMaxSlice < C) cs <<= 1;
+    return cs;
 }
 
 kvr_status select_dispatch(const LaunchCtx &c, const kvr_select_params &p, const SelectPlan &plan,
@@ -1213,12 +1244,10 @@ kvr_status select_dispatch(const LaunchCtx &c, const kvr_select_params &p, const
         if (st != KVR_OK) return st;
     }
     const int cs = select_cluster_size(c.shape.B * c.shape.Hkv, p.C);
-    const bool bf = c.shape.dtype == KVR_BF16;
-    if (c.shape.d == 128)
-        return bf ? launch_select_vb<128, __nv_bfloat16>(c, a, cs, vb)
-                  : launch_select_vb<128, float>(c, a, cs, vb);
-    return bf ? launch_select_vb<64, __nv_bfloat16>(c, a, cs, vb)
-              : launch_select_vb<64, float>(c, a, cs, vb);
+    if (a.rsq || a.votes) return select_launch_ext(c, a, cs, vb);
+    return launch_select<false>(c, a, cs, vb);
 }
+
+#endif  // KVR_SELECT_EXT_TU
 
 }  // namespace kvr
