@@ -270,3 +270,32 @@ def test_attend_many_segments_long_list():
     for h in (0, 5):
         sl = slice(4 * h, 4 * h + 4)
         assert np.max(np.abs(out[:, sl] - ref[:, sl])) <= ATOL
+
+
+@pytest.mark.parametrize("C,k", [(4096, 1000), (6000, 5999)])
+def test_select_massive_ties_take_the_all_keys_path(C, k):
+    """More than 2048 candidates share the boundary score bin (identical
+    keys): the selection falls back to every CTA gathering all C' scores;
+    ties still go to the lowest indices, bit-exact with the oracle."""
+    d = 64
+    row = torch.randn(d)
+    K = row.expand(1, 2, 9000, d).clone()
+    q = torch.randn(1, 4, d)
+    params = kvr.SelectParams(C, k, 64)
+    res, out = run_and_compare(K, q, [9000], params, wl.srht_signs(d))
+    for u in range(2):
+        assert list(res["idx"][0, u]) == list(range(k))
+    assert res["err"] == 0
+
+
+def test_select_near_ties_across_the_boundary_bin():
+    """Keys on a handful of distinct score levels with thousands per level:
+    the boundary bin holds more than 2048 keys of several exact scores."""
+    d, N = 64, 12000
+    g = torch.Generator().manual_seed(5)
+    base = torch.randn(4, d, generator=g)
+    K = base[torch.randint(0, 4, (N,), generator=g)].reshape(1, 1, N, d).contiguous()
+    q = torch.randn(1, 2, d, generator=g)
+    params = kvr.SelectParams(8000, 3000, 64)
+    res, out = run_and_compare(K, q, [N], params, wl.srht_signs(d))
+    assert res["err"] == 0
