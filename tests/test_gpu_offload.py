@@ -98,3 +98,55 @@ def test_host_resident_cache_matches_oracle_and_device_cache(rerank):
             assert host["cnt"][b, h] == rc and np.array_equal(host["idx"][b, h], ri), (b, h)
             ref = oracle.attend_unit(qg, Ku, oracle.f32(V[b, h, :N]), N, ri[:rc], rc, w.W, scale)
             assert np.abs(host["out"][b, h * w.G:(h + 1) * w.G] - ref).max() <= ATOL, (b, h)
+
+
+def test_host_resident_cache_with_regions_and_records():
+    """The one-call step over a host-resident cache with reranker records and
+    cache regions equals the same step over the device-resident cache, and the
+    oracle's selection and attention over the regions."""
+    seq0 = [7000, 5000]
+    w = wl.Workload("offreg", B=2, Hq=8, Hkv=2, d=128, N=max(seq0) + 1, dtype="bf16", C=1024,
+                    k=256, W=128, rank=32, planted=16, seed=72)
+    K, V, q = wl.make_cache(w, device="cpu", cap=7200, seq_len=[n + 1 for n in seq0])
+    sgn = wl.srht_signs(w.d)
+    sgn_d, qd = sgn.to(DEV), q.to(DEV)
+    S, L, U = 4, 128, 32
+    runs = []
+    for Kx, Vx in ((pinned(K), pinned(V)), (K.to(DEV), V.to(DEV))):
+        shape = kvr.Shape.of(Kx, qd)
+        codes = kvr.codes_buffer(shape, DEV)
+        rec = kvr.rsq_buffer(Kx)
+        p0 = torch.zeros(2, dtype=torch.int32, device=DEV)
+        kvr.kvr_encode_keys(Kx, p0, 7000, sgn_d, codes)
+        kvr.kvr_encode_rsq(Kx, p0, 7000, sgn_d, rec)
+        seq = torch.tensor([n + 1 for n in seq0], dtype=torch.int32, device=DEV)
+        rend = torch.zeros(2, dtype=torch.int32, device=DEV)
+        kvr.kvr_regions_update(seq, S, L, U, rend, init=True)
+        params = kvr.SelectParams(w.C, w.k, 0, w.lut, rsq_records=rec, sink=S, region_end=rend)
+        ws = kvr.workspace(kvr.kvr_select_workspace_size(shape, params))
+        idx = torch.empty((2, 2, w.k), dtype=torch.int32, device=DEV)
+        cnt = torch.empty((2, 2), dtype=torch.int32, device=DEV)
+        out = torch.empty(qd.shape, dtype=torch.float32, device=DEV)
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        pos = torch.tensor(seq0, dtype=torch.int32, device=DEV)
+        kvr.kvr_decode_step(qd, Kx, Vx, codes, seq, pos, sgn_d, params, idx, cnt,
+                            1 / math.sqrt(w.d), out, ws, err)
+        torch.cuda.synchronize()
+        assert kvr.kvr_read_error(err) == 0
+        runs.append((idx.cpu().numpy(), cnt.cpu().numpy(), out.cpu().numpy(),
+                     rend.cpu().tolist()))
+    for a, b in zip(runs[0], runs[1]):
+        assert np.array_equal(np.asarray(a), np.asarray(b))
+    idx, cnt, out, rl = runs[0]
+    sg = sgn.numpy()
+    for b in range(2):
+        N = seq0[b] + 1
+        for h in range(2):
+            Ku = oracle.f32(K[b, h, :N])
+            qg = q[b, h * 4:(h + 1) * 4]
+            ri, rc = oracle.select_unit_regions(qg, Ku, oracle.encode(Ku, sg), N, S, rl[b], sg,
+                                                w.C, w.k, w.lut, rec_unit=oracle.rsq_encode(Ku, sg))
+            assert cnt[b, h] == rc and np.array_equal(idx[b, h], ri), (b, h)
+            ref = oracle.attend_unit_regions(qg, Ku, oracle.f32(V[b, h, :N]), N, S, rl[b], ri[:rc],
+                                             rc, np.float32(1 / math.sqrt(w.d)))
+            assert np.abs(out[b, h * 4:(h + 1) * 4] - ref).max() <= ATOL
