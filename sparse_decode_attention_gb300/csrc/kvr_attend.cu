@@ -228,24 +228,27 @@ __global__ void __launch_bounds__(AttCfg<D, T, G>::kThreads, (G >= 16) ? 1 : 2) 
             const int32_t *tok = sTok + (bi * TOK - c0);
             const uint8_t *buf = smem + (bi & 1) * CF::kBatchBytes;
             const int rows = min(TOK, n - bi * TOK);
+            // Branch-free over the warp's TPW slots (j < TOK: always inside the
+            // buffer), so the slots' shuffle chains interleave; a slot past the
+            // batch or of a skipped token scores -inf and adds nothing below.
             float s[TPW];
+            bool live[TPW];
 #pragma unroll
             for (int jj = 0; jj < TPW; jj++) {
                 const int j = warp + jj * kAttWarps;
-                s[jj] = -INFINITY;
-                if (j < rows && tok[j] >= 0) {  // warp-uniform
-                    float kv[E];
-                    load_lane<E, T>(buf + j * RB, lane, kv);
-                    float part[G];
+                live[jj] = j < rows && tok[j] >= 0;  // warp-uniform
+                float kv[E];
+                load_lane<E, T>(buf + j * RB, lane, kv);
+                float part[G];
 #pragma unroll
-                    for (int g = 0; g < G; g++) {
-                        float d = 0.0f;
+                for (int g = 0; g < G; g++) {
+                    float d = 0.0f;
 #pragma unroll
-                        for (int e = 0; e < E; e++) d = fmaf(qr[g][e], kv[e], d);
-                        part[g] = d;
-                    }
-                    s[jj] = reduce_heads<G>(part, lane);
+                    for (int e = 0; e < E; e++) d = fmaf(qr[g][e], kv[e], d);
+                    part[g] = d;
                 }
+                const float sc = reduce_heads<G>(part, lane);
+                s[jj] = live[jj] ? sc : -INFINITY;
             }
             float mb = -INFINITY;
 #pragma unroll
@@ -269,15 +272,15 @@ __global__ void __launch_bounds__(AttCfg<D, T, G>::kThreads, (G >= 16) ? 1 : 2) 
 #pragma unroll
             for (int jj = 0; jj < TPW; jj++) {
                 const int j = warp + jj * kAttWarps;
-                if (j < rows && tok[j] >= 0) {
-                    float vv[E];
-                    load_lane<E, T>(buf + (TOK + j) * RB, lane, vv);
+                float vv[E];
+                load_lane<E, T>(buf + (TOK + j) * RB, lane, vv);
 #pragma unroll
-                    for (int g = 0; g < G; g++) {
-                        const float pg = __shfl_sync(kFull, p[jj], g * LPH);
+                for (int e = 0; e < E; e++) vv[e] = live[jj] ? vv[e] : 0.0f;  // stale rows may hold NaN
 #pragma unroll
-                        for (int e = 0; e < E; e++) acc[g][e] = fmaf(pg, vv[e], acc[g][e]);
-                    }
+                for (int g = 0; g < G; g++) {
+                    const float pg = __shfl_sync(kFull, p[jj], g * LPH);
+#pragma unroll
+                    for (int e = 0; e < E; e++) acc[g][e] = fmaf(pg, vv[e], acc[g][e]);
                 }
             }
             __syncthreads();

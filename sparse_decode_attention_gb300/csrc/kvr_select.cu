@@ -22,13 +22,14 @@
 //   P3 candidates are compacted in index order into the workspace and, via
 //      distributed shared memory, into the CTA that rescores them.
 //   P4 after a cluster barrier every CTA takes an equal slice of the candidate
-//      list, copies the K rows (cp.async, 16 threads per 256-byte row) into
-//      double-buffered shared memory and computes the canonical fp32 dot
-//      q_bar . k (half-warp per row).
+//      list, loads the K rows (prefetched into L2 in P3) straight into
+//      registers, 16 lanes per row and 8 rows in flight per half-warp, and
+//      computes the canonical fp32 dot q_bar . k (half-warp per row).
 //   P5 the k'-th largest exact score (order-preserving uint32 keys) in three
 //      small cluster exchanges: the score range, a 256-bin linear histogram
 //      of every CTA's slice over that range, then the keys of the one
-//      boundary bin, ranked by one warp (8-bit radix passes); a boundary bin
+//      boundary bin, located in one of 256 sub-bins of that bin and ranked
+//      there by counting (a few keys: directly); a boundary bin
 //      too large to gather (massive ties) falls back to every CTA gathering
 //      all C' keys. Each CTA also gets its output offset.
 //   P6 winners are written ascending by index.
@@ -173,7 +174,8 @@ __device__ __forceinline__ uint32_t pool_mask(int64_t blk, int64_t p0, int64_t p
 template <int D, typename T> struct SelSmem {
     static constexpr int kChunks = D / 4;             // 16-byte chunks (4 planes) per block
     static constexpr int kHalfBytes = kChunks * 256;  // 16 blocks = 512 tokens
-    // P1 code slots, P4 row buffers, P5 order keys of up to 16384 candidates
+    // P1 code slots; in P5 the published boundary keys and the keys of one
+    // sub-bin, or (massive ties) the order keys of up to 16384 candidates
     static constexpr int kRingBytes =
         (kSelWarps * kHalfBytes > 16384 * 4) ? kSelWarps * kHalfBytes : 16384 * 4;
     static constexpr int kRowBytes = D * (int)sizeof(T);
@@ -194,11 +196,12 @@ template <int D, typename T> struct SelSmem {
     static constexpr int oLev = oPl + 8 * kPlaneCap * 4;  // float [16] signed reranker levels
     static constexpr int bytes = oLev + 16 * 4;
     static_assert(16 * 256 * 4 <= kRingBytes, "radix exchange scratch must fit the ring");
+    static_assert(oWH % 16 == 0, "boundary keys are read 16 bytes at a time");
     static_assert((D / 8) * kVoteStride * 2 <= 2 * kMaxSlice * 4, "vote lists must fit sS + sI");
 };
 
 enum {
-    M_U1 = 0, M_REM1, M_T, M_TAKE, M_OFF, M_KTAKE, M_KOFF, M_DIGIT, M_BEFORE, M_KEYT, M_QUOTA,
+    M_U1 = 0, M_REM1, M_T, M_TAKE, M_OFF, M_KTAKE, M_KOFF, M_NSUB, M_KEYT, M_QUOTA,
     M_CNT, M_ABOVEB,
     M_BOUND = 16,  // [17] first candidate position of each CTA's P4 slice, then C'
     M_KMIN = 33, M_KMAX, M_GMIN, M_GMAX, M_AOWN,
@@ -592,6 +595,10 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         const int take = sMisc[M_TAKE];
         int allow = max(0, min(take - eq_before, n_eq));
         int pos = gt_before + min(take, eq_before) + sMisc[M_OFF];
+        // owner CTA of list position pos and its slice [s_lo, s_hi), advanced
+        // as pos grows (positions only increase)
+        int r2 = slice_owner(pos);
+        int s_lo = sMisc[M_BOUND + r2], s_hi = sMisc[M_BOUND + r2 + 1];
         for (int64_t blk = my0; blk < my1; blk++) {
             uint32_t p[ACC], gt = 0, eq = 0;
 #pragma unroll
@@ -617,8 +624,12 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
                     cidx[pos] = id;
                     // straight into the shared memory of the CTA whose P4
                     // slice [r*C'/CS, (r+1)*C'/CS) holds list position pos
-                    const int r2 = slice_owner(pos);
-                    *cluster.map_shared_rank(&sI[pos - sMisc[M_BOUND + r2]], r2) = id;
+                    while (r2 + 1 < CS && pos >= s_hi) {
+                        r2++;
+                        s_lo = s_hi;
+                        s_hi = sMisc[M_BOUND + r2 + 1];
+                    }
+                    *cluster.map_shared_rank(&sI[pos - s_lo], r2) = id;
                     pos++;
                 }
             }
@@ -885,8 +896,12 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     const float fmin = key_float((uint32_t)sMisc[M_GMIN]);
     float scale = 256.0f / (key_float((uint32_t)sMisc[M_GMAX]) - fmin);
     if (!(scale < INFINITY) || !(scale > 0.0f)) scale = 0.0f;  // one value, or no spread
+    // the position of a key in the linear bin map, in bin units; the bin is
+    // its integer part (clamped), a sub-bin of it 1/256 of that unit
+    // (rounded operations: never contracted, so every use maps a key alike)
+    auto lin_pos = [&](uint32_t key) { return __fmul_rn(__fsub_rn(key_float(key), fmin), scale); };
     auto lin_bin = [&](uint32_t key) {
-        const int x = (int)((key_float(key) - fmin) * scale);
+        const int x = (int)lin_pos(key);
         return min(255, max(0, x));
     };
     // (2) this slice's linear histogram
@@ -969,23 +984,60 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
             }
             if (tid < 3) sScan[tid] = 0;
             __syncthreads();
-            if (NB <= kSelThreads) {
-                // rank by counting: thread t ranks key t against all NB keys
-                if (tid < NB) {
-                    const uint32_t k = sB[tid];
-                    int gt = 0, eq = 0;
-                    for (int j = 0; j < NB; j++) {
-                        const uint32_t kj = sB[j];
+            // rank by counting: thread t < nk ranks keys[t] against all nk keys
+            // (keys 16-byte aligned); the copy of the rk-th largest key sets it
+            auto rank_count = [&](const uint32_t *keys, int nk, int rk) {
+                if (tid < nk) {
+                    const uint32_t k = keys[tid];
+                    int gt = 0, eq = 0, j = 0;
+                    // independent 16-byte broadcast loads, several in flight
+#pragma unroll 4
+                    for (; j + 4 <= nk; j += 4) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(keys + j);
+                        gt += (int)(v.x > k) + (int)(v.y > k) + (int)(v.z > k) + (int)(v.w > k);
+                        eq += (int)(v.x == k) + (int)(v.y == k) + (int)(v.z == k) + (int)(v.w == k);
+                    }
+                    for (; j < nk; j++) {
+                        const uint32_t kj = keys[j];
                         gt += kj > k;
                         eq += kj == k;
                     }
-                    if (gt < rem && rem <= gt + eq) {  // every copy of the key agrees
+                    if (gt < rk && rk <= gt + eq) {  // every copy of the key agrees
                         sMisc[M_KEYT] = (int)k;
-                        sMisc[M_QUOTA] = rem - gt;
+                        sMisc[M_QUOTA] = rk - gt;
                     }
                 }
-            } else if (warp == 0) {
-                radix_warp(sB, NB, rem);
+            };
+            if (NB <= 32) {
+                rank_count(sB, NB, rem);
+            } else {
+                // 256 sub-bins of the boundary bin (a monotone refinement of
+                // the bin map): the sub-bin of the k'-th key, then its keys
+                // gathered and ranked by counting (past 256 of them, by one
+                // warp's radix passes). The unit's histogram in sRad + 256 has
+                // been read; the gathered keys follow the published ones.
+                int *sSub = sRad + 256;
+                uint32_t *sC = reinterpret_cast<uint32_t *>(ring) + kMaxSlice;
+                auto sub_bin = [&](uint32_t key) {
+                    const int x = (int)__fmul_rn(__fsub_rn(lin_pos(key), (float)b_lin), 256.0f);
+                    return min(255, max(0, x));
+                };
+                sSub[tid] = 0;
+                if (tid == 0) sMisc[M_NSUB] = 0;
+                __syncthreads();
+                for (int t = tid; t < NB; t += kSelThreads) atomicAdd(&sSub[sub_bin(sB[t])], 1);
+                __syncthreads();
+                int sbin, sabove;
+                find_bin_in(sSub, rem, sbin, sabove);
+                const int rem2 = rem - sabove;
+                for (int t = tid; t < NB; t += kSelThreads) {
+                    const uint32_t k = sB[t];
+                    if (sub_bin(k) == sbin) sC[atomicAdd(&sMisc[M_NSUB], 1)] = k;
+                }
+                __syncthreads();
+                const int NC = sMisc[M_NSUB];
+                if (NC <= kSelThreads) rank_count(sC, NC, rem2);
+                else if (warp == 0) radix_warp(sC, NC, rem2);
             }
             __syncthreads();
             keyT = (uint32_t)sMisc[M_KEYT];

@@ -299,3 +299,40 @@ def test_select_near_ties_across_the_boundary_bin():
     params = kvr.SelectParams(8000, 3000, 64)
     res, out = run_and_compare(K, q, [N], params, wl.srht_signs(d))
     assert res["err"] == 0
+
+
+def dense_band_case(band, seed=3):
+    """Keys that are positive multiples of one unit vector u, queries equal to
+    u: every code ties (the candidates are the lowest pool positions) and the
+    exact score of key i is about s_i. s: one key at 1000 and one at 1 span the
+    range; 546 keys in [600, 900]; the rest form a band inside one 256th of
+    the range, which therefore holds the k-th largest (k = 700) and hundreds
+    of keys."""
+    d, N = 64, 4000
+    g = np.random.default_rng(seed)
+    u = g.standard_normal(d).astype(np.float32)
+    u /= np.linalg.norm(u)
+    nb = 2048 - 2 - 546
+    if band == "spread":
+        b = g.uniform(500.0, 501.5, nb)
+    elif band == "identical":
+        b = np.full(nb, 500.5)
+    else:  # "levels<L>": L distinct scores, each repeated
+        L = int(band[len("levels"):])
+        b = 500.0 + 0.15 * g.integers(0, L, nb)
+    s = np.concatenate([[1000.0, 1.0], g.uniform(600.0, 900.0, 546), b])
+    s = np.concatenate([s[:2], g.permutation(s[2:]), g.uniform(1.0, 1000.0, N - 2048)])
+    K = torch.from_numpy((s[:, None] * u[None, :]).astype(np.float32)).reshape(1, 1, N, d)
+    q = torch.from_numpy(np.stack([u, u])).reshape(1, 2, d)
+    return K, q, N
+
+
+@pytest.mark.parametrize("band", ["spread", "identical", "levels10", "levels3"])
+def test_select_dense_boundary_bin(band):
+    """Hundreds of candidates in the boundary score bin: their sub-bin
+    refinement, ranking by counting or by radix passes (ties inside a
+    sub-bin), bit-exact with the oracle."""
+    K, q, N = dense_band_case(band)
+    params = kvr.SelectParams(2048, 700, 64)
+    res, out = run_and_compare(K, q, [N], params, wl.srht_signs(64))
+    assert res["err"] == 0
