@@ -138,6 +138,22 @@ __global__ void __launch_bounds__(AttCfg<D, T, G>::kThreads, (G >= 16) ? 1 : 2) 
     const int u = blockIdx.y;
     const int b = u / a.Hkv, hk = u % a.Hkv;
 
+    // The selection normally returns kmax indices and the window is full: the
+    // slice's index reads are issued on that assumption together with the
+    // length and count reads (one round trip instead of two), and used only
+    // if the token count confirms it (Sink and region runs load after).
+    const bool spec = !a.region_end && a.sink <= 0;
+    const int64_t nT_s = (int64_t)a.kmax + a.W;
+    const int64_t lo_s = (int64_t)rank * nT_s / CS, hi_s = (int64_t)(rank + 1) * nT_s / CS;
+    constexpr int SPN = (CF::kChunk + kAttThreads - 1) / kAttThreads;
+    int32_t sp[SPN];
+#pragma unroll
+    for (int i = 0; i < SPN; i++) {
+        const int64_t p = lo_s + tid + (int64_t)i * kAttThreads;
+        sp[i] = (spec && tid + i * kAttThreads < CF::kChunk && p < hi_s && p < a.kmax)
+                    ? a.idx[(size_t)u * a.kmax + p]
+                    : -1;
+    }
     int64_t N = a.seq_len[b];
     if (N < 0 || N > a.cap) {
         if (rank == 0 && tid == 0 && hk == 0) set_err(a.err, KVR_DEVERR_SEQ_LEN);
@@ -157,14 +173,18 @@ __global__ void __launch_bounds__(AttCfg<D, T, G>::kThreads, (G >= 16) ? 1 : 2) 
     const uint8_t *Vu = static_cast<const uint8_t *>(a.V) + (size_t)u * a.cap * RB;
     constexpr int PPR = RB / 16;
     constexpr int CH = CF::kChunk;
+    const bool spec_ok = spec && nT == nT_s;  // then lo, hi and cnt are as assumed
     // token ids of the slice positions [c0, c0 + CH), loaded at once (-1 = skip)
     auto load_ids = [&](int c0) {
         const int cn = min(CH, n - c0);
-        for (int j = tid; j < cn; j += kAttThreads) {
+#pragma unroll
+        for (int i = 0; i < SPN; i++) {
+            const int j = tid + i * kAttThreads;
+            if (j >= cn) break;
             const int64_t p = lo + c0 + j;
             int32_t t;
             if (p < cnt) {
-                t = a.idx[(size_t)u * a.kmax + p];
+                t = (spec_ok && c0 == 0) ? sp[i] : a.idx[(size_t)u * a.kmax + p];
                 if (t < p0 || t >= w0) {
                     set_err(a.err, KVR_DEVERR_INDEX);
                     t = -1;

@@ -324,18 +324,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         cp_async_commit();
     };
     if (hh < h1) issue_half(hh);
-    // The half-tiles copied in later rounds: start them into L2 now (up to 32
-    // ahead), so each later copy waits on L2 rather than on DRAM. Whole tiles,
-    // one 128-byte line per prefetch.
-    if (Cp > 0 || a.coarse != nullptr) {
-        const int64_t pf0 = h0 + kSelWarps, pf1 = min(h1, h0 + kSelWarps + 32);
-        if (pf0 < pf1) {
-            const uint8_t *pbase = codes_u + (size_t)(pf0 >> 1) * (D * 128);
-            const int64_t pbytes = (((pf1 + 1) >> 1) - (pf0 >> 1)) * (int64_t)(D * 128);
-            for (int64_t o = (int64_t)tid * 128; o < pbytes; o += (int64_t)kSelThreads * 128)
-                prefetch_l2_line(pbase + o);
-        }
-    }
     if (a.early) grid_dependency_wait();  // q may come from the previous grid
     if (EXT && a.votes) {
         // this unit's vote lists (written by the previous grid) into the
@@ -400,6 +388,19 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
 #pragma unroll
         for (int m = 0; m < 9; m++) L[j][m] = ((a.leaf[j] >> m) & 1u) ? 0xffffffffu : 0u;
     __syncthreads();
+    // The half-tiles copied in later rounds: start them into L2 now (up to 32
+    // ahead), so each later copy waits on L2 rather than on DRAM. Whole tiles,
+    // one 128-byte line per prefetch. Issued after the query load, which
+    // they would otherwise queue ahead of.
+    if (Cp > 0 || a.coarse != nullptr) {
+        const int64_t pf0 = h0 + kSelWarps, pf1 = min(h1, h0 + kSelWarps + 32);
+        if (pf0 < pf1) {
+            const uint8_t *pbase = codes_u + (size_t)(pf0 >> 1) * (D * 128);
+            const int64_t pbytes = (((pf1 + 1) >> 1) - (pf0 >> 1)) * (int64_t)(D * 128);
+            for (int64_t o = (int64_t)tid * 128; o < pbytes; o += (int64_t)kSelThreads * 128)
+                prefetch_l2_line(pbase + o);
+        }
+    }
 
     // ---------------------------------------------------------------- P1
     int cnt1[NL1];
