@@ -43,14 +43,17 @@ def peaks():
         return 6800.0, "fallback"
 
 
-def measured_traffic(kernel):
-    """DRAM bytes per launch of `kernel` from the ncu capture recorded in
-    profiles/traffic.json, or None when the kernel's sources have changed
-    since that capture (the counters then describe another kernel)."""
+def measured_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from the ncu capture
+    recorded in profiles/traffic.json, or None when that kernel was captured
+    on another workload or its sources have changed since the capture (the
+    counters then describe another launch)."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)[kernel]
+        if rec["workload"] != workload:
+            return None
         m = hashlib.sha256()
         for name in rec["sources"]:
             with open(os.path.join(ROOT, "sparse_decode_attention_gb300", "csrc", name), "rb") as f:
@@ -437,15 +440,17 @@ def run_gpu(args, w):
     if rank != 0:
         return
     ab = algorithmic_bytes(w, rerank)
-    # the reranking select reads records, not K rows: its own counters
-    sel_key = "select_kernel_rsq" if rerank == "rsq" else "select_kernel"
+    # the reranking select reads records, not K rows, and the magnitude votes
+    # run the optional-mode kernels: each its own counters
+    sel_key = ("select_kernel_rsq" if rerank == "rsq" else
+               "select_kernel_mag" if args.votes == "magnitude" else "select_kernel")
     peak, peak_kind = peaks()
     roof = None
     if avg["select"]:
         ach = ab["select"] / (avg["select"] * 1e-3) / 1e9
         roof = {"bound": "hbm", "kernel": "select_kernel (kvr_select, one launch)",
                 "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-                "peak_kind": peak_kind, "traffic": measured_traffic(sel_key),
+                "peak_kind": peak_kind, "traffic": measured_traffic(sel_key, w.name),
                 "algorithmic_bytes": ab["select"], "avg_ms": avg["select"]}
     path = None
     if avg["select"] and avg["attend"]:
@@ -454,10 +459,10 @@ def run_gpu(args, w):
         path = {"calls": "kvr_select + kvr_sparse_attend", "achieved": ach, "peak": peak,
                 "unit": "GB/s", "frac": ach / peak, "frac_of_8TBs": ach / 8000.0,
                 "us": tsum * 1e6, "algorithmic_bytes": ab["select"] + ab["attend"],
-                "traffic": (None if host or None in (measured_traffic(sel_key),
-                                                     measured_traffic("attend_kernel"))
-                            else measured_traffic(sel_key)
-                            + measured_traffic("attend_kernel")),
+                "traffic": (None if host or None in (measured_traffic(sel_key, w.name),
+                                                     measured_traffic("attend_kernel", w.name))
+                            else measured_traffic(sel_key, w.name)
+                            + measured_traffic("attend_kernel", w.name)),
                 "attend_us": avg["attend"] * 1e3, "encode_us": avg["encode"] * 1e3}
     link = None
     if host and avg["attend"]:
@@ -757,7 +762,7 @@ def run_gpu_tiered(args, w):
         "roofline": {"bound": "hbm", "kernel": "tiered_attend_kernel + tiered_combine_kernel "
                      "(kvr_sparse_attend_tiered)", "achieved": ach, "peak": peak,
                      "unit": "GB/s", "frac": ach / peak, "peak_kind": peak_kind,
-                     "traffic": measured_traffic("tiered_attend_kernel"),
+                     "traffic": measured_traffic("tiered_attend_kernel", w.name),
                      "algorithmic_bytes": ab, "avg_ms": att_ms},
         "tier_update_us": upd_ms * 1e3, "windows_bf16_int2_per_unit": [n_bf, n_q],
         "moves_last_step": {"promotions": st_tot[0], "demotions": st_tot[1],
