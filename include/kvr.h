@@ -276,12 +276,19 @@ kvr_status kvr_select(const kvr_shape *shape, const kvr_select_params *p, const 
 /*
  * kvr_decode_step -- one decode step of every unit in one call: the code
  * (and, with p->rsq_records, the reranker record) of the appended key at row
- * pos_new[b], then kvr_select, then the attention over its output (over the
- * cache regions when p->region_end is set, else over the top-k and the
- * window W), all enqueued on `stream` in that order. Arguments as in those
- * calls; out_idx must hold p->k entries per unit; the attention needs no
- * workspace. KVR_SELECT_EARLY_INPUTS is ignored (the selection follows the
- * encode that writes its codes). Validation errors of any part are returned
+ * pos_new[b], kvr_select, and the attention over its output (over the cache
+ * regions when p->region_end is set, else over the top-k and the window W),
+ * all enqueued on `stream`. Order: with p->region_end set or W == 0, the
+ * encodes first, then the selection (KVR_SELECT_EARLY_INPUTS is ignored: it
+ * follows the encode that writes its codes), then the attention. With W >= 1
+ * and no regions the appended key must lie in the window,
+ * pos_new[b] >= seq_len[b] - W (the decode case: pos_new[b] = seq_len[b] - 1),
+ * where the selection reads no code or record; the selection and attention
+ * come first (KVR_SELECT_EARLY_INPUTS as in kvr_select) and the encodes run
+ * beside the attention, finishing after it, so work enqueued after this call
+ * follows all of it; a key before the window sets KVR_DEVERR_POSITION.
+ * Arguments as in those calls; out_idx must hold p->k entries per unit; the
+ * attention needs no workspace. Validation errors of any part are returned
  * before that part is enqueued; the parts before it stay enqueued.
  */
 kvr_status kvr_decode_step(const kvr_shape *shape, const kvr_select_params *p, const void *q,

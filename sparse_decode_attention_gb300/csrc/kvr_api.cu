@@ -264,24 +264,39 @@ kvr_status kvr_decode_step(const kvr_shape *shape, const kvr_select_params *p, c
     if (!V || !aligned16(V) || !aligned16(out)) return KVR_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(pos_new) & 3u) != 0) return KVR_ERR_INVALID_ARG;
     if (workspace_bytes < plan_select(*shape, *p).bytes) return KVR_ERR_WORKSPACE;
-    // the appended key's code is written by the first launch: the selection
-    // must not start on its inputs early
+    // the appended key's code and record, checked here with the rest
+    if (!K || !srht_sign || !codes || !aligned16(K) || !aligned16(codes)) return KVR_ERR_INVALID_ARG;
+    uint8_t *records = const_cast<uint8_t *>(p->rsq_records);
+    LaunchCtx c{*shape, static_cast<cudaStream_t>(stream)};
+    // With a window (W >= 1, no regions) the appended key lies in it, where
+    // the step's selection reads no code or record: they are written after
+    // the attention, beside it (the encodes wait for the attention before
+    // they finish). Otherwise they come first and the selection must not
+    // start on its inputs early.
+    const bool late = !p->region_end && p->W >= 1;
     kvr_select_params ps = *p;
-    ps.flags &= ~KVR_SELECT_EARLY_INPUTS;
-    if ((st = kvr_encode_keys(shape, K, pos_new, 1, srht_sign, codes, err_word, stream)) != KVR_OK)
-        return st;
-    if (p->rsq_records &&
-        (st = kvr_encode_rsq(shape, K, pos_new, 1, srht_sign, const_cast<uint8_t *>(p->rsq_records),
-                             err_word, stream)) != KVR_OK)
-        return st;
+    if (!late) {
+        ps.flags &= ~KVR_SELECT_EARLY_INPUTS;
+        if ((st = encode_dispatch(c, K, pos_new, 1, srht_sign, codes, err_word)) != KVR_OK) return st;
+        if (records &&
+            (st = rsq_encode_dispatch(c, K, pos_new, 1, srht_sign, records, err_word)) != KVR_OK)
+            return st;
+    }
     if ((st = kvr_select(shape, &ps, q, K, codes, seq_len, srht_sign, out_idx, out_count, workspace,
                          workspace_bytes, err_word, stream)) != KVR_OK)
         return st;
     if (p->region_end)
         return kvr_sparse_attend_regions(shape, q, K, V, out_idx, p->k, out_count, seq_len, p->sink,
                                          p->region_end, scale, out, nullptr, 0, err_word, stream);
-    return kvr_sparse_attend(shape, q, K, V, out_idx, p->k, out_count, seq_len, p->W, scale, out,
-                             nullptr, 0, err_word, stream);
+    if ((st = kvr_sparse_attend(shape, q, K, V, out_idx, p->k, out_count, seq_len, p->W, scale, out,
+                                nullptr, 0, err_word, stream)) != KVR_OK)
+        return st;
+    if ((st = encode_dispatch(c, K, pos_new, 1, srht_sign, codes, err_word, seq_len, p->W)) != KVR_OK)
+        return st;
+    if (records && (st = rsq_encode_dispatch(c, K, pos_new, 1, srht_sign, records, err_word, true)) !=
+                       KVR_OK)
+        return st;
+    return KVR_OK;
 }
 
 size_t kvr_attend_workspace_size(const kvr_shape *shape, int kmax, int W)

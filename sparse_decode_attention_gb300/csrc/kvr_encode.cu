@@ -23,10 +23,11 @@
 namespace kvr {
 
 template <int D, typename T>
-__global__ void __launch_bounds__(256)
-encode_kernel(const T *__restrict__ K, int Hkv, int64_t cap, int64_t tiles,
-              const int32_t *__restrict__ pos0, int n_new, int64_t units, int blocks_per_unit,
-              const int8_t *__restrict__ sgn, uint8_t *__restrict__ codes, int32_t *err)
+__device__ __forceinline__ void encode_body(const T *__restrict__ K, int Hkv, int64_t cap,
+                                            int64_t tiles, const int32_t *__restrict__ pos0,
+                                            int n_new, int64_t units, int blocks_per_unit,
+                                            const int8_t *__restrict__ sgn,
+                                            uint8_t *__restrict__ codes, int32_t *err)
 {
     constexpr int E = Elem<T>::kVec;  // elements per lane
     constexpr int L = D / E;          // lanes per row
@@ -115,30 +116,68 @@ encode_kernel(const T *__restrict__ K, int Hkv, int64_t cap, int64_t tiles,
     }
 }
 
+// LATE: launched after a decode step's attention as its programmatic
+// dependent, so it runs beside it; before finishing it waits for that grid,
+// so whatever follows on the stream still follows the attention. The key
+// must lie in the window [seq_len - W, seq_len), which the step's selection
+// does not read; a key before it sets KVR_DEVERR_POSITION.
+template <int D, typename T, bool LATE>
+__global__ void __launch_bounds__(256)
+encode_kernel(const T *__restrict__ K, int Hkv, int64_t cap, int64_t tiles,
+              const int32_t *__restrict__ pos0, int n_new, int64_t units, int blocks_per_unit,
+              const int8_t *__restrict__ sgn, uint8_t *__restrict__ codes, int32_t *err,
+              const int32_t *__restrict__ seq_len, int W)
+{
+    encode_body<D, T>(K, Hkv, cap, tiles, pos0, n_new, units, blocks_per_unit, sgn, codes, err);
+    if constexpr (LATE) {
+        if (blockIdx.x == 0)
+            for (int64_t b = threadIdx.x; b < units / Hkv; b += blockDim.x)
+                if ((int64_t)pos0[b] < (int64_t)seq_len[b] - W) set_err(err, KVR_DEVERR_POSITION);
+        grid_dependency_wait();
+    }
+}
+
 template <int D, typename T>
 static kvr_status launch_encode(const LaunchCtx &c, const void *K, const int32_t *pos0, int n_new,
-                                const int8_t *sgn, uint8_t *codes, int32_t *err)
+                                const int8_t *sgn, uint8_t *codes, int32_t *err,
+                                const int32_t *late_seq_len, int W)
 {
     const int64_t units = (int64_t)c.shape.B * c.shape.Hkv;
     const int bpu = (int)((n_new + 31) / 32 + 1);  // blocks a range of n_new tokens can touch
     const int64_t warps = units * bpu;
     const int64_t blocks = (warps + 7) / 8;
     const int64_t tiles = (c.shape.cap + 1023) / 1024;
-    encode_kernel<D, T><<<(unsigned)blocks, 256, 0, c.stream>>>(
-        static_cast<const T *>(K), c.shape.Hkv, c.shape.cap, tiles, pos0, n_new, units, bpu, sgn,
-        codes, err);
+    const T *Kt = static_cast<const T *>(K);
+    if (!late_seq_len) {
+        encode_kernel<D, T, false><<<(unsigned)blocks, 256, 0, c.stream>>>(
+            Kt, c.shape.Hkv, c.shape.cap, tiles, pos0, n_new, units, bpu, sgn, codes, err, nullptr, 0);
+        return check_launch();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, encode_kernel<D, T, true>, Kt, c.shape.Hkv, c.shape.cap, tiles, pos0,
+                           n_new, units, bpu, sgn, codes, err, late_seq_len, W) != cudaSuccess)
+        return KVR_ERR_CUDA;
     return check_launch();
 }
 
 kvr_status encode_dispatch(const LaunchCtx &c, const void *K, const int32_t *pos0, int n_new,
-                           const int8_t *sgn, uint8_t *codes, int32_t *err)
+                           const int8_t *sgn, uint8_t *codes, int32_t *err,
+                           const int32_t *late_seq_len, int W)
 {
     const bool bf = c.shape.dtype == KVR_BF16;
     if (c.shape.d == 128)
-        return bf ? launch_encode<128, __nv_bfloat16>(c, K, pos0, n_new, sgn, codes, err)
-                  : launch_encode<128, float>(c, K, pos0, n_new, sgn, codes, err);
-    return bf ? launch_encode<64, __nv_bfloat16>(c, K, pos0, n_new, sgn, codes, err)
-              : launch_encode<64, float>(c, K, pos0, n_new, sgn, codes, err);
+        return bf ? launch_encode<128, __nv_bfloat16>(c, K, pos0, n_new, sgn, codes, err, late_seq_len, W)
+                  : launch_encode<128, float>(c, K, pos0, n_new, sgn, codes, err, late_seq_len, W);
+    return bf ? launch_encode<64, __nv_bfloat16>(c, K, pos0, n_new, sgn, codes, err, late_seq_len, W)
+              : launch_encode<64, float>(c, K, pos0, n_new, sgn, codes, err, late_seq_len, W);
 }
 
 }  // namespace kvr

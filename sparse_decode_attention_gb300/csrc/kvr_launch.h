@@ -64,8 +64,11 @@ struct AttendPlan {
 };
 AttendPlan plan_attend(const kvr_shape &s, int kmax, int W);
 
+// late_seq_len != null: the decode step's late form (after the attention, as
+// its programmatic dependent; the keys must lie in the window of width W).
 kvr_status encode_dispatch(const LaunchCtx &c, const void *K, const int32_t *pos0, int n_new,
-                           const int8_t *sgn, uint8_t *codes, int32_t *err);
+                           const int8_t *sgn, uint8_t *codes, int32_t *err,
+                           const int32_t *late_seq_len = nullptr, int W = 0);
 
 kvr_status select_dispatch(const LaunchCtx &c, const kvr_select_params &p, const SelectPlan &plan,
                            const void *q, const void *K, const uint8_t *codes,
@@ -91,7 +94,7 @@ struct RsqTables {
 };
 const RsqTables &rsq_tables();
 kvr_status rsq_encode_dispatch(const LaunchCtx &c, const void *K, const int32_t *pos0, int n_new,
-                               const int8_t *sgn, uint8_t *rec, int32_t *err);
+                               const int8_t *sgn, uint8_t *rec, int32_t *err, bool late = false);
 
 // Tiered window cache (kvr_tiers.cu).
 bool tier_shape_ok(const kvr_shape &s, int64_t n_win);

@@ -106,10 +106,11 @@ RsqTables make_tables()
 // the block's lanes in coordinate order. Word of the block: nibble j =
 // mag_j | sign_j << 3.
 template <int D, typename T>
-__global__ void __launch_bounds__(256)
-rsq_encode_kernel(const T *__restrict__ K, int Hkv, int64_t cap, const int32_t *__restrict__ pos0,
-                  int n_new, int64_t units, const int8_t *__restrict__ sgn, RsqTables tab,
-                  uint8_t *__restrict__ rec, int32_t *err)
+__device__ __forceinline__ void rsq_encode_body(const T *__restrict__ K, int Hkv, int64_t cap,
+                                                const int32_t *__restrict__ pos0, int n_new,
+                                                int64_t units, const int8_t *__restrict__ sgn,
+                                                const RsqTables &tab, uint8_t *__restrict__ rec,
+                                                int32_t *err)
 {
     constexpr int E = D / 32;       // coordinates per lane
     constexpr int LPB = kM / E;     // lanes per sub-block
@@ -188,6 +189,47 @@ rsq_encode_kernel(const T *__restrict__ K, int Hkv, int64_t cap, const int32_t *
     }
 }
 
+// LATE: the decode step's form, launched after the attention as its
+// programmatic dependent; it waits for that grid before finishing, so what
+// follows on the stream still follows the attention.
+template <int D, typename T, bool LATE>
+__global__ void __launch_bounds__(256)
+rsq_encode_kernel(const T *__restrict__ K, int Hkv, int64_t cap, const int32_t *__restrict__ pos0,
+                  int n_new, int64_t units, const int8_t *__restrict__ sgn, RsqTables tab,
+                  uint8_t *__restrict__ rec, int32_t *err)
+{
+    rsq_encode_body<D, T>(K, Hkv, cap, pos0, n_new, units, sgn, tab, rec, err);
+    if constexpr (LATE) grid_dependency_wait();
+}
+
+template <int D, typename T>
+kvr_status launch_rsq_encode(const LaunchCtx &c, const void *K, const int32_t *pos0, int n_new,
+                             int64_t units, int64_t blocks, const int8_t *sgn, uint8_t *rec,
+                             int32_t *err, bool late)
+{
+    const kvr_shape &s = c.shape;
+    const T *Kt = static_cast<const T *>(K);
+    const RsqTables &tab = rsq_tables();
+    if (!late) {
+        rsq_encode_kernel<D, T, false><<<(unsigned)blocks, 256, 0, c.stream>>>(
+            Kt, s.Hkv, s.cap, pos0, n_new, units, sgn, tab, rec, err);
+        return check_launch();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, rsq_encode_kernel<D, T, true>, Kt, s.Hkv, s.cap, pos0, n_new, units,
+                           sgn, tab, rec, err) != cudaSuccess)
+        return KVR_ERR_CUDA;
+    return check_launch();
+}
+
 }  // namespace
 
 const RsqTables &rsq_tables()
@@ -197,29 +239,19 @@ const RsqTables &rsq_tables()
 }
 
 kvr_status rsq_encode_dispatch(const LaunchCtx &c, const void *K, const int32_t *pos0, int n_new,
-                               const int8_t *sgn, uint8_t *rec, int32_t *err)
+                               const int8_t *sgn, uint8_t *rec, int32_t *err, bool late)
 {
     const kvr_shape &s = c.shape;
     const int64_t units = (int64_t)s.B * s.Hkv;
     const int64_t warps = units * n_new;
     const int64_t blocks = (warps * 32 + 255) / 256;
     if (blocks > 0x7fffffff) return KVR_ERR_UNSUPPORTED;
-    const RsqTables &tab = rsq_tables();
-    const dim3 grid((unsigned)blocks);
-    if (s.dtype == KVR_BF16) {
-        const auto *Kb = static_cast<const __nv_bfloat16 *>(K);
-        if (s.d == 128)
-            rsq_encode_kernel<128, __nv_bfloat16><<<grid, 256, 0, c.stream>>>(Kb, s.Hkv, s.cap, pos0, n_new, units, sgn, tab, rec, err);
-        else
-            rsq_encode_kernel<64, __nv_bfloat16><<<grid, 256, 0, c.stream>>>(Kb, s.Hkv, s.cap, pos0, n_new, units, sgn, tab, rec, err);
-    } else {
-        const auto *Kf = static_cast<const float *>(K);
-        if (s.d == 128)
-            rsq_encode_kernel<128, float><<<grid, 256, 0, c.stream>>>(Kf, s.Hkv, s.cap, pos0, n_new, units, sgn, tab, rec, err);
-        else
-            rsq_encode_kernel<64, float><<<grid, 256, 0, c.stream>>>(Kf, s.Hkv, s.cap, pos0, n_new, units, sgn, tab, rec, err);
-    }
-    return check_launch();
+    if (s.dtype == KVR_BF16)
+        return s.d == 128
+                   ? launch_rsq_encode<128, __nv_bfloat16>(c, K, pos0, n_new, units, blocks, sgn, rec, err, late)
+                   : launch_rsq_encode<64, __nv_bfloat16>(c, K, pos0, n_new, units, blocks, sgn, rec, err, late);
+    return s.d == 128 ? launch_rsq_encode<128, float>(c, K, pos0, n_new, units, blocks, sgn, rec, err, late)
+                      : launch_rsq_encode<64, float>(c, K, pos0, n_new, units, blocks, sgn, rec, err, late);
 }
 
 }  // namespace kvr

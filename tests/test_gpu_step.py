@@ -24,7 +24,7 @@ def _cuda():
     oracle.build()
 
 
-@pytest.mark.parametrize("mode", ["window", "regions_rsq"])
+@pytest.mark.parametrize("mode", ["window", "window_rsq", "regions_rsq"])
 def test_decode_step_equals_the_separate_calls(mode):
     seq0 = [9000, 6000]
     w = wl.Workload("step", B=2, Hq=8, Hkv=2, d=128, N=max(seq0) + 1, dtype="bf16", rank=32,
@@ -39,9 +39,10 @@ def test_decode_step_equals_the_separate_calls(mode):
         kvr.kvr_encode_keys(K, torch.zeros(B, dtype=torch.int32, device=DEV), 9000, sgn, codes)
         rec = rend = None
         S = 0
-        if mode == "regions_rsq":
+        if mode.endswith("rsq"):
             rec = kvr.rsq_buffer(K)
             kvr.kvr_encode_rsq(K, torch.zeros(B, dtype=torch.int32, device=DEV), 9000, sgn, rec)
+        if mode == "regions_rsq":
             S = 4
             rend = torch.tensor([8850, 5880], dtype=torch.int32, device=DEV)
         params = kvr.SelectParams(1024, 256, 128, wl.DEFAULT_LUT, rsq_records=rec, sink=S,
@@ -69,6 +70,11 @@ def test_decode_step_equals_the_separate_calls(mode):
         elif how == "fused":
             kvr.kvr_decode_step(q, K, V, codes, seq, pos, sgn, params, idx, cnt, scale, out, ws,
                                 err)
+            # a copy enqueued after the call sees the finished attention
+            host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+            host.copy_(out, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+            assert torch.equal(host, out.cpu())
         else:
             kvr.DecodeStep(q, K, V, codes, seq, pos, sgn, params, idx, cnt, scale, out, ws, err)()
         torch.cuda.synchronize()
@@ -80,3 +86,27 @@ def test_decode_step_equals_the_separate_calls(mode):
             if a is not None:
                 assert np.array_equal(a, b)
     assert runs[0][3].min() > 0
+
+
+def test_decode_step_flags_an_appended_key_before_the_window():
+    """With a window the step writes the appended key's code after the
+    attention; a key before the window (read by that selection) is flagged."""
+    w = wl.Workload("step", B=1, Hq=4, Hkv=1, d=64, N=3000, dtype="f32", rank=16, planted=4,
+                    seed=5)
+    K, V, qb = wl.make_cache(w, device=DEV, cap=3000)
+    sgn = wl.srht_signs(64, device=DEV)
+    shape = kvr.Shape.of(K, qb)
+    codes = kvr.codes_buffer(shape, DEV)
+    kvr.kvr_encode_keys(K, torch.zeros(1, dtype=torch.int32, device=DEV), 3000, sgn, codes)
+    params = kvr.SelectParams(256, 64, 32, wl.DEFAULT_LUT)
+    ws = kvr.workspace(kvr.kvr_select_workspace_size(shape, params))
+    idx = torch.zeros((1, 1, 64), dtype=torch.int32, device=DEV)
+    cnt = torch.zeros((1, 1), dtype=torch.int32, device=DEV)
+    out = torch.zeros((1, 4, 64), dtype=torch.float32, device=DEV)
+    seq = torch.tensor([3000], dtype=torch.int32, device=DEV)
+    for pos_new, flagged in ((2999, False), (2968, False), (2967, True)):
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        pos = torch.tensor([pos_new], dtype=torch.int32, device=DEV)
+        kvr.kvr_decode_step(qb, K, V, codes, seq, pos, sgn, params, idx, cnt, 0.125, out, ws, err)
+        torch.cuda.synchronize()
+        assert bool(kvr.kvr_read_error(err) & kvr.DEVERR["position"]) == flagged, pos_new
