@@ -6,16 +6,19 @@
 // recent tokens stay in a local region that is always attended.
 //
 // One thread-block cluster per (batch, kv head) unit. The unit's token list
-// (selected indices, then the window) is cut into equal slices, one per CTA.
-// A CTA copies the K and V rows of its slice, in batches of 32 KB, into
-// double-buffered shared memory with 16-byte cp.async pieces. Each
-// warp takes a strided share of a batch: a token's K row is spread over the
-// 32 lanes (d/32 dims each), the G per-head partial dots are reduced with a
-// butterfly that hands head h to lanes [h*32/G, (h+1)*32/G), the softmax
-// state is updated once per batch (log2 domain), and p*v is accumulated in
-// registers for all heads. Warps merge in shared memory, CTAs merge their
-// (max, sum, output) partials through distributed shared memory, each CTA
-// finishing an equal share of the output.
+// (selected indices, then the Local window, then the Sink) is cut into equal
+// slices, one per CTA; the slice's index reads go out with the length and
+// count reads, on the assumption of k indices and a full window, and are
+// redone when the token count says otherwise. A CTA copies the K and V rows
+// of its slice, in batches of 48 KB (K and V), into double-buffered shared
+// memory with 16-byte cp.async pieces. Each warp takes a strided share of a
+// batch, its slots without branches (so their shuffle chains interleave): a
+// token's K row is spread over the 32 lanes (d/32 dims each), the G per-head
+// partial dots are reduced with a butterfly that hands head h to lanes
+// [h*32/G, (h+1)*32/G), the softmax state is updated once per batch (log2
+// domain), and p*v is accumulated in registers for all heads. Warps merge in
+// shared memory, CTAs merge their (max, sum, output) partials through
+// distributed shared memory, each CTA finishing an equal share of the output.
 #include <cooperative_groups.h>
 
 #include "kvr_device.cuh"
