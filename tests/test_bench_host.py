@@ -123,3 +123,24 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
     lines = json_lines(r.stdout)
     assert len(lines) == 1
     assert lines[0]["impl"] == "reference" and lines[0]["n_gpus"] == 2
+
+
+def test_algorithmic_bytes_follow_the_documented_per_unit_counts():
+    """Per unit and step at pool P = N - W, C' = min(C, P), k' = min(k, C'),
+    row = 2d bytes: select P d/8 + C' row + G d 2 (records: C' 6d/8 in place
+    of the rows), attend (k' + W) 2 row + G d 2, encode row + d/8 (records:
+    + 6d/8); times the B Hkv units. At 128K: 33.55 MB and 8.92 MB."""
+    import bench
+    import workloads as wl
+    w = wl.LLAMA_128K
+    P = w.N - w.W
+    Cp, row, G, U = min(w.C, P), 2 * w.d, w.Hq // w.Hkv, w.B * w.Hkv
+    kp = min(w.k, Cp)
+    ab = bench.algorithmic_bytes(w)
+    assert ab["units"] == U
+    assert ab["select"] == U * (P * w.d // 8 + Cp * row + G * w.d * 2) == 33546240
+    assert ab["attend"] == U * ((kp + w.W) * 2 * row + G * w.d * 2) == 8921088
+    assert ab["encode"] == U * (row + w.d // 8)
+    rs = bench.algorithmic_bytes(w, "rsq")
+    assert rs["select"] == U * (P * w.d // 8 + Cp * 6 * w.d // 8 + G * w.d * 2)
+    assert rs["encode"] == U * (row + w.d // 8 + 6 * w.d // 8)
