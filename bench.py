@@ -4,10 +4,13 @@
 Workload: one Llama-3-8B-shaped decode-attention layer at 128K context
 (B=1, 32 query / 8 KV heads, head_dim 128, bf16 K/V, candidate budget 8192,
 top-k 2048, local window 128). A step is one pass of the whole hot path for
-one layer: encode the appended key, kvr_select (coarse score, candidates,
-exact rescoring, top-k) and kvr_sparse_attend. Steps rotate over 32 layer
-caches (17.7 GB) so every step reads its cache cold from HBM (inputs larger
-than L2). Each layer's step is one captured CUDA graph.
+one layer: append one token (encode its key), select (coarse score,
+candidates, exact rescoring, top-k) and attend, by default through
+kvr_select_attend (one launch). Steps rotate over 32 layer caches (17.7 GB)
+so every step reads its cache cold from HBM (inputs larger than L2); each
+step appends a token and takes a fresh query. The timed loop replays one
+CUDA graph per decode iteration (every layer once) plus one for a remainder
+of steps, so any step count times the same chained kernels.
 
 Output: one JSON line (rank 0). --impl reference times the CPU oracle on the
 host cores instead, on the same workload.
@@ -29,6 +32,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sparse decode-attention steps/s at 128K ctx; achieved HBM GB/s vs peak"
 OFFLOAD_METRIC = "sparse decode-attention steps/s at 1M ctx, K/V in host memory"
+MILLION_METRIC = "sparse decode-attention steps/s at 1M ctx, K/V in HBM; achieved HBM GB/s vs peak"
 LAYERS = 32
 LAYERS_DEFAULT = LAYERS
 
@@ -163,31 +167,30 @@ def max_over_ranks(x, world):
 # CPU oracle arm (cpu_baseline leg and --impl reference)
 # --------------------------------------------------------------------------
 
-def oracle_unit_inputs(w, device):
-    """Unit (b=0, h=0) of layer 0 of the workload, as host fp32 arrays."""
-    import numpy as np
+def oracle_unit_inputs(w, device, h=0):
+    """Unit (b=0, kv head h) of layer 0 of the workload, as host fp32 arrays,
+    with 64 of its per-step query groups."""
     import torch
     import workloads as wl
     import oracle
     K, V, qb = wl.make_cache(w.with_(B=1), device=device, cap=w.N)
-    K0 = oracle.f32(K[0, 0].cpu())
-    V0 = oracle.f32(V[0, 0].cpu())
+    K0 = oracle.f32(K[0, h].cpu())
+    V0 = oracle.f32(V[0, h].cpu())
     sgn = wl.srht_signs(w.d).numpy()
     codes = oracle.encode(K0, sgn)
-    qs = [oracle.f32(wl.step_query(w, qb, t)[0, :w.G].cpu()) for t in range(64)]
+    G = w.G
+    qs = [oracle.f32(wl.step_query(w, qb, t)[0, h * G:(h + 1) * G].cpu()) for t in range(64)]
     del K, V
     if device != "cpu":
         torch.cuda.empty_cache()
     return K0, V0, codes, sgn, qs
 
 
-def time_oracle(w, budget_s, device, min_steps=1, max_steps=None):
-    """Oracle decode steps on the host: each step runs one unit and counts
-    1/units of a whole step. Returns (steps/s, seconds, unit-steps done)."""
+def _oracle_steps(w, inputs, budget_s, min_steps=1, max_steps=None):
+    """Oracle decode steps of one unit until the budget is spent: (unit-steps, s)."""
     import numpy as np
     import oracle
-    K0, V0, codes, sgn, qs = oracle_unit_inputs(w, device)
-    units = w.B * w.Hkv
+    K0, V0, codes, sgn, qs = inputs
     scale = np.float32(1 / math.sqrt(w.d))
     done, t0 = 0, time.perf_counter()
     while True:
@@ -198,7 +201,53 @@ def time_oracle(w, budget_s, device, min_steps=1, max_steps=None):
         el = time.perf_counter() - t0
         if (el >= budget_s and done >= min_steps) or (max_steps and done >= max_steps):
             break
+    return done, el
+
+
+def time_oracle(w, budget_s, device, min_steps=1, max_steps=None):
+    """Oracle decode steps on one host core: each step runs one unit and
+    counts 1/units of a whole step. Returns (steps/s, seconds, unit-steps)."""
+    units = w.B * w.Hkv
+    done, el = _oracle_steps(w, oracle_unit_inputs(w, device), budget_s, min_steps, max_steps)
     return (done / units) / el, el, done
+
+
+def box_cores():
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def time_oracle_all_cores(w, budget_s, device):
+    """The oracle on every host core: one thread per (batch 0, kv head) unit,
+    up to the core count (the oracle's C calls release the interpreter lock).
+    Returns (steps/s, seconds, unit-steps, threads)."""
+    import concurrent.futures as cf
+    threads = max(1, min(box_cores(), w.B * w.Hkv))
+    inputs = [oracle_unit_inputs(w, device, h=h % w.Hkv) for h in range(threads)]
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        res = list(ex.map(lambda x: _oracle_steps(w, x, budget_s), inputs))
+    el = time.perf_counter() - t0
+    done = sum(r[0] for r in res)
+    return (done / (w.B * w.Hkv)) / el, el, done, threads
+
+
+def cpu_baseline_line(w, seconds, device):
+    """cpu_baseline: the oracle on all host cores (headline) and on one."""
+    units = w.B * w.Hkv
+    v1, el1, d1 = time_oracle(w, seconds / 2, device)
+    va, ela, da, th = time_oracle_all_cores(w, seconds / 2, device)
+    return {"value": va, "unit": "steps/s", "cores": th, "kind": "oracle",
+            "box_cores": box_cores(),
+            "sample": "%d unit-steps of the %s workload on %d threads (one per kv head of batch "
+                      "entry 0) in %.1f s; steps/s = unit-steps / %d / s"
+                      % (da, w.name, th, ela, units),
+            "single_thread": {"value": v1, "unit": "steps/s", "cores": 1,
+                              "sample": "%d unit-steps (batch 0, kv head 0) in %.1f s"
+                                        % (d1, el1)}}
 
 
 def run_reference(args, w):
@@ -219,9 +268,10 @@ def run_reference(args, w):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": dict(config_of(w), rerank="exact", votes="hamming"),
         "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle",
-                         "sample": "%d unit-steps (batch 0, kv head 0 of %d units) of the 128K "
+                         "box_cores": box_cores(),
+                         "sample": "%d unit-steps (batch 0, kv head 0 of %d units) of the %s "
                                    "workload, %.1f s; steps/s = unit-steps / %d / s"
-                                   % (done, w.B * w.Hkv, el, w.B * w.Hkv)},
+                                   % (done, w.B * w.Hkv, w.name, el, w.B * w.Hkv)},
         "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -241,19 +291,18 @@ def config_of(w):
 # --------------------------------------------------------------------------
 
 class Layer:
-    def __init__(self, w, l, kvr, wl, torch, sgn, rerank="exact", host=False, mag=False):
+    def __init__(self, w, l, kvr, wl, torch, sgn, cap, nq, rerank="exact", host=False, mag=False):
         dev = "cuda"
-        K, V, qb = wl.make_cache(w, device=dev, cap=w.N, seed=w.seed + 1000 * l)
+        # rows [N, cap) hold the keys and values the appending steps add
+        K, V, qb = wl.make_cache(w, device=dev, cap=cap, seed=w.seed + 1000 * l)
         self.K, self.V = K, V
-        self.q = wl.step_query(w, qb, 0, seed=w.seed + 1000 * l).contiguous()
+        # fresh per-step queries q_t = q_base + 0.1 N(0, 1), one per decode iteration
+        self.qs = [wl.step_query(w, qb, t, seed=w.seed + 1000 * l).contiguous() for t in range(nq)]
+        self.q = self.qs[0]
         self.codes = kvr.codes_buffer(kvr.Shape.of(K, self.q), dev)
         kvr.kvr_encode_keys(K, torch.zeros(w.B, dtype=torch.int32, device=dev), w.N, sgn,
                             self.codes)
         self.out = torch.empty((w.B, w.Hq, w.d), dtype=torch.float32, device=dev)
-        # the V cache as an L2-prefetch hint for the attention that follows;
-        # the codes, K, V and lengths are never written by the kernel before a
-        # selection in the step chain (the previous layer's attention), so it
-        # may start on them early
         self.rec = None
         if rerank == "rsq":
             # reranker records of every key, kept beside the codes
@@ -269,6 +318,10 @@ class Layer:
             self.V.copy_(V)
             del K, V
             torch.cuda.empty_cache()
+        # the codes, K, V and lengths are never written by the kernel before a
+        # selection in the step chain (the previous layer's attention), so it
+        # may start on them early; V as an L2-prefetch hint for the separate
+        # attention (the fused call reads V itself)
         flags = kvr.SELECT_EARLY_INPUTS | (kvr.SELECT_MAGNITUDE_VOTES if mag else 0)
         self.params = kvr.SelectParams(w.C, w.k, w.W, w.lut, flags=flags,
                                        V_prefetch=None if host else self.V, rsq_records=self.rec)
@@ -281,7 +334,6 @@ class Layer:
 
 
 def run_gpu(args, w):
-    import numpy as np
     import torch
     import sparse_decode_attention_gb300 as kvr
     import workloads as wl
@@ -293,116 +345,104 @@ def run_gpu(args, w):
     host = args.workload == "million_offload"
     rerank = args.rerank or ("rsq" if host else "exact")
     mag = args.votes == "magnitude"
-    layers = [Layer(w, l, kvr, wl, torch, sgn, rerank, host, mag) for l in range(LAYERS)]
+    fused = args.path == "fused"
+    NQ = 16
+    e2e_n = min(args.steps, args.e2e_steps)
+    warm_iters = max(1, -(-args.warmup // LAYERS))
+    timed_iters, rem = divmod(args.steps, LAYERS)
+    # every appending step of a layer adds one row: warm-up and timed
+    # iterations, the remainder, and the end-to-end passes (two modes)
+    margin = warm_iters + timed_iters + 2 + 2 * (e2e_n // LAYERS + 2) + 8
+    cap = w.N + margin
+    layers = [Layer(w, l, kvr, wl, torch, sgn, cap, NQ, rerank, host, mag) for l in range(LAYERS)]
     shape = kvr.Shape.of(layers[0].K, layers[0].q)
     params = layers[0].params   # the flags of every layer's selection (workspace size)
     ws_s = kvr.workspace(kvr.kvr_select_workspace_size(shape, params), dev)
     ws_a = kvr.workspace(kvr.kvr_attend_workspace_size(shape, w.k, w.W), dev)
     idx = torch.empty((w.B, w.Hkv, w.k), dtype=torch.int32, device=dev)
     cnt = torch.empty((w.B, w.Hkv), dtype=torch.int32, device=dev)
-    seq = torch.full((w.B,), w.N, dtype=torch.int32, device=dev)
-    pos_new = torch.full((w.B,), w.N - 1, dtype=torch.int32, device=dev)
+    # the sequence lengths, then the appended key's rows; every decode
+    # iteration first adds one to both (one small torch kernel per iteration)
+    seqpos = torch.tensor([w.N] * w.B + [w.N - 1] * w.B, dtype=torch.int32, device=dev)
+    seq, pos_new = seqpos[:w.B], seqpos[w.B:]
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     scale = 1.0 / math.sqrt(w.d)
+
+    def call(L, j):
+        if fused:
+            kvr.kvr_select_attend(L.qs[j], L.K, L.V, L.codes, seq, sgn, L.params, scale, idx, cnt,
+                                  L.out, ws_s, err)
+        else:
+            kvr.kvr_select(L.qs[j], L.K, L.codes, seq, sgn, L.params, idx, cnt, ws_s, err)
+            kvr.kvr_sparse_attend(L.qs[j], L.K, L.V, idx, cnt, seq, w.W, scale, L.out, ws_a, err)
 
     side = torch.cuda.Stream(device=dev)
     fork, join = torch.cuda.Event(), torch.cuda.Event()
 
-    def step(L, ev=None):
-        # The appended key's code is not read by this step's selection (the
-        # newest W tokens are the local window), so its encode runs on a side
-        # stream next to kvr_select; the step ends when both are done.
+    def iteration(nl, j):
+        # One decode iteration over the first nl layers: the lengths advance,
+        # then each layer appends its key and runs its step. A key's code is
+        # first read when it leaves the window, W iterations later, so the
+        # encodes form one chain on a side stream, joined at the end; the main
+        # stream is a chain of selection (+ attention) kernels linked by
+        # programmatic dependent launch.
         main = torch.cuda.current_stream()
+        seqpos.add_(1)
         fork.record(main)
         side.wait_event(fork)
-        if ev:
-            ev[0].record(side)
-        L.encode_new(kvr, pos_new, sgn, err, stream=side)
-        if ev:
-            ev[1].record(side)
+        for L in layers[:nl]:
+            L.encode_new(kvr, pos_new, sgn, err, stream=side)
+            call(L, j)
         join.record(side)
-        if ev:
-            ev[2].record(main)
-        kvr.kvr_select(L.q, L.K, L.codes, seq, sgn, L.params, idx, cnt, ws_s, err)
-        if ev:
-            ev[3].record(main)
-        kvr.kvr_sparse_attend(L.q, L.K, L.V, idx, cnt, seq, w.W, scale, L.out, ws_a, err)
-        if ev:
-            ev[4].record(main)
         main.wait_event(join)
 
-    # encode(s), select (plus its vote lists), attend
-    launches_per_step = (4 if rerank == "rsq" else 3) + (1 if mag else 0)
+    # encode(s), selection (+ its vote lists), attention (fused: one launch)
+    launches_per_step = (2 if fused else 3) + (1 if rerank == "rsq" else 0) + (1 if mag else 0)
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
-    # eager warm-up on the capture stream, then one graph per layer
-    with torch.cuda.stream(stream):
-        for L in layers[:2]:
-            step(L)
+    with torch.cuda.stream(stream):   # eager warm-up of the calls (no append)
+        seqpos.sub_(1)
+        iteration(2, 0)
     stream.synchronize()
     if kvr.kvr_read_error(err):
         raise RuntimeError("device error bits during warm-up")
-    try:
-        mk = lambda: torch.cuda.Event(enable_timing=True, external=True)
-        mk()
-        external = True
-    except TypeError:
-        external = False
-    # Timed graphs carry no event nodes: an event between two kernels
-    # serialises them and turns off programmatic dependent launch, which lets
-    # the next kernel's CTAs become resident while the previous one drains.
-    # One graph runs a whole decode iteration (every layer once), as a serving
-    # loop would; per-layer graphs cover a remainder of steps. Graphs with
-    # event nodes time the calls in a separate, untimed pass.
-    graphs, graphs_ev, evs = [], [], []
-    for L in layers:
+    # Timed graphs carry no event nodes between kernels: an event between two
+    # kernels serialises them and turns off programmatic dependent launch.
+    # One graph per query set runs a whole decode iteration; the last graph
+    # covers a remainder of steps (the first `rem` layers), so any step count
+    # times the same chained path.
+    graphs = []
+    for j in range(NQ):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            step(L)
+            iteration(LAYERS, j)
         graphs.append(g)
-        if external:
-            ge = torch.cuda.CUDAGraph()
-            ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
-            with torch.cuda.graph(ge, stream=stream):
-                step(L, ev)
-            graphs_ev.append(ge)
-            evs.append(ev)
-    # the decode iteration: the appended keys' encodes form one chain on the
-    # side stream, joined once at the end (a key's code is first read when it
-    # leaves the window, W steps later), so the main stream is a chain of
-    # select -> attend kernels linked by programmatic dependent launch
-    g_iter = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_iter, stream=stream):
-        main = torch.cuda.current_stream()
-        fork.record(main)
-        side.wait_event(fork)
-        for L in layers:
-            L.encode_new(kvr, pos_new, sgn, err, stream=side)
-            kvr.kvr_select(L.q, L.K, L.codes, seq, sgn, L.params, idx, cnt, ws_s, err)
-            kvr.kvr_sparse_attend(L.q, L.K, L.V, idx, cnt, seq, w.W, scale, L.out, ws_a, err)
-        join.record(side)
-        main.wait_event(join)
+    g_rem = None
+    if rem:
+        g_rem = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_rem, stream=stream):
+            iteration(rem, (warm_iters + timed_iters) % NQ)
     torch.cuda.synchronize()
 
-    def run_steps(n):
-        for _ in range(n // LAYERS):
-            g_iter.replay()
-        for i in range(n % LAYERS):
-            graphs[i].replay()
-
     with torch.cuda.stream(stream):
-        run_steps(max(args.warmup, LAYERS))
+        for i in range(warm_iters):
+            graphs[i % NQ].replay()
     stream.synchronize()
 
     clocks = ClockSampler(local) if rank == 0 else None
     time.sleep(0.25 if clocks else 0)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(timed_iters)]
     barrier(world)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         t_start.record()
-        run_steps(args.steps)
+        for i in range(timed_iters):
+            graphs[(warm_iters + i) % NQ].replay()
+            marks[i].record()
+        if g_rem is not None:
+            g_rem.replay()
         t_end.record()
     torch.cuda.synchronize()
     barrier(world)
@@ -411,11 +451,39 @@ def run_gpu(args, w):
     ms = max_over_ranks(ms, world)
     if kvr.kvr_read_error(err):
         raise RuntimeError("device error bits during the timed region")
+    iter_us = []
+    prev = t_start
+    for m in marks:
+        iter_us.append(prev.elapsed_time(m) * 1e3 / LAYERS)
+        prev = m
+    n_mid = w.N + warm_iters + timed_iters // 2
 
     # per-call durations: every layer's event graph, replayed in layer order
-    # (each layer's inputs cold again), after the timed region
-    per = {"encode": [], "select": [], "attend": []}
+    # (each layer's inputs cold again), after the timed region, no append
+    try:
+        mk = lambda: torch.cuda.Event(enable_timing=True, external=True)
+        mk()
+        external = True
+    except TypeError:
+        external = False
+    per = {"encode": [], "call": [], "select": [], "attend": []}
     if external:
+        graphs_ev, evs = [], []
+        for L in layers:
+            ge = torch.cuda.CUDAGraph()
+            ev = [mk() for _ in range(5)]
+            with torch.cuda.graph(ge, stream=stream):
+                ev[0].record()
+                L.encode_new(kvr, pos_new, sgn, err)
+                ev[1].record()
+                call(L, 0)
+                ev[2].record()
+                kvr.kvr_select(L.q, L.K, L.codes, seq, sgn, L.params, idx, cnt, ws_s, err)
+                ev[3].record()
+                kvr.kvr_sparse_attend(L.q, L.K, L.V, idx, cnt, seq, w.W, scale, L.out, ws_a, err)
+                ev[4].record()
+            graphs_ev.append(ge)
+            evs.append(ev)
         for rep in range(2):
             with torch.cuda.stream(stream):
                 for ge in graphs_ev:
@@ -425,45 +493,81 @@ def run_gpu(args, w):
                 continue
             for ev in evs:
                 per["encode"].append(ev[0].elapsed_time(ev[1]))
+                per["call"].append(ev[1].elapsed_time(ev[2]))
                 per["select"].append(ev[2].elapsed_time(ev[3]))
                 per["attend"].append(ev[3].elapsed_time(ev[4]))
+        del graphs_ev
     avg = {k: (sum(v) / len(v) if v else None) for k, v in per.items()}
 
+    # warm figure: layer 0's step replayed back to back (its inputs in L2), no append
+    g_w = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_w, stream=stream):
+        main = torch.cuda.current_stream()
+        fork.record(main)
+        side.wait_event(fork)
+        layers[0].encode_new(kvr, pos_new, sgn, err, stream=side)
+        call(layers[0], 0)
+        join.record(side)
+        main.wait_event(join)
+    with torch.cuda.stream(stream):
+        for _ in range(32):
+            g_w.replay()
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0.record()
+        for _ in range(256):
+            g_w.replay()
+        w1.record()
+    stream.synchronize()
+    warm_us = w0.elapsed_time(w1) * 1e3 / 256
+
     # end to end through the public API with pinned host buffers
-    e2e = run_e2e(args, w, layers, kvr, torch, sgn, params, ws_s, ws_a, idx, cnt, seq, pos_new,
-                  err, scale, world)
+    e2e = run_e2e(args, w, layers, kvr, torch, sgn, ws_s, idx, cnt, seqpos, err, scale, world,
+                  e2e_n, fused)
 
     recall = rerank_recall(w, layers[0], kvr, torch, sgn, ws_s, seq) if rerank == "rsq" else None
+    if kvr.kvr_read_error(err):
+        raise RuntimeError("device error bits after the timed region")
 
     steps_total = args.steps * world
     value = steps_total / (ms / 1000.0)
     if rank != 0:
         return
-    ab = algorithmic_bytes(w, rerank)
-    # the reranking select reads records, not K rows, and the magnitude votes
-    # run the optional-mode kernels: each its own counters
+    ab = algorithmic_bytes(w.with_(N=n_mid), rerank)
     sel_key = ("select_kernel_rsq" if rerank == "rsq" else
                "select_kernel_mag" if args.votes == "magnitude" else "select_kernel")
     peak, peak_kind = peaks()
     roof = None
-    if avg["select"]:
-        ach = ab["select"] / (avg["select"] * 1e-3) / 1e9
-        roof = {"bound": "hbm", "kernel": "select_kernel (kvr_select, one launch)",
-                "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-                "peak_kind": peak_kind, "traffic": measured_traffic(sel_key, w.name),
-                "algorithmic_bytes": ab["select"], "avg_ms": avg["select"]}
+    if avg["call"]:
+        if fused:
+            byts = ab["select"] + ab["attend"]
+            ach = byts / (avg["call"] * 1e-3) / 1e9
+            roof = {"bound": "hbm", "kernel": "select_kernel with the attention tail "
+                    "(kvr_select_attend, one launch)", "achieved": ach, "peak": peak,
+                    "unit": "GB/s", "frac": ach / peak, "frac_of_8TBs": ach / 8000.0,
+                    "peak_kind": peak_kind,
+                    "traffic": measured_traffic("select_attend_kernel", w.name),
+                    "algorithmic_bytes": byts, "avg_ms": avg["call"]}
+        else:
+            ach = ab["select"] / (avg["select"] * 1e-3) / 1e9
+            roof = {"bound": "hbm", "kernel": "select_kernel (kvr_select, one launch)",
+                    "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                    "peak_kind": peak_kind, "traffic": measured_traffic(sel_key, w.name),
+                    "algorithmic_bytes": ab["select"], "avg_ms": avg["select"]}
     path = None
     if avg["select"] and avg["attend"]:
+        # the two separate calls (each timed alone), for comparison
         tsum = (avg["select"] + avg["attend"]) * 1e-3
         ach = (ab["select"] + ab["attend"]) / tsum / 1e9
-        path = {"calls": "kvr_select + kvr_sparse_attend", "achieved": ach, "peak": peak,
-                "unit": "GB/s", "frac": ach / peak, "frac_of_8TBs": ach / 8000.0,
-                "us": tsum * 1e6, "algorithmic_bytes": ab["select"] + ab["attend"],
+        path = {"calls": "kvr_select + kvr_sparse_attend (two launches, each timed alone)",
+                "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                "frac_of_8TBs": ach / 8000.0, "us": tsum * 1e6,
+                "algorithmic_bytes": ab["select"] + ab["attend"],
+                "select_us": avg["select"] * 1e3, "attend_us": avg["attend"] * 1e3,
+                "select_frac": ab["select"] / (avg["select"] * 1e-3) / 1e9 / peak,
                 "traffic": (None if host or None in (measured_traffic(sel_key, w.name),
                                                      measured_traffic("attend_kernel", w.name))
                             else measured_traffic(sel_key, w.name)
-                            + measured_traffic("attend_kernel", w.name)),
-                "attend_us": avg["attend"] * 1e3, "encode_us": avg["encode"] * 1e3}
+                            + measured_traffic("attend_kernel", w.name))}
     link = None
     if host and avg["attend"]:
         # the attention's gathers cross the host link: its bytes over its time
@@ -476,29 +580,40 @@ def run_gpu(args, w):
                 "algorithmic_bytes": ab["attend"], "avg_ms": avg["attend"]}
     # the whole step against its measured time: every byte the step must read
     # (codes, candidate rows, selected K / V, query, the appended key) over
-    # ms_per_step; select and attend overlap across their launch boundary, so
-    # this is the path's effective fraction
+    # ms_per_step
     step_bytes = ab["select"] + ab["attend"] + ab["encode"]
     step_ach = step_bytes / (ms / args.steps * 1e-3) / 1e9
     step_roof = {"bytes": step_bytes, "achieved": step_ach, "peak": peak, "unit": "GB/s",
-                 "frac": step_ach / peak, "us": ms / args.steps * 1e3}
+                 "frac": step_ach / peak, "frac_of_8TBs": step_ach / 8000.0,
+                 "us": ms / args.steps * 1e3}
+    timing = {"iterations_timed": timed_iters, "remainder_steps": rem,
+              "median_us_per_step": statistics.median(iter_us) if iter_us else None,
+              "min_us_per_step": min(iter_us) if iter_us else None,
+              "max_us_per_step": max(iter_us) if iter_us else None,
+              "warm_single_layer_us_per_step": warm_us,
+              "warm_single_layer_steps_per_s": 1e6 / warm_us,
+              "encode_us": avg["encode"] * 1e3 if avg["encode"] else None,
+              "call_us": avg["call"] * 1e3 if avg["call"] else None}
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        v, el, done = time_oracle(w, args.cpu_seconds, "cuda")
-        cpu = {"value": v, "unit": "steps/s", "cores": 1, "kind": "oracle",
-               "sample": "%d unit-steps (batch 0, kv head 0) of the %s workload in %.1f s, "
-                         "single-threaded; steps/s = unit-steps / %d / s"
-                         % (done, w.name, el, ab["units"])}
-    cfg = dict(config_of(w), rerank=rerank, votes=args.votes)
+        cpu = cpu_baseline_line(w, args.cpu_seconds, "cuda")
+    cfg = dict(config_of(w), rerank=rerank, votes=args.votes,
+               path="kvr_select_attend (one launch)" if fused else
+               "kvr_select + kvr_sparse_attend (two launches)",
+               appending="each step appends one token (its K / V row and code) and uses a "
+                         "fresh query; lengths %d -> %d over the run"
+                         % (w.N, w.N + warm_iters + timed_iters + (1 if rem else 0)))
     if host:
         cfg["kv_residency"] = "K, V in page-locked host memory read through the device mapping"
     line = {
-        "metric": OFFLOAD_METRIC if host else METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+        "metric": OFFLOAD_METRIC if host else (MILLION_METRIC if w.name == "million_token"
+                                               else METRIC),
+        "value": value, "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": cfg, "roofline": roof,
         "path_roofline": path, "link_roofline": link, "rerank_recall": recall,
-        "step_roofline": step_roof,
+        "step_roofline": step_roof, "timing": timing,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
@@ -539,79 +654,124 @@ def rerank_recall(w, L, kvr, torch, sgn, ws_s, seq):
     return {"of": "exact q_bar.k top-%d" % w.k, "mean": sum(kept) / len(kept), "min": min(kept)}
 
 
-def run_e2e(args, w, layers, kvr, torch, sgn, params, ws_s, ws_a, idx, cnt, seq, pos_new, err,
-            scale, world):
-    """Per step: copy the query and the appended K/V row from pinned host memory,
-    run the step through the public API (kvr_decode_step: the appended key's
-    code, selection, attention, one library call, arguments marshalled once
-    per layer), copy the output back, synchronise."""
+def run_e2e(args, w, layers, kvr, torch, sgn, ws_s, idx, cnt, seqpos, err, scale, world, n,
+            fused):
+    """End to end through the public API, appending: per step the host
+    provides the step's query, the appended token's K and V rows and the new
+    lengths in pinned memory; they are copied to the device, the step runs as
+    one library call (kvr_decode_step: the appended key's code, selection and
+    attention), the output is copied back and the host synchronises."""
     dev = layers[0].K.device
-    n = min(args.steps, args.e2e_steps)
-    hq = [L.q.cpu().pin_memory() for L in layers]
-    hk = [L.K[:, :, w.N - 1].cpu().pin_memory() for L in layers]
-    hv = [L.V[:, :, w.N - 1].cpu().pin_memory() for L in layers]
+    B = w.B
+    NQ = len(layers[0].qs)
+    on_dev = layers[0].K.is_cuda
+    hq = [[q.cpu().pin_memory() for q in L.qs] for L in layers]
+    n_it = -(-n // LAYERS) + 1
+    N0 = int(seqpos[0].item())   # the lengths so far: the e2e steps append after them
+    # the rows these steps append, per layer, in pinned host memory
+    hk = [L.K[:, :, N0:N0 + 2 * n_it].cpu().pin_memory() if on_dev else None for L in layers]
+    hv = [L.V[:, :, N0:N0 + 2 * n_it].cpu().pin_memory() if on_dev else None for L in layers]
+    hsp = torch.empty(2 * B, dtype=torch.int32).pin_memory()
     hout = torch.empty((w.B, w.Hq, w.d), dtype=torch.float32).pin_memory()
+    qd = [torch.empty_like(L.q) for L in layers]
+    seq, pos = seqpos[:B], seqpos[B:]
     # a host-resident cache takes the appended K/V row by a host-side write
-    # (the kernels read it through the mapping): only q crosses to the device
-    row_h2d = 0 if not layers[0].K.is_cuda else 2 * hk[0].numel() * hk[0].element_size()
-    h2d = hq[0].numel() * hq[0].element_size() + row_h2d
+    # (the kernels read it through the mapping): only q and the lengths cross
+    row_bytes = 2 * B * w.Hkv * w.d * 2 if on_dev else 0
+    h2d = hq[0][0].numel() * hq[0][0].element_size() + row_bytes + hsp.numel() * 4
     d2h = hout.numel() * hout.element_size()
+    steps = [kvr.DecodeStep(qd[l], L.K, L.V, L.codes, seq, pos, sgn, L.params, idx, cnt, scale,
+                            L.out, ws_s, err) for l, L in enumerate(layers)]
 
-    steps = [kvr.DecodeStep(L.q, L.K, L.V, L.codes, seq, pos_new, sgn, L.params, idx, cnt, scale,
-                            L.out, ws_s, err) for L in layers]
+    def host_inputs(i, base):
+        """Lengths of step i (counted from `base`), in the pinned buffer."""
+        it = i // LAYERS + 1
+        hsp[:B] = base + it
+        hsp[B:] = base + it - 1
+        return it - 1
 
-    def one(i):
-        L = layers[i % LAYERS]
-        L.q.copy_(hq[i % LAYERS], non_blocking=True)
-        L.K[:, :, w.N - 1].copy_(hk[i % LAYERS], non_blocking=True)
-        L.V[:, :, w.N - 1].copy_(hv[i % LAYERS], non_blocking=True)
-        steps[i % LAYERS]()
+    def one(i, base, off):
+        l = i % LAYERS
+        L = layers[l]
+        r = host_inputs(i, base)
+        seqpos.copy_(hsp, non_blocking=True)
+        qd[l].copy_(hq[l][(i // LAYERS) % NQ], non_blocking=True)
+        if on_dev:
+            L.K[:, :, base + r].copy_(hk[l][:, :, off + r], non_blocking=True)
+            L.V[:, :, base + r].copy_(hv[l][:, :, off + r], non_blocking=True)
+        steps[l]()
         hout.copy_(L.out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
+    base = N0
     for i in range(min(args.warmup, 8)):
-        one(i)
+        one(i, base, 0)
     barrier(world)
     t0 = time.perf_counter()
     for i in range(n):
-        one(i)
+        one(i, base, 0)
     el = time.perf_counter() - t0
     el = max_over_ranks(el, world)
     eager = n * world / el
     res = {"value": eager, "unit": "steps/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "steps": n,
-           "mode": "kvr_decode_step per step (one C-ABI call), sync per step"}
-    if not layers[0].K.is_cuda:
+           "mode": "kvr_decode_step per step (one C-ABI call), appending, sync per step"}
+    if not on_dev:
         return res   # the appended rows are host-side writes: nothing to capture
-    # the serving form: per layer one CUDA graph of the same step (copies of q
-    # and the appended K / V row from the pinned host buffers, the decode step,
-    # the output copied back), replayed and synchronised every step
+    # the serving form: per layer one CUDA graph of the same step (copies of q,
+    # the lengths and the appended K / V rows from pinned host buffers, the
+    # rows scattered into the cache at the appended position, the decode step,
+    # the output copied back), replayed and synchronised every step; the host
+    # refills the pinned buffers before each replay
+    base = N0 + n_it
+    stage_q = [torch.empty_like(hq[0][0]).pin_memory() for _ in layers]
+    stage_k = torch.empty_like(hk[0][:, :, :1]).pin_memory()
+    stage_v = torch.empty_like(hv[0][:, :, :1]).pin_memory()
+    hpos = torch.empty(1, dtype=torch.int64).pin_memory()
+    krow = torch.empty((B, w.Hkv, 1, w.d), dtype=layers[0].K.dtype, device=dev)
+    vrow = torch.empty_like(krow)
+    dpos = torch.empty(1, dtype=torch.int64, device=dev)
     gstream = torch.cuda.Stream(device=dev)
     graphs = []
     for l, L in enumerate(layers):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=gstream):
-            L.q.copy_(hq[l], non_blocking=True)
-            L.K[:, :, w.N - 1].copy_(hk[l], non_blocking=True)
-            L.V[:, :, w.N - 1].copy_(hv[l], non_blocking=True)
-            kvr.DecodeStep(L.q, L.K, L.V, L.codes, seq, pos_new, sgn, L.params, idx, cnt, scale,
+            seqpos.copy_(hsp, non_blocking=True)
+            qd[l].copy_(stage_q[l], non_blocking=True)
+            krow.copy_(stage_k, non_blocking=True)
+            vrow.copy_(stage_v, non_blocking=True)
+            dpos.copy_(hpos, non_blocking=True)
+            L.K.index_copy_(2, dpos, krow)
+            L.V.index_copy_(2, dpos, vrow)
+            kvr.DecodeStep(qd[l], L.K, L.V, L.codes, seq, pos, sgn, L.params, idx, cnt, scale,
                            L.out, ws_s, err)()
             hout.copy_(L.out, non_blocking=True)
         graphs.append(g)
     torch.cuda.synchronize()
-    for i in range(min(args.warmup, 8)):
-        graphs[i % LAYERS].replay()
+
+    def replay(i):
+        l = i % LAYERS
+        r = host_inputs(i, base)
+        hpos[0] = base + r
+        stage_q[l].copy_(hq[l][(i // LAYERS) % NQ])
+        stage_k.copy_(hk[l][:, :, n_it + r:n_it + r + 1])
+        stage_v.copy_(hv[l][:, :, n_it + r:n_it + r + 1])
+        graphs[l].replay()
         torch.cuda.current_stream().synchronize()
+
+    for i in range(min(args.warmup, 8)):
+        replay(i)
     barrier(world)
     t0 = time.perf_counter()
     for i in range(n):
-        graphs[i % LAYERS].replay()
-        torch.cuda.current_stream().synchronize()
+        replay(i)
     el = max_over_ranks(time.perf_counter() - t0, world)
     res.update(value=n * world / el, eager_value=eager,
-               mode="per step: one CUDA-graph replay (pinned-host copies of q and the appended "
-                    "K / V row in, kvr_decode_step, output copied out) and a sync; eager_value: "
-                    "the same calls issued one by one")
+               mode="per step: one CUDA-graph replay (pinned-host copies of q, the lengths and "
+                    "the appended K / V rows in, the rows scattered into the cache, "
+                    "kvr_decode_step%s, output copied out) and a sync, appending; eager_value: "
+                    "the same calls issued one by one"
+                    % (" = encode + kvr_select_attend" if fused else ""))
     return res
 
 
@@ -1012,10 +1172,13 @@ def main():
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layer caches rotated (fewer = a small case for profiling; the "
                          "default keeps every step's inputs cold in L2)")
-    ap.add_argument("--workload", choices=["llama3_8b_128k", "tiered_window_cache",
+    ap.add_argument("--workload", choices=["llama3_8b_128k", "million_token", "tiered_window_cache",
                                            "batched_drift", "million_offload"],
                     default="llama3_8b_128k",
                     help="the timed workload (the 128K decode layer is the headline)")
+    ap.add_argument("--path", choices=["fused", "separate"], default="fused",
+                    help="selection and attention as one call (kvr_select_attend: one launch "
+                         "where it fuses them) or as kvr_select + kvr_sparse_attend")
     ap.add_argument("--diagnostics", type=int, default=0, metavar="STEPS",
                     help="tiered_window_cache only: also run STEPS untimed appending steps and "
                          "report Future Missed Mass, Global LIR and selection churn")
@@ -1059,6 +1222,17 @@ def main():
         if args.layers == LAYERS_DEFAULT:
             globals()["LAYERS"] = 2
         run_gpu(args, wl.MILLION)
+        return
+    if args.workload == "million_token":
+        # 2^20 tokens with K / V in HBM: 8 layers (34.6 GB; codes alone 1.07 GB,
+        # every step's inputs cold in L2)
+        if args.layers == LAYERS_DEFAULT:
+            globals()["LAYERS"] = 8
+        w = wl.MILLION
+        if args.impl == "reference":
+            run_reference(args, w)
+        else:
+            run_gpu(args, w)
         return
     w = wl.LLAMA_128K
     if args.impl == "reference":

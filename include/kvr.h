@@ -274,11 +274,43 @@ kvr_status kvr_select(const kvr_shape *shape, const kvr_select_params *p, const 
                       void *stream);
 
 /*
+ * kvr_select_attend -- kvr_select followed by the attention over its output,
+ * as one call: steps 3-5 of a decode step (ParisKV, "Pipeline di Recupero
+ * Nativa su GPU in Due Stadi" for the selection; "Problematica" and
+ * "Meccanismo di Aggiornamento a Finestra Scorrevole" for the attention).
+ *
+ * out_idx / out_count are exactly kvr_select's. out [B, Hq, d] fp32 is the
+ * attention of kvr_sparse_attend over {out_idx[b,h,0..k'-1]} U [N - W, N)
+ * (kvr_sparse_attend_regions over the Sink, the top-k and [region_end[b], N)
+ * when p->region_end is set), within the same floating-point tolerance of
+ * the exact value; the summation order differs from the separate calls, so
+ * the bits may too.
+ * With Hq/Hkv <= 4, exact rescoring (p->rsq_records NULL) and Hamming-ring
+ * votes, both run in one kernel launch: each thread-block cluster that
+ * selects a unit's tokens attends over them, each CTA over the winners it
+ * rescored plus a share of the window (and Sink), so the selected indices
+ * never leave the chip before the attention; otherwise the two calls run one
+ * after the other. p->V_prefetch is ignored (V is read anyway).
+ *   q, K, codes, seq_len, srht_sign, p, out_idx, out_count, workspace: as
+ *             in kvr_select (the workspace as kvr_select_workspace_size).
+ *   V         device [B, Hkv, cap, d] (shape->dtype), or page-locked host
+ *             memory as for kvr_sparse_attend.
+ *   scale     logit scale (normally 1/sqrt(d)); NaN is KVR_ERR_INVALID_ARG.
+ *   out       device float [B, Hq, d] (written).
+ */
+kvr_status kvr_select_attend(const kvr_shape *shape, const kvr_select_params *p, const void *q,
+                             const void *K, const void *V, const uint8_t *codes,
+                             const int32_t *seq_len, const int8_t *srht_sign, float scale,
+                             int32_t *out_idx, int32_t *out_count, float *out, void *workspace,
+                             size_t workspace_bytes, int32_t *err_word, void *stream);
+
+/*
  * kvr_decode_step -- one decode step of every unit in one call: the code
  * (and, with p->rsq_records, the reranker record) of the appended key at row
  * pos_new[b], kvr_select, and the attention over its output (over the cache
  * regions when p->region_end is set, else over the top-k and the window W),
- * all enqueued on `stream`. Order: with p->region_end set or W == 0, the
+ * all enqueued on `stream` (the selection and attention as kvr_select_attend,
+ * one launch where it fuses them). Order: with p->region_end set or W == 0, the
  * encodes first, then the selection (KVR_SELECT_EARLY_INPUTS is ignored: it
  * follows the encode that writes its codes), then the attention. With W >= 1
  * and no regions the appended key must lie in the window,

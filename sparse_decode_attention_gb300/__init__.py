@@ -29,6 +29,7 @@ __all__ = [
     "kvr_tier_update_workspace_size", "kvr_tier_update",
     "kvr_rsq_record_bytes", "kvr_rsq_tables", "kvr_encode_rsq", "rsq_buffer",
     "kvr_sparse_attend_regions", "kvr_regions_update", "kvr_decode_step", "DecodeStep",
+    "kvr_select_attend", "SelectAttend",
 ]
 
 KVR_F32, KVR_BF16 = 0, 1
@@ -184,11 +185,16 @@ def load(build_if_missing: bool = True):
                                      ctypes.c_int, _P, _P, _P]
     L.kvr_decode_step.argtypes = [S, Pp, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P,
                                   _P, ctypes.c_size_t, _P, _P]
+    L.kvr_select_attend.argtypes = [S, Pp, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P,
+                                    ctypes.c_size_t, _P, _P]
+    L.kvr_testing_tiered_withheld_copy.argtypes = [S, T, _P, _P, _P, _P, ctypes.c_float, _P, _P,
+                                                   _P, ctypes.c_size_t, _P, _P, ctypes.c_int64]
     for fn in ("kvr_encode_keys", "kvr_select_workspace_views", "kvr_select",
                "kvr_select_static_scratch", "kvr_tier_init", "kvr_sparse_attend_tiered",
                "kvr_tier_update", "kvr_rsq_tables", "kvr_encode_rsq",
                "kvr_sparse_attend_regions", "kvr_regions_update", "kvr_decode_step",
-               "kvr_sparse_attend", "kvr_read_error"):
+               "kvr_select_attend", "kvr_sparse_attend", "kvr_read_error",
+               "kvr_testing_tiered_withheld_copy"):
         getattr(L, fn).restype = ctypes.c_int
     _lib = L
     return L
@@ -572,3 +578,69 @@ class DecodeStep:
         st = self._fn(*self._args)
         if st != 0:
             raise KvrError(st, "kvr_decode_step")
+
+
+def _select_attend_args(q, K, V, codes, seq_len, srht_sign, params, scale, out_idx, out_count, out,
+                        workspace, err, stream):
+    shape = Shape.of(_kv(K, "K"), _cuda(q, "q", K.dtype))
+    _kv(V, "V")
+    if V.dtype != K.dtype or V.shape != K.shape:
+        raise TypeError("V must have K's dtype and shape")
+    _codes(codes, shape)
+    for t, n, dt in ((seq_len, "seq_len", torch.int32), (srht_sign, "srht_sign", torch.int8),
+                     (out_idx, "out_idx", torch.int32), (out_count, "out_count", torch.int32),
+                     (out, "out", torch.float32)):
+        _cuda(t, n, dt)
+    _cuda(workspace, "workspace")
+    if out_idx.shape[-1] != params.k:
+        raise ValueError("out_idx rows must hold params.k entries")
+    return (ctypes.byref(shape.c()), ctypes.byref(params.c()), _ptr(q), _ptr(K), _ptr(V),
+            _ptr(codes), _ptr(seq_len), _ptr(srht_sign), float(scale), _ptr(out_idx),
+            _ptr(out_count), _ptr(out), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream))
+
+
+def kvr_select_attend(q, K, V, codes, seq_len, srht_sign, params: SelectParams, scale, out_idx,
+                      out_count, out, workspace, err=None, stream=None):
+    """kvr_select, then the attention over its top-k and the window (one
+    kernel launch for groups of up to 4 heads with exact rescoring)."""
+    _check(load().kvr_select_attend(*_select_attend_args(q, K, V, codes, seq_len, srht_sign,
+                                                         params, scale, out_idx, out_count, out,
+                                                         workspace, err, stream)),
+           "kvr_select_attend")
+
+
+class SelectAttend:
+    """kvr_select_attend with its arguments marshalled once (the tensors must
+    stay alive and in place); calling it enqueues the call."""
+
+    def __init__(self, q, K, V, codes, seq_len, srht_sign, params: SelectParams, scale, out_idx,
+                 out_count, out, workspace, err=None, stream=None):
+        self._keep = (q, K, V, codes, seq_len, srht_sign, params, out_idx, out_count, out,
+                      workspace, err, stream)
+        self._args = _select_attend_args(q, K, V, codes, seq_len, srht_sign, params, scale,
+                                         out_idx, out_count, out, workspace, err, stream)
+        self._fn = load().kvr_select_attend
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != 0:
+            raise KvrError(st, "kvr_select_attend")
+
+
+def _testing_tiered_withheld_copy(state: TierState, q, K, V, seq_len, scale, out, window_mass,
+                                  workspace, wait_ns, err=None, stream=None):
+    """Test hook (kvr_testing.h): the tiered attention with each CTA's last
+    bulk copy withheld and every copy wait limited to wait_ns; its wait runs
+    out and sets the timeout bit. Outputs are invalid afterwards."""
+    shape = Shape.of(_cuda(K, "K", torch.bfloat16), _cuda(q, "q", torch.bfloat16))
+    _cuda(V, "V", torch.bfloat16)
+    _cuda(seq_len, "seq_len", torch.int32)
+    _cuda(out, "out", torch.float32)
+    _cuda(window_mass, "window_mass", torch.float32)
+    _cuda(workspace, "workspace")
+    st = load().kvr_testing_tiered_withheld_copy(
+        ctypes.byref(shape.c()), ctypes.byref(state.c()), _ptr(q), _ptr(K), _ptr(V),
+        _ptr(seq_len), float(scale), _ptr(out), _ptr(window_mass), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream), int(wait_ns))
+    _check(st, "kvr_testing_tiered_withheld_copy")

@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "kvr_launch.h"
+#include "kvr_testing.h"
 
 namespace kvr {
 
@@ -250,6 +251,41 @@ kvr_status kvr_select(const kvr_shape *shape, const kvr_select_params *p, const 
                            static_cast<uint8_t *>(workspace), err_word);
 }
 
+kvr_status kvr_select_attend(const kvr_shape *shape, const kvr_select_params *p, const void *q,
+                             const void *K, const void *V, const uint8_t *codes,
+                             const int32_t *seq_len, const int8_t *srht_sign, float scale,
+                             int32_t *out_idx, int32_t *out_count, float *out, void *workspace,
+                             size_t workspace_bytes, int32_t *err_word, void *stream)
+{
+    kvr_status st = check_shape(shape);
+    if (st != KVR_OK) return st;
+    if ((st = check_params(p)) != KVR_OK) return st;
+    if (!q || !K || !V || !codes || !seq_len || !srht_sign || !out_count || !out || !workspace)
+        return KVR_ERR_INVALID_ARG;
+    if (p->k > 0 && !out_idx) return KVR_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(codes) ||
+        !aligned16(out_idx) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return KVR_ERR_INVALID_ARG;
+    if (!(scale == scale)) return KVR_ERR_INVALID_ARG;
+    const SelectPlan pl = plan_select(*shape, *p);
+    if (workspace_bytes < pl.bytes) return KVR_ERR_WORKSPACE;
+    LaunchCtx c{*shape, static_cast<cudaStream_t>(stream)};
+    if (select_attend_fusable(*shape, *p)) {
+        const FusedAttend att{V, scale, out};
+        return select_dispatch(c, *p, pl, q, K, codes, seq_len, srht_sign, out_idx, out_count,
+                               static_cast<uint8_t *>(workspace), err_word, &att);
+    }
+    if ((st = select_dispatch(c, *p, pl, q, K, codes, seq_len, srht_sign, out_idx, out_count,
+                              static_cast<uint8_t *>(workspace), err_word)) != KVR_OK)
+        return st;
+    if (p->region_end)
+        return attend_dispatch(c, plan_attend(*shape, p->k, 0), q, K, V, out_idx, p->k, out_count,
+                               seq_len, 0, p->sink, p->region_end, scale, out, nullptr, err_word);
+    return attend_dispatch(c, plan_attend(*shape, p->k, p->W), q, K, V, out_idx, p->k, out_count,
+                           seq_len, p->W, 0, nullptr, scale, out, nullptr, err_word);
+}
+
 kvr_status kvr_decode_step(const kvr_shape *shape, const kvr_select_params *p, const void *q,
                            const void *K, const void *V, uint8_t *codes, const int32_t *seq_len,
                            const int32_t *pos_new, const int8_t *srht_sign, int32_t *out_idx,
@@ -282,15 +318,11 @@ kvr_status kvr_decode_step(const kvr_shape *shape, const kvr_select_params *p, c
             (st = rsq_encode_dispatch(c, K, pos_new, 1, srht_sign, records, err_word)) != KVR_OK)
             return st;
     }
-    if ((st = kvr_select(shape, &ps, q, K, codes, seq_len, srht_sign, out_idx, out_count, workspace,
-                         workspace_bytes, err_word, stream)) != KVR_OK)
+    if ((st = kvr_select_attend(shape, &ps, q, K, V, codes, seq_len, srht_sign, scale, out_idx,
+                                out_count, out, workspace, workspace_bytes, err_word, stream)) !=
+        KVR_OK)
         return st;
-    if (p->region_end)
-        return kvr_sparse_attend_regions(shape, q, K, V, out_idx, p->k, out_count, seq_len, p->sink,
-                                         p->region_end, scale, out, nullptr, 0, err_word, stream);
-    if ((st = kvr_sparse_attend(shape, q, K, V, out_idx, p->k, out_count, seq_len, p->W, scale, out,
-                                nullptr, 0, err_word, stream)) != KVR_OK)
-        return st;
+    if (!late) return KVR_OK;
     if ((st = encode_dispatch(c, K, pos_new, 1, srht_sign, codes, err_word, seq_len, p->W)) != KVR_OK)
         return st;
     if (records && (st = rsq_encode_dispatch(c, K, pos_new, 1, srht_sign, records, err_word, true)) !=
@@ -431,6 +463,29 @@ kvr_status kvr_sparse_attend_tiered(const kvr_shape *shape, const kvr_tier_state
     LaunchCtx c{*shape, static_cast<cudaStream_t>(stream)};
     return tiered_attend_dispatch(c, *state, q, K, V, seq_len, scale, out, window_mass,
                                   static_cast<uint8_t *>(workspace), err_word);
+}
+
+kvr_status kvr_testing_tiered_withheld_copy(const kvr_shape *shape, const kvr_tier_state *state,
+                                            const void *q, const void *K, const void *V,
+                                            const int32_t *seq_len, float scale, float *out,
+                                            float *window_mass, void *workspace,
+                                            size_t workspace_bytes, int32_t *err_word,
+                                            void *stream, int64_t wait_ns)
+{
+    kvr_status st = check_tiers(shape, state, true);
+    if (st != KVR_OK) return st;
+    if (!q || !K || !V || !seq_len || !out || !window_mass || !workspace)
+        return KVR_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(window_mass) & 3u) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return KVR_ERR_INVALID_ARG;
+    if (!(scale == scale) || wait_ns < 1 || wait_ns > 10000000000ll) return KVR_ERR_INVALID_ARG;
+    if (workspace_bytes < tiered_attend_ws_bytes(*shape, state->n_win)) return KVR_ERR_WORKSPACE;
+    LaunchCtx c{*shape, static_cast<cudaStream_t>(stream)};
+    return tiered_attend_dispatch(c, *state, q, K, V, seq_len, scale, out, window_mass,
+                                  static_cast<uint8_t *>(workspace), err_word, (uint64_t)wait_ns,
+                                  true);
 }
 
 size_t kvr_tier_update_workspace_size(const kvr_shape *shape, int64_t n_win)

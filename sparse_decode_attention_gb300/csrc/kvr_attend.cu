@@ -69,49 +69,6 @@ template <int D, typename T, int G> struct AttCfg {
     static_assert(kTok % kWarps == 0, "batch split");
 };
 
-template <int E, typename T>
-__device__ __forceinline__ void load_lane(const uint8_t *row, int lane, float (&x)[E])
-{
-    const T *p = reinterpret_cast<const T *>(row) + lane * E;
-    if constexpr (sizeof(T) == 2 && E == 2) {
-        const uint32_t w = *reinterpret_cast<const uint32_t *>(p);
-        x[0] = bf16_lo(w);
-        x[1] = bf16_hi(w);
-    } else if constexpr (sizeof(T) == 4 && E == 2) {
-        const float2 v = *reinterpret_cast<const float2 *>(p);
-        x[0] = v.x;
-        x[1] = v.y;
-    } else {
-        widen<E>(p, x);
-    }
-}
-
-// Sum G per-lane values over the warp; lane l returns the total of head
-// l / (32 / G). Splitting halves of the value set between partner lanes costs
-// G - 1 + 5 - log2(G) shuffles instead of 5G.
-template <int G>
-__device__ __forceinline__ float reduce_heads(float (&v)[G], int lane)
-{
-    __syncwarp();
-    constexpr int LG = (G >= 16) ? 4 : (G >= 8) ? 3 : (G >= 4) ? 2 : (G >= 2) ? 1 : 0;
-#pragma unroll
-    for (int s = 0; s < LG; s++) {
-        const int o = 16 >> s;
-        const int half = G >> (s + 1);
-        const bool upper = (lane & o) != 0;
-#pragma unroll
-        for (int i = 0; i < half; i++) {
-            const float send = upper ? v[i] : v[i + half];
-            const float keep = upper ? v[i + half] : v[i];
-            v[i] = keep + __shfl_xor_sync(kFull, send, o);
-        }
-    }
-    float x = v[0];
-#pragma unroll
-    for (int o = 16 >> LG; o >= 1; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
-    return x;
-}
-
 template <int D, typename T, int G>
 __global__ void __launch_bounds__(AttCfg<D, T, G>::kThreads, (G >= 16) ? 1 : 2) attend_kernel(AttArgs a)
 {

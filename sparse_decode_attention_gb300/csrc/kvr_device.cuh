@@ -56,6 +56,52 @@ template <int N> __device__ __forceinline__ void widen(const __nv_bfloat16 *p, f
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
 
+// ---------------------------------------------------------------- attention rows
+
+// The E consecutive elements of a row that lane `lane` holds (d = 32 E).
+template <int E, typename T>
+__device__ __forceinline__ void load_lane(const uint8_t *row, int lane, float (&x)[E])
+{
+    const T *p = reinterpret_cast<const T *>(row) + lane * E;
+    if constexpr (sizeof(T) == 2 && E == 2) {
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(p);
+        x[0] = bf16_lo(w);
+        x[1] = bf16_hi(w);
+    } else if constexpr (sizeof(T) == 4 && E == 2) {
+        const float2 v = *reinterpret_cast<const float2 *>(p);
+        x[0] = v.x;
+        x[1] = v.y;
+    } else {
+        widen<E>(p, x);
+    }
+}
+
+// Sum G per-lane values over the warp; lane l returns the total of head
+// l / (32 / G). Splitting halves of the value set between partner lanes costs
+// G - 1 + 5 - log2(G) shuffles instead of 5G.
+template <int G>
+__device__ __forceinline__ float reduce_heads(float (&v)[G], int lane)
+{
+    __syncwarp();
+    constexpr int LG = (G >= 16) ? 4 : (G >= 8) ? 3 : (G >= 4) ? 2 : (G >= 2) ? 1 : 0;
+#pragma unroll
+    for (int s = 0; s < LG; s++) {
+        const int o = 16 >> s;
+        const int half = G >> (s + 1);
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < half; i++) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(kFull, send, o);
+        }
+    }
+    float x = v[0];
+#pragma unroll
+    for (int o = 16 >> LG; o >= 1; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+    return x;
+}
+
 // ---------------------------------------------------------------- rotation
 
 // Natural-order fast Walsh-Hadamard transform of one vector spread over a
@@ -293,13 +339,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for phase `parity` of an mbarrier with an iteration limit; on expiry the
-// error bit is set and the caller carries on (every cluster barrier is still
-// reached, so no CTA is left waiting).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err)
+__device__ __forceinline__ uint64_t global_ns()
 {
-    for (int i = 0; i < (1 << 24); i++)
-        if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Default limit of a wait for a bulk copy: a copy lands within microseconds,
+// so a wait still open after a second means the copy was never issued.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// Wait for phase `parity` of an mbarrier for at most limit_ns nanoseconds
+// (device global timer); on expiry the error bit is set, false is returned
+// and the caller carries on (its outputs are invalid; it must stop issuing
+// copies and wait, again with a limit, for those still in flight).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err,
+                                          uint64_t limit_ns = kWaitLimitNs)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        for (int i = 0; i < 32; i++)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > limit_ns) break;
+    }
     set_err(err, KVR_DEVERR_TIMEOUT);
     return false;
 }
@@ -364,6 +428,19 @@ __device__ __forceinline__ void grid_dependency_wait()
 __device__ __forceinline__ void grid_launch_dependents()
 {
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+// Split cluster barrier: every thread of every CTA of the cluster arrives
+// (release: its earlier memory accesses, including reads of other CTAs'
+// shared memory, are complete) and later waits (acquire). Work between the
+// two must not arrive at another cluster barrier.
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
 // fp32 -> uint32 key whose unsigned order is the float order; -0 maps as +0.

@@ -70,10 +70,25 @@ kvr_status encode_dispatch(const LaunchCtx &c, const void *K, const int32_t *pos
                            const int8_t *sgn, uint8_t *codes, int32_t *err,
                            const int32_t *late_seq_len = nullptr, int W = 0);
 
+// The attention fused into the selection's launch: value cache, logit
+// scale (1/sqrt(d) in the caller's units) and output [B, Hq, d] fp32.
+struct FusedAttend {
+    const void *V;
+    float scale;
+    float *out;
+};
+
+// Whether kvr_select_attend runs as one launch for these arguments: query
+// groups of up to 4 heads, exact rescoring, Hamming-ring votes.
+bool select_attend_fusable(const kvr_shape &s, const kvr_select_params &p);
+
+// att != null: the selection kernel also runs the step's attention (only
+// when select_attend_fusable; KVR_ERR_UNSUPPORTED otherwise).
 kvr_status select_dispatch(const LaunchCtx &c, const kvr_select_params &p, const SelectPlan &plan,
                            const void *q, const void *K, const uint8_t *codes,
                            const int32_t *seq_len, const int8_t *sgn, int32_t *out_idx,
-                           int32_t *out_count, uint8_t *ws, int32_t *err);
+                           int32_t *out_count, uint8_t *ws, int32_t *err,
+                           const FusedAttend *att = nullptr);
 
 kvr_status attend_dispatch(const LaunchCtx &c, const AttendPlan &plan, const void *q,
                            const void *K, const void *V, const int32_t *idx, int kmax,
@@ -102,9 +117,12 @@ size_t tiered_attend_ws_bytes(const kvr_shape &s, int64_t n_win);
 size_t tier_update_ws_bytes(const kvr_shape &s, int64_t n_win);
 kvr_status tier_init_dispatch(const LaunchCtx &c, const kvr_tier_state &s, const int8_t *init,
                               const void *K, const void *V, const int32_t *seq_len, int32_t *err);
+// wait_ns: limit of each wait for a bulk copy; withhold_last: the test hook
+// of kvr_testing_tiered_withheld_copy (each CTA never issues its last copy).
 kvr_status tiered_attend_dispatch(const LaunchCtx &c, const kvr_tier_state &s, const void *q,
                                   const void *K, const void *V, const int32_t *seq_len,
-                                  float scale, float *out, float *mass, uint8_t *ws, int32_t *err);
+                                  float scale, float *out, float *mass, uint8_t *ws, int32_t *err,
+                                  uint64_t wait_ns = 1000000000ull, bool withhold_last = false);
 kvr_status tier_update_dispatch(const LaunchCtx &c, const kvr_tier_state &s, const float *mass,
                                 const int32_t *seq_len, void *K, void *V, int32_t *stats,
                                 uint8_t *ws, int32_t *err);

@@ -18,13 +18,16 @@
 //      ripple adder into the score planes; a histogram of the top score bits
 //      is kept in registers.
 //   P2 two cluster exchanges of 16-bin histograms fix the threshold score T,
-//      the tie quota and every CTA's output offset (ties by lowest index).
-//   P3 candidates are compacted in index order into the workspace and, via
-//      distributed shared memory, into the CTA that rescores them.
-//   P4 after a cluster barrier every CTA takes an equal slice of the candidate
-//      list, loads the K rows (prefetched into L2 in P3) straight into
-//      registers, 16 lanes per row and 8 rows in flight per half-warp, and
-//      computes the canonical fp32 dot q_bar . k (half-warp per row).
+//      the tie quota and every CTA's candidate count and list offset (ties by
+//      lowest index).
+//   P3 candidates are compacted in index order into the workspace and, when
+//      their spread over the CTAs is near even, kept by the CTA that found
+//      them; otherwise they move through distributed shared memory to the CTA
+//      whose equal slice of the list holds them (one more cluster barrier).
+//   P4 every CTA rescores its slice: it loads the K rows (prefetched into L2
+//      in P3) straight into registers, 16 lanes per row and 8 rows in flight
+//      per half-warp, and computes the canonical fp32 dot q_bar . k
+//      (half-warp per row).
 //   P5 the k'-th largest exact score (order-preserving uint32 keys) in three
 //      small cluster exchanges: the score range, a 256-bin linear histogram
 //      of every CTA's slice over that range, then the keys of the one
@@ -33,6 +36,9 @@
 //      too large to gather (massive ties) falls back to every CTA gathering
 //      all C' keys. Each CTA also gets its output offset.
 //   P6 winners are written ascending by index.
+//   P7 (the kvr_select_attend instantiations) the attention over the step's
+//      tokens in the same cluster: each CTA over its winners and a share of
+//      the window, partials merged through distributed shared memory.
 // Every cluster barrier is reached by every CTA on every path (control flow
 // around them depends only on per-unit values).
 #include <cooperative_groups.h>
@@ -76,6 +82,10 @@ struct SelArgs {
     uint8_t *coarse;  // [U][cap_pad] or null
     int64_t nblk, cap_pad, tiles;
     int32_t *err;
+    // fused attention (instantiations with GA > 0): output [B, Hq, d] fp32
+    // and the logit scale in the log2 domain; V above is the value cache
+    float *att_out;
+    float att_scale_log2;
 };
 
 __host__ __device__ constexpr int bit_width(int v)
@@ -194,7 +204,11 @@ template <int D, typename T> struct SelSmem {
     static constexpr int oWH = oMisc + 64 * 4;  // [kSelWarps][256] per-warp histograms
     static constexpr int oPl = oWH + kSelWarps * 256 * 4;  // [8][kPlaneCap] score planes
     static constexpr int oLev = oPl + 8 * kPlaneCap * 4;  // float [16] signed reranker levels
-    static constexpr int bytes = oLev + 16 * 4;
+    static constexpr int oAtt = oLev + 16 * 4;  // fused attention: m[4], l[4], o[4][D] of the CTA
+    static constexpr int bytes = oAtt + (8 + 4 * D) * 4;
+    // fused attention: K and V rows of a chunk of tokens are staged over the
+    // code ring and the candidate arrays (free once the winners are known)
+    static constexpr int kStage = oQm;
     static_assert(16 * 256 * 4 <= kRingBytes, "radix exchange scratch must fit the ring");
     static_assert(oWH % 16 == 0, "boundary keys are read 16 bytes at a time");
     static_assert((D / 8) * kVoteStride * 2 <= 2 * kMaxSlice * 4, "vote lists must fit sS + sI");
@@ -202,16 +216,221 @@ template <int D, typename T> struct SelSmem {
 
 enum {
     M_U1 = 0, M_REM1, M_T, M_TAKE, M_OFF, M_KTAKE, M_KOFF, M_NSUB, M_KEYT, M_QUOTA,
-    M_CNT, M_ABOVEB,
+    M_CNT, M_ABOVEB, M_LOCAL, M_NW,
     M_BOUND = 16,  // [17] first candidate position of each CTA's P4 slice, then C'
     M_KMIN = 33, M_KMAX, M_GMIN, M_GMAX, M_AOWN,
     M_SEG = 40,    // [17] first boundary-key position of each CTA, then the total
 };
 
+// ---------------------------------------------------------------- P7
+// Fused attention of one unit's step, run by each CTA of the selection's
+// cluster after P6 (ParisKV, "Problematica": decode attends to the top-k
+// subset; "Meccanismo di Aggiornamento a Finestra Scorrevole": the Local
+// region is always attended). CTA `rank` takes its own winners (sWin, nw of
+// them), every CS-th token of the Local (+ buffer) region [pool, N) and every
+// CS-th Sink token [0, p0). The K and V rows of up to CH tokens at a time are
+// staged in shared memory with 16-byte cp.async copies (over the code ring
+// and the candidate arrays, dead by now). A token's row is spread over a
+// warp (d/32 dims per lane); the GA per-head dots are reduced so that head g
+// lands in lanes [g*32/GA, (g+1)*32/GA); online softmax in the log2 domain;
+// p*v accumulated in registers. Heads past the group size G score against a
+// zero query and are never written. Warps merge in shared memory, CTAs
+// through distributed shared memory; each CTA writes an equal share of the
+// unit's G*d outputs. Contains cluster barriers: every CTA calls it, after
+// arriving at the split barrier that this function's first wait completes.
+template <int D, typename T, int GA>
+__device__ __forceinline__ void attend_tail(const SelArgs &a, uint8_t *smem, const int32_t *sWin,
+                                            int nw, int b, int h, int64_t N, int64_t p0,
+                                            int64_t pool, int rank, int CS)
+{
+    using SM = SelSmem<D, T>;
+    constexpr int E = D / 32, RB = SM::kRowBytes, PPR = RB / 16, LPH = 32 / GA;
+    constexpr int CH = SM::kStage / (2 * RB);  // tokens staged at once
+    constexpr int TPW = 8;                     // tokens per warp per round
+    static_assert(CH >= kSelWarps * TPW, "a round fits the stage");
+    static_assert(kSelWarps * GA * (D + 2) * 4 <= SM::kStage, "warp partials fit the stage");
+    cg::cluster_group cluster = cg::this_cluster();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = a.G;
+    const int u = blockIdx.y;
+    float *sPm = reinterpret_cast<float *>(smem + SM::oAtt);
+    float *sPl = sPm + 4;
+    float *sPo = sPm + 8;
+
+    const int64_t nloc = N - pool;
+    const int nlm = nloc > rank ? (int)((nloc - rank + CS - 1) / CS) : 0;
+    const int nsm = p0 > rank ? (int)((p0 - rank + CS - 1) / CS) : 0;
+    const int total = nw + nlm + nsm;
+    auto token = [&](int i) -> int64_t {
+        if (i < nw) return sWin[i];
+        if (i < nw + nlm) return pool + rank + (int64_t)CS * (i - nw);
+        return rank + (int64_t)CS * (i - nw - nlm);
+    };
+
+    float qr[GA][E];
+    {
+        const T *qg = static_cast<const T *>(a.q) + ((int64_t)b * a.Hq + (int64_t)h * G) * D;
+#pragma unroll
+        for (int g = 0; g < GA; g++)
+#pragma unroll
+            for (int e = 0; e < E; e++)
+                qr[g][e] = (g < G) ? to_f32(qg[g * D + lane * E + e]) * a.att_scale_log2 : 0.0f;
+    }
+    float acc[GA][E];
+#pragma unroll
+    for (int g = 0; g < GA; g++)
+#pragma unroll
+        for (int e = 0; e < E; e++) acc[g][e] = 0.0f;
+    float m = -INFINITY, l = 0.0f;  // softmax state of head lane / LPH
+
+    const uint8_t *Ku = static_cast<const uint8_t *>(a.K) + (size_t)u * a.cap * RB;
+    const uint8_t *Vu = static_cast<const uint8_t *>(a.V) + (size_t)u * a.cap * RB;
+    uint8_t *stK = smem, *stV = smem + CH * RB;
+    __syncwarp();
+    cluster_wait_acquire();  // no CTA reads this one's ring or scores any more (arrived after P5)
+    for (int c0 = 0; c0 < total; c0 += CH) {
+        const int ch = min(CH, total - c0);
+        for (int pc = tid; pc < ch * PPR; pc += kSelThreads) {
+            const int j = pc / PPR, part = pc % PPR;
+            const size_t t = (size_t)token(c0 + j);
+            cp_async16(stK + j * RB + part * 16, Ku + t * RB + part * 16);
+            cp_async16(stV + j * RB + part * 16, Vu + t * RB + part * 16);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
+        for (int jb = 0; jb < ch; jb += kSelWarps * TPW) {
+            // branch-free over the warp's slots (the shuffle chains interleave);
+            // a slot past the chunk scores -inf and adds nothing
+            float s[TPW];
+#pragma unroll
+            for (int jj = 0; jj < TPW; jj++) {
+                const int j = jb + jj * kSelWarps + warp;
+                const bool live = j < ch;
+                float kv[E];
+                load_lane<E, T>(stK + (live ? j : 0) * RB, lane, kv);
+                float part[GA];
+#pragma unroll
+                for (int g = 0; g < GA; g++) {
+                    float d = 0.0f;
+#pragma unroll
+                    for (int e = 0; e < E; e++) d = fmaf(qr[g][e], kv[e], d);
+                    part[g] = d;
+                }
+                const float sc = reduce_heads<GA>(part, lane);
+                s[jj] = live ? sc : -INFINITY;
+            }
+            float mb = -INFINITY;
+#pragma unroll
+            for (int jj = 0; jj < TPW; jj++) mb = fmaxf(mb, s[jj]);
+            const float m_new = fmaxf(m, mb);
+            const float alpha = (m == -INFINITY) ? 0.0f : exp2f(m - m_new);
+            float p[TPW], ps = 0.0f;
+#pragma unroll
+            for (int jj = 0; jj < TPW; jj++) {
+                p[jj] = (s[jj] == -INFINITY) ? 0.0f : exp2f(s[jj] - m_new);
+                ps += p[jj];
+            }
+            l = l * alpha + ps;
+            m = m_new;
+#pragma unroll
+            for (int g = 0; g < GA; g++) {
+                const float ag = __shfl_sync(kFull, alpha, g * LPH);
+#pragma unroll
+                for (int e = 0; e < E; e++) acc[g][e] *= ag;
+            }
+#pragma unroll
+            for (int jj = 0; jj < TPW; jj++) {
+                const int j = jb + jj * kSelWarps + warp;
+                const bool live = j < ch;
+                float vv[E];
+                load_lane<E, T>(stV + (live ? j : 0) * RB, lane, vv);
+#pragma unroll
+                for (int e = 0; e < E; e++) vv[e] = live ? vv[e] : 0.0f;
+#pragma unroll
+                for (int g = 0; g < GA; g++) {
+                    const float pg = __shfl_sync(kFull, p[jj], g * LPH);
+#pragma unroll
+                    for (int e = 0; e < E; e++) acc[g][e] = fmaf(pg, vv[e], acc[g][e]);
+                }
+            }
+        }
+        __syncthreads();  // the stage is refilled (or reused for the warp partials)
+    }
+
+    // merge the warps (their partials over the stage)
+    float *sWm = reinterpret_cast<float *>(smem);  // [warps][GA]
+    float *sWl = sWm + kSelWarps * GA;             // [warps][GA]
+    float *sWo = sWl + kSelWarps * GA;             // [warps][GA][D]
+    if ((lane % LPH) == 0) {
+        sWm[warp * GA + lane / LPH] = m;
+        sWl[warp * GA + lane / LPH] = l;
+    }
+#pragma unroll
+    for (int g = 0; g < GA; g++)
+#pragma unroll
+        for (int e = 0; e < E; e++) sWo[(warp * GA + g) * D + lane * E + e] = acc[g][e];
+    __syncthreads();
+    for (int t = tid; t < G * D; t += kSelThreads) {
+        const int g = t / D, dim = t % D;
+        float M = -INFINITY;
+        for (int w = 0; w < kSelWarps; w++) M = fmaxf(M, sWm[w * GA + g]);
+        float L = 0.0f, O = 0.0f;
+        if (M != -INFINITY) {
+            for (int w = 0; w < kSelWarps; w++) {
+                const float mw = sWm[w * GA + g];
+                if (mw == -INFINITY) continue;
+                const float f = exp2f(mw - M);
+                L = fmaf(sWl[w * GA + g], f, L);
+                O = fmaf(sWo[(w * GA + g) * D + dim], f, O);
+            }
+        }
+        sPo[t] = O;
+        if (dim == 0) {
+            sPm[g] = M;
+            sPl[g] = L;
+        }
+    }
+    __syncthreads();
+    cluster.sync();  // CTA partials published
+
+    // this CTA's share of the outputs: a 16-lane group per output, lane r
+    // reading CTA r's partial (all remote loads in flight at once), then
+    // butterfly reductions of the group's max and weighted sums
+    const int e0 = rank * (G * D) / CS, e1 = (rank + 1) * (G * D) / CS;
+    const int grp = tid >> 4, r = tid & 15;
+    for (int t0 = e0; t0 < e1; t0 += kSelThreads / 16) {
+        const int t = t0 + grp;
+        const bool on = t < e1;
+        const int tt = on ? t : e0;
+        const int g = tt / D, dim = tt % D;
+        float mr = -INFINITY, lr = 0.0f, orr = 0.0f;
+        if (r < CS) {
+            mr = *cluster.map_shared_rank(&sPm[g], r);
+            lr = *cluster.map_shared_rank(&sPl[g], r);
+            orr = *cluster.map_shared_rank(&sPo[tt], r);
+        }
+        float M = mr;
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+        const float f = (mr == -INFINITY) ? 0.0f : exp2f(mr - M);
+        float L = lr * f, O = orr * f;
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) {
+            L += __shfl_xor_sync(kFull, L, o);
+            O += __shfl_xor_sync(kFull, O, o);
+        }
+        if (on && r == 0)
+            a.att_out[((size_t)b * a.Hq + (size_t)h * G + g) * D + dim] = (L > 0.0f) ? O / L : 0.0f;
+    }
+}
+
 // EXT: the instantiation carries the optional modes (reranker records,
 // magnitude-aware votes); without it their code is compiled out, which keeps
 // the common kernel smaller (instruction fetch is its top stall).
-template <int D, typename T, int VB, bool EXT>
+// GA > 0: the attention over the step's tokens runs in the same cluster
+// after the selection (P7), for query groups of up to GA heads.
+template <int D, typename T, int VB, bool EXT, int GA>
 __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
 {
     using SM = SelSmem<D, T>;
@@ -481,94 +700,116 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     cluster.sync();  // #1: level-1 histograms published
 
     // ---------------------------------------------------------------- P2
-    for (int t = tid; t < CS * NL1; t += kSelThreads) {
-        const int r = t / NL1, v = t % NL1;
-        sAll[r * 16 + v] = *cluster.map_shared_rank(&sH1[v], r);
-    }
-    __syncthreads();
-    if (warp == 0) {
-        // lane v: cluster-wide count of bucket v; the C'-th key sits in the
-        // highest bucket whose suffix count reaches C'
-        int tot = 0;
-        if (lane < NL1)
-            for (int r = 0; r < CS; r++) tot += sAll[r * 16 + lane];
-        const int suf = warp_suffix_sum(tot);
-        int u1 = -1, rem = Cp;
-        if (Cp > 0) {
-            const unsigned ok = __ballot_sync(kFull, lane < NL1 && suf >= Cp);
-            u1 = __popc(ok) - 1;
-            rem = Cp - __shfl_sync(kFull, suf - tot, u1);
-        }
-        if (lane == 0) {
-            sMisc[M_U1] = u1;
-            sMisc[M_REM1] = rem;
-        }
-    }
-    __syncthreads();
-    const int u1 = sMisc[M_U1];
-    if (u1 >= 0) {
-        int cnt2[NL2];
-#pragma unroll
-        for (int i = 0; i < NL2; i++) cnt2[i] = 0;
-        for (int64_t blk = blk0 + tid; blk < blk1; blk += kSelThreads) {
-            uint32_t p[ACC];
-#pragma unroll
-            for (int j = 0; j < ACC; j++) p[j] = plane(j, blk);
-            uint32_t inb = pool_mask(blk, p0, pool);
-#pragma unroll
-            for (int j = 0; j < H1; j++) inb &= ((u1 >> j) & 1) ? p[LOWB + j] : ~p[LOWB + j];
-#pragma unroll
-            for (int v = 0; v < NL2; v++) {
-                uint32_t m = inb;
-#pragma unroll
-                for (int j = 0; j < LOWB; j++) m &= ((v >> j) & 1) ? p[j] : ~p[j];
-                cnt2[v] += __popc(m);
-            }
-        }
-        const int s = warp_reduce_split<NL2>(cnt2);  // lane l: value l / (32 / NL2)
-        if ((lane % (32 / NL2)) == 0 && s) atomicAdd(&sH2[lane / (32 / NL2)], s);
-    }
-    __syncthreads();
-    cluster.sync();  // #2: level-2 histograms published
-
-    for (int t = tid; t < CS * NL2; t += kSelThreads) {
-        const int r = t / NL2, v = t % NL2;
-        sAll[256 + r * 16 + v] = *cluster.map_shared_rank(&sH2[v], r);
-    }
-    __syncthreads();
-    if (warp == 0) {
-        int Tthr = 1 << 30, take = 0, off = 0;
-        if (u1 >= 0) {
-            const int rem = sMisc[M_REM1];
-            int tot = 0;
-            if (lane < NL2)
-                for (int r = 0; r < CS; r++) tot += sAll[256 + r * 16 + lane];
-            const int suf = warp_suffix_sum(tot);
-            const unsigned ok = __ballot_sync(kFull, lane < NL2 && suf >= rem);
-            const int v2 = __popc(ok) - 1;
-            const int quota = rem - __shfl_sync(kFull, suf - tot, v2);  // ties at T taken
-            Tthr = (u1 << LOWB) | v2;
-            // lane r: CTA r's keys above T and ties at T; ties go to the lowest indices
-            int gt = 0, eq = 0;
-            if (lane < CS) {
-                for (int v = u1 + 1; v < NL1; v++) gt += sAll[lane * 16 + v];
-                for (int v = v2 + 1; v < NL2; v++) gt += sAll[256 + lane * 16 + v];
-                eq = sAll[256 + lane * 16 + v2];
-            }
-            const int eq_before = warp_exclusive_scan(eq);
-            const int tk = (lane < CS) ? max(0, min(quota - eq_before, eq)) : 0;
-            const int sel_before = warp_exclusive_scan(gt + tk);
-            take = __shfl_sync(kFull, tk, rank);
-            off = __shfl_sync(kFull, sel_before, rank);
-        }
+    // The threshold score T (the C'-th largest), the ties at T taken, and
+    // every CTA's count of candidates and its offset in the index-ordered
+    // list. When the candidates spread near evenly over the CTAs, each CTA
+    // rescores its own (its P4 slice is its list segment: no redistribution,
+    // no cluster barrier before P4); otherwise the list is cut into equal
+    // slices and the candidates move to the CTA whose slice holds them.
+    // Warp 0, lane r = CTA r: gt / eq = keys above / at T; the ties go to the
+    // lowest indices, so to the CTAs in rank order.
+    auto finish_threshold = [&](int Tthr, int quota, int gt, int eq) {
+        const int eq_before = warp_exclusive_scan(eq);
+        const int tk = (lane < CS) ? max(0, min(quota - eq_before, eq)) : 0;
+        const int cnt = gt + tk;
+        const int sel_before = warp_exclusive_scan(cnt);
+        // local only when the spread is near even: ties go to the lowest
+        // indices, so the first CTAs can hold many more than C'/CS, and the
+        // slowest rescoring CTA sets every later barrier
+        const int nmax = __reduce_max_sync(kFull, (unsigned)cnt);
+        const int even = (Cp + CS - 1) / CS;
+        const bool local = nmax <= kMaxSlice && nmax <= even + even / 16 + 16;
+        if (local && lane <= CS) sMisc[M_BOUND + lane] = sel_before;  // lane CS: C'
         if (lane == 0) {
             sMisc[M_T] = Tthr;
-            sMisc[M_TAKE] = take;
-            sMisc[M_OFF] = off;
-            if (rank == 0) a.cand_count[u] = Cp;
+            sMisc[M_LOCAL] = local ? 1 : 0;
         }
+        if (lane == rank) {
+            sMisc[M_TAKE] = tk;
+            sMisc[M_OFF] = sel_before;
+        }
+    };
+    {
+        for (int t = tid; t < CS * NL1; t += kSelThreads) {
+            const int r = t / NL1, v = t % NL1;
+            sAll[r * 16 + v] = *cluster.map_shared_rank(&sH1[v], r);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // lane v: cluster-wide count of bucket v; the C'-th key sits in the
+            // highest bucket whose suffix count reaches C'
+            int tot = 0;
+            if (lane < NL1)
+                for (int r = 0; r < CS; r++) tot += sAll[r * 16 + lane];
+            const int suf = warp_suffix_sum(tot);
+            int u1 = -1, rem = Cp;
+            if (Cp > 0) {
+                const unsigned ok = __ballot_sync(kFull, lane < NL1 && suf >= Cp);
+                u1 = __popc(ok) - 1;
+                rem = Cp - __shfl_sync(kFull, suf - tot, u1);
+            }
+            if (lane == 0) {
+                sMisc[M_U1] = u1;
+                sMisc[M_REM1] = rem;
+            }
+        }
+        __syncthreads();
+        const int u1 = sMisc[M_U1];
+        if (u1 >= 0) {
+            int cnt2[NL2];
+#pragma unroll
+            for (int i = 0; i < NL2; i++) cnt2[i] = 0;
+            for (int64_t blk = blk0 + tid; blk < blk1; blk += kSelThreads) {
+                uint32_t p[ACC];
+#pragma unroll
+                for (int j = 0; j < ACC; j++) p[j] = plane(j, blk);
+                uint32_t inb = pool_mask(blk, p0, pool);
+#pragma unroll
+                for (int j = 0; j < H1; j++) inb &= ((u1 >> j) & 1) ? p[LOWB + j] : ~p[LOWB + j];
+#pragma unroll
+                for (int v = 0; v < NL2; v++) {
+                    uint32_t m = inb;
+#pragma unroll
+                    for (int j = 0; j < LOWB; j++) m &= ((v >> j) & 1) ? p[j] : ~p[j];
+                    cnt2[v] += __popc(m);
+                }
+            }
+            const int s = warp_reduce_split<NL2>(cnt2);  // lane l: value l / (32 / NL2)
+            if ((lane % (32 / NL2)) == 0 && s) atomicAdd(&sH2[lane / (32 / NL2)], s);
+        }
+        __syncthreads();
+        cluster.sync();  // #2: level-2 histograms published
+
+        for (int t = tid; t < CS * NL2; t += kSelThreads) {
+            const int r = t / NL2, v = t % NL2;
+            sAll[256 + r * 16 + v] = *cluster.map_shared_rank(&sH2[v], r);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            int Tthr = 1 << 30, quota = 0, gt = 0, eq = 0;
+            if (u1 >= 0) {
+                const int rem = sMisc[M_REM1];
+                int tot = 0;
+                if (lane < NL2)
+                    for (int r = 0; r < CS; r++) tot += sAll[256 + r * 16 + lane];
+                const int suf = warp_suffix_sum(tot);
+                const unsigned ok = __ballot_sync(kFull, lane < NL2 && suf >= rem);
+                const int v2 = __popc(ok) - 1;
+                quota = rem - __shfl_sync(kFull, suf - tot, v2);  // ties at T taken
+                Tthr = (u1 << LOWB) | v2;
+                if (lane < CS) {
+                    for (int v = u1 + 1; v < NL1; v++) gt += sAll[lane * 16 + v];
+                    for (int v = v2 + 1; v < NL2; v++) gt += sAll[256 + lane * 16 + v];
+                    eq = sAll[256 + lane * 16 + v2];
+                }
+            }
+            finish_threshold(Tthr, quota, gt, eq);
+            if (lane == 0 && rank == 0) a.cand_count[u] = Cp;
+        }
+        __syncthreads();
     }
-    __syncthreads();
+    const int u1 = sMisc[M_U1];
+    const bool local = sMisc[M_LOCAL] != 0;
 
     // ---------------------------------------------------------------- P3
     const int Tthr = sMisc[M_T];
@@ -597,8 +838,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         int allow = max(0, min(take - eq_before, n_eq));
         int pos = gt_before + min(take, eq_before) + sMisc[M_OFF];
         // owner CTA of list position pos and its slice [s_lo, s_hi), advanced
-        // as pos grows (positions only increase)
-        int r2 = slice_owner(pos);
+        // as pos grows (positions only increase); in the local mode this CTA
+        int r2 = local ? rank : slice_owner(pos);
         int s_lo = sMisc[M_BOUND + r2], s_hi = sMisc[M_BOUND + r2 + 1];
         for (int64_t blk = my0; blk < my1; blk++) {
             uint32_t p[ACC], gt = 0, eq = 0;
@@ -613,7 +854,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
                 for (uint32_t m = eq; m && allow > 0; m &= m - 1, allow--) te |= m & (0u - m);
                 for (uint32_t m = gt | te; m; m &= m - 1) {
                     const int32_t id = (int32_t)(blk * 32 + __ffs(m) - 1);
-                    // the row (or record) is read in P4, a cluster barrier later: start it now
+                    // the row (or record) is read in P4: start it now
                     if (EXT && a.rsq) {
                         constexpr int RBQ = 6 * (D / 8);
                         const uint8_t *rp = a.rsq + ((size_t)u * a.cap + id) * RBQ;
@@ -623,14 +864,18 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
                         prefetch_l2(static_cast<const uint8_t *>(a.K) + ((size_t)u * a.cap + id) * RB, RB);
                     }
                     cidx[pos] = id;
-                    // straight into the shared memory of the CTA whose P4
-                    // slice [r*C'/CS, (r+1)*C'/CS) holds list position pos
-                    while (r2 + 1 < CS && pos >= s_hi) {
-                        r2++;
-                        s_lo = s_hi;
-                        s_hi = sMisc[M_BOUND + r2 + 1];
+                    if (local) {
+                        sI[pos - s_lo] = id;
+                    } else {
+                        // straight into the shared memory of the CTA whose P4
+                        // slice [r*C'/CS, (r+1)*C'/CS) holds list position pos
+                        while (r2 + 1 < CS && pos >= s_hi) {
+                            r2++;
+                            s_lo = s_hi;
+                            s_hi = sMisc[M_BOUND + r2 + 1];
+                        }
+                        *cluster.map_shared_rank(&sI[pos - s_lo], r2) = id;
                     }
-                    *cluster.map_shared_rank(&sI[pos - s_lo], r2) = id;
                     pos++;
                 }
             }
@@ -647,11 +892,13 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         }
     }
     __syncthreads();
-    cluster.sync();  // #3: the unit's candidate list is complete
+    if (!local) cluster.sync();  // #3: the unit's candidate list is complete
 
     // ---------------------------------------------------------------- P4
-    const int lo = (int)((int64_t)rank * Cp / CS), hi = (int)((int64_t)(rank + 1) * Cp / CS);
-    const int n = hi - lo;  // <= kMaxSlice (the host picks CS so); sI filled in P3
+    // this CTA's slice of the candidate list: its own segment (local mode)
+    // or an equal share (<= kMaxSlice: the host picks CS so); sI filled in P3
+    const int lo = sMisc[M_BOUND + rank], hi = sMisc[M_BOUND + rank + 1];
+    const int n = hi - lo;
     if (tid == 0) {  // P5 accumulators, ordered by the barrier below
         sMisc[M_KMIN] = (int)0xffffffffu;
         sMisc[M_KMAX] = 0;
@@ -670,7 +917,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
 #pragma unroll
         for (int e = 0; e < 8; e++) zqv[e] = (gl < NB) ? sQbar[gl * 8 + e] : 0.0f;
         const uint8_t *recu = a.rsq + (size_t)u * a.cap * RBQ;
-        __syncthreads();  // sI complete (filled by the cluster in P3)
+        __syncthreads();  // sI complete (filled in P3)
         for (int base = 0; base < n; base += NHW * RR) {
             uint32_t wd[RR];
             uint32_t ws[RR];
@@ -719,7 +966,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         const uint32_t *Kw = reinterpret_cast<const uint32_t *>(static_cast<const uint8_t *>(a.K) +
                                                                (size_t)u * a.cap * RB);
         const int hw = tid >> 4, gl = tid & 15;
-        __syncthreads();  // sI complete (filled by the cluster in P3)
+        __syncthreads();  // sI complete (filled in P3)
         for (int base = 0; base < n; base += NHW * R) {
             uint32_t raw[R][WPR];
 #pragma unroll
@@ -1129,7 +1376,22 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         }
     }
 
+    // With the fused attention, P7 stages rows over the code ring and the
+    // candidate arrays, which the other CTAs read until they have finished
+    // P5 (published boundary keys, and scores in the all-keys path): arrive
+    // here, after this CTA's last read of another's shared memory, and wait
+    // before the first staging write.
+    if constexpr (GA > 0) {
+        __syncwarp();
+        cluster_arrive_release();
+    }
+
     // ---------------------------------------------------------------- P6
+    // winners of this slice, ascending by index; with the fused attention
+    // they are also listed (in the plane area, free since P3) for P7
+    int32_t *sWin = reinterpret_cast<int32_t *>(smem + SM::oPl);
+    static_assert(8 * kPlaneCap >= kMaxSlice, "the winner list fits the plane area");
+    if (GA > 0 && tid == 0 && kp == 0) sMisc[M_NW] = 0;
     if (kp > 0) {
         const int spt = (n + kSelThreads - 1) / kSelThreads;
         const int j0 = min(tid * spt, n), j1 = min(j0 + spt, n);
@@ -1147,6 +1409,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         const int allow0 = max(0, min(ktake - eq_before, n_eq));
         int pos = gt_before + min(ktake, eq_before) + sMisc[M_KOFF];
         int32_t *orow = a.out_idx + (size_t)u * a.k;
+        const int koff = sMisc[M_KOFF];
         int allow = allow0;
         for (int j = j0; j < j1; j++) {
             const uint32_t key = order_key(sS[j]);
@@ -1156,17 +1419,25 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
                 allow--;
             }
             if (take) {
-                orow[pos++] = sI[j];
+                if constexpr (GA > 0) sWin[pos - koff] = sI[j];
+                // the attention reads the winner's V row next: start it into L2
                 if (a.V)
                     prefetch_l2(static_cast<const uint8_t *>(a.V) + ((size_t)u * a.cap + sI[j]) * RB,
                                 RB);
+                orow[pos++] = sI[j];
             }
         }
+        // the last thread's end position closes this CTA's winner segment
+        if (GA > 0 && tid == kSelThreads - 1) sMisc[M_NW] = pos - koff;
     }
     if (rank == 0) {
         int32_t *orow = a.out_idx + (size_t)u * a.k;
         for (int j = kp + tid; j < a.k; j += kSelThreads) orow[j] = -1;
         if (tid == 0) a.out_count[u] = kp;
+    }
+    if constexpr (GA > 0) {
+        __syncthreads();  // sWin and its length complete; sS / sI no longer read
+        attend_tail<D, T, GA>(a, smem, sWin, sMisc[M_NW], b, h, N, p0, pool, rank, CS);
     }
     __syncthreads();
     cluster.sync();  // exit: no CTA leaves while another may read its shared memory
@@ -1174,15 +1445,17 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
 
 // ------------------------------------------------------------------ host side
 //
-// This file is compiled twice: as itself (the common kernels, EXT = false,
-// and the host code) and through kvr_select_ext.cu with KVR_SELECT_EXT_TU
-// defined (only the EXT = true kernels and their launcher), so the two sets
-// of instantiations build in parallel.
+// This file is compiled three times: as itself (the common kernels, EXT =
+// false, GA = 0, and the host code), through kvr_select_ext.cu with
+// KVR_SELECT_EXT_TU defined (the EXT = true kernels: reranker records and
+// magnitude-aware votes) and through kvr_select_att.cu with
+// KVR_SELECT_ATT_TU defined (the GA = 4 kernels: selection + attention), so
+// the three sets of instantiations build in parallel.
 
-template <int D, typename T, int VB, bool EXT>
+template <int D, typename T, int VB, bool EXT, int GA>
 static kvr_status launch_select_t(const LaunchCtx &c, const SelArgs &a, int cs)
 {
-    auto kern = select_kernel<D, T, VB, EXT>;
+    auto kern = select_kernel<D, T, VB, EXT, GA>;
     const int smem = SelSmem<D, T>::bytes;
     kvr_status st = prepare_cluster_kernel(reinterpret_cast<const void *>(kern), smem);
     if (st != KVR_OK) return st;
@@ -1204,39 +1477,47 @@ static kvr_status launch_select_t(const LaunchCtx &c, const SelArgs &a, int cs)
     return check_launch();
 }
 
-template <int D, typename T, bool EXT>
+template <int D, typename T, bool EXT, int GA>
 static kvr_status launch_select_vb(const LaunchCtx &c, const SelArgs &a, int cs, int vb)
 {
     switch (vb) {
-    case 1: return launch_select_t<D, T, 1, EXT>(c, a, cs);
-    case 2: return launch_select_t<D, T, 2, EXT>(c, a, cs);
-    case 3: return launch_select_t<D, T, 3, EXT>(c, a, cs);
-    default: return launch_select_t<D, T, 4, EXT>(c, a, cs);
+    case 1: return launch_select_t<D, T, 1, EXT, GA>(c, a, cs);
+    case 2: return launch_select_t<D, T, 2, EXT, GA>(c, a, cs);
+    case 3: return launch_select_t<D, T, 3, EXT, GA>(c, a, cs);
+    default: return launch_select_t<D, T, 4, EXT, GA>(c, a, cs);
     }
 }
 
-template <bool EXT>
+template <bool EXT, int GA>
 static kvr_status launch_select(const LaunchCtx &c, const SelArgs &a, int cs, int vb)
 {
     const bool bf = c.shape.dtype == KVR_BF16;
     if (c.shape.d == 128)
-        return bf ? launch_select_vb<128, __nv_bfloat16, EXT>(c, a, cs, vb)
-                  : launch_select_vb<128, float, EXT>(c, a, cs, vb);
-    return bf ? launch_select_vb<64, __nv_bfloat16, EXT>(c, a, cs, vb)
-              : launch_select_vb<64, float, EXT>(c, a, cs, vb);
+        return bf ? launch_select_vb<128, __nv_bfloat16, EXT, GA>(c, a, cs, vb)
+                  : launch_select_vb<128, float, EXT, GA>(c, a, cs, vb);
+    return bf ? launch_select_vb<64, __nv_bfloat16, EXT, GA>(c, a, cs, vb)
+              : launch_select_vb<64, float, EXT, GA>(c, a, cs, vb);
 }
 
-#ifdef KVR_SELECT_EXT_TU
+#if defined(KVR_SELECT_EXT_TU)
 
 kvr_status select_launch_ext(const LaunchCtx &c, const SelArgs &a, int cs, int vb)
 {
-    return launch_select<true>(c, a, cs, vb);
+    return launch_select<true, 0>(c, a, cs, vb);
+}
+
+#elif defined(KVR_SELECT_ATT_TU)
+
+kvr_status select_launch_att(const LaunchCtx &c, const SelArgs &a, int cs, int vb)
+{
+    return launch_select<false, 4>(c, a, cs, vb);
 }
 
 #else
 
-// defined in the KVR_SELECT_EXT_TU compilation of this file
+// defined in the KVR_SELECT_EXT_TU / KVR_SELECT_ATT_TU compilations of this file
 kvr_status select_launch_ext(const LaunchCtx &c, const SelArgs &a, int cs, int vb);
+kvr_status select_launch_att(const LaunchCtx &c, const SelArgs &a, int cs, int vb);
 
 int select_cluster_size(int U, int C)
 {
@@ -1246,10 +1527,15 @@ int select_cluster_size(int U, int C)
     return cs;
 }
 
+bool select_attend_fusable(const kvr_shape &s, const kvr_select_params &p)
+{
+    return s.Hq / s.Hkv <= 4 && !p.rsq_records && !(p.flags & KVR_SELECT_MAGNITUDE_VOTES);
+}
+
 kvr_status select_dispatch(const LaunchCtx &c, const kvr_select_params &p, const SelectPlan &plan,
                            const void *q, const void *K, const uint8_t *codes,
                            const int32_t *seq_len, const int8_t *sgn, int32_t *out_idx,
-                           int32_t *out_count, uint8_t *ws, int32_t *err)
+                           int32_t *out_count, uint8_t *ws, int32_t *err, const FusedAttend *att)
 {
     SelArgs a;
     a.Hq = c.shape.Hq;
@@ -1269,7 +1555,7 @@ kvr_status select_dispatch(const LaunchCtx &c, const kvr_select_params &p, const
     }
     a.q = q;
     a.K = K;
-    a.V = p.V_prefetch;
+    a.V = att ? att->V : p.V_prefetch;
     a.early = (p.flags & KVR_SELECT_EARLY_INPUTS) != 0;
     a.rsq = p.rsq_records;
     a.sink = p.sink;
@@ -1291,16 +1577,20 @@ kvr_status select_dispatch(const LaunchCtx &c, const kvr_select_params &p, const
     a.cap_pad = plan.cap_pad;
     a.tiles = plan.tiles;
     a.err = err;
+    a.att_out = att ? att->out : nullptr;
+    a.att_scale_log2 = att ? att->scale * 1.4426950408889634f : 0.0f;
+    if (att && !select_attend_fusable(c.shape, p)) return KVR_ERR_UNSUPPORTED;
     if (plan.has_votes) {
         const kvr_status st = vote_list_dispatch(c, q, sgn, p.lut,
                                                  reinterpret_cast<uint16_t *>(ws + plan.off_votes));
         if (st != KVR_OK) return st;
     }
     const int cs = select_cluster_size(c.shape.B * c.shape.Hkv, p.C);
+    if (att) return select_launch_att(c, a, cs, vb);
     if (a.rsq || a.votes) return select_launch_ext(c, a, cs, vb);
-    return launch_select<false>(c, a, cs, vb);
+    return launch_select<false, 0>(c, a, cs, vb);
 }
 
-#endif  // KVR_SELECT_EXT_TU
+#endif  // KVR_SELECT_EXT_TU / KVR_SELECT_ATT_TU
 
 }  // namespace kvr

@@ -268,6 +268,8 @@ struct TieredArgs {
     float *part;       // [U, S, 2G + G*D]: m[G], l[G], o[G][D]
     float *lse;        // [U, n_win, G] log2-sum-exp of each window's scores (-inf: none)
     int32_t *err;
+    uint64_t wait_ns;  // limit of each wait for a copy
+    int withhold_last; // test hook: each CTA never issues its last copy (its wait runs out)
 };
 
 // ---- warp-level tensor-core helpers: mma.sync m16n8k16, bf16 in, fp32 accumulate.
@@ -421,9 +423,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         sSt[(tid / 8) * 24 + tid % 8] = -CUDART_INF_F;
         sSt[(tid / 8) * 24 + 8 + tid % 8] = 0.0f;
     }
+    // set when a wait for a copy ran out: the CTA then stops after the
+    // current pair of windows, waits (bounded) for the copies it issued and
+    // leaves its (invalid) partial behind, KVR_DEVERR_TIMEOUT set
+    __shared__ int s_dead;
     if (tid == 0) {
         for (int i = 0; i < C::NS; i++) mbar_init(&sBar[i], 1);
         mbar_fence_init();
+        s_dead = 0;
     }
     __syncthreads();
 
@@ -436,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     float acc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 
     int li = 0, lc = 0;  // loads issued, loads consumed (block-uniform, across passes)
+    bool dead = false;   // s_dead as read after a barrier (block-uniform)
     for (int64_t p0 = w_begin; p0 < w_end; p0 += C::LMAX) {
         const int64_t p1 = (p0 + C::LMAX < w_end) ? p0 + C::LMAX : w_end;
         // the live windows of [p0, p1) in order, bit 30 set for INT2 ones;
@@ -486,7 +494,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int slot = li % C::NS;
                 uint8_t *dst = smem + slot * C::SLOT;
                 const bool q2 = (e >> 30) & 1;
-                if (tid == 0) {
+                const bool withheld =
+                    a.withhold_last && p1 == w_end && pi == nlive - 1 && (q2 || ppart);
+                if (tid == 0 && !withheld) {
                     fence_proxy_async();  // earlier reads of the slot before the async writes
                     if (q2) {
                         mbar_arrive_expect_tx(&sBar[slot], C::LB);
@@ -528,7 +538,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int nvB = (int)(N - cwB * kWin < kWin ? N - cwB * kWin : kWin);
             issue_ahead();
             for (int L = lc; L < lc + needA + needB; L++)
-                mbar_wait(&sBar[L % C::NS], (uint32_t)((L / C::NS) & 1), a.err);
+                if (!mbar_wait(&sBar[L % C::NS], (uint32_t)((L / C::NS) & 1), a.err, a.wait_ns))
+                    s_dead = 1;
 #pragma unroll
             for (int st = 0; st < 2; st++) {
                 const bool q2s = st ? q2B : q2A;
@@ -546,6 +557,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
             __syncthreads();
+            // every write of s_dead (the waits above) precedes this read, every
+            // later one follows the pair's last barrier: `dead` is block-uniform
+            dead = s_dead != 0;
 
             // ---- scores: warp -> window (warp / 4), 16 tokens (warp % 4), all dims
             {
@@ -748,8 +762,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             fence_proxy_async();  // this thread's slot accesses before the next copies into it
             __syncthreads();      // the pair's slots, P and the scores are reused next
             lc += needA + needB;
+            if (dead) break;
         }
+        if (dead) break;
     }
+    if (dead)  // copies issued ahead of the pair that timed out
+        for (int L = lc; L < li; L++)
+            mbar_wait(&sBar[L % C::NS], (uint32_t)((L / C::NS) & 1), a.err, a.wait_ns);
     __syncthreads();
 
     // ---- merge the two streams into this CTA's partial: o[head][dim]
@@ -1118,7 +1137,8 @@ static kvr_status tiered_launch(const LaunchCtx &c, TieredArgs a, float *out, fl
 
 kvr_status tiered_attend_dispatch(const LaunchCtx &c, const kvr_tier_state &s, const void *q,
                                   const void *K, const void *V, const int32_t *seq_len,
-                                  float scale, float *out, float *mass, uint8_t *ws, int32_t *err)
+                                  float scale, float *out, float *mass, uint8_t *ws, int32_t *err,
+                                  uint64_t wait_ns, bool withhold_last)
 {
     const kvr_shape &sh = c.shape;
     const int64_t U = (int64_t)sh.B * sh.Hkv;
@@ -1139,6 +1159,8 @@ kvr_status tiered_attend_dispatch(const LaunchCtx &c, const kvr_tier_state &s, c
     a.part = reinterpret_cast<float *>(ws);
     a.lse = reinterpret_cast<float *>(ws + align_up((size_t)U * a.S * (2 * G + G * sh.d) * 4, 256));
     a.err = err;
+    a.wait_ns = wait_ns;
+    a.withhold_last = withhold_last ? 1 : 0;
     if (sh.d == 128) {
         switch (G) {
         case 1: return tiered_launch<128, 1>(c, a, out, mass);

@@ -1,7 +1,9 @@
 """kvr_decode_step (encode of the appended key, selection, attention in one
-library call) gives bit-identical results to the three separate calls, with
-the plain window and with records + cache regions; and the prepared caller
-(DecodeStep) equals it."""
+library call) gives the results of the three separate calls, with the plain
+window and with records + cache regions: codes, records, index sets and
+counts bit for bit, the output bit for bit where the step runs the separate
+attention and up to the summation order where selection and attention share
+one launch; the prepared caller (DecodeStep) equals kvr_decode_step."""
 import math
 
 import numpy as np
@@ -82,9 +84,15 @@ def test_decode_step_equals_the_separate_calls(mode):
         runs.append((codes.cpu().numpy(), None if rec is None else rec.cpu().numpy(),
                      idx.cpu().numpy(), cnt.cpu().numpy(), out.cpu().numpy()))
     for other in runs[1:]:
-        for a, b in zip(runs[0], other):
+        for a, b in zip(runs[0][:4], other[:4]):
             if a is not None:
                 assert np.array_equal(a, b)
+    fused = mode == "window"   # exact rescoring, Hamming votes, 4 heads: one launch
+    if fused:
+        assert np.abs(runs[0][4] - runs[1][4]).max() <= 1e-5
+    else:
+        assert np.array_equal(runs[0][4], runs[1][4])
+    assert np.array_equal(runs[1][4], runs[2][4])
     assert runs[0][3].min() > 0
 
 
