@@ -945,7 +945,7 @@ def tiered_dynamics(w, steps, dev):
     import torch
     import sparse_decode_attention_gb300 as kvr
     import workloads as wl
-    from sparse_decode_attention_gb300 import diagnostics as dg
+    import bench_diagnostics as dg
 
     cap = w.N + steps + 8
     n_win = -(-cap // 64)

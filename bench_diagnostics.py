@@ -5,7 +5,8 @@ attention that falls on states a policy has already discarded), Global LIR
 (how often windows that were inactive re-enter the active set) and selection
 churn (how much the active set changes between routing steps).
 
-This is evaluation tooling around the hot path, not part of it: the
+This is evaluation tooling beside the benchmark, not part of the library or
+its hot path (it lives next to bench.py for that reason): the
 full-attention window masses come from the library's tiered attention run on
 a state that keeps every window in bf16 (``full_mass_state`` +
 ``kvr_sparse_attend_tiered`` over the unmodified K / V), and the per-step
@@ -24,7 +25,7 @@ Definitions used:
 import numpy as np
 import torch
 
-from . import TIER_BF16, TIER_EVICTED, WINDOW, TierState, kvr_tier_init
+from sparse_decode_attention_gb300 import TIER_BF16, TIER_EVICTED, WINDOW, TierState, kvr_tier_init
 
 __all__ = ["full_mass_state", "CacheDynamics"]
 

@@ -351,7 +351,9 @@ kvr_status kvr_decode_step(const kvr_shape *shape, const kvr_select_params *p, c
  * 128K tokens at C = 8192 about 2.1 MiB).
  *   - Set-up: the first call on a device looks up the array's device address
  *     with that device current (cudaGetSymbolAddress); make that first call
- *     before any stream capture on the device.
+ *     before any stream capture on the device. The address is kept with the
+ *     device's context: after a device reset (a new context) the next call
+ *     looks it up again, so it too must come before any stream capture.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind; kvr_select reads nothing from scratch that the same call did not
  *     write first, so no clearing is needed. Calls whose GPU work overlaps

@@ -252,6 +252,23 @@ def _kv(t, name):
     return t
 
 
+def _device(*tensors):
+    """The one CUDA device of the CUDA tensors among `tensors` (host-resident
+    caches are skipped); raises when they are spread over devices."""
+    devs = {t.device for t in tensors if isinstance(t, torch.Tensor) and t.is_cuda}
+    if len(devs) != 1:
+        raise ValueError("the tensors of one call must all be on one CUDA device, got %s"
+                         % sorted(str(d) for d in devs))
+    return devs.pop()
+
+
+def _records(params, shape):
+    """The reranker records, when given, must hold every key of the cache."""
+    if params.rsq_records is not None and (
+            params.rsq_records.numel() < shape.B * shape.Hkv * shape.cap * kvr_rsq_record_bytes(shape.d)):
+        raise ValueError("rsq_records buffer too small")
+
+
 def _codes(codes, shape):
     _cuda(codes, "codes", torch.uint8)
     if codes.numel() < kvr_codes_bytes(shape):
@@ -266,8 +283,9 @@ def kvr_encode_keys(K, pos0, n_new, srht_sign, codes, err=None, stream=None, sha
     _cuda(pos0, "pos0", torch.int32)
     _cuda(srht_sign, "srht_sign", torch.int8)
     _codes(codes, shape)
-    st = load().kvr_encode_keys(ctypes.byref(shape.c()), _ptr(K), _ptr(pos0), int(n_new),
-                                _ptr(srht_sign), _ptr(codes), _ptr(err), _stream(stream))
+    with torch.cuda.device(_device(K, pos0, srht_sign, codes, err)):
+        st = load().kvr_encode_keys(ctypes.byref(shape.c()), _ptr(K), _ptr(pos0), int(n_new),
+                                    _ptr(srht_sign), _ptr(codes), _ptr(err), _stream(stream))
     _check(st, "kvr_encode_keys")
 
 
@@ -294,14 +312,15 @@ def kvr_select(q, K, codes, seq_len, srht_sign, params: SelectParams, out_idx, o
     _cuda(out_idx, "out_idx", torch.int32)
     _cuda(out_count, "out_count", torch.int32)
     _cuda(workspace, "workspace")
-    if params.rsq_records is not None and (
-            params.rsq_records.numel() < shape.B * shape.Hkv * shape.cap * kvr_rsq_record_bytes(shape.d)):
-        raise ValueError("rsq_records buffer too small")
-    st = load().kvr_select(ctypes.byref(shape.c()), ctypes.byref(params.c()), _ptr(q), _ptr(K),
-                           _ptr(codes), _ptr(seq_len), _ptr(srht_sign), _ptr(out_idx),
-                           _ptr(out_count), _ptr(workspace),
-                           workspace.numel() * workspace.element_size(), _ptr(err),
-                           _stream(stream))
+    _records(params, shape)
+    dev = _device(q, K, codes, seq_len, srht_sign, out_idx, out_count, workspace, err,
+                  params.V_prefetch, params.rsq_records, params.region_end)
+    with torch.cuda.device(dev):
+        st = load().kvr_select(ctypes.byref(shape.c()), ctypes.byref(params.c()), _ptr(q), _ptr(K),
+                               _ptr(codes), _ptr(seq_len), _ptr(srht_sign), _ptr(out_idx),
+                               _ptr(out_count), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _ptr(err),
+                               _stream(stream))
     _check(st, "kvr_select")
 
 
@@ -315,10 +334,15 @@ def kvr_select_static_scratch(q, K, codes, seq_len, srht_sign, params: SelectPar
     _cuda(srht_sign, "srht_sign", torch.int8)
     _cuda(out_idx, "out_idx", torch.int32)
     _cuda(out_count, "out_count", torch.int32)
-    st = load().kvr_select_static_scratch(ctypes.byref(shape.c()), ctypes.byref(params.c()),
-                                          _ptr(q), _ptr(K), _ptr(codes), _ptr(seq_len),
-                                          _ptr(srht_sign), _ptr(out_idx), _ptr(out_count),
-                                          _ptr(err), _stream(stream))
+    _records(params, shape)
+    # the scratch array used is the current device's: make it the tensors' device
+    dev = _device(q, K, codes, seq_len, srht_sign, out_idx, out_count, err, params.V_prefetch,
+                  params.rsq_records, params.region_end)
+    with torch.cuda.device(dev):
+        st = load().kvr_select_static_scratch(ctypes.byref(shape.c()), ctypes.byref(params.c()),
+                                              _ptr(q), _ptr(K), _ptr(codes), _ptr(seq_len),
+                                              _ptr(srht_sign), _ptr(out_idx), _ptr(out_count),
+                                              _ptr(err), _stream(stream))
     _check(st, "kvr_select_static_scratch")
 
 
@@ -339,11 +363,13 @@ def kvr_sparse_attend(q, K, V, idx, count, seq_len, W, scale, out, workspace, er
     _cuda(out, "out", torch.float32)
     _cuda(workspace, "workspace")
     kmax = idx.shape[-1]
-    st = load().kvr_sparse_attend(ctypes.byref(shape.c()), _ptr(q), _ptr(K), _ptr(V), _ptr(idx),
-                                  int(kmax), _ptr(count), _ptr(seq_len), int(W), float(scale),
-                                  _ptr(out), _ptr(workspace),
-                                  workspace.numel() * workspace.element_size(), _ptr(err),
-                                  _stream(stream))
+    dev = _device(q, K, V, idx, count, seq_len, out, workspace, err)
+    with torch.cuda.device(dev):
+        st = load().kvr_sparse_attend(ctypes.byref(shape.c()), _ptr(q), _ptr(K), _ptr(V),
+                                      _ptr(idx), int(kmax), _ptr(count), _ptr(seq_len), int(W),
+                                      float(scale), _ptr(out), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _ptr(err),
+                                      _stream(stream))
     _check(st, "kvr_sparse_attend")
 
 
@@ -396,9 +422,10 @@ def kvr_tier_init(state: TierState, initial_tier, K, V, seq_len, q_heads: int, e
         raise ValueError("initial_tier must hold [U, n_win] entries")
     B, Hkv, cap, d = K.shape
     shape = Shape(B, q_heads, Hkv, d, cap, torch.bfloat16)
-    st = load().kvr_tier_init(ctypes.byref(shape.c()), ctypes.byref(state.c()),
-                              _ptr(initial_tier), _ptr(K), _ptr(V), _ptr(seq_len), _ptr(err),
-                              _stream(stream))
+    with torch.cuda.device(_device(initial_tier, K, V, seq_len, err, state.tier)):
+        st = load().kvr_tier_init(ctypes.byref(shape.c()), ctypes.byref(state.c()),
+                                  _ptr(initial_tier), _ptr(K), _ptr(V), _ptr(seq_len), _ptr(err),
+                                  _stream(stream))
     _check(st, "kvr_tier_init")
 
 
@@ -417,12 +444,14 @@ def kvr_sparse_attend_tiered(state: TierState, q, K, V, seq_len, scale, out, win
     _cuda(workspace, "workspace")
     if window_mass.numel() < state.U * state.n_win:
         raise ValueError("window_mass must hold [U, n_win] entries")
-    st = load().kvr_sparse_attend_tiered(ctypes.byref(shape.c()), ctypes.byref(state.c()),
-                                         _ptr(q), _ptr(K), _ptr(V), _ptr(seq_len),
-                                         float(scale), _ptr(out), _ptr(window_mass),
-                                         _ptr(workspace),
-                                         workspace.numel() * workspace.element_size(),
-                                         _ptr(err), _stream(stream))
+    with torch.cuda.device(_device(q, K, V, seq_len, out, window_mass, workspace, err,
+                                   state.tier)):
+        st = load().kvr_sparse_attend_tiered(ctypes.byref(shape.c()), ctypes.byref(state.c()),
+                                             _ptr(q), _ptr(K), _ptr(V), _ptr(seq_len),
+                                             float(scale), _ptr(out), _ptr(window_mass),
+                                             _ptr(workspace),
+                                             workspace.numel() * workspace.element_size(),
+                                             _ptr(err), _stream(stream))
     _check(st, "kvr_sparse_attend_tiered")
 
 
@@ -442,11 +471,13 @@ def kvr_tier_update(state: TierState, window_mass, seq_len, K, V, q_heads: int, 
         _cuda(stats, "stats", torch.int32)
     B, Hkv, cap, d = K.shape
     shape = Shape(B, q_heads, Hkv, d, cap, torch.bfloat16)
-    st = load().kvr_tier_update(ctypes.byref(shape.c()), ctypes.byref(state.c()),
-                                _ptr(window_mass), _ptr(seq_len), _ptr(K), _ptr(V),
-                                _ptr(stats), _ptr(workspace),
-                                workspace.numel() * workspace.element_size(), _ptr(err),
-                                _stream(stream))
+    with torch.cuda.device(_device(window_mass, seq_len, K, V, stats, workspace, err,
+                                   state.tier)):
+        st = load().kvr_tier_update(ctypes.byref(shape.c()), ctypes.byref(state.c()),
+                                    _ptr(window_mass), _ptr(seq_len), _ptr(K), _ptr(V),
+                                    _ptr(stats), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _ptr(err),
+                                    _stream(stream))
     _check(st, "kvr_tier_update")
 
 
@@ -492,8 +523,9 @@ def kvr_encode_rsq(K, pos0, n_new, srht_sign, records, err=None, stream=None):
     _cuda(records, "records", torch.uint8)
     if records.numel() < K.shape[0] * K.shape[1] * K.shape[2] * kvr_rsq_record_bytes(K.shape[3]):
         raise ValueError("records buffer too small")
-    st = load().kvr_encode_rsq(ctypes.byref(shape.c()), _ptr(K), _ptr(pos0), int(n_new),
-                               _ptr(srht_sign), _ptr(records), _ptr(err), _stream(stream))
+    with torch.cuda.device(_device(K, pos0, srht_sign, records, err)):
+        st = load().kvr_encode_rsq(ctypes.byref(shape.c()), _ptr(K), _ptr(pos0), int(n_new),
+                                   _ptr(srht_sign), _ptr(records), _ptr(err), _stream(stream))
     _check(st, "kvr_encode_rsq")
 
 
@@ -510,12 +542,15 @@ def kvr_sparse_attend_regions(q, K, V, idx, count, seq_len, sink, region_end, sc
     _cuda(region_end, "region_end", torch.int32)
     _cuda(out, "out", torch.float32)
     _cuda(workspace, "workspace")
-    st = load().kvr_sparse_attend_regions(ctypes.byref(shape.c()), _ptr(q), _ptr(K), _ptr(V),
-                                          _ptr(idx), int(idx.shape[-1]), _ptr(count),
-                                          _ptr(seq_len), int(sink), _ptr(region_end),
-                                          float(scale), _ptr(out), _ptr(workspace),
-                                          workspace.numel() * workspace.element_size(), _ptr(err),
-                                          _stream(stream))
+    with torch.cuda.device(_device(q, K, V, idx, count, seq_len, region_end, out, workspace,
+                                   err)):
+        st = load().kvr_sparse_attend_regions(ctypes.byref(shape.c()), _ptr(q), _ptr(K),
+                                              _ptr(V), _ptr(idx), int(idx.shape[-1]),
+                                              _ptr(count), _ptr(seq_len), int(sink),
+                                              _ptr(region_end), float(scale), _ptr(out),
+                                              _ptr(workspace),
+                                              workspace.numel() * workspace.element_size(),
+                                              _ptr(err), _stream(stream))
     _check(st, "kvr_sparse_attend_regions")
 
 
@@ -526,9 +561,10 @@ def kvr_regions_update(seq_len, sink, local, buffer, region_end, init=False, err
     _cuda(region_end, "region_end", torch.int32)
     if region_end.numel() < seq_len.numel():
         raise ValueError("region_end needs one entry per batch entry")
-    st = load().kvr_regions_update(int(seq_len.numel()), _ptr(seq_len), int(sink), int(local),
-                                   int(buffer), 1 if init else 0, _ptr(region_end), _ptr(err),
-                                   _stream(stream))
+    with torch.cuda.device(_device(seq_len, region_end, err)):
+        st = load().kvr_regions_update(int(seq_len.numel()), _ptr(seq_len), int(sink),
+                                       int(local), int(buffer), 1 if init else 0,
+                                       _ptr(region_end), _ptr(err), _stream(stream))
     _check(st, "kvr_regions_update")
 
 
@@ -546,19 +582,25 @@ def _decode_args(q, K, V, codes, seq_len, pos_new, srht_sign, params, out_idx, o
     _cuda(workspace, "workspace")
     if out_idx.shape[-1] != params.k:
         raise ValueError("out_idx rows must hold params.k entries")
+    _records(params, shape)
+    dev = _device(q, K, V, codes, seq_len, pos_new, srht_sign, out_idx, out_count, out,
+                  workspace, err, params.rsq_records, params.region_end)
+    with torch.cuda.device(dev):
+        strm = _stream(stream)
     return (ctypes.byref(shape.c()), ctypes.byref(params.c()), _ptr(q), _ptr(K), _ptr(V),
             _ptr(codes), _ptr(seq_len), _ptr(pos_new), _ptr(srht_sign), _ptr(out_idx),
             _ptr(out_count), float(scale), _ptr(out), _ptr(workspace),
-            workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream))
+            workspace.numel() * workspace.element_size(), _ptr(err), strm), dev
 
 
 def kvr_decode_step(q, K, V, codes, seq_len, pos_new, srht_sign, params: SelectParams, out_idx,
                     out_count, scale, out, workspace, err=None, stream=None):
     """Code (and record) of the appended key at pos_new, selection and
     attention, in one library call."""
-    _check(load().kvr_decode_step(*_decode_args(q, K, V, codes, seq_len, pos_new, srht_sign,
-                                                params, out_idx, out_count, scale, out,
-                                                workspace, err, stream)), "kvr_decode_step")
+    args, dev = _decode_args(q, K, V, codes, seq_len, pos_new, srht_sign, params, out_idx,
+                             out_count, scale, out, workspace, err, stream)
+    with torch.cuda.device(dev):
+        _check(load().kvr_decode_step(*args), "kvr_decode_step")
 
 
 class DecodeStep:
@@ -570,12 +612,14 @@ class DecodeStep:
                  out_count, scale, out, workspace, err=None, stream=None):
         self._keep = (q, K, V, codes, seq_len, pos_new, srht_sign, params, out_idx, out_count,
                       out, workspace, err, stream)
-        self._args = _decode_args(q, K, V, codes, seq_len, pos_new, srht_sign, params, out_idx,
-                                  out_count, scale, out, workspace, err, stream)
+        self._args, self._dev = _decode_args(q, K, V, codes, seq_len, pos_new, srht_sign, params,
+                                             out_idx, out_count, scale, out, workspace, err,
+                                             stream)
         self._fn = load().kvr_decode_step
 
     def __call__(self):
-        st = self._fn(*self._args)
+        with torch.cuda.device(self._dev):
+            st = self._fn(*self._args)
         if st != 0:
             raise KvrError(st, "kvr_decode_step")
 
@@ -594,20 +638,25 @@ def _select_attend_args(q, K, V, codes, seq_len, srht_sign, params, scale, out_i
     _cuda(workspace, "workspace")
     if out_idx.shape[-1] != params.k:
         raise ValueError("out_idx rows must hold params.k entries")
+    _records(params, shape)
+    dev = _device(q, K, V, codes, seq_len, srht_sign, out_idx, out_count, out, workspace, err,
+                  params.rsq_records, params.region_end)
+    with torch.cuda.device(dev):
+        strm = _stream(stream)
     return (ctypes.byref(shape.c()), ctypes.byref(params.c()), _ptr(q), _ptr(K), _ptr(V),
             _ptr(codes), _ptr(seq_len), _ptr(srht_sign), float(scale), _ptr(out_idx),
             _ptr(out_count), _ptr(out), _ptr(workspace),
-            workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream))
+            workspace.numel() * workspace.element_size(), _ptr(err), strm), dev
 
 
 def kvr_select_attend(q, K, V, codes, seq_len, srht_sign, params: SelectParams, scale, out_idx,
                       out_count, out, workspace, err=None, stream=None):
     """kvr_select, then the attention over its top-k and the window (one
     kernel launch for groups of up to 4 heads with exact rescoring)."""
-    _check(load().kvr_select_attend(*_select_attend_args(q, K, V, codes, seq_len, srht_sign,
-                                                         params, scale, out_idx, out_count, out,
-                                                         workspace, err, stream)),
-           "kvr_select_attend")
+    args, dev = _select_attend_args(q, K, V, codes, seq_len, srht_sign, params, scale, out_idx,
+                                    out_count, out, workspace, err, stream)
+    with torch.cuda.device(dev):
+        _check(load().kvr_select_attend(*args), "kvr_select_attend")
 
 
 class SelectAttend:
@@ -618,12 +667,14 @@ class SelectAttend:
                  out_count, out, workspace, err=None, stream=None):
         self._keep = (q, K, V, codes, seq_len, srht_sign, params, out_idx, out_count, out,
                       workspace, err, stream)
-        self._args = _select_attend_args(q, K, V, codes, seq_len, srht_sign, params, scale,
-                                         out_idx, out_count, out, workspace, err, stream)
+        self._args, self._dev = _select_attend_args(q, K, V, codes, seq_len, srht_sign, params,
+                                                    scale, out_idx, out_count, out, workspace,
+                                                    err, stream)
         self._fn = load().kvr_select_attend
 
     def __call__(self):
-        st = self._fn(*self._args)
+        with torch.cuda.device(self._dev):
+            st = self._fn(*self._args)
         if st != 0:
             raise KvrError(st, "kvr_select_attend")
 

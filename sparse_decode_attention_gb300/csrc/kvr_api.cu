@@ -90,6 +90,22 @@ SmemTable g_plain, g_cluster;
 
 }  // namespace
 
+int sm_count()
+{
+    static std::mutex mu;
+    static int count[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
+    std::lock_guard<std::mutex> lock(mu);
+    if (count[dev] <= 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+            n = 152;
+        count[dev] = n;
+    }
+    return count[dev];
+}
+
 kvr_status raise_smem_limit(const void *kernel, int bytes)
 {
     return raise_in(g_plain, kernel, bytes, false);

@@ -344,7 +344,7 @@ int attend_cluster_size(int U, int64_t most_tokens)
     // barrier; 12-CTA clusters keep each CTA on its own SM (attention per
     // call 16.6 -> 14.4 us at 128K).
     int cs = (U == 8) ? 12 : 16;
-    while (cs > 1 && (int64_t)U * cs > 2 * 152) cs >>= 1;
+    while (cs > 1 && (int64_t)U * cs > 2 * sm_count()) cs >>= 1;
     while (cs > 1 && most_tokens < (int64_t)cs * 32) cs >>= 1;  // >= 32 tokens per CTA
     return cs;
 }

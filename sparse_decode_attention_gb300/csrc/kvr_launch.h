@@ -29,6 +29,10 @@ kvr_status raise_smem_limit(const void *kernel, int bytes);
 // raise_smem_limit plus permission for cluster sizes above 8.
 kvr_status prepare_cluster_kernel(const void *kernel, int smem_bytes);
 
+// Streaming multiprocessors of the current device (queried once per device;
+// 152 on GB300 if the query fails), for grid sizing.
+int sm_count();
+
 // Bytes of the bit-plane code buffer of one unit: ceil(cap/1024) tiles of d*128 bytes.
 inline size_t codes_bytes_per_unit(int64_t cap, int d) { return (size_t)((cap + 1023) / 1024) * d * 128; }
 

@@ -246,7 +246,7 @@ __device__ __forceinline__ void attend_tail(const SelArgs &a, uint8_t *smem, con
     using SM = SelSmem<D, T>;
     constexpr int E = D / 32, RB = SM::kRowBytes, PPR = RB / 16, LPH = 32 / GA;
     constexpr int CH = SM::kStage / (2 * RB);  // tokens staged at once
-    constexpr int TPW = 8;                     // tokens per warp per round
+    constexpr int TPW = 4;                     // tokens per warp per round
     static_assert(CH >= kSelWarps * TPW, "a round fits the stage");
     static_assert(kSelWarps * GA * (D + 2) * 4 <= SM::kStage, "warp partials fit the stage");
     cg::cluster_group cluster = cg::this_cluster();
@@ -394,34 +394,32 @@ __device__ __forceinline__ void attend_tail(const SelArgs &a, uint8_t *smem, con
     __syncthreads();
     cluster.sync();  // CTA partials published
 
-    // this CTA's share of the outputs: a 16-lane group per output, lane r
-    // reading CTA r's partial (all remote loads in flight at once), then
-    // butterfly reductions of the group's max and weighted sums
+    // every CTA finishes an equal share of the unit's G*D outputs; the
+    // remote loads of an output are all issued before its arithmetic
     const int e0 = rank * (G * D) / CS, e1 = (rank + 1) * (G * D) / CS;
-    const int grp = tid >> 4, r = tid & 15;
-    for (int t0 = e0; t0 < e1; t0 += kSelThreads / 16) {
-        const int t = t0 + grp;
-        const bool on = t < e1;
-        const int tt = on ? t : e0;
-        const int g = tt / D, dim = tt % D;
-        float mr = -INFINITY, lr = 0.0f, orr = 0.0f;
-        if (r < CS) {
-            mr = *cluster.map_shared_rank(&sPm[g], r);
-            lr = *cluster.map_shared_rank(&sPl[g], r);
-            orr = *cluster.map_shared_rank(&sPo[tt], r);
-        }
-        float M = mr;
+    for (int t = e0 + tid; t < e1; t += kSelThreads) {
+        const int g = t / D, dim = t % D;
+        float mr[16], lr[16], orr[16];
 #pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-        const float f = (mr == -INFINITY) ? 0.0f : exp2f(mr - M);
-        float L = lr * f, O = orr * f;
-#pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) {
-            L += __shfl_xor_sync(kFull, L, o);
-            O += __shfl_xor_sync(kFull, O, o);
+        for (int r = 0; r < 16; r++) {
+            mr[r] = (r < CS) ? *cluster.map_shared_rank(&sPm[g], r) : -INFINITY;
+            lr[r] = (r < CS) ? *cluster.map_shared_rank(&sPl[g], r) : 0.0f;
+            orr[r] = (r < CS) ? *cluster.map_shared_rank(&sPo[t], r) : 0.0f;
         }
-        if (on && r == 0)
-            a.att_out[((size_t)b * a.Hq + (size_t)h * G + g) * D + dim] = (L > 0.0f) ? O / L : 0.0f;
+        float M = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < 16; r++) M = fmaxf(M, mr[r]);
+        float L = 0.0f, O = 0.0f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int r = 0; r < 16; r++) {
+                if (mr[r] == -INFINITY) continue;
+                const float f = exp2f(mr[r] - M);
+                L = fmaf(lr[r], f, L);
+                O = fmaf(orr[r], f, O);
+            }
+        }
+        a.att_out[((size_t)b * a.Hq + (size_t)h * G + g) * D + dim] = (L > 0.0f) ? O / L : 0.0f;
     }
 }
 
@@ -679,6 +677,16 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         __syncwarp();
         const int64_t blk = hh * 16 + jb;
         if (hh + kSelWarps < h1) issue_half(hh + kSelWarps);
+        // long ranges (past the 32 half-tiles prefetched at the start): keep
+        // the half-tile 32 ahead streaming into L2, so every later copy
+        // waits on L2 rather than on DRAM
+        {
+            const int64_t pfh = hh + 32;
+            if (pfh >= h0 + kSelWarps + 32 && pfh < h1) {
+                const uint8_t *pt = codes_u + (size_t)(pfh >> 1) * (D * 128) + (size_t)(pfh & 1) * 256;
+                for (int i = lane; i < 2 * NCH; i += 32) prefetch_l2_line(pt + (i >> 1) * 512 + (i & 1) * 128);
+            }
+        }
         if (sh == 0 && blk < nb_pool) {
             const uint32_t vm = pool_mask(blk, p0, pool);
 #pragma unroll
@@ -1522,7 +1530,7 @@ kvr_status select_launch_att(const LaunchCtx &c, const SelArgs &a, int cs, int v
 int select_cluster_size(int U, int C)
 {
     int cs = 16;
-    while (cs > 1 && (int64_t)U * cs > 2 * 152) cs >>= 1;
+    while (cs > 1 && (int64_t)U * cs > 2 * sm_count()) cs >>= 1;
     while (cs < 16 && (int64_t)cs * kMaxSlice < C) cs <<= 1;
     return cs;
 }

@@ -48,7 +48,6 @@ constexpr int kRankThreads = 1024;
 constexpr int kInitX = 64;      // init CTAs per unit
 constexpr int kMoveX = 16;      // move CTAs per unit
 constexpr int kMaxWin = 16384;  // windows per unit the ranking holds in shared memory
-constexpr int kSms = 152;       // GB300 streaming multiprocessors (grid sizing)
 
 __host__ __device__ constexpr int ledger_bytes_of(int d) { return 2 * kWin * (d / kQG) * 12; }
 
@@ -302,16 +301,29 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Two 2-bit codes as the bf16 pair (ca, cb) of their values 0..3 (ca in the
-// low half). bf16 of 0, 1, 2, 3 is 0x0000, 0x3f80, 0x4000, 0x4040: a byte
-// permute picks the low bytes from 0x40008000 and the high bytes from
-// 0x40403f00.
-__device__ __forceinline__ uint32_t codes2_bf16(uint32_t ca, uint32_t cb)
+// Two 2-bit codes at bits 0-1 and 16-17 of t (the other bits ignored) as the
+// bf16 pair (128 + c0, 128 + c1): 128 is 0x4300 in bf16 and its mantissa step
+// is 1, so OR-ing a code into the low bits is exact (one LOP3). A product
+// over such values carries 128 times the sum of the other operand, which the
+// caller subtracts.
+__device__ __forceinline__ uint32_t codes_off128(uint32_t t)
 {
-    const uint32_t sel = ca * 0x11u + cb * 0x1100u + 0x4040u;
-    uint32_t r;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(0x40008000u), "r"(0x40403f00u), "r"(sel));
-    return r;
+    return (t & 0x00030003u) | 0x43004300u;
+}
+
+// (x0, x1) ~ hi + lo, hi = bf16(x), lo = bf16(x - hi), as bf16x2 words (x0 in
+// the low half): about 16 bits of each value kept; r0, r1 are the values the
+// tensor core sees (hi + lo).
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, uint32_t &lo,
+                                             float &r0, float &r1)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - h0, x1 - h1);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+    r0 = h0 + __uint_as_float(lo << 16);
+    r1 = h1 + __uint_as_float(lo & 0xffff0000u);
 }
 
 // 2-D tensor-map copy of one box into shared memory, completing on `bar`
@@ -340,27 +352,50 @@ template <int D, int G> struct TieredCfg {
     static_assert(LB <= SLOT, "a ledger fits a slot");
     static constexpr int KS = D / 16;                  // k-steps of the score product
     static constexpr int MT = D / 16;                  // 16-dim tiles of the output
-    static constexpr int PST = kWin + 8;               // bf16 stride of a P row (no bank conflicts)
     static constexpr int NSTR = 2;                     // softmax streams: even / odd windows
-    // shared memory after the ring: slot barriers, scores, P (hi, lo), the
-    // scale-weighted P of each INT2 group (hi, lo), z terms, q sums, stream
-    // states, the live-window list
-    static constexpr int oBar = NS * SLOT;                        // uint64 [NS]
-    static constexpr int oSp = oBar + 64;                         // float [NSTR][kWin][8]
-    static constexpr int oP = oSp + NSTR * kWin * 8 * 4;          // bf16 [NSTR][2][8][PST]
-    static constexpr int oSP = oP + NSTR * 2 * 8 * PST * 2;       // bf16 [NSTR][NG][2][8][PST]
-    static constexpr int oZt = oSP + NSTR * NG * 2 * 8 * PST * 2; // float [NSTR][NG][8]
-    static constexpr int oQs = oZt + NSTR * NG * 8 * 4;           // float [NG][8]
-    static constexpr int oSt = oQs + NG * 8 * 4;                  // float [NSTR][m, l, alpha][8]
-    static constexpr int LMAX = 1024;                             // windows per listing pass
-    static constexpr int oLive = oSt + NSTR * 3 * 8 * 4;          // int32 [LMAX]
-    static constexpr int oCnt = oLive + LMAX * 4;                 // int [8]
-    static constexpr int bytes = oCnt + 8 * 4 + 1024;             // + alignment of the ring
+    // P, and the scale-weighted P of each INT2 group, are kept as [token][8
+    // heads] bf16 rows of 16 bytes (a hi and a lo array each): the output's B
+    // operand for 16 tokens is one ldmatrix.x4.trans (hi and lo)
+    static constexpr int PT = kWin * 8 * 2;                      // bytes of a [64][8] bf16 array
+    static constexpr int oBar = NS * SLOT;                       // uint64 [NS]
+    static constexpr int oP = oBar + 64;                         // [NSTR][hi, lo][64][8] bf16
+    static constexpr int oSP = oP + NSTR * 2 * PT;               // [NSTR][NG][hi, lo][64][8] bf16
+    static constexpr int oQp = oSP + NSTR * NG * 2 * PT;         // uint32 [KS][32 lanes][2]
+    static constexpr int oMx = oQp + KS * 32 * 8;                // float [NSTR][4 tiles][8]
+    static constexpr int oLs = oMx + NSTR * 4 * 8 * 4;           // float [NSTR][4 tiles][8]
+    static constexpr int oZc = oLs + NSTR * 4 * 8 * 4;           // float [NSTR][4 tiles][NG][8]
+    static constexpr int oQs = oZc + NSTR * 4 * NG * 8 * 4;      // float [NG][8]
+    static constexpr int oSt = oQs + NG * 8 * 4;                 // float [NSTR][m, l, alpha, m_new][8]
+    static constexpr int LMAX = 1024;                            // windows per listing pass
+    static constexpr int oLive = oSt + NSTR * 4 * 8 * 4;         // int32 [LMAX]
+    static constexpr int oCnt = oLive + LMAX * 4;                // int [8]
+    static constexpr int bytes = oCnt + 8 * 4 + 1024;            // + alignment of the ring
     static_assert(G <= 8, "one 8-column tile of heads");
     static_assert(NS >= 4, "a pair of bf16 windows takes four slots");
     static_assert(8 * 32 * 4 * 4 <= NS * SLOT, "the d=64 stream merge fits the ring");
 };
 
+// Per pair of windows (stream 0 takes window ci, stream 1 window ci + 1) and
+// three block barriers:
+//   1. warp (stream, tile) scores its 16 tokens against the G heads on the
+//      tensor cores (mma.sync m16n8k16, fp32 accumulate) and reduces their
+//      maximum per head;
+//   2. the same warp turns its scores into softmax weights against the
+//      stream's running maximum, writes them (bf16 hi + lo) as the output's B
+//      operand, and its partial sums per head; for an INT2 window also the
+//      weights times each group's V scale and the group's zero and offset
+//      terms;
+//   3. warp (dim tile) accumulates O^T += V^T P^T for both streams; one warp
+//      commits the streams' states and the windows' log2-sum-exps.
+// INT2 codes enter the products as the bf16 values 128 + code (one shift and
+// one LOP3 per pair of codes); the 128 times the other operand's sum is
+// subtracted with the group's scale: a key's score over group g is
+// s (codes . q) + z sum(q) = s (mma - 128 sum(q)) + z sum(q), and V's share
+// is (s p) . codes + sum_t p z = mma(s p) - 128 sum_t (s p) + sum_t p z, with
+// s p as the tensor core sees it (hi + lo). For the scores the k order inside
+// each 16-channel step is permuted (k = 2c, 2c+1, 2c+8, 2c+9 of lane c are
+// channels c, c+8, c+4, c+12: the code bits 2c and 2c+16 of one word), with
+// the query permuted alike.
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 2)
     tiered_attend_kernel(TieredArgs a, const __grid_constant__ CUtensorMap tmK,
@@ -371,17 +406,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     // the ring's 128-byte swizzle repeats every 1 KB: align its base to 1 KB
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *sBar = reinterpret_cast<uint64_t *>(smem + C::oBar);
-    float *sSp = reinterpret_cast<float *>(smem + C::oSp);
-    __nv_bfloat16 *sP = reinterpret_cast<__nv_bfloat16 *>(smem + C::oP);
-    __nv_bfloat16 *sSP = reinterpret_cast<__nv_bfloat16 *>(smem + C::oSP);
-    float *sZt = reinterpret_cast<float *>(smem + C::oZt);
+    uint8_t *sP = smem + C::oP;
+    uint8_t *sSP = smem + C::oSP;
+    uint2 *sQp = reinterpret_cast<uint2 *>(smem + C::oQp);
+    float *sMx = reinterpret_cast<float *>(smem + C::oMx);
+    float *sLs = reinterpret_cast<float *>(smem + C::oLs);
+    float *sZc = reinterpret_cast<float *>(smem + C::oZc);
     float *sQs = reinterpret_cast<float *>(smem + C::oQs);
-    float *sSt = reinterpret_cast<float *>(smem + C::oSt);  // stream st: m at st*24, l +8, alpha +16
+    float *sSt = reinterpret_cast<float *>(smem + C::oSt);  // stream st: m at 32 st, l +8, alpha +16, m_new +24
     int32_t *sLive = reinterpret_cast<int32_t *>(smem + C::oLive);
     int *sCnt = reinterpret_cast<int *>(smem + C::oCnt);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gq = lane >> 2, cq = lane & 3;  // fragment row group, column pair
+    const int lm = lane >> 3, lr = lane & 7;  // ldmatrix: matrix, row
     const int x = blockIdx.x, u = blockIdx.y, b = u / a.Hkv, h = u % a.Hkv;
     int64_t N = a.seq_len[b];
     if (N < 0 || N > a.cap) {
@@ -395,7 +433,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     const __nv_bfloat16 *qg = a.q + ((size_t)b * a.Hkv * G + (size_t)h * G) * D;
     const uint8_t *Lu = a.ledger + uw * (size_t)C::LB;
 
-    // q as B fragments (column n = head gq; heads >= G are zero)
+    // q as B fragments (column n = head gq; heads >= G are zero): in the
+    // natural k order in registers (bf16 windows), in the permuted order of
+    // the INT2 scores in shared memory
     uint32_t qf[C::KS][2];
 #pragma unroll
     for (int ks = 0; ks < C::KS; ks++) {
@@ -406,8 +446,17 @@ __global__ void __launch_bounds__(kThreads, 2)
             qf[ks][1] = row[(16 * ks + 8 + 2 * cq) / 2];
         }
     }
-    // per-group sums of q (the zero's share of an INT2 score); zero P rows of
-    // the padding heads; stream states; slot barriers
+    for (int i = tid; i < C::KS * 32; i += kThreads) {
+        const int ks = i / 32, n = (i % 32) >> 2, c = i & 3;
+        uint32_t v0 = 0u, v1 = 0u;
+        if (n < G) {
+            const uint16_t *row = reinterpret_cast<const uint16_t *>(qg + (size_t)n * D) + 16 * ks;
+            v0 = (uint32_t)row[c] | ((uint32_t)row[c + 8] << 16);
+            v1 = (uint32_t)row[c + 4] | ((uint32_t)row[c + 12] << 16);
+        }
+        sQp[i] = make_uint2(v0, v1);
+    }
+    // per-group sums of q (the zero's share of an INT2 score); stream states
     if (tid < C::NG * 8) {
         const int g = tid / 8, hh = tid % 8;
         float sum = 0.0f;
@@ -415,13 +464,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int j = 0; j < kQG; j++) sum += __bfloat162float(qg[(size_t)hh * D + g * kQG + j]);
         sQs[tid] = sum;
     }
-    for (int i = tid; i < C::NSTR * (2 + 2 * C::NG) * 8 * C::PST; i += kThreads) {
-        const int row = (i / C::PST) % 8;
-        if (row >= G) sP[i] = __float2bfloat16_rn(0.0f);  // sP and sSP are contiguous
-    }
     if (tid < C::NSTR * 8) {
-        sSt[(tid / 8) * 24 + tid % 8] = -CUDART_INF_F;
-        sSt[(tid / 8) * 24 + 8 + tid % 8] = 0.0f;
+        sSt[(tid / 8) * 32 + tid % 8] = -CUDART_INF_F;
+        sSt[(tid / 8) * 32 + 8 + tid % 8] = 0.0f;
     }
     // set when a wait for a copy ran out: the CTA then stops after the
     // current pair of windows, waits (bounded) for the copies it issued and
@@ -522,7 +567,6 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         };
 
-        // windows in pairs: window ci feeds stream 0, ci + 1 stream 1
         for (int ci = 0; ci < nlive; ci += 2) {
             const bool hasB = ci + 1 < nlive;
             // per window (A: stream 0, B: stream 1) as scalars, picked with
@@ -545,7 +589,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const bool q2s = st ? q2B : q2A;
                 const int nvs = st ? nvB : nvA, sls = st ? slB : slA;
                 // rows past the sequence in the open window: whatever the cache
-                // holds there must not reach the sum (0 * NaN), so zero them
+                // holds there must not reach the sum (0 * NaN), so zero them in
+                // V (their scores are -inf by index); read after the barrier below
                 if ((st == 0 || hasB) && !q2s && nvs < kWin) {
                     uint8_t *vb = smem + ((sls + 1) % C::NS) * C::SLOT;
                     const int nz = kWin - nvs;
@@ -556,211 +601,260 @@ __global__ void __launch_bounds__(kThreads, 2)
                     }
                 }
             }
+
+            // ---- 1. scores: warp -> window (warp / 4), 16 tokens (warp % 4), all dims
+            const int st = warp >> 2, mt = warp & 3;
+            const bool act = st == 0 || hasB;
+            const bool q2s = st ? q2B : q2A;
+            const int nvs = st ? nvB : nvA;
+            const uint8_t *kbuf = smem + ((st ? slB : slA) % C::NS) * C::SLOT;
+            const int t0 = 16 * mt + gq;  // the lane's tokens t0, t0 + 8; heads 2cq, 2cq + 1
+            float sc[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+            if (act) {
+                float c4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                if (!q2s) {
+                    // row r, 16-byte chunk c of a box sits at r*128 + ((c ^ (r % 8)) * 16);
+                    // even and odd k-steps in two accumulators (two shorter chains)
+                    const uint8_t *rowp = kbuf + (16 * mt + lr + ((lm & 1) ? 8 : 0)) * 128;
+                    float c4b[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                    for (int ks = 0; ks < C::KS; ks++) {
+                        const int ch = 2 * ks + ((lm & 2) ? 1 : 0);
+                        uint32_t af[4];
+                        ldsm_x4(af, rowp + (ch >> 3) * kWin * 128 + (((ch & 7) ^ lr) << 4));
+                        mma16816((ks & 1) ? c4b : c4, af, qf[ks][0], qf[ks][1]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; i++) c4[i] += c4b[i];
+                } else {
+                    const int r1 = t0 + 8;
+#pragma unroll
+                    for (int g = 0; g < C::NG; g++) {
+                        const uint2 w0 = *reinterpret_cast<const uint2 *>(kbuf + (t0 * C::NG + g) * 8);
+                        const uint2 w1 = *reinterpret_cast<const uint2 *>(kbuf + (r1 * C::NG + g) * 8);
+                        float cg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                        for (int j = 0; j < 2; j++) {
+                            const uint32_t x0 = j ? w0.y : w0.x, x1 = j ? w1.y : w1.x;
+                            uint32_t af[4];
+                            af[0] = codes_off128(x0 >> (2 * cq));
+                            af[1] = codes_off128(x1 >> (2 * cq));
+                            af[2] = codes_off128(x0 >> (2 * cq + 8));
+                            af[3] = codes_off128(x1 >> (2 * cq + 8));
+                            const uint2 qp = sQp[(2 * g + j) * 32 + lane];
+                            mma16816(cg, af, qp.x, qp.y);
+                        }
+                        const uint32_t pa = *reinterpret_cast<const uint32_t *>(kbuf + C::CB + (t0 * C::NG + g) * 4);
+                        const uint32_t pb = *reinterpret_cast<const uint32_t *>(kbuf + C::CB + (r1 * C::NG + g) * 4);
+                        const float s0f = __half2float(__ushort_as_half((unsigned short)(pa & 0xffffu)));
+                        const float z0f = __half2float(__ushort_as_half((unsigned short)(pa >> 16)));
+                        const float s1f = __half2float(__ushort_as_half((unsigned short)(pb & 0xffffu)));
+                        const float z1f = __half2float(__ushort_as_half((unsigned short)(pb >> 16)));
+                        const float qa = sQs[g * 8 + 2 * cq], qb = sQs[g * 8 + 2 * cq + 1];
+                        const float y0 = fmaf(-128.0f, s0f, z0f), y1 = fmaf(-128.0f, s1f, z1f);
+                        c4[0] += fmaf(s0f, cg[0], y0 * qa);
+                        c4[1] += fmaf(s0f, cg[1], y0 * qb);
+                        c4[2] += fmaf(s1f, cg[2], y1 * qa);
+                        c4[3] += fmaf(s1f, cg[3], y1 * qb);
+                    }
+                }
+                // log2-domain scores; rows past the sequence (open window) -inf
+                if (t0 < nvs) {
+                    sc[0] = c4[0] * a.scale_log2;
+                    sc[1] = c4[1] * a.scale_log2;
+                }
+                if (t0 + 8 < nvs) {
+                    sc[2] = c4[2] * a.scale_log2;
+                    sc[3] = c4[3] * a.scale_log2;
+                }
+                float ma = fmaxf(sc[0], sc[2]), mb = fmaxf(sc[1], sc[3]);
+                __syncwarp();
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    ma = fmaxf(ma, __shfl_xor_sync(kFull, ma, o));
+                    mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o));
+                }
+                if (gq == 0) {
+                    sMx[(st * 4 + mt) * 8 + 2 * cq] = ma;
+                    sMx[(st * 4 + mt) * 8 + 2 * cq + 1] = mb;
+                }
+            }
             __syncthreads();
             // every write of s_dead (the waits above) precedes this read, every
             // later one follows the pair's last barrier: `dead` is block-uniform
             dead = s_dead != 0;
 
-            // ---- scores: warp -> window (warp / 4), 16 tokens (warp % 4), all dims
-            {
-                const int st = warp >> 2, mt = warp & 3;
-                if (st == 0 || hasB) {
-                    const uint8_t *buf = smem + ((st ? slB : slA) % C::NS) * C::SLOT;
-                    float c4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                    if (!(st ? q2B : q2A)) {
-                        const int lm = lane >> 3, lr = lane & 7;  // ldmatrix: matrix, row
-                        // row r, 16-byte chunk c of a box sits at r*128 + ((c ^ (r % 8)) * 16)
-                        const uint8_t *rowp = buf + (16 * mt + lr + ((lm & 1) ? 8 : 0)) * 128;
+            // ---- 2. softmax weights of the warp's tokens, B operands of the output
+            if (act) {
+                const int ha = 2 * cq, hb = ha + 1;
+                float *stt = sSt + st * 32;
+                float mwa = sMx[st * 32 + ha], mwb = sMx[st * 32 + hb];
 #pragma unroll
-                        for (int ks = 0; ks < C::KS; ks++) {
-                            const int ch = 2 * ks + ((lm & 2) ? 1 : 0);
-                            uint32_t af[4];
-                            ldsm_x4(af, rowp + (ch >> 3) * kWin * 128 + (((ch & 7) ^ lr) << 4));
-                            mma16816(c4, af, qf[ks][0], qf[ks][1]);
-                        }
-                    } else {
-                        const int r0 = 16 * mt + gq, r1 = r0 + 8;
-#pragma unroll
-                        for (int g = 0; g < C::NG; g++) {
-                            const uint2 w0 = *reinterpret_cast<const uint2 *>(buf + (r0 * C::NG + g) * 8);
-                            const uint2 w1 = *reinterpret_cast<const uint2 *>(buf + (r1 * C::NG + g) * 8);
-                            float cg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                            for (int j = 0; j < 2; j++) {
-                                const uint32_t x0 = j ? w0.y : w0.x, x1 = j ? w1.y : w1.x;
-                                const int s0 = 4 * cq, s1 = 4 * cq + 16;
-                                uint32_t af[4];
-                                af[0] = codes2_bf16((x0 >> s0) & 3u, (x0 >> (s0 + 2)) & 3u);
-                                af[1] = codes2_bf16((x1 >> s0) & 3u, (x1 >> (s0 + 2)) & 3u);
-                                af[2] = codes2_bf16((x0 >> s1) & 3u, (x0 >> (s1 + 2)) & 3u);
-                                af[3] = codes2_bf16((x1 >> s1) & 3u, (x1 >> (s1 + 2)) & 3u);
-                                mma16816(cg, af, qf[2 * g + j][0], qf[2 * g + j][1]);
-                            }
-                            // value = code * s + z: score = s * (codes . q) + z * sum(q)
-                            const uint32_t pa = *reinterpret_cast<const uint32_t *>(buf + C::CB + (r0 * C::NG + g) * 4);
-                            const uint32_t pb = *reinterpret_cast<const uint32_t *>(buf + C::CB + (r1 * C::NG + g) * 4);
-                            const float s0f = __half2float(__ushort_as_half((unsigned short)(pa & 0xffffu)));
-                            const float z0f = __half2float(__ushort_as_half((unsigned short)(pa >> 16)));
-                            const float s1f = __half2float(__ushort_as_half((unsigned short)(pb & 0xffffu)));
-                            const float z1f = __half2float(__ushort_as_half((unsigned short)(pb >> 16)));
-                            const float qa = sQs[g * 8 + 2 * cq], qb = sQs[g * 8 + 2 * cq + 1];
-                            c4[0] += fmaf(s0f, cg[0], z0f * qa);
-                            c4[1] += fmaf(s0f, cg[1], z0f * qb);
-                            c4[2] += fmaf(s1f, cg[2], z1f * qa);
-                            c4[3] += fmaf(s1f, cg[3], z1f * qb);
-                        }
-                    }
-                    float *sp = sSp + (size_t)st * kWin * 8;
-                    *reinterpret_cast<float2 *>(sp + (16 * mt + gq) * 8 + 2 * cq) = make_float2(c4[0], c4[1]);
-                    *reinterpret_cast<float2 *>(sp + (16 * mt + gq + 8) * 8 + 2 * cq) = make_float2(c4[2], c4[3]);
+                for (int m2 = 1; m2 < 4; m2++) {
+                    mwa = fmaxf(mwa, sMx[(st * 4 + m2) * 8 + ha]);
+                    mwb = fmaxf(mwb, sMx[(st * 4 + m2) * 8 + hb]);
                 }
-            }
-            __syncthreads();
-
-            // ---- softmax: warp -> stream (warp / 4), heads warp % 4, + 4
-            {
-                const int st = warp >> 2;
-                if (st == 0 || hasB) {
-                    const float *sp = sSp + (size_t)st * kWin * 8;
-                    __nv_bfloat16 *pst = sP + (size_t)st * 2 * 8 * C::PST;
-                    __nv_bfloat16 *sps = sSP + (size_t)st * C::NG * 2 * 8 * C::PST;
-                    float *zts = sZt + st * C::NG * 8;
-                    float *stt = sSt + st * 24;
-                    const uint8_t *buf = smem + ((st ? slB : slA) % C::NS) * C::SLOT;
-                    const int nvs = st ? nvB : nvA;
-                    const bool q2s = st ? q2B : q2A;
-                    const int64_t cws = st ? cwB : cwA;
-                    for (int g = warp & 3; g < G; g += 4) {
-                        float s0 = -CUDART_INF_F, s1 = -CUDART_INF_F;
-                        if (lane < nvs) s0 = sp[lane * 8 + g] * a.scale_log2;
-                        if (lane + 32 < nvs) s1 = sp[(lane + 32) * 8 + g] * a.scale_log2;
-                        float wm = fmaxf(s0, s1);
-                        __syncwarp();
+                const float ma_old = stt[ha], mb_old = stt[hb];
+                const float ma_new = fmaxf(ma_old, mwa), mb_new = fmaxf(mb_old, mwb);
+                // heads past G weigh nothing
+                const bool va = ha < G, vb = hb < G;
+                float p[4];
+                p[0] = (va && sc[0] != -CUDART_INF_F) ? exp2f(sc[0] - ma_new) : 0.0f;
+                p[1] = (vb && sc[1] != -CUDART_INF_F) ? exp2f(sc[1] - mb_new) : 0.0f;
+                p[2] = (va && sc[2] != -CUDART_INF_F) ? exp2f(sc[2] - ma_new) : 0.0f;
+                p[3] = (vb && sc[3] != -CUDART_INF_F) ? exp2f(sc[3] - mb_new) : 0.0f;
+                float la = p[0] + p[2], lb = p[1] + p[3];
 #pragma unroll
-                        for (int o = 16; o; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(kFull, wm, o));
-                        const float m_old = stt[g];
-                        const float m_new = fmaxf(m_old, wm);
-                        const float p0 = exp2f(s0 - m_new), p1 = exp2f(s1 - m_new);
-                        float ls = p0 + p1;
+                for (int o = 4; o < 32; o <<= 1) {
+                    la += __shfl_xor_sync(kFull, la, o);
+                    lb += __shfl_xor_sync(kFull, lb, o);
+                }
+                if (gq == 0) {
+                    sLs[(st * 4 + mt) * 8 + ha] = la;
+                    sLs[(st * 4 + mt) * 8 + hb] = lb;
+                    if (mt == 0) {  // the stream's new maximum and rescale factor
+                        stt[24 + ha] = ma_new;
+                        stt[24 + hb] = mb_new;
+                        stt[16 + ha] = (ma_old == -CUDART_INF_F) ? 0.0f : exp2f(ma_old - ma_new);
+                        stt[16 + hb] = (mb_old == -CUDART_INF_F) ? 0.0f : exp2f(mb_old - mb_new);
+                    }
+                }
+                // P (hi, lo) at [token][head]: this lane's heads ha, hb of t0 and t0 + 8
+                uint8_t *pst = sP + st * 2 * C::PT;
+                uint32_t hi, lo;
+                float r0, r1;
+                split_bf16x2(p[0], p[1], hi, lo, r0, r1);
+                *reinterpret_cast<uint32_t *>(pst + t0 * 16 + 4 * cq) = hi;
+                *reinterpret_cast<uint32_t *>(pst + C::PT + t0 * 16 + 4 * cq) = lo;
+                split_bf16x2(p[2], p[3], hi, lo, r0, r1);
+                *reinterpret_cast<uint32_t *>(pst + (t0 + 8) * 16 + 4 * cq) = hi;
+                *reinterpret_cast<uint32_t *>(pst + C::PT + (t0 + 8) * 16 + 4 * cq) = lo;
+                if (q2s) {
+                    // V values are code * s + z per (token, group): the output
+                    // takes B = s p (hi, lo) per group, and adds this group's
+                    // sum_t (p z - 128 (s p as seen))
+                    const uint8_t *vp = kbuf + 2 * C::CB + C::PB;  // V params
 #pragma unroll
-                        for (int o = 16; o; o >>= 1) ls += __shfl_xor_sync(kFull, ls, o);
-                        // P split into bf16 hi + lo (about 16 bits kept)
-                        const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
-                        pst[g * C::PST + lane] = h0;
-                        pst[g * C::PST + lane + 32] = h1;
-                        pst[(8 + g) * C::PST + lane] = __float2bfloat16_rn(p0 - __bfloat162float(h0));
-                        pst[(8 + g) * C::PST + lane + 32] = __float2bfloat16_rn(p1 - __bfloat162float(h1));
-                        if (q2s) {
-                            // V values = code * s + z: P weighted by each group's
-                            // scale, and the zero's share sum_t z p per group
-                            const uint8_t *vp = buf + 2 * C::CB + C::PB;  // V params
+                    for (int g = 0; g < C::NG; g++) {
+                        const uint32_t q0 = *reinterpret_cast<const uint32_t *>(vp + (t0 * C::NG + g) * 4);
+                        const uint32_t q1 = *reinterpret_cast<const uint32_t *>(vp + ((t0 + 8) * C::NG + g) * 4);
+                        const float s0 = __half2float(__ushort_as_half((unsigned short)(q0 & 0xffffu)));
+                        const float z0 = __half2float(__ushort_as_half((unsigned short)(q0 >> 16)));
+                        const float s1 = __half2float(__ushort_as_half((unsigned short)(q1 & 0xffffu)));
+                        const float z1 = __half2float(__ushort_as_half((unsigned short)(q1 >> 16)));
+                        uint8_t *spg = sSP + (size_t)(st * C::NG + g) * 2 * C::PT;
+                        float e0, e1, e2, e3;
+                        split_bf16x2(s0 * p[0], s0 * p[1], hi, lo, e0, e1);
+                        *reinterpret_cast<uint32_t *>(spg + t0 * 16 + 4 * cq) = hi;
+                        *reinterpret_cast<uint32_t *>(spg + C::PT + t0 * 16 + 4 * cq) = lo;
+                        split_bf16x2(s1 * p[2], s1 * p[3], hi, lo, e2, e3);
+                        *reinterpret_cast<uint32_t *>(spg + (t0 + 8) * 16 + 4 * cq) = hi;
+                        *reinterpret_cast<uint32_t *>(spg + C::PT + (t0 + 8) * 16 + 4 * cq) = lo;
+                        float za = fmaf(z0, p[0], fmaf(z1, p[2], -128.0f * (e0 + e2)));
+                        float zb = fmaf(z0, p[1], fmaf(z1, p[3], -128.0f * (e1 + e3)));
 #pragma unroll
-                            for (int gg = 0; gg < C::NG; gg++) {
-                                const uint32_t q0 = *reinterpret_cast<const uint32_t *>(vp + (lane * C::NG + gg) * 4);
-                                const uint32_t q1 = *reinterpret_cast<const uint32_t *>(vp + ((lane + 32) * C::NG + gg) * 4);
-                                const float sa = __half2float(__ushort_as_half((unsigned short)(q0 & 0xffffu)));
-                                const float za = __half2float(__ushort_as_half((unsigned short)(q0 >> 16)));
-                                const float sb = __half2float(__ushort_as_half((unsigned short)(q1 & 0xffffu)));
-                                const float zb = __half2float(__ushort_as_half((unsigned short)(q1 >> 16)));
-                                const float w0 = sa * p0, w1 = sb * p1;
-                                const __nv_bfloat16 k0 = __float2bfloat16_rn(w0), k1 = __float2bfloat16_rn(w1);
-                                __nv_bfloat16 *spg = sps + (size_t)gg * 2 * 8 * C::PST;
-                                spg[g * C::PST + lane] = k0;
-                                spg[g * C::PST + lane + 32] = k1;
-                                spg[(8 + g) * C::PST + lane] = __float2bfloat16_rn(w0 - __bfloat162float(k0));
-                                spg[(8 + g) * C::PST + lane + 32] = __float2bfloat16_rn(w1 - __bfloat162float(k1));
-                                float zs = za * p0 + zb * p1;
-#pragma unroll
-                                for (int o = 16; o; o >>= 1) zs += __shfl_xor_sync(kFull, zs, o);
-                                if (lane == 0) zts[gg * 8 + g] = zs;
-                            }
+                        for (int o = 4; o < 32; o <<= 1) {
+                            za += __shfl_xor_sync(kFull, za, o);
+                            zb += __shfl_xor_sync(kFull, zb, o);
                         }
-                        if (lane == 0) {
-                            const float al = exp2f(m_old - m_new);
-                            stt[16 + g] = al;
-                            stt[8 + g] = stt[8 + g] * al + ls;
-                            stt[g] = m_new;
-                            a.lse[(uw + cws) * G + g] = m_new + log2f(ls);
+                        if (gq == 0) {
+                            sZc[((st * 4 + mt) * C::NG + g) * 8 + ha] = za;
+                            sZc[((st * 4 + mt) * C::NG + g) * 8 + hb] = zb;
                         }
                     }
                 }
             }
             __syncthreads();
 
-            // ---- output: O^T (dims x heads) += V^T P^T, per stream
+            // ---- 3. output: O^T (dims x heads) += V^T P^T, per stream
 #pragma unroll
-            for (int st = 0; st < 2; st++) {
-                if (!BOTH && st != my_st) continue;
-                if (st == 1 && !hasB) continue;
-                float *ac = acc[BOTH ? st : 0];
-                const float *stt = sSt + st * 24;
+            for (int so = 0; so < 2; so++) {
+                if (!BOTH && so != my_st) continue;
+                if (so == 1 && !hasB) continue;
+                float *ac = acc[BOTH ? so : 0];
+                const float *stt = sSt + so * 32;
                 const float al0 = (2 * cq < G) ? stt[16 + 2 * cq] : 0.0f;
                 const float al1 = (2 * cq + 1 < G) ? stt[16 + 2 * cq + 1] : 0.0f;
                 ac[0] *= al0;
                 ac[1] *= al1;
                 ac[2] *= al0;
                 ac[3] *= al1;
-                const __nv_bfloat16 *pst = sP + (size_t)st * 2 * 8 * C::PST;
-                const int sls = st ? slB : slA;
-                if (!(st ? q2B : q2A)) {
+                const int sls = so ? slB : slA;
+                // B operand rows: matrices hi t..t+7, hi t+8.., lo t.., lo t+8..
+                const int brow = (lm & 1) * 8 + lr, bpart = (lm & 2) ? C::PT : 0;
+                if (!(so ? q2B : q2A)) {
+                    const uint8_t *pst = sP + so * 2 * C::PT + bpart + brow * 16;
                     const uint8_t *vbuf = smem + ((sls + 1) % C::NS) * C::SLOT;
-                    const int lm = lane >> 3, lr = lane & 7;  // ldmatrix: matrix, row
                     const int ch = 2 * mt_d + ((lm & 1) ? 1 : 0);
                     const uint8_t *vrow = vbuf + (ch >> 3) * kWin * 128 +
                                           (lr + ((lm & 2) ? 8 : 0)) * 128 + (((ch & 7) ^ lr) << 4);
+                    // the lo products in their own accumulator: two chains of 4
+                    float lo4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                     for (int j = 0; j < 4; j++) {
-                        const int t0 = 16 * j;
-                        uint32_t af[4];
-                        ldsm_x4_t(af, vrow + t0 * 128);
-                        const __nv_bfloat16 *ph = pst + gq * C::PST + t0 + 2 * cq;
-                        const __nv_bfloat16 *pl = pst + (8 + gq) * C::PST + t0 + 2 * cq;
-                        mma16816(*reinterpret_cast<float(*)[4]>(ac), af,
-                                 *reinterpret_cast<const uint32_t *>(ph),
-                                 *reinterpret_cast<const uint32_t *>(ph + 8));
-                        mma16816(*reinterpret_cast<float(*)[4]>(ac), af,
-                                 *reinterpret_cast<const uint32_t *>(pl),
-                                 *reinterpret_cast<const uint32_t *>(pl + 8));
+                        uint32_t af[4], bq[4];
+                        ldsm_x4_t(af, vrow + 16 * j * 128);
+                        ldsm_x4_t(bq, pst + 16 * j * 16);
+                        mma16816(*reinterpret_cast<float(*)[4]>(ac), af, bq[0], bq[1]);
+                        mma16816(lo4, af, bq[2], bq[3]);
                     }
+#pragma unroll
+                    for (int i = 0; i < 4; i++) ac[i] += lo4[i];
                 } else {
                     const uint8_t *buf = smem + (sls % C::NS) * C::SLOT;
                     const int g = (16 * mt_d) / kQG, wsel = ((16 * mt_d) % kQG) / 16;
-                    const uint8_t *vc = buf + C::CB + C::PB;  // V codes
-                    const __nv_bfloat16 *spg = sSP + ((size_t)st * C::NG + g) * 2 * 8 * C::PST;
+                    const uint8_t *vc = buf + C::CB + C::PB + 4 * wsel;  // V codes of the tile
+                    const uint8_t *spg = sSP + (size_t)(so * C::NG + g) * 2 * C::PT + bpart + brow * 16;
+                    float lo4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                     for (int j = 0; j < 4; j++) {
-                        const int t0 = 16 * j;
-                        const int ta = t0 + 2 * cq;
-                        const uint32_t wa = *reinterpret_cast<const uint32_t *>(vc + (ta * C::NG + g) * 8 + 4 * wsel);
-                        const uint32_t wb = *reinterpret_cast<const uint32_t *>(vc + ((ta + 1) * C::NG + g) * 8 + 4 * wsel);
-                        const uint32_t wc = *reinterpret_cast<const uint32_t *>(vc + ((ta + 8) * C::NG + g) * 8 + 4 * wsel);
-                        const uint32_t wd = *reinterpret_cast<const uint32_t *>(vc + ((ta + 9) * C::NG + g) * 8 + 4 * wsel);
-                        const int e0 = 2 * gq, e1 = 2 * (gq + 8);
-                        uint32_t af[4];
-                        af[0] = codes2_bf16((wa >> e0) & 3u, (wb >> e0) & 3u);
-                        af[1] = codes2_bf16((wa >> e1) & 3u, (wb >> e1) & 3u);
-                        af[2] = codes2_bf16((wc >> e0) & 3u, (wd >> e0) & 3u);
-                        af[3] = codes2_bf16((wc >> e1) & 3u, (wd >> e1) & 3u);
-                        const __nv_bfloat16 *ph = spg + gq * C::PST + t0 + 2 * cq;
-                        const __nv_bfloat16 *pl = spg + (8 + gq) * C::PST + t0 + 2 * cq;
-                        mma16816(*reinterpret_cast<float(*)[4]>(ac), af,
-                                 *reinterpret_cast<const uint32_t *>(ph),
-                                 *reinterpret_cast<const uint32_t *>(ph + 8));
-                        mma16816(*reinterpret_cast<float(*)[4]>(ac), af,
-                                 *reinterpret_cast<const uint32_t *>(pl),
-                                 *reinterpret_cast<const uint32_t *>(pl + 8));
+                        const int ta = 16 * j + 2 * cq;
+                        const uint32_t wa = *reinterpret_cast<const uint32_t *>(vc + (ta * C::NG + g) * 8);
+                        const uint32_t wb = *reinterpret_cast<const uint32_t *>(vc + ((ta + 1) * C::NG + g) * 8);
+                        const uint32_t wc = *reinterpret_cast<const uint32_t *>(vc + ((ta + 8) * C::NG + g) * 8);
+                        const uint32_t wd = *reinterpret_cast<const uint32_t *>(vc + ((ta + 9) * C::NG + g) * 8);
+                        // the tile's channels 0-7 of two tokens in the halves of
+                        // one word, channels 8-15 in another
+                        const uint32_t ab0 = __byte_perm(wa, wb, 0x5410), ab1 = __byte_perm(wa, wb, 0x7632);
+                        const uint32_t cd0 = __byte_perm(wc, wd, 0x5410), cd1 = __byte_perm(wc, wd, 0x7632);
+                        uint32_t af[4], bq[4];
+                        af[0] = codes_off128(ab0 >> (2 * gq));  // dim gq, tokens ta, ta + 1
+                        af[1] = codes_off128(ab1 >> (2 * gq));  // dim gq + 8
+                        af[2] = codes_off128(cd0 >> (2 * gq));  // dim gq, tokens ta + 8, ta + 9
+                        af[3] = codes_off128(cd1 >> (2 * gq));
+                        ldsm_x4_t(bq, spg + 16 * j * 16);
+                        mma16816(*reinterpret_cast<float(*)[4]>(ac), af, bq[0], bq[1]);
+                        mma16816(lo4, af, bq[2], bq[3]);
                     }
-                    const float *zts = sZt + st * C::NG * 8;
-                    const float za = (2 * cq < G) ? zts[g * 8 + 2 * cq] : 0.0f;
-                    const float zb = (2 * cq + 1 < G) ? zts[g * 8 + 2 * cq + 1] : 0.0f;
-                    ac[0] += za;
-                    ac[1] += zb;
-                    ac[2] += za;
-                    ac[3] += zb;
+                    float za = 0.0f, zb = 0.0f;
+#pragma unroll
+                    for (int m2 = 0; m2 < 4; m2++) {
+                        za += sZc[((so * 4 + m2) * C::NG + g) * 8 + 2 * cq];
+                        zb += sZc[((so * 4 + m2) * C::NG + g) * 8 + 2 * cq + 1];
+                    }
+                    ac[0] += lo4[0] + za;
+                    ac[1] += lo4[1] + zb;
+                    ac[2] += lo4[2] + za;
+                    ac[3] += lo4[3] + zb;
+                }
+            }
+            // the streams' states (the rescale factors above were read from
+            // their own slots) and the windows' log2-sum-exps
+            if (warp == kThreads / 32 - 1) {
+                const int so = lane >> 3, hh = lane & 7;
+                if (hh < G && (so == 0 || (so == 1 && hasB))) {
+                    float *stt = sSt + so * 32;
+                    float ls = 0.0f;
+#pragma unroll
+                    for (int m2 = 0; m2 < 4; m2++) ls += sLs[(so * 4 + m2) * 8 + hh];
+                    const float mn = stt[24 + hh];
+                    stt[8 + hh] = stt[8 + hh] * stt[16 + hh] + ls;
+                    stt[hh] = mn;
+                    a.lse[(uw + (so ? cwB : cwA)) * G + hh] = mn + log2f(ls);
                 }
             }
             fence_proxy_async();  // this thread's slot accesses before the next copies into it
-            __syncthreads();      // the pair's slots, P and the scores are reused next
+            __syncthreads();      // the pair's slots, P and the states are reused next
             lc += needA + needB;
             if (dead) break;
         }
@@ -774,10 +868,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     // ---- merge the two streams into this CTA's partial: o[head][dim]
     // (unnormalised), m, l per head
     float *part = a.part + ((size_t)u * a.S + x) * (2 * G + G * D);
-    auto factor = [&](int st, int hh) {  // weight of stream st's head hh in the merge
-        const float m0 = sSt[hh], m1 = sSt[24 + hh];
+    auto factor = [&](int st2, int hh) {  // weight of stream st2's head hh in the merge
+        const float m0 = sSt[hh], m1 = sSt[32 + hh];
         const float M = fmaxf(m0, m1);
-        const float m = st ? m1 : m0;
+        const float m = st2 ? m1 : m0;
         return (m == -CUDART_INF_F) ? 0.0f : exp2f(m - M);
     };
     if (!BOTH) {
@@ -808,9 +902,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     }
     if (tid < G) {
-        const float m0 = sSt[tid], m1 = sSt[24 + tid];
+        const float m0 = sSt[tid], m1 = sSt[32 + tid];
         part[tid] = fmaxf(m0, m1);
-        part[G + tid] = sSt[8 + tid] * factor(0, tid) + sSt[32 + tid] * factor(1, tid);
+        part[G + tid] = sSt[8 + tid] * factor(0, tid) + sSt[40 + tid] * factor(1, tid);
     }
 }
 
@@ -1032,7 +1126,7 @@ __global__ void __launch_bounds__(kThreads) tier_move_kernel(TierArgs a, const i
 
 int tiered_splits(int64_t U, int64_t n_win)
 {
-    const int64_t target = (4 * kSms + U - 1) / U;
+    const int64_t target = (4 * (int64_t)sm_count() + U - 1) / U;
     const int64_t by_len = (n_win + 7) / 8;
     const int64_t s = target < by_len ? target : by_len;
     return (int)(s < 1 ? 1 : s);

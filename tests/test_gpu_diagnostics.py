@@ -17,7 +17,7 @@ import oracle
 import workloads as wl
 import sparse_decode_attention_gb300 as kvr
 from oracle import diagnostics as odg
-from sparse_decode_attention_gb300 import diagnostics as dg
+import bench_diagnostics as dg
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
