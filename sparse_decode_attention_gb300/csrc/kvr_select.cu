@@ -230,27 +230,34 @@ enum {
 // them), every CS-th token of the Local (+ buffer) region [pool, N) and every
 // CS-th Sink token [0, p0). The K and V rows of up to CH tokens at a time are
 // staged in shared memory with 16-byte cp.async copies (over the code ring
-// and the candidate arrays, dead by now). A token's row is spread over a
-// warp (d/32 dims per lane); the GA per-head dots are reduced so that head g
-// lands in lanes [g*32/GA, (g+1)*32/GA); online softmax in the log2 domain;
-// p*v accumulated in registers. Heads past the group size G score against a
-// zero query and are never written. Warps merge in shared memory, CTAs
-// through distributed shared memory; each CTA writes an equal share of the
-// unit's G*d outputs. Contains cluster barriers: every CTA calls it, after
-// arriving at the split barrier that this function's first wait completes.
+// and the candidate arrays, dead by now). bf16 caches: warp w takes the
+// 16-token tiles w, w + 8, ...; scores = K q^T and O^T += V^T P^T on the
+// tensor cores (mma.sync m16n8k16, fp32 accumulate; the staged rows
+// XOR-swizzled by 16-byte chunk so ldmatrix is conflict-free; P split into
+// bf16 hi + lo), online softmax per warp in the log2 domain. fp32 caches: a
+// token's row is spread over a warp (d/32 dims per lane) and the dots run on
+// the CUDA cores. Heads past the group size G score against a zero query and
+// are never written. Warps merge in shared memory, CTAs through distributed
+// shared memory; each CTA writes an equal share of the unit's G*d outputs.
+// Contains cluster barriers: every CTA calls it, after arriving at the split
+// barrier that this function's first wait completes.
 template <int D, typename T, int GA>
 __device__ __forceinline__ void attend_tail(const SelArgs &a, uint8_t *smem, const int32_t *sWin,
                                             int nw, int b, int h, int64_t N, int64_t p0,
                                             int64_t pool, int rank, int CS)
 {
     using SM = SelSmem<D, T>;
+    constexpr bool TC = sizeof(T) == 2;        // tensor-core path (bf16)
     constexpr int E = D / 32, RB = SM::kRowBytes, PPR = RB / 16, LPH = 32 / GA;
     constexpr int CH = SM::kStage / (2 * RB);  // tokens staged at once
-    constexpr int TPW = 4;                     // tokens per warp per round
-    static_assert(CH >= kSelWarps * TPW, "a round fits the stage");
+    constexpr int TPW = 4;                     // CUDA-core path: tokens per warp per round
+    static_assert(CH >= kSelWarps * TPW && CH % 16 == 0, "a round fits the stage");
     static_assert(kSelWarps * GA * (D + 2) * 4 <= SM::kStage, "warp partials fit the stage");
+    static_assert(kMaxSlice * 4 + kSelWarps * 512 <= 8 * kPlaneCap * 4, "P tiles fit the plane area");
     cg::cluster_group cluster = cg::this_cluster();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gq = lane >> 2, cq = lane & 3;  // fragment row group, column pair
+    const int lm = lane >> 3, lr = lane & 7;  // ldmatrix: matrix, row
     const int G = a.G;
     const int u = blockIdx.y;
     float *sPm = reinterpret_cast<float *>(smem + SM::oAtt);
@@ -266,26 +273,48 @@ __device__ __forceinline__ void attend_tail(const SelArgs &a, uint8_t *smem, con
         if (i < nw + nlm) return pool + rank + (int64_t)CS * (i - nw);
         return rank + (int64_t)CS * (i - nw - nlm);
     };
+    const T *qg = static_cast<const T *>(a.q) + ((int64_t)b * a.Hq + (int64_t)h * G) * D;
 
+    // CUDA-core state: the group's heads (log2 domain) per lane, softmax
+    // state of head lane / LPH
     float qr[GA][E];
-    {
-        const T *qg = static_cast<const T *>(a.q) + ((int64_t)b * a.Hq + (int64_t)h * G) * D;
+    float acc[GA][E];
+    float m = -INFINITY, l = 0.0f;
+    // tensor-core state: q as B fragments (column n = head gq; zero past G),
+    // O^T tiles (16 dims x 8 heads), softmax state of heads 2cq, 2cq + 1
+    constexpr int KS = TC ? D / 16 : 1, MD = TC ? D / 16 : 1;
+    uint32_t qf[KS][2];
+    float oacc[MD][4];
+    float m2[2] = {-INFINITY, -INFINITY}, l2[2] = {0.0f, 0.0f};
+    if constexpr (TC) {
+#pragma unroll
+        for (int ks = 0; ks < KS; ks++) {
+            qf[ks][0] = qf[ks][1] = 0u;
+            if (gq < G) {
+                const uint32_t *row = reinterpret_cast<const uint32_t *>(qg + (size_t)gq * D);
+                qf[ks][0] = row[(16 * ks + 2 * cq) / 2];
+                qf[ks][1] = row[(16 * ks + 8 + 2 * cq) / 2];
+            }
+        }
+#pragma unroll
+        for (int md = 0; md < MD; md++)
+#pragma unroll
+            for (int i = 0; i < 4; i++) oacc[md][i] = 0.0f;
+    } else {
 #pragma unroll
         for (int g = 0; g < GA; g++)
 #pragma unroll
-            for (int e = 0; e < E; e++)
+            for (int e = 0; e < E; e++) {
                 qr[g][e] = (g < G) ? to_f32(qg[g * D + lane * E + e]) * a.att_scale_log2 : 0.0f;
+                acc[g][e] = 0.0f;
+            }
     }
-    float acc[GA][E];
-#pragma unroll
-    for (int g = 0; g < GA; g++)
-#pragma unroll
-        for (int e = 0; e < E; e++) acc[g][e] = 0.0f;
-    float m = -INFINITY, l = 0.0f;  // softmax state of head lane / LPH
 
     const uint8_t *Ku = static_cast<const uint8_t *>(a.K) + (size_t)u * a.cap * RB;
     const uint8_t *Vu = static_cast<const uint8_t *>(a.V) + (size_t)u * a.cap * RB;
     uint8_t *stK = smem, *stV = smem + CH * RB;
+    // this warp's P tile: [16 tokens][8 heads] bf16, hi then lo (after the winner list)
+    uint8_t *sPt = smem + SM::oPl + kMaxSlice * 4 + warp * 512;
     __syncwarp();
     cluster_wait_acquire();  // no CTA reads this one's ring or scores any more (arrived after P5)
     for (int c0 = 0; c0 < total; c0 += CH) {
@@ -293,65 +322,151 @@ __device__ __forceinline__ void attend_tail(const SelArgs &a, uint8_t *smem, con
         for (int pc = tid; pc < ch * PPR; pc += kSelThreads) {
             const int j = pc / PPR, part = pc % PPR;
             const size_t t = (size_t)token(c0 + j);
-            cp_async16(stK + j * RB + part * 16, Ku + t * RB + part * 16);
-            cp_async16(stV + j * RB + part * 16, Vu + t * RB + part * 16);
+            // bf16: chunk `part` of row j at chunk position part ^ (j % 8)
+            const int dpart = TC ? (part ^ (j & 7)) : part;
+            cp_async16(stK + j * RB + dpart * 16, Ku + t * RB + part * 16);
+            cp_async16(stV + j * RB + dpart * 16, Vu + t * RB + part * 16);
         }
         cp_async_commit();
+        if constexpr (TC) {
+            // V rows of the last tile past the chunk: zero (P is 0 there, 0 * NaN is not)
+            const int pad = ((ch + 15) & ~15) - ch;
+            for (int i = tid; i < pad * PPR; i += kSelThreads)
+                *reinterpret_cast<uint4 *>(stV + (ch + i / PPR) * RB + (i % PPR) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+        }
         cp_async_wait<0>();
         __syncthreads();
-        for (int jb = 0; jb < ch; jb += kSelWarps * TPW) {
-            // branch-free over the warp's slots (the shuffle chains interleave);
-            // a slot past the chunk scores -inf and adds nothing
-            float s[TPW];
+        if constexpr (TC) {
+            for (int mt = warp; 16 * mt < ch; mt += kSelWarps) {
+                // scores of tokens 16 mt + gq, + 8 against heads 2cq, 2cq + 1
+                float c4[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c4b[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                const uint8_t *rowp = stK + (16 * mt + lr + ((lm & 1) ? 8 : 0)) * RB;
 #pragma unroll
-            for (int jj = 0; jj < TPW; jj++) {
-                const int j = jb + jj * kSelWarps + warp;
-                const bool live = j < ch;
-                float kv[E];
-                load_lane<E, T>(stK + (live ? j : 0) * RB, lane, kv);
-                float part[GA];
-#pragma unroll
-                for (int g = 0; g < GA; g++) {
-                    float d = 0.0f;
-#pragma unroll
-                    for (int e = 0; e < E; e++) d = fmaf(qr[g][e], kv[e], d);
-                    part[g] = d;
+                for (int ks = 0; ks < KS; ks++) {
+                    const int chk = 2 * ks + ((lm & 2) ? 1 : 0);
+                    uint32_t af[4];
+                    ldsm_x4(af, rowp + ((chk ^ lr) << 4));
+                    mma16816((ks & 1) ? c4b : c4, af, qf[ks][0], qf[ks][1]);
                 }
-                const float sc = reduce_heads<GA>(part, lane);
-                s[jj] = live ? sc : -INFINITY;
+                const int t0 = 16 * mt + gq;
+                float sc[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const bool ok = ((i < 2) ? t0 : t0 + 8) < ch;
+                    sc[i] = ok ? (c4[i] + c4b[i]) * a.att_scale_log2 : -INFINITY;
+                }
+                float ma = fmaxf(sc[0], sc[2]), mb = fmaxf(sc[1], sc[3]);
+                __syncwarp();
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    ma = fmaxf(ma, __shfl_xor_sync(kFull, ma, o));
+                    mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o));
+                }
+                const float na = fmaxf(m2[0], ma), nb = fmaxf(m2[1], mb);
+                const float ala = (m2[0] == -INFINITY) ? 0.0f : exp2f(m2[0] - na);
+                const float alb = (m2[1] == -INFINITY) ? 0.0f : exp2f(m2[1] - nb);
+                float p[4];
+                p[0] = (sc[0] == -INFINITY) ? 0.0f : exp2f(sc[0] - na);
+                p[1] = (sc[1] == -INFINITY) ? 0.0f : exp2f(sc[1] - nb);
+                p[2] = (sc[2] == -INFINITY) ? 0.0f : exp2f(sc[2] - na);
+                p[3] = (sc[3] == -INFINITY) ? 0.0f : exp2f(sc[3] - nb);
+                float la = p[0] + p[2], lb = p[1] + p[3];
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    la += __shfl_xor_sync(kFull, la, o);
+                    lb += __shfl_xor_sync(kFull, lb, o);
+                }
+                l2[0] = l2[0] * ala + la;
+                l2[1] = l2[1] * alb + lb;
+                m2[0] = na;
+                m2[1] = nb;
+#pragma unroll
+                for (int md = 0; md < MD; md++) {
+                    oacc[md][0] *= ala;
+                    oacc[md][1] *= alb;
+                    oacc[md][2] *= ala;
+                    oacc[md][3] *= alb;
+                }
+                // P (hi, lo) as [token][head] rows: the B operand of O^T += V^T P^T
+                uint32_t hi, lo;
+                float r0, r1;
+                split_bf16x2(p[0], p[1], hi, lo, r0, r1);
+                *reinterpret_cast<uint32_t *>(sPt + gq * 16 + 4 * cq) = hi;
+                *reinterpret_cast<uint32_t *>(sPt + 256 + gq * 16 + 4 * cq) = lo;
+                split_bf16x2(p[2], p[3], hi, lo, r0, r1);
+                *reinterpret_cast<uint32_t *>(sPt + (gq + 8) * 16 + 4 * cq) = hi;
+                *reinterpret_cast<uint32_t *>(sPt + 256 + (gq + 8) * 16 + 4 * cq) = lo;
+                __syncwarp();
+                uint32_t bq[4];
+                ldsm_x4_t(bq, sPt + ((lm & 2) ? 256 : 0) + ((lm & 1) * 8 + lr) * 16);
+                // A = V^T tile (16 dims x 16 tokens) from the token rows
+                const uint8_t *vrow = stV + (16 * mt + lr + ((lm & 2) ? 8 : 0)) * RB;
+#pragma unroll
+                for (int md = 0; md < MD; md++) {
+                    const int chk = 2 * md + (lm & 1);
+                    uint32_t af[4];
+                    ldsm_x4_t(af, vrow + ((chk ^ lr) << 4));
+                    mma16816(oacc[md], af, bq[0], bq[1]);
+                    mma16816(oacc[md], af, bq[2], bq[3]);
+                }
+                __syncwarp();  // the P tile is rewritten by the warp's next tile
             }
-            float mb = -INFINITY;
+        } else {
+            for (int jb = 0; jb < ch; jb += kSelWarps * TPW) {
+                // branch-free over the warp's slots (the shuffle chains interleave);
+                // a slot past the chunk scores -inf and adds nothing
+                float s[TPW];
 #pragma unroll
-            for (int jj = 0; jj < TPW; jj++) mb = fmaxf(mb, s[jj]);
-            const float m_new = fmaxf(m, mb);
-            const float alpha = (m == -INFINITY) ? 0.0f : exp2f(m - m_new);
-            float p[TPW], ps = 0.0f;
+                for (int jj = 0; jj < TPW; jj++) {
+                    const int j = jb + jj * kSelWarps + warp;
+                    const bool live = j < ch;
+                    float kv[E];
+                    load_lane<E, T>(stK + (live ? j : 0) * RB, lane, kv);
+                    float part[GA];
 #pragma unroll
-            for (int jj = 0; jj < TPW; jj++) {
-                p[jj] = (s[jj] == -INFINITY) ? 0.0f : exp2f(s[jj] - m_new);
-                ps += p[jj];
-            }
-            l = l * alpha + ps;
-            m = m_new;
+                    for (int g = 0; g < GA; g++) {
+                        float d = 0.0f;
 #pragma unroll
-            for (int g = 0; g < GA; g++) {
-                const float ag = __shfl_sync(kFull, alpha, g * LPH);
+                        for (int e = 0; e < E; e++) d = fmaf(qr[g][e], kv[e], d);
+                        part[g] = d;
+                    }
+                    const float sc = reduce_heads<GA>(part, lane);
+                    s[jj] = live ? sc : -INFINITY;
+                }
+                float mb = -INFINITY;
 #pragma unroll
-                for (int e = 0; e < E; e++) acc[g][e] *= ag;
-            }
+                for (int jj = 0; jj < TPW; jj++) mb = fmaxf(mb, s[jj]);
+                const float m_new = fmaxf(m, mb);
+                const float alpha = (m == -INFINITY) ? 0.0f : exp2f(m - m_new);
+                float p[TPW], ps = 0.0f;
 #pragma unroll
-            for (int jj = 0; jj < TPW; jj++) {
-                const int j = jb + jj * kSelWarps + warp;
-                const bool live = j < ch;
-                float vv[E];
-                load_lane<E, T>(stV + (live ? j : 0) * RB, lane, vv);
-#pragma unroll
-                for (int e = 0; e < E; e++) vv[e] = live ? vv[e] : 0.0f;
+                for (int jj = 0; jj < TPW; jj++) {
+                    p[jj] = (s[jj] == -INFINITY) ? 0.0f : exp2f(s[jj] - m_new);
+                    ps += p[jj];
+                }
+                l = l * alpha + ps;
+                m = m_new;
 #pragma unroll
                 for (int g = 0; g < GA; g++) {
-                    const float pg = __shfl_sync(kFull, p[jj], g * LPH);
+                    const float ag = __shfl_sync(kFull, alpha, g * LPH);
 #pragma unroll
-                    for (int e = 0; e < E; e++) acc[g][e] = fmaf(pg, vv[e], acc[g][e]);
+                    for (int e = 0; e < E; e++) acc[g][e] *= ag;
+                }
+#pragma unroll
+                for (int jj = 0; jj < TPW; jj++) {
+                    const int j = jb + jj * kSelWarps + warp;
+                    const bool live = j < ch;
+                    float vv[E];
+                    load_lane<E, T>(stV + (live ? j : 0) * RB, lane, vv);
+#pragma unroll
+                    for (int e = 0; e < E; e++) vv[e] = live ? vv[e] : 0.0f;
+#pragma unroll
+                    for (int g = 0; g < GA; g++) {
+                        const float pg = __shfl_sync(kFull, p[jj], g * LPH);
+#pragma unroll
+                        for (int e = 0; e < E; e++) acc[g][e] = fmaf(pg, vv[e], acc[g][e]);
+                    }
                 }
             }
         }
@@ -362,14 +477,32 @@ __device__ __forceinline__ void attend_tail(const SelArgs &a, uint8_t *smem, con
     float *sWm = reinterpret_cast<float *>(smem);  // [warps][GA]
     float *sWl = sWm + kSelWarps * GA;             // [warps][GA]
     float *sWo = sWl + kSelWarps * GA;             // [warps][GA][D]
-    if ((lane % LPH) == 0) {
-        sWm[warp * GA + lane / LPH] = m;
-        sWl[warp * GA + lane / LPH] = l;
+    if constexpr (TC) {
+#pragma unroll
+        for (int e = 0; e < 2; e++) {
+            const int hh = 2 * cq + e;
+            if (hh < GA) {
+                if (gq == 0) {
+                    sWm[warp * GA + hh] = m2[e];
+                    sWl[warp * GA + hh] = l2[e];
+                }
+#pragma unroll
+                for (int md = 0; md < MD; md++) {
+                    sWo[(warp * GA + hh) * D + 16 * md + gq] = oacc[md][e];
+                    sWo[(warp * GA + hh) * D + 16 * md + gq + 8] = oacc[md][2 + e];
+                }
+            }
+        }
+    } else {
+        if ((lane % LPH) == 0) {
+            sWm[warp * GA + lane / LPH] = m;
+            sWl[warp * GA + lane / LPH] = l;
+        }
+#pragma unroll
+        for (int g = 0; g < GA; g++)
+#pragma unroll
+            for (int e = 0; e < E; e++) sWo[(warp * GA + g) * D + lane * E + e] = acc[g][e];
     }
-#pragma unroll
-    for (int g = 0; g < GA; g++)
-#pragma unroll
-        for (int e = 0; e < E; e++) sWo[(warp * GA + g) * D + lane * E + e] = acc[g][e];
     __syncthreads();
     for (int t = tid; t < G * D; t += kSelThreads) {
         const int g = t / D, dim = t % D;
@@ -399,11 +532,11 @@ __device__ __forceinline__ void attend_tail(const SelArgs &a, uint8_t *smem, con
     const int e0 = rank * (G * D) / CS, e1 = (rank + 1) * (G * D) / CS;
     for (int t = e0 + tid; t < e1; t += kSelThreads) {
         const int g = t / D, dim = t % D;
-        float mr[16], lr[16], orr[16];
+        float mr[16], lr2[16], orr[16];
 #pragma unroll
         for (int r = 0; r < 16; r++) {
             mr[r] = (r < CS) ? *cluster.map_shared_rank(&sPm[g], r) : -INFINITY;
-            lr[r] = (r < CS) ? *cluster.map_shared_rank(&sPl[g], r) : 0.0f;
+            lr2[r] = (r < CS) ? *cluster.map_shared_rank(&sPl[g], r) : 0.0f;
             orr[r] = (r < CS) ? *cluster.map_shared_rank(&sPo[t], r) : 0.0f;
         }
         float M = -INFINITY;
@@ -415,7 +548,7 @@ __device__ __forceinline__ void attend_tail(const SelArgs &a, uint8_t *smem, con
             for (int r = 0; r < 16; r++) {
                 if (mr[r] == -INFINITY) continue;
                 const float f = exp2f(mr[r] - M);
-                L = fmaf(lr[r], f, L);
+                L = fmaf(lr2[r], f, L);
                 O = fmaf(orr[r], f, O);
             }
         }

@@ -271,36 +271,6 @@ struct TieredArgs {
     int withhold_last; // test hook: each CTA never issues its last copy (its wait runs out)
 };
 
-// ---- warp-level tensor-core helpers: mma.sync m16n8k16, bf16 in, fp32 accumulate.
-// Fragment layouts (g = lane / 4, c = lane % 4): A (16x16, row-major) holds
-// (g, 2c..2c+1), (g+8, 2c..), (g, 2c+8..), (g+8, 2c+8..); B (16x8, k-major
-// columns) holds (k = 2c..2c+1, n = g), (k = 2c+8.., n = g); C (16x8) holds
-// (g, 2c..2c+1), (g+8, 2c..2c+1).
-
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(smem_u32(p)));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *p)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(smem_u32(p)));
-}
-
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};\n"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 // Two 2-bit codes at bits 0-1 and 16-17 of t (the other bits ignored) as the
 // bf16 pair (128 + c0, 128 + c1): 128 is 0x4300 in bf16 and its mantissa step
 // is 1, so OR-ing a code into the low bits is exact (one LOP3). A product
@@ -309,21 +279,6 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
 __device__ __forceinline__ uint32_t codes_off128(uint32_t t)
 {
     return (t & 0x00030003u) | 0x43004300u;
-}
-
-// (x0, x1) ~ hi + lo, hi = bf16(x), lo = bf16(x - hi), as bf16x2 words (x0 in
-// the low half): about 16 bits of each value kept; r0, r1 are the values the
-// tensor core sees (hi + lo).
-__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, uint32_t &lo,
-                                             float &r0, float &r1)
-{
-    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-    hi = *reinterpret_cast<const uint32_t *>(&h);
-    const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - h0, x1 - h1);
-    lo = *reinterpret_cast<const uint32_t *>(&l);
-    r0 = h0 + __uint_as_float(lo << 16);
-    r1 = h1 + __uint_as_float(lo & 0xffff0000u);
 }
 
 // 2-D tensor-map copy of one box into shared memory, completing on `bar`
