@@ -106,6 +106,44 @@ int sm_count()
     return count[dev];
 }
 
+int max_active_clusters(const void *kernel, int cluster, int threads, int smem_bytes)
+{
+    static std::mutex mu;
+    struct Entry {
+        const void *kernel;
+        int cluster, threads, smem, count;
+    };
+    static Entry table[kMaxDevices][128];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    int slot = -1;
+    for (int i = 0; i < 128; i++) {
+        const Entry &e = table[dev][i];
+        if (e.kernel == kernel && e.cluster == cluster && e.threads == threads && e.smem == smem_bytes)
+            return e.count;
+        if (!e.kernel && slot < 0) slot = i;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cluster, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();  // a refused query is an answer of none, not a sticky error
+        n = 0;
+    }
+    if (slot >= 0) table[dev][slot] = Entry{kernel, cluster, threads, smem_bytes, n};
+    return n;
+}
+
 kvr_status raise_smem_limit(const void *kernel, int bytes)
 {
     return raise_in(g_plain, kernel, bytes, false);

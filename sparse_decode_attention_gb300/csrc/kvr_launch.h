@@ -33,6 +33,11 @@ kvr_status prepare_cluster_kernel(const void *kernel, int smem_bytes);
 // 152 on GB300 if the query fails), for grid sizing.
 int sm_count();
 
+// Clusters of `cluster` CTAs of `kernel` (`threads` threads, `smem_bytes` of
+// dynamic shared memory, limits already raised) resident on the current
+// device at once; 0 if the query fails. Cached per device.
+int max_active_clusters(const void *kernel, int cluster, int threads, int smem_bytes);
+
 // Bytes of the bit-plane code buffer of one unit: ceil(cap/1024) tiles of d*128 bytes.
 inline size_t codes_bytes_per_unit(int64_t cap, int d) { return (size_t)((cap + 1023) / 1024) * d * 128; }
 

@@ -1593,11 +1593,37 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
 // KVR_SELECT_ATT_TU defined (the GA = 4 kernels: selection + attention), so
 // the three sets of instantiations build in parallel.
 
+// Long contexts: the scan and the rescoring dominate, and a CTA that shares
+// its SM with another runs them at about half speed while every cluster
+// barrier waits for it (two CTAs of this kernel fit an SM, and 16-CTA
+// clusters cannot all take SMs of their own). There, the largest cluster
+// size (16 down to 8, even, at least C / kMaxSlice) whose U clusters can all
+// be resident at one CTA per SM is used, the shared memory padded past half
+// an SM. Measured on the Llama-3-8B-shaped layer (8 units): 12 CTAs per unit
+// on SMs of their own took the million-token step from 116.6 to 109.1 us;
+// at 128K (16 half-tiles per CTA) the same took it from 39.8 to 41.7 us, so
+// the spread form starts at kSpreadCap tokens of capacity.
+constexpr int64_t kSpreadCap = 1 << 19;
+constexpr int kSpreadSmem = 120 * 1024;
+
 template <int D, typename T, int VB, bool EXT, int GA>
 static kvr_status launch_select_t(const LaunchCtx &c, const SelArgs &a, int cs)
 {
     auto kern = select_kernel<D, T, VB, EXT, GA>;
-    const int smem = SelSmem<D, T>::bytes;
+    int smem = SelSmem<D, T>::bytes;
+    static_assert(SelSmem<D, T>::bytes <= kSpreadSmem, "the padded form holds the layout");
+    if (c.shape.cap >= kSpreadCap) {
+        const int U = c.shape.B * c.shape.Hkv;
+        const int cmin = (a.C + kMaxSlice - 1) / kMaxSlice;
+        if (prepare_cluster_kernel(reinterpret_cast<const void *>(kern), kSpreadSmem) == KVR_OK)
+            for (int cs1 = 16; cs1 >= 8 && cs1 >= cmin; cs1 -= 2)
+                if (max_active_clusters(reinterpret_cast<const void *>(kern), cs1, kSelThreads,
+                                        kSpreadSmem) >= U) {
+                    cs = cs1;
+                    smem = kSpreadSmem;
+                    break;
+                }
+    }
     kvr_status st = prepare_cluster_kernel(reinterpret_cast<const void *>(kern), smem);
     if (st != KVR_OK) return st;
     cudaLaunchConfig_t cfg = {};

@@ -134,6 +134,17 @@ def test_rsq_select_fp32_d64():
     assert res["err"] == 0
 
 
+def test_rsq_select_long_ranges():
+    """Past 256K tokens (score planes mostly in global memory; the
+    optional-mode kernel set): estimates and top-k sets of two units of a
+    ragged batch against the oracle."""
+    seq = [300000, 270000]
+    K, V, q = lowrank_case(2, 8, 2, 128, 300000, seq, seed=63)
+    res, *_ = run_rsq(K, q, seq, 2048, 512, 128, wl.DEFAULT_LUT, wl.srht_signs(128),
+                      units=[0, 3])
+    assert res["err"] == 0
+
+
 @pytest.mark.parametrize("C,k,W,seq", [
     (64, 16, 200, [150]),       # window covers the whole context: nothing selected
     (64, 16, 200, [201]),       # pool of one token

@@ -8,8 +8,8 @@ default and narrower vote tables) and the two-level one (the linear table),
 candidates rescored by the CTA that found them and, when one CTA finds more
 than its share allows, by equal slices; ragged batches, GQA groups of 1, 2
 and 4 (one launch) and 8 (two launches), cache regions, the edge cases of the
-selection, and the 128K and million-token layers at full size on sampled
-units.
+selection, contexts past 256K tokens on every unit, and the 128K and
+million-token layers at full size on sampled units.
 """
 import math
 
@@ -242,6 +242,30 @@ def test_select_attend_equals_the_two_calls(mode):
     assert bits == 0
     assert np.array_equal(i1.cpu().numpy(), i2) and np.array_equal(c1.cpu().numpy(), c2)
     assert np.abs(o1.cpu().numpy() - o2).max() <= 1e-5
+
+
+def test_select_attend_long_ranges_every_unit():
+    """Contexts past 256K tokens: every CTA scans 32 or more half-tiles and
+    keeps most of its score planes in global memory (past the 512 blocks it
+    holds on chip); a capacity past 512K tokens also puts the 8 units'
+    clusters on SMs of their own (12 CTAs each on a GB300). Every unit of a
+    ragged batch of 8 against the oracle, and kvr_select's index sets equal
+    to the one-launch call's."""
+    seq = [300000, 280000]
+    K, V, q = lowrank_case(2, 16, 4, 128, 560000, seq, seed=77)
+    params = kvr.SelectParams(4096, 1024, 128)
+    sgn = wl.srht_signs(128)
+    idx, cnt, _ = check_against_oracle(K, V, q, seq, params, sgn, codes_check=False)
+    Kd, qd, sgn_d = K.to(DEV), q.to(DEV), sgn.to(DEV)
+    codes = encode_gpu(Kd, sgn_d, 560000)
+    seq_d = torch.tensor(seq, dtype=torch.int32, device=DEV)
+    ws = kvr.workspace(kvr.kvr_select_workspace_size(kvr.Shape.of(Kd, qd), params))
+    idx2 = torch.full((2, 4, 1024), 7, dtype=torch.int32, device=DEV)
+    cnt2 = torch.zeros((2, 4), dtype=torch.int32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kvr.kvr_select(qd, Kd, codes, seq_d, sgn_d, params, idx2, cnt2, ws, err)
+    assert kvr.kvr_read_error(err) == 0
+    assert np.array_equal(idx2.cpu().numpy(), idx) and np.array_equal(cnt2.cpu().numpy(), cnt)
 
 
 def test_select_attend_128k_full_size_chain():
