@@ -49,14 +49,16 @@ def peaks():
 
 def measured_traffic(kernel, workload):
     """DRAM bytes per launch of `kernel` on `workload` from the ncu capture
-    recorded in profiles/traffic.json, or None when that kernel was captured
-    on another workload or its sources have changed since the capture (the
-    counters then describe another launch)."""
+    recorded in profiles/traffic.json (under "kernel/workload", or under
+    "kernel" when captured on that workload), or None when there is no
+    capture of that kernel on that workload or its sources have changed
+    since the capture (the counters then describe another launch)."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            rec = json.load(f)[kernel]
-        if rec["workload"] != workload:
+            table = json.load(f)
+        rec = table.get(kernel + "/" + workload, table.get(kernel))
+        if rec is None or rec["workload"] != workload:
             return None
         m = hashlib.sha256()
         for name in rec["sources"]:

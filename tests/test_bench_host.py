@@ -73,14 +73,18 @@ def test_recorded_traffic_is_attached_only_to_its_capture(tmp_path, monkeypatch)
     digest = hashlib.sha256(b"kernel a\nheader\n").hexdigest()
     (tmp_path / "profiles").mkdir()
     rec = {"k": {"dram_bytes_per_launch": 1234, "sources": ["a.cu", "b.h"],
-                 "workload": "w128", "sources_sha256": digest}}
+                 "workload": "w128", "sources_sha256": digest},
+           "k/w1m": {"dram_bytes_per_launch": 5678, "sources": ["a.cu", "b.h"],
+                     "workload": "w1m", "sources_sha256": digest}}
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.measured_traffic("k", "w128") == 1234
-    assert bench.measured_traffic("k", "w1m") is None       # another workload
+    assert bench.measured_traffic("k", "w1m") == 5678       # its own capture
+    assert bench.measured_traffic("k", "w32k") is None      # another workload
     assert bench.measured_traffic("k_mag", "w128") is None  # another kernel variant
     (csrc / "a.cu").write_text("kernel a, changed\n")
     assert bench.measured_traffic("k", "w128") is None      # sources changed since
+    assert bench.measured_traffic("k", "w1m") is None
 
 
 def _gloo_rank(rank, port, q):
