@@ -30,9 +30,9 @@
 //      (half-warp per row).
 //   P5 the k'-th largest exact score (order-preserving uint32 keys) in three
 //      small cluster exchanges: the score range, a 256-bin linear histogram
-//      of every CTA's slice over that range, then the keys of the one
-//      boundary bin, located in one of 256 sub-bins of that bin and ranked
-//      there by counting (a few keys: directly); a boundary bin
+//      of every CTA's slice over that range (16 bits per bin), then the keys
+//      of the one boundary bin, located in one of 256 sub-bins of that bin
+//      and ranked there by counting (a few keys: directly); a boundary bin
 //      too large to gather (massive ties) falls back to every CTA gathering
 //      all C' keys. Each CTA also gets its output offset.
 //   P6 winners are written ascending by index.
@@ -896,8 +896,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
             // highest bucket whose suffix count reaches C'
             int tot = 0;
             if (lane < NL1)
-#pragma unroll 1
-                for (int r = 0; r < CS; r++) tot += sAll[r * 16 + lane];
+#pragma unroll
+                for (int r = 0; r < 16; r++) tot += (r < CS) ? sAll[r * 16 + lane] : 0;
             const int suf = warp_suffix_sum(tot);
             int u1 = -1, rem = Cp;
             if (Cp > 0) {
@@ -950,8 +950,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
                 const int rem = sMisc[M_REM1];
                 int tot = 0;
                 if (lane < NL2)
-#pragma unroll 1
-                    for (int r = 0; r < CS; r++) tot += sAll[256 + r * 16 + lane];
+#pragma unroll
+                    for (int r = 0; r < 16; r++) tot += (r < CS) ? sAll[256 + r * 16 + lane] : 0;
                 const int suf = warp_suffix_sum(tot);
                 const unsigned ok = __ballot_sync(kFull, lane < NL2 && suf >= rem);
                 const int v2 = __popc(ok) - 1;
@@ -1326,19 +1326,31 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         const int x = (int)lin_pos(key);
         return min(255, max(0, x));
     };
-    // (2) this slice's linear histogram
+    // (2) this slice's linear histogram, two 16-bit bins per word (a slice
+    // holds at most 2048 keys): reading every slice's histogram is bound by
+    // the bytes moved between the CTAs, so they move half as many
+    uint32_t *sHist = reinterpret_cast<uint32_t *>(sRad);
     if (kp > 0)
 #pragma unroll 1
-        for (int j = tid; j < n; j += kSelThreads) atomicAdd(&sRad[lin_bin(order_key(sS[j]))], 1);
+        for (int j = tid; j < n; j += kSelThreads) {
+            const int bn = lin_bin(order_key(sS[j]));
+            atomicAdd(&sHist[bn >> 1], 1u << ((bn & 1) * 16));
+        }
     __syncthreads();
     cluster.sync();  // #5: slice histograms published
     int b_lin = 0, rem = 0;
-    if (kp > 0) {
-        int col = 0;
+    if (kp > 0 && tid < 128) {
+        uint32_t w[16];
 #pragma unroll
-        for (int r = 0; r < 16; r++)
-            if (r < CS) col += *cluster.map_shared_rank(&sRad[tid], r);
-        sRad[256 + tid] = col;
+        for (int r = 0; r < 16; r++) w[r] = (r < CS) ? *cluster.map_shared_rank(&sHist[tid], r) : 0u;
+        int lo16 = 0, hi16 = 0;
+#pragma unroll
+        for (int r = 0; r < 16; r++) {
+            lo16 += (int)(w[r] & 0xffffu);
+            hi16 += (int)(w[r] >> 16);
+        }
+        sRad[256 + 2 * tid] = lo16;
+        sRad[256 + 2 * tid + 1] = hi16;
     }
     if (tid == 0) sMisc[M_CNT] = 0;
     __syncthreads();
