@@ -256,7 +256,7 @@ __device__ __forceinline__ void attend_tail(const SelArgs &a, uint8_t *smem, con
     constexpr int CH = SM::kStage / (2 * RB);  // tokens staged at once
     constexpr int TPW = 4;                     // CUDA-core path: tokens per warp per round
     static_assert(CH >= kSelWarps * TPW && CH % 16 == 0, "a round fits the stage");
-    static_assert(kSelWarps * GA * (D + 2) * 4 <= SM::kStage, "warp partials fit the stage");
+    static_assert(kSelWarps * GA * (D + 3) * 4 <= SM::kStage, "warp partials fit the stage");
     static_assert(kMaxSlice * 4 + kSelWarps * 512 <= 8 * kPlaneCap * 4, "P tiles fit the plane area");
     cg::cluster_group cluster = cg::this_cluster();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -508,23 +508,30 @@ __device__ __forceinline__ void attend_tail(const SelArgs &a, uint8_t *smem, con
             for (int e = 0; e < E; e++) sWo[(warp * GA + g) * D + lane * E + e] = acc[g][e];
     }
     __syncthreads();
+    // every warp's weight per head, 2^(m_w - M) against the heads' maximum
+    // (0 for a warp without tokens: its partial is zero), once per (warp,
+    // head); then every output an fma chain over the warps in order
+    float *sWf = sWo + kSelWarps * GA * D;  // [warps][GA]
+    if (tid < kSelWarps * GA) {
+        const int g = tid % GA;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kSelWarps; w++) M = fmaxf(M, sWm[w * GA + g]);
+        const float mw = sWm[tid];
+        sWf[tid] = (mw == -INFINITY) ? 0.0f : exp2f(mw - M);
+        if (tid < GA) sPm[g] = M;
+    }
+    __syncthreads();
     for (int t = tid; t < G * D; t += kSelThreads) {
         const int g = t / D, dim = t % D;
-        float M = -INFINITY;
-        for (int w = 0; w < kSelWarps; w++) M = fmaxf(M, sWm[w * GA + g]);
-        float L = 0.0f, O = 0.0f;
-        if (M != -INFINITY) {
-            for (int w = 0; w < kSelWarps; w++) {
-                const float mw = sWm[w * GA + g];
-                if (mw == -INFINITY) continue;
-                const float f = exp2f(mw - M);
-                L = fmaf(sWl[w * GA + g], f, L);
-                O = fmaf(sWo[(w * GA + g) * D + dim], f, O);
-            }
-        }
+        float O = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kSelWarps; w++) O = fmaf(sWo[(w * GA + g) * D + dim], sWf[w * GA + g], O);
         sPo[t] = O;
         if (dim == 0) {
-            sPm[g] = M;
+            float L = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kSelWarps; w++) L = fmaf(sWl[w * GA + g], sWf[w * GA + g], L);
             sPl[g] = L;
         }
     }
@@ -1482,30 +1489,48 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
             __syncthreads();
             keyT = (uint32_t)sMisc[M_KEYT];
             const int quota = sMisc[M_QUOTA];
-            // ties at keyT go to the lowest indices: boundary keys of earlier slices
-            int gt_b = 0, eq_b = 0, eq_m = 0;
-#pragma unroll 1
-            for (int t = tid; t < NB; t += kSelThreads) {
-                const int r2 = seg_owner(t);
-                const uint32_t k = sB[t];
-                if (r2 < rank) {
-                    gt_b += k > keyT;
-                    eq_b += k == keyT;
-                } else if (r2 == rank) {
-                    eq_m += k == keyT;
+            // ties at keyT go to the lowest indices: boundary keys of earlier
+            // slices (up to 256 keys: one per thread, counted by the barrier)
+            int gt_before, eq_before, eq_mine;
+            if (NB <= kSelThreads) {
+                bool gtb = false, eqb = false, eqm = false;
+                if (tid < NB) {
+                    const int r2 = seg_owner(tid);
+                    const uint32_t k = sB[tid];
+                    gtb = r2 < rank && k > keyT;
+                    eqb = r2 < rank && k == keyT;
+                    eqm = r2 == rank && k == keyT;
                 }
+                gt_before = __syncthreads_count(gtb);
+                eq_before = __syncthreads_count(eqb);
+                eq_mine = __syncthreads_count(eqm);
+            } else {
+                int gt_b = 0, eq_b = 0, eq_m = 0;
+#pragma unroll 1
+                for (int t = tid; t < NB; t += kSelThreads) {
+                    const int r2 = seg_owner(t);
+                    const uint32_t k = sB[t];
+                    if (r2 < rank) {
+                        gt_b += k > keyT;
+                        eq_b += k == keyT;
+                    } else if (r2 == rank) {
+                        eq_m += k == keyT;
+                    }
+                }
+                gt_b = warp_sum(gt_b);
+                eq_b = warp_sum(eq_b);
+                eq_m = warp_sum(eq_m);
+                if (lane == 0) {
+                    if (gt_b) atomicAdd(&sScan[0], gt_b);
+                    if (eq_b) atomicAdd(&sScan[1], eq_b);
+                    if (eq_m) atomicAdd(&sScan[2], eq_m);
+                }
+                __syncthreads();
+                gt_before = sScan[0];
+                eq_before = sScan[1];
+                eq_mine = sScan[2];
             }
-            gt_b = warp_sum(gt_b);
-            eq_b = warp_sum(eq_b);
-            eq_m = warp_sum(eq_m);
-            if (lane == 0) {
-                if (gt_b) atomicAdd(&sScan[0], gt_b);
-                if (eq_b) atomicAdd(&sScan[1], eq_b);
-                if (eq_m) atomicAdd(&sScan[2], eq_m);
-            }
-            __syncthreads();
             if (tid == 0) {
-                const int gt_before = sScan[0], eq_before = sScan[1], eq_mine = sScan[2];
                 sMisc[M_KTAKE] = max(0, min(quota - eq_before, eq_mine));
                 sMisc[M_KOFF] = sMisc[M_ABOVEB] + gt_before + min(eq_before, quota);
             }
