@@ -222,7 +222,7 @@ enum {
     M_U1 = 0, M_REM1, M_T, M_TAKE, M_OFF, M_KTAKE, M_KOFF, M_NSUB, M_KEYT, M_QUOTA,
     M_CNT, M_ABOVEB, M_LOCAL, M_NW,
     M_BOUND = 16,  // [17] first candidate position of each CTA's P4 slice, then C'
-    M_KMIN = 33, M_KMAX, M_GMIN, M_GMAX, M_AOWN,
+    M_KMIN = 33, M_KMAX, M_AOWN,
     M_SEG = 40,    // [17] first boundary-key position of each CTA, then the total
 };
 
@@ -943,14 +943,14 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
             if ((lane % (32 / NL2)) == 0 && s) atomicAdd(&sH2[lane / (32 / NL2)], s);
         }
         __syncthreads();
-        cluster.sync();  // #2: level-2 histograms published
-
+        // pushed into row `rank` of every CTA's table: a remote store ahead of
+        // the barrier costs no round trip after it
 #pragma unroll 1
         for (int t = tid; t < CS * NL2; t += kSelThreads) {
             const int r = t / NL2, v = t % NL2;
-            sAll[256 + r * 16 + v] = *cluster.map_shared_rank(&sH2[v], r);
+            *cluster.map_shared_rank(&sAll[256 + rank * 16 + v], r) = sH2[v];
         }
-        __syncthreads();
+        cluster.sync();  // #2: level-2 histograms published
         if (warp == 0) {
             int Tthr = 1 << 30, quota = 0, gt = 0, eq = 0;
             if (u1 >= 0) {
@@ -1305,25 +1305,20 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
             atomicMax(reinterpret_cast<unsigned *>(&sMisc[M_KMAX]), lmax);
         }
     }
-    __syncthreads();
-    cluster.sync();  // #4: slice ranges published
-    if (warp == 0) {
-        uint32_t g0 = 0xffffffffu, g1 = 0u;
-        if (lane < CS) {
-            g0 = (uint32_t)*cluster.map_shared_rank(&sMisc[M_KMIN], lane);
-            g1 = (uint32_t)*cluster.map_shared_rank(&sMisc[M_KMAX], lane);
-        }
-        g0 = __reduce_min_sync(kFull, g0);
-        g1 = __reduce_max_sync(kFull, g1);
-        if (lane == 0) {
-            sMisc[M_GMIN] = (int)g0;
-            sMisc[M_GMAX] = (int)g1;
-        }
-    }
     sRad[tid] = 0;
     __syncthreads();
-    const float fmin = key_float((uint32_t)sMisc[M_GMIN]);
-    float scale = 256.0f / (key_float((uint32_t)sMisc[M_GMAX]) - fmin);
+    // pushed into slot `rank` of every CTA (the first-level histogram slots,
+    // free since barrier #2): min in sH1, max in sH2
+    if (tid < CS) {
+        *cluster.map_shared_rank(&sH1[rank], tid) = sMisc[M_KMIN];
+        *cluster.map_shared_rank(&sH2[rank], tid) = sMisc[M_KMAX];
+    }
+    cluster.sync();  // #4: slice ranges published
+    // every warp reduces the ranges itself (empty slices: ~0 / 0)
+    const uint32_t g0 = __reduce_min_sync(kFull, lane < CS ? (uint32_t)sH1[lane] : 0xffffffffu);
+    const uint32_t g1 = __reduce_max_sync(kFull, lane < CS ? (uint32_t)sH2[lane] : 0u);
+    const float fmin = key_float(g0);
+    float scale = 256.0f / (key_float(g1) - fmin);
     if (!(scale < INFINITY) || !(scale > 0.0f)) scale = 0.0f;  // one value, or no spread
     // the position of a key in the linear bin map, in bin units; the bin is
     // its integer part (clamped), a sub-bin of it 1/256 of that unit
@@ -1381,6 +1376,12 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         if (lane == 0 && s) atomicAdd(&sMisc[M_AOWN], s);  // slot cleared before P4
     }
     __syncthreads();
+    // the counts pushed into slot `rank` of every CTA (the first rows of the
+    // P2 table, free since P2)
+    if (tid < CS) {
+        *cluster.map_shared_rank(&sAll[rank], tid) = sMisc[M_AOWN];
+        *cluster.map_shared_rank(&sAll[16 + rank], tid) = sMisc[M_CNT];
+    }
     cluster.sync();  // #6: above counts and boundary keys published
 
     uint32_t keyT = 0;
@@ -1389,8 +1390,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         if (warp == 0) {
             int ab = 0, nb = 0;
             if (lane < CS) {
-                ab = *cluster.map_shared_rank(&sMisc[M_AOWN], lane);
-                nb = *cluster.map_shared_rank(&sMisc[M_CNT], lane);
+                ab = sAll[lane];
+                nb = sAll[16 + lane];
             }
             const int ab_before = warp_exclusive_scan(ab);
             const int nb_before = warp_exclusive_scan(nb);
