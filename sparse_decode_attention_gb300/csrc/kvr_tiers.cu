@@ -867,6 +867,10 @@ template <int D, int G>
 __global__ void __launch_bounds__(kThreads) tiered_combine_kernel(TieredArgs a, float *out,
                                                                   float *mass)
 {
+    // the partials' (m, l) are read into shared memory by all threads at
+    // once (a chain of dependent global loads per head was the kernel's
+    // length), then the weights 2^(m - M) are kept there for the outputs
+    extern __shared__ float sDyn[];  // [S][G] m, then weights; [S][G] l
     __shared__ float sM[16], sL[16];
     const int u = blockIdx.x, b = u / a.Hkv, h = u % a.Hkv, tid = threadIdx.x;
     int64_t N = a.seq_len[b];
@@ -874,33 +878,45 @@ __global__ void __launch_bounds__(kThreads) tiered_combine_kernel(TieredArgs a, 
     const int64_t nw = (N + kWin - 1) / kWin;
     const float *part = a.part + (size_t)u * a.S * (2 * G + G * D);
     constexpr int PS = 2 * G + G * D;
+    float *sF = sDyn, *sLp = sDyn + a.S * G;
+    for (int i = tid; i < a.S * G; i += kThreads) {
+        const int x = i / G, g = i - x * G;
+        sF[i] = part[x * PS + g];
+        sLp[i] = part[x * PS + G + g];
+    }
+    __syncthreads();
     if (tid < G) {
         float M = -CUDART_INF_F;
-        for (int x = 0; x < a.S; x++) M = fmaxf(M, part[x * PS + tid]);
+        for (int x = 0; x < a.S; x++) M = fmaxf(M, sF[x * G + tid]);
         float L = 0.0f;
         if (M != -CUDART_INF_F)
             for (int x = 0; x < a.S; x++) {
-                const float m = part[x * PS + tid];
-                if (m != -CUDART_INF_F) L += part[x * PS + G + tid] * exp2f(m - M);
+                const float m = sF[x * G + tid];
+                if (m != -CUDART_INF_F) L += sLp[x * G + tid] * exp2f(m - M);
             }
         sM[tid] = M;
         sL[tid] = L;
     }
     __syncthreads();
+    // weights (0 for a split without tokens: its partial output is zero)
+    for (int i = tid; i < a.S * G; i += kThreads) {
+        const float m = sF[i];
+        sF[i] = (m == -CUDART_INF_F) ? 0.0f : exp2f(m - sM[i % G]);
+    }
+    __syncthreads();
     for (int i = tid; i < G * D; i += kThreads) {
         const int g = i / D;
-        const float M = sM[g], L = sL[g];
+        const float L = sL[g];
         float o = 0.0f;
         if (L > 0.0f) {
-            for (int x = 0; x < a.S; x++) {
-                const float m = part[x * PS + g];
-                if (m != -CUDART_INF_F) o += part[x * PS + 2 * G + i] * exp2f(m - M);
-            }
+#pragma unroll 4
+            for (int x = 0; x < a.S; x++) o += part[x * PS + 2 * G + i] * sF[x * G + g];
             o /= L;
         }
         out[((size_t)b * a.Hkv * G + (size_t)h * G) * D + i] = o;
     }
     const size_t uw = (size_t)u * a.n_win;
+#pragma unroll 4
     for (int64_t w = tid; w < a.n_win; w += kThreads) {
         float m = 0.0f;
         if (w < nw) {
@@ -994,7 +1010,10 @@ __global__ void __launch_bounds__(kRankThreads) tier_rank_kernel(RankArgs r)
         win[i] = INT32_MAX;
     }
     __syncthreads();
-    // bitonic sort of [0, P) into rank order
+    // bitonic sort of [0, P) into rank order; the pair (i, i ^ j) goes to
+    // the thread of the lower index, so while consecutive stages have j < 32
+    // every element a stage reads was written in the same warp: those stages
+    // are separated by a warp barrier only
     for (int k = 2; k <= P; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
             for (int i = tid; i < P; i += kRankThreads) {
@@ -1012,9 +1031,13 @@ __global__ void __launch_bounds__(kRankThreads) tier_rank_kernel(RankArgs r)
                     }
                 }
             }
-            __syncthreads();
+            // the next stage: (k, j / 2), or (2k, k) when j == 1
+            const int jn = (j > 1) ? (j >> 1) : k;
+            if (j < 32 && jn < 32) __syncwarp();
+            else __syncthreads();
         }
     }
+    __syncthreads();
     // 3. new tiers and 4. moves
     const int64_t quota = a.quota[u], budget = a.budget[u];
     const int64_t BFB = (int64_t)kWin * 4 * a.d, LBB = ledger_bytes_of(a.d);
@@ -1180,7 +1203,10 @@ static kvr_status tiered_launch(const LaunchCtx &c, TieredArgs a, float *out, fl
     if (!rows_map(&tmK, a.K, D, rows) || !rows_map(&tmV, a.V, D, rows)) return KVR_ERR_CUDA;
     tiered_attend_kernel<D, G><<<dim3(a.S, U), kThreads, C::bytes, c.stream>>>(a, tmK, tmV);
     if (check_launch() != KVR_OK) return KVR_ERR_CUDA;  // the combine reads its partials
-    tiered_combine_kernel<D, G><<<U, kThreads, 0, c.stream>>>(a, out, mass);
+    const int csmem = 2 * a.S * G * (int)sizeof(float);
+    if (raise_smem_limit(reinterpret_cast<const void *>(&tiered_combine_kernel<D, G>), csmem) != KVR_OK)
+        return KVR_ERR_CUDA;
+    tiered_combine_kernel<D, G><<<U, kThreads, csmem, c.stream>>>(a, out, mass);
     return check_launch();
 }
 
