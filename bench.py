@@ -539,15 +539,23 @@ def run_gpu(args, w):
                "select_kernel_mag" if args.votes == "magnitude" else "select_kernel")
     peak, peak_kind = peaks()
     roof = None
+    # kvr_select_attend runs as one launch for groups of up to 4 heads with
+    # exact rescoring and Hamming-ring votes, otherwise as the two kernels
+    one_launch = w.G <= 4 and rerank == "exact" and args.votes == "hamming"
     if avg["call"]:
         if fused:
             byts = ab["select"] + ab["attend"]
             ach = byts / (avg["call"] * 1e-3) / 1e9
-            roof = {"bound": "hbm", "kernel": "select_kernel with the attention tail "
-                    "(kvr_select_attend, one launch)", "achieved": ach, "peak": peak,
+            if one_launch:
+                kern = "select_kernel with the attention tail (kvr_select_attend, one launch)"
+                traffic = measured_traffic("select_attend_kernel", w.name)
+            else:
+                kern = "select_kernel then attend_kernel (kvr_select_attend, two launches)"
+                t_sel, t_att = measured_traffic(sel_key, w.name), measured_traffic("attend_kernel", w.name)
+                traffic = None if host or None in (t_sel, t_att) else t_sel + t_att
+            roof = {"bound": "hbm", "kernel": kern, "achieved": ach, "peak": peak,
                     "unit": "GB/s", "frac": ach / peak, "frac_of_8TBs": ach / 8000.0,
-                    "peak_kind": peak_kind,
-                    "traffic": measured_traffic("select_attend_kernel", w.name),
+                    "peak_kind": peak_kind, "traffic": traffic,
                     "algorithmic_bytes": byts, "avg_ms": avg["call"]}
         else:
             ach = ab["select"] / (avg["select"] * 1e-3) / 1e9
@@ -600,7 +608,8 @@ def run_gpu(args, w):
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline_line(w, args.cpu_seconds, "cuda")
     cfg = dict(config_of(w), rerank=rerank, votes=args.votes,
-               path="kvr_select_attend (one launch)" if fused else
+               path=("kvr_select_attend (one launch)" if one_launch else
+                     "kvr_select_attend (two launches: optional modes)") if fused else
                "kvr_select + kvr_sparse_attend (two launches)",
                appending="each step appends one token (its K / V row and code) and uses a "
                          "fresh query; lengths %d -> %d over the run"
