@@ -1197,12 +1197,15 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     __syncthreads();
 
     // ---------------------------------------------------------------- P5
-    // Top-k over the cluster in three small exchanges: (1) the score range;
-    // (2) a 256-bin linear histogram of every slice over that range (the bin
-    // map is monotone, so the k'-th largest key sits in one boundary bin);
-    // (3) the boundary bin's keys, among which one warp finds the exact key
-    // with 8-bit radix passes. A boundary bin too large to gather (massive
-    // ties) falls back to every CTA gathering all C' keys.
+    // Top-k over the cluster in three small exchanges: (1) the score range
+    // (every CTA's min and max pushed into every CTA); (2) a 256-bin linear
+    // histogram of every slice over that range, 16 bits per bin (the bin map
+    // is monotone, so the k'-th largest key sits in one boundary bin); (3)
+    // the counts above and in the boundary bin (pushed) and the bin's keys
+    // (gathered), ranked by counting (past 32 of them inside one of 256
+    // sub-bins of the bin; past 256 in that sub-bin, by one warp's 8-bit
+    // radix passes). A boundary bin too large to gather (massive ties) falls
+    // back to every CTA gathering all C' keys.
     static_assert(kSelThreads == 256, "one histogram bin per thread");
     int *sWH = reinterpret_cast<int *>(smem + SM::oWH);
     uint32_t *sPub = reinterpret_cast<uint32_t *>(ring);  // own boundary keys, published
